@@ -1,0 +1,227 @@
+"""Python binding of the GB300 4-bit MoE layer library (libmoe_gb300.so).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA kernels.
+Tensors are torch CUDA tensors; bf16 data may be passed as torch.bfloat16 or as 16-bit
+integer bit patterns.  The C declarations and contracts are in include/moe.h.
+
+There is no fallback: importing works without a GPU (so the exported symbols can be
+inspected), but every call needs the built library and a CUDA device, and raises otherwise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libmoe_gb300.so")
+
+# Symbols declared in include/moe.h.
+EXPORTED = ("moe_status_string", "moe_max_tiles", "moe_workspace_bytes", "moe_route",
+            "moe_expert_forward", "moe_layer_forward", "moe_read_error_flags")
+
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_MISALIGNED",
+          4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA"}
+ERR_WAIT_TIMEOUT, ERR_FP16_RANGE, ERR_BAD_ROUTING = 1, 2, 4
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("F", ctypes.c_int32), ("F_shared", ctypes.c_int32)]
+
+
+class QMat(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("biases", ctypes.c_void_p)]
+
+
+class ExpertsC(ctypes.Structure):
+    _fields_ = [("gate", QMat), ("up", QMat), ("down", QMat)]
+
+
+class RoutingC(ctypes.Structure):
+    _fields_ = [("idx", ctypes.c_void_p), ("w", ctypes.c_void_p), ("counts", ctypes.c_void_p),
+                ("offsets", ctypes.c_void_p), ("perm", ctypes.c_void_p), ("inv", ctypes.c_void_p),
+                ("tiles", ctypes.c_void_p), ("num_tiles", ctypes.c_void_p), ("tile_n", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the shared library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} not found: build it with `python -m bit_quantized_expert_gb300.build`")
+    try:
+        import torch  # noqa: F401  (loads the CUDA runtime the library links against)
+    except Exception:
+        pass
+    lib = ctypes.CDLL(path)
+    P, S, I32, VP = ctypes.POINTER, ctypes.c_size_t, ctypes.c_int32, ctypes.c_void_p
+    lib.moe_status_string.restype = ctypes.c_char_p
+    lib.moe_status_string.argtypes = [ctypes.c_int]
+    lib.moe_max_tiles.restype = S
+    lib.moe_max_tiles.argtypes = [P(Dims), I32]
+    lib.moe_workspace_bytes.restype = S
+    lib.moe_workspace_bytes.argtypes = [P(Dims)]
+    lib.moe_route.restype = ctypes.c_int
+    lib.moe_route.argtypes = [P(Dims), VP, P(RoutingC), VP, S, VP]
+    lib.moe_expert_forward.restype = ctypes.c_int
+    lib.moe_expert_forward.argtypes = [P(Dims), VP, P(RoutingC), P(ExpertsC), P(ExpertsC), VP, VP, S, VP]
+    lib.moe_layer_forward.restype = ctypes.c_int
+    lib.moe_layer_forward.argtypes = [P(Dims), VP, VP, P(ExpertsC), P(ExpertsC), VP, VP, P(RoutingC), VP, S, VP]
+    lib.moe_read_error_flags.restype = ctypes.c_int
+    lib.moe_read_error_flags.argtypes = [VP, S, P(ctypes.c_uint32), VP]
+    _lib = lib
+    return lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise MoeError(status, what)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def dims(T, d, E, k, F, F_shared) -> Dims:
+    return Dims(int(T), int(d), int(E), int(k), int(F), int(F_shared))
+
+
+def experts_struct(ex: dict | None) -> ExpertsC | None:
+    """{"gate"|"up"|"down": {"codes", "scales", "biases"}} of CUDA tensors -> C struct."""
+    if ex is None:
+        return None
+
+    def q(m):
+        return QMat(_ptr(m["codes"]), _ptr(m["scales"]), _ptr(m["biases"]))
+
+    return ExpertsC(q(ex["gate"]), q(ex["up"]), q(ex["down"]))
+
+
+def routing_struct(r: dict) -> RoutingC:
+    return RoutingC(_ptr(r["idx"]), _ptr(r["w"]), _ptr(r["counts"]), _ptr(r["offsets"]), _ptr(r["perm"]),
+                    _ptr(r["inv"]), _ptr(r["tiles"]), _ptr(r["num_tiles"]), int(r["tile_n"]))
+
+
+def max_tiles(dm: Dims, tile_n: int) -> int:
+    return load_library().moe_max_tiles(ctypes.byref(dm), int(tile_n))
+
+
+def workspace_bytes(dm: Dims) -> int:
+    n = load_library().moe_workspace_bytes(ctypes.byref(dm))
+    if n == 0:
+        raise MoeError(1, "moe_workspace_bytes")
+    return n
+
+
+def alloc_workspace(dm: Dims, device="cuda"):
+    import torch
+    return torch.empty(workspace_bytes(dm), dtype=torch.uint8, device=device)
+
+
+def alloc_routing(dm: Dims, tile_n: int = 128, device="cuda") -> dict:
+    import torch
+    T, k, E = dm.T, dm.k, dm.E
+    i32 = dict(dtype=torch.int32, device=device)
+    return {"idx": torch.empty((T, k), **i32), "w": torch.empty((T, k), dtype=torch.float32, device=device),
+            "counts": torch.empty(E, **i32), "offsets": torch.empty(E + 1, **i32),
+            "perm": torch.empty(T * k, **i32), "inv": torch.empty(T * k, **i32),
+            "tiles": torch.empty((max(1, max_tiles(dm, tile_n)), 4), **i32),
+            "num_tiles": torch.empty(1, **i32), "tile_n": tile_n}
+
+
+def route(dm: Dims, logits, routing: dict, workspace, stream=None):
+    r = routing_struct(routing)
+    _check(load_library().moe_route(ctypes.byref(dm), _ptr(logits), ctypes.byref(r), _ptr(workspace),
+                                    workspace.numel(), _stream(stream)), "moe_route")
+
+
+def expert_forward(dm: Dims, x, routing: dict, routed: dict, shared: dict | None, y_perm, workspace,
+                   stream=None):
+    r = routing_struct(routing)
+    re, se = experts_struct(routed), experts_struct(shared)
+    _check(load_library().moe_expert_forward(ctypes.byref(dm), _ptr(x), ctypes.byref(r), ctypes.byref(re),
+                                             ctypes.byref(se) if se is not None else None, _ptr(y_perm),
+                                             _ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_expert_forward")
+
+
+def layer_forward(dm: Dims, x, logits, routed: dict, shared: dict | None, w_sg, y, workspace,
+                  routing: dict | None = None, stream=None):
+    re, se = experts_struct(routed), experts_struct(shared)
+    r = routing_struct(routing) if routing is not None else None
+    _check(load_library().moe_layer_forward(ctypes.byref(dm), _ptr(x), _ptr(logits), ctypes.byref(re),
+                                            ctypes.byref(se) if se is not None else None, _ptr(w_sg), _ptr(y),
+                                            ctypes.byref(r) if r is not None else None, _ptr(workspace),
+                                            workspace.numel(), _stream(stream)), "moe_layer_forward")
+
+
+def read_error_flags(workspace, stream=None) -> int:
+    out = ctypes.c_uint32(0)
+    _check(load_library().moe_read_error_flags(_ptr(workspace), workspace.numel(), ctypes.byref(out),
+                                               _stream(stream)), "moe_read_error_flags")
+    return out.value
+
+
+class Layer:
+    """Device-resident weights of one MoE layer plus the dims, for repeated calls."""
+
+    def __init__(self, routed: dict, shared: dict | None, w_sg, d: int, E: int, k: int, F: int):
+        self.routed, self.shared, self.w_sg = routed, shared, w_sg
+        self.d, self.E, self.k, self.F = d, E, k, F
+        self._re = experts_struct(routed)
+        self._se = experts_struct(shared)
+
+    def dims(self, T: int) -> Dims:
+        return dims(T, self.d, self.E, self.k, self.F, self.F if self.shared is not None else 0)
+
+    def forward(self, x, logits, y, workspace, routing: dict | None = None, stream=None):
+        dm = self.dims(x.shape[0])
+        r = routing_struct(routing) if routing is not None else None
+        _check(load_library().moe_layer_forward(ctypes.byref(dm), _ptr(x), _ptr(logits), ctypes.byref(self._re),
+                                                ctypes.byref(self._se) if self._se is not None else None,
+                                                _ptr(self.w_sg), _ptr(y), ctypes.byref(r) if r is not None else None,
+                                                _ptr(workspace), workspace.numel(), _stream(stream)),
+               "moe_layer_forward")
+
+
+def to_device_layer(layer: dict, device="cuda") -> dict:
+    """numpy layer (synth.make_layer) -> the same nesting of contiguous CUDA tensors."""
+    import numpy as np
+    import torch
+
+    def t(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint32:
+            a = a.view(np.int32)
+        elif a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(a).to(device)
+
+    def ex(e):
+        if e is None:
+            return None
+        return {m: {f: t(e[m][f]) for f in ("codes", "scales", "biases")} for m in ("gate", "up", "down")}
+
+    return {"routed": ex(layer["routed"]), "shared": ex(layer.get("shared")), "w_sg": t(layer["w_sg"])}

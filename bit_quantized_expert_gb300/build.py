@@ -1,0 +1,77 @@
+"""Build the sm_103a MoE library in-tree: one nvcc process per translation unit (in parallel),
+then one link step.  Output: bit_quantized_expert_gb300/libmoe_gb300.so.
+
+    python -m bit_quantized_expert_gb300.build [--force]
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import os
+import shutil
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(PKG, "csrc")
+BUILD = os.path.join(PKG, "_build")
+LIB = os.path.join(PKG, "libmoe_gb300.so")
+SOURCES = ["api.cu", "route.cu", "gemm.cu", "decode.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
+         "-Xptxas", "-v"]
+
+
+def _nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: the MoE library needs the CUDA 13 toolkit")
+
+
+def _deps() -> list[str]:
+    hdrs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
+    hdrs.append(os.path.join(os.path.dirname(PKG), "include", "moe.h"))
+    return hdrs
+
+
+def _stale(target: str, inputs: list[str]) -> bool:
+    if not os.path.exists(target):
+        return True
+    t = os.path.getmtime(target)
+    return any(os.path.getmtime(p) > t for p in inputs if os.path.exists(p))
+
+
+def _compile(nvcc: str, src: str, obj: str) -> str:
+    cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+    return r.stderr
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    nvcc = _nvcc()
+    os.makedirs(BUILD, exist_ok=True)
+    deps = _deps()
+    objs, jobs = [], []
+    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        for src in SOURCES:
+            obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+            objs.append(obj)
+            if force or _stale(obj, [os.path.join(CSRC, src), *deps]):
+                jobs.append((src, ex.submit(_compile, nvcc, src, obj)))
+        logs = [(src, f.result()) for src, f in jobs]
+    if verbose:
+        for src, log in logs:
+            print(f"--- {src}\n{log}", file=sys.stderr)
+    if force or jobs or _stale(LIB, objs):
+        cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", LIB, *objs,
+               "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

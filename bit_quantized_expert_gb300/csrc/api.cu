@@ -1,0 +1,389 @@
+// C ABI of the MoE layer (declarations and contracts in include/moe.h).  Host-side argument
+// checks, workspace layout, TMA descriptor encoding and launch order; no allocation and no
+// host synchronisation except moe_read_error_flags.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kTileN = 128;   // block-map tile of the layer call (token rows per MMA tile)
+
+struct Layout {
+  size_t err, x16p, gs, idx, w, counts, offsets, perm, inv, tiles, num_tiles, h, yperm, hdec, total;
+};
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+size_t max_tiles_of(long long T, long long k, long long E, long long tile_n, bool shared) {
+  return (size_t)(T * k / tile_n + std::min(E, T * k) + (shared ? (T + tile_n - 1) / tile_n : 0));
+}
+
+Layout layout_of(const moe_dims& d) {
+  Layout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
+  const size_t T = d.T, k = d.k, E = d.E, D = d.d, F = d.F;
+  const bool sh = d.F_shared > 0;
+  const size_t slots = T * k + (sh ? T : 0);
+  L.err = take(256);
+  L.x16p = take(T * D * 2);
+  L.gs = take(T * 4);
+  L.idx = take(T * k * 4);
+  L.w = take(T * k * 4);
+  L.counts = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.perm = take(T * k * 4);
+  L.inv = take(T * k * 4);
+  L.tiles = take(max_tiles_of(d.T, d.k, d.E, kTileN, sh) * 16);
+  L.num_tiles = take(16);
+  L.h = take(slots * F * 2);
+  L.yperm = take(slots * D * 4);
+  L.hdec = take(33 * F * 4);
+  L.total = o;
+  return L;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_dims(const moe_dims* d) {
+  if (d == nullptr) return MOE_ERR_INVALID_ARG;
+  if (d->T < 0 || d->k < 1 || d->E < 1 || d->k > d->E || d->d < 1 || d->F < 1 || d->F_shared < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (d->k > 32 || d->E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (d->d % 128 != 0 || d->F % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (d->F_shared != 0 && d->F_shared != d->F) return MOE_ERR_UNSUPPORTED;
+  if ((long long)d->T * (d->k + 1) >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  if ((long long)d->d * d->F >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status check_qmat(const moe_qmat& q) {
+  if (!q.codes || !q.scales || !q.biases) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(q.codes) || !aligned16(q.scales) || !aligned16(q.biases)) return MOE_ERR_MISALIGNED;
+  return MOE_OK;
+}
+
+moe_status check_experts(const moe_experts* x) {
+  if (x == nullptr) return MOE_ERR_INVALID_ARG;
+  moe_status s;
+  if ((s = check_qmat(x->gate)) != MOE_OK) return s;
+  if ((s = check_qmat(x->up)) != MOE_OK) return s;
+  return check_qmat(x->down);
+}
+
+moe_status check_ptr(const void* p) {
+  if (p == nullptr) return MOE_ERR_INVALID_ARG;
+  return aligned16(p) ? MOE_OK : MOE_ERR_MISALIGNED;
+}
+
+moe_status check_routing(const moe_routing* r) {
+  if (r == nullptr) return MOE_ERR_INVALID_ARG;
+  const void* ps[] = {r->idx, r->w, r->counts, r->offsets, r->perm, r->inv, r->tiles, r->num_tiles};
+  for (const void* p : ps) {
+    moe_status s = check_ptr(p);
+    if (s != MOE_OK) return s;
+  }
+  if (r->tile_n < 16 || r->tile_n > 128 || r->tile_n % 16 != 0) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// ---------------------------------------------------------------- TMA descriptors
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Packed codes of n stacked [R, C] matrices as a 3-D uint32 tensor {C/8, R, n}; box 8 x 128 x 1
+// (64 codes of 128 rows = one 4 KB quantisation-group column of a tile).
+bool encode_codes(CUtensorMap* m, const uint32_t* codes, int n, int R, int C) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)(C / 8), (cuuint64_t)R, (cuuint64_t)n};
+  const cuuint64_t strides[2] = {(cuuint64_t)(C / 8) * 4, (cuuint64_t)R * (C / 8) * 4};
+  const cuuint32_t box[3] = {8, 128, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(codes), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// h [slots, F] fp16 with a 64 x 128 box in the 128-byte swizzle (the MMA operand layout).
+bool encode_h(CUtensorMap* m, const uint16_t* h, long long slots, int F) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)F, (cuuint64_t)slots};
+  const cuuint64_t strides[1] = {(cuuint64_t)F * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t es[2] = {1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(h), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int counts[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev < 0 || dev >= 64) return 1;
+  if (counts[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    counts[dev] = n > 0 ? n : 1;
+  }
+  return counts[dev];
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+struct RoutingPtrs {
+  int32_t *idx, *counts, *offsets, *perm, *inv, *tiles, *num_tiles;
+  float* w;
+  int tile_n;
+};
+
+RoutingPtrs internal_routing(void* ws, const Layout& L) {
+  return {at<int32_t>(ws, L.idx),   at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
+          at<int32_t>(ws, L.perm),  at<int32_t>(ws, L.inv),    at<int32_t>(ws, L.tiles),
+          at<int32_t>(ws, L.num_tiles), at<float>(ws, L.w),    kTileN};
+}
+
+RoutingPtrs caller_routing(const moe_routing* r) {
+  return {r->idx, r->counts, r->offsets, r->perm, r->inv, r->tiles, r->num_tiles, r->w, r->tile_n};
+}
+
+cudaError_t run_routing(const moe_dims& d, const float* logits, const RoutingPtrs& R, const uint16_t* x,
+                        const uint16_t* w_sg, uint16_t* x16p, float* gs, uint32_t* err, cudaStream_t st) {
+  RouteArgs ra{logits, d.T, d.E, d.k, d.d, R.idx, R.w, x, w_sg, x16p, gs, err};
+  cudaError_t e = launch_topk(ra, st);
+  if (e != cudaSuccess) return e;
+  TablesArgs ta{R.idx, d.T, d.E, d.k, R.tile_n, d.F_shared > 0 ? 1 : 0, R.counts, R.offsets, R.perm, R.inv,
+                R.tiles, R.num_tiles, err};
+  return launch_tables(ta, st);
+}
+
+QPtr qptr(const moe_qmat& q) { return QPtr{q.codes, q.scales, q.biases}; }
+
+// Gate/up GEMM (h) then down GEMM (y_perm) over the block map in R.
+moe_status run_experts(const moe_dims& d, const RoutingPtrs& R, const moe_experts* routed, const moe_experts* shared,
+                       const uint16_t* x16p, uint16_t* h, float* y_perm, uint32_t* err, cudaStream_t st) {
+  const bool sh = shared != nullptr && d.F_shared > 0;
+  const long long slots = (long long)d.T * d.k + (sh ? d.T : 0);
+  const moe_experts* s_or_r = sh ? shared : routed;
+  const int ns = sh ? 1 : d.E;
+
+  GemmMaps m0{}, m1{};
+  bool ok = encode_codes(&m0.codes[0][0], routed->gate.codes, d.E, d.F, d.d) &&
+            encode_codes(&m0.codes[0][1], s_or_r->gate.codes, ns, d.F, d.d) &&
+            encode_codes(&m0.codes[1][0], routed->up.codes, d.E, d.F, d.d) &&
+            encode_codes(&m0.codes[1][1], s_or_r->up.codes, ns, d.F, d.d) &&
+            encode_codes(&m1.codes[0][0], routed->down.codes, d.E, d.d, d.F) &&
+            encode_codes(&m1.codes[0][1], s_or_r->down.codes, ns, d.d, d.F) &&
+            encode_h(&m1.h, h, slots, d.F);
+  if (!ok) return MOE_ERR_CUDA;
+  m0.h = m1.h;
+  m1.codes[1][0] = m1.codes[0][0];
+  m1.codes[1][1] = m1.codes[0][1];
+
+  const size_t maxt = max_tiles_of(d.T, d.k, d.E, R.tile_n, sh);
+  GemmArgs a{};
+  a.tiles = R.tiles;
+  a.num_tiles = R.num_tiles;
+  a.perm = R.perm;
+  a.x16p = x16p;
+  a.T = d.T;
+  a.k = d.k;
+  a.E = d.E;
+  a.d = d.d;
+  a.F = d.F;
+  a.h = h;
+  a.y_perm = y_perm;
+  a.err = err;
+  a.mat[0][0] = qptr(routed->gate);
+  a.mat[0][1] = qptr(s_or_r->gate);
+  a.mat[1][0] = qptr(routed->up);
+  a.mat[1][1] = qptr(s_or_r->up);
+  const int sms = sm_count();
+  const int g0 = (int)std::max<size_t>(1, std::min<size_t>((size_t)sms, maxt * (d.F / 128)));
+  cudaError_t e = launch_gemm(0, m0, a, g0, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  a.mat[0][0] = qptr(routed->down);
+  a.mat[0][1] = qptr(s_or_r->down);
+  a.mat[1][0] = a.mat[0][0];
+  a.mat[1][1] = a.mat[0][1];
+  const int g1 = (int)std::max<size_t>(1, std::min<size_t>((size_t)sms, maxt * (d.d / 128)));
+  e = launch_gemm(1, m1, a, g1, st);
+  return cuda_status(e);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: null pointer or argument out of range";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: dimensions outside the supported limits";
+    case MOE_ERR_MISALIGNED: return "MOE_ERR_MISALIGNED: a pointer is not 16-byte aligned";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace missing or too small";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call or kernel launch failed";
+  }
+  return "unknown moe_status";
+}
+
+size_t moe_max_tiles(const moe_dims* dims, int32_t tile_n) {
+  if (check_dims(dims) != MOE_OK || tile_n < 16 || tile_n > 128 || tile_n % 16 != 0) return 0;
+  return max_tiles_of(dims->T, dims->k, dims->E, tile_n, dims->F_shared > 0);
+}
+
+size_t moe_workspace_bytes(const moe_dims* dims) {
+  if (check_dims(dims) != MOE_OK) return 0;
+  return layout_of(*dims).total;
+}
+
+moe_status moe_route(const moe_dims* dims, const float* logits, const moe_routing* out, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  moe_status s = check_dims(dims);
+  if (s != MOE_OK) return s;
+  if ((s = check_routing(out)) != MOE_OK) return s;
+  if (dims->T == 0) return MOE_OK;
+  if ((s = check_ptr(logits)) != MOE_OK) return s;
+  if ((s = check_ptr(workspace)) != MOE_OK) return s == MOE_ERR_INVALID_ARG ? MOE_ERR_WORKSPACE : s;
+  const Layout L = layout_of(*dims);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* err = at<uint32_t>(workspace, L.err);
+  if (cudaMemsetAsync(err, 0, 4, st) != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(run_routing(*dims, logits, caller_routing(out), nullptr, nullptr, nullptr, nullptr, err, st));
+}
+
+moe_status moe_expert_forward(const moe_dims* dims, const uint16_t* x, const moe_routing* routing,
+                              const moe_experts* routed, const moe_experts* shared, float* y_perm, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  moe_status s = check_dims(dims);
+  if (s != MOE_OK) return s;
+  if ((s = check_routing(routing)) != MOE_OK) return s;
+  if ((s = check_experts(routed)) != MOE_OK) return s;
+  if (shared != nullptr && (s = check_experts(shared)) != MOE_OK) return s;
+  if (shared != nullptr && dims->F_shared == 0) return MOE_ERR_INVALID_ARG;
+  if (shared == nullptr && dims->F_shared != 0) return MOE_ERR_INVALID_ARG;
+  if (dims->T == 0) return MOE_OK;
+  if ((s = check_ptr(x)) != MOE_OK) return s;
+  if ((s = check_ptr(y_perm)) != MOE_OK) return s;
+  if ((s = check_ptr(workspace)) != MOE_OK) return s == MOE_ERR_INVALID_ARG ? MOE_ERR_WORKSPACE : s;
+  const Layout L = layout_of(*dims);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* err = at<uint32_t>(workspace, L.err);
+  if (cudaMemsetAsync(err, 0, 4, st) != cudaSuccess) return MOE_ERR_CUDA;
+  uint16_t* x16p = at<uint16_t>(workspace, L.x16p);
+  ConvertArgs ca{x, x16p, dims->T, dims->d, err};
+  if (launch_convert(ca, st) != cudaSuccess) return MOE_ERR_CUDA;
+  return run_experts(*dims, caller_routing(routing), routed, shared, x16p, at<uint16_t>(workspace, L.h), y_perm, err,
+                     st);
+}
+
+moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const float* logits, const moe_experts* routed,
+                             const moe_experts* shared, const uint16_t* w_shared_gate, float* y,
+                             const moe_routing* routing_out, void* workspace, size_t workspace_bytes, void* stream) {
+  moe_status s = check_dims(dims);
+  if (s != MOE_OK) return s;
+  if ((s = check_experts(routed)) != MOE_OK) return s;
+  if (shared != nullptr && (s = check_experts(shared)) != MOE_OK) return s;
+  if (shared != nullptr && dims->F_shared == 0) return MOE_ERR_INVALID_ARG;
+  if (shared == nullptr && dims->F_shared != 0) return MOE_ERR_INVALID_ARG;
+  if (routing_out != nullptr && (s = check_routing(routing_out)) != MOE_OK) return s;
+  if (dims->T == 0) return MOE_OK;
+  if ((s = check_ptr(x)) != MOE_OK) return s;
+  if ((s = check_ptr(logits)) != MOE_OK) return s;
+  if ((s = check_ptr(y)) != MOE_OK) return s;
+  if (shared != nullptr && (s = check_ptr(w_shared_gate)) != MOE_OK) return s;
+  if ((s = check_ptr(workspace)) != MOE_OK) return s == MOE_ERR_INVALID_ARG ? MOE_ERR_WORKSPACE : s;
+  const Layout L = layout_of(*dims);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* err = at<uint32_t>(workspace, L.err);
+  if (cudaMemsetAsync(err, 0, 4, st) != cudaSuccess) return MOE_ERR_CUDA;
+  const bool sh = shared != nullptr;
+  const moe_dims& d = *dims;
+
+  if (d.T == 1 && decode_supported(d.d, d.E, d.k, d.F)) {
+    DecodeArgs da{};
+    da.x = x;
+    da.logits = logits;
+    da.gate[0] = qptr(routed->gate);
+    da.up[0] = qptr(routed->up);
+    da.down[0] = qptr(routed->down);
+    if (sh) {
+      da.gate[1] = qptr(shared->gate);
+      da.up[1] = qptr(shared->up);
+      da.down[1] = qptr(shared->down);
+    }
+    da.w_sg = sh ? w_shared_gate : nullptr;
+    da.d = d.d;
+    da.E = d.E;
+    da.k = d.k;
+    da.F = d.F;
+    da.has_shared = sh ? 1 : 0;
+    da.h = at<float>(workspace, L.hdec);
+    da.y = y;
+    da.err = err;
+    if (launch_decode(da, st, true) != cudaSuccess) return MOE_ERR_CUDA;
+    if (routing_out != nullptr)
+      return cuda_status(run_routing(d, logits, caller_routing(routing_out), nullptr, nullptr, nullptr, nullptr, err, st));
+    return MOE_OK;
+  }
+
+  const RoutingPtrs R = routing_out ? caller_routing(routing_out) : internal_routing(workspace, L);
+  uint16_t* x16p = at<uint16_t>(workspace, L.x16p);
+  float* gs = sh ? at<float>(workspace, L.gs) : nullptr;
+  cudaError_t e = run_routing(d, logits, R, x, sh ? w_shared_gate : nullptr, x16p, gs, err, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  float* yperm = at<float>(workspace, L.yperm);
+  s = run_experts(d, R, routed, sh ? shared : nullptr, x16p, at<uint16_t>(workspace, L.h), yperm, err, st);
+  if (s != MOE_OK) return s;
+  CombineArgs cb{yperm, R.inv, R.w, gs, d.T, d.k, d.d, y};
+  return cuda_status(launch_combine(cb, st));
+}
+
+moe_status moe_read_error_flags(const void* workspace, size_t workspace_bytes, uint32_t* flags, void* stream) {
+  if (workspace == nullptr || flags == nullptr) return MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < 4) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(flags, workspace, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // extern "C"

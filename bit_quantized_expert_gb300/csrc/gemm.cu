@@ -1,0 +1,523 @@
+// Fused-dequant grouped GEMM of the MoE experts on sm_103a tensor cores (tcgen05 + TMEM).
+//
+// The pages describe the prefill expert GEMM as rebuilding the 4-bit weights one tile at a
+// time in on-chip memory and accumulating in FP32, so the expanded weights never reach DRAM,
+// and report the expert GEMMs as about 90% of prefill time ("Perplexity libera Lily:
+// inferencia en Rust y Metal para Mac", section "Prefill: pesos comprimidos y enrutamiento en
+// la GPU").  This kernel is that design re-thought for GB300:
+//
+//   * Swap-AB: the weight rows of one expert form the MMA's M = 128 side, the (few, uneven)
+//     tokens routed to the expert form N (16..128, rounded up to 16).  D[m, n] = sum_k W[m, k]
+//     X[n, k] lands in TMEM (fp32), lane m, column n.
+//   * Work unit = (block-map tile of <= 128 slots of one expert, 128-row slice of the weight
+//     matrix), iterated over K in chunks of 64 (= one quantisation group).  A persistent grid of
+//     one CTA per SM walks the units; every role walks the same list.
+//   * Warp roles (12 warps): 0 = TMA producer (packed codes; the h operand of the down
+//     projection), 1 = MMA issuer (one thread) and TMEM owner, 2-3 = row gather of x for the
+//     gate/up projection (16-byte cp.async into the swizzled operand layout), 4-7 = dequant
+//     (one weight row per thread: 4-bit codes -> fp16 w = q*scale + bias, single rounding),
+//     8-11 = epilogue (TMEM -> registers; SwiGLU -> fp16 h, or fp32 expert outputs).
+//   * Gate/up mode keeps the gate and up accumulators of the same 128 F-rows side by side in
+//     TMEM so the epilogue applies silu(g) * u in registers.  Two accumulator buffers let the
+//     epilogue of one unit overlap the MMAs of the next.
+//   * Operands are fp16 (the dequantised weights, x and h), accumulation fp32.  Within every
+//     8-element K chunk both operands are stored in the order (0,4,1,5,2,6,3,7), which lets the
+//     dequant turn one 32-bit code word into four fp16 pairs with one LOP3 each.
+//   * Every wait is bounded (mbar_wait); on timeout the CTA sets the error word and winds down.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kThreads = 384;
+constexpr uint32_t kTileBytes = 128 * 128;   // one 128-row x 64-column fp16 operand tile
+constexpr uint32_t kRawBytes = 128 * 32;     // 128 rows x 64 packed 4-bit codes
+
+template <int MODE>
+struct Cfg {
+  static constexpr int NMAT = MODE == 0 ? 2 : 1;
+  static constexpr int S_RAW = MODE == 0 ? 6 : 8;
+  static constexpr int S_W = MODE == 0 ? 3 : 4;
+  static constexpr int S_X = MODE == 0 ? 3 : 4;
+  static constexpr int NBAR = 2 * S_RAW + 2 * S_W + 2 * S_X + 4;
+  static constexpr uint32_t OFF_W = 0;
+  static constexpr uint32_t OFF_X = OFF_W + S_W * NMAT * kTileBytes;
+  static constexpr uint32_t OFF_RAW = OFF_X + S_X * kTileBytes;
+  static constexpr uint32_t OFF_BAR = OFF_RAW + S_RAW * NMAT * kRawBytes;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
+  static constexpr uint32_t ACC_COLS = NMAT * 128;          // TMEM columns of one accumulator buffer
+};
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Eight bf16 scale (or bias) values of groups g0 .. g0+7 of one weight row.
+__device__ __forceinline__ uint4 load_group_block(const uint16_t* row, int g0, int G) {
+  if ((G & 7) == 0) return ldg_nc_v4(row + g0);
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (g0 + j < G) w[j >> 1] |= (uint32_t)__ldg(row + g0 + j) << (16 * (j & 1));
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <int J>
+__device__ __forceinline__ uint32_t pick_bf16(const uint4& v) {
+  const uint32_t w = (J >> 1) == 0 ? v.x : (J >> 1) == 1 ? v.y : (J >> 1) == 2 ? v.z : v.w;
+  return (J & 1) ? (w >> 16) : (w & 0xFFFFu);
+}
+
+// One packed word (8 codes, logical columns 0..7) -> four fp16x2 words holding
+// (w0,w4), (w1,w5), (w2,w6), (w3,w7) with w = q * s + b rounded once to fp16.
+__device__ __forceinline__ void dequant_word(uint32_t q, __half2 s2, __half2 b2, uint32_t (&o)[4]) {
+  const __half2 magic = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));   // 1024
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const uint32_t t = ((q >> (4 * p)) & 0x000F000Fu) | 0x64006400u;   // (1024 + q_p, 1024 + q_{p+4})
+    __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&t), magic);   // exact codes
+    v = __hfma2(v, s2, b2);
+    o[p] = *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
+  using C = Cfg<MODE>;
+  constexpr int NMAT = C::NMAT;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t s_raw0 = smem_u32(smem_raw);
+  const uint32_t sbase = (s_raw0 + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (sbase - s_raw0);
+  const uint32_t sW = sbase + C::OFF_W, sX = sbase + C::OFF_X, sRaw = sbase + C::OFF_RAW;
+  const uint32_t sBar = sbase + C::OFF_BAR;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::OFF_MISC);
+  volatile int* abort_s = reinterpret_cast<volatile int*>(gbase + C::OFF_MISC + 4);
+
+  auto RF = [&](int i) { return sBar + 8u * i; };
+  auto RE = [&](int i) { return sBar + 8u * (C::S_RAW + i); };
+  auto WF = [&](int i) { return sBar + 8u * (2 * C::S_RAW + i); };
+  auto WE = [&](int i) { return sBar + 8u * (2 * C::S_RAW + C::S_W + i); };
+  auto XF = [&](int i) { return sBar + 8u * (2 * C::S_RAW + 2 * C::S_W + i); };
+  auto XE = [&](int i) { return sBar + 8u * (2 * C::S_RAW + 2 * C::S_W + C::S_X + i); };
+  auto AF = [&](int i) { return sBar + 8u * (2 * C::S_RAW + 2 * C::S_W + 2 * C::S_X + i); };
+  auto AE = [&](int i) { return sBar + 8u * (2 * C::S_RAW + 2 * C::S_W + 2 * C::S_X + 2 + i); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::S_RAW; ++i) {
+      mbar_init(RF(i), 1);
+      mbar_init(RE(i), 4);
+    }
+    for (int i = 0; i < C::S_W; ++i) {
+      mbar_init(WF(i), 4);
+      mbar_init(WE(i), 1);
+    }
+    for (int i = 0; i < C::S_X; ++i) {
+      mbar_init(XF(i), MODE == 0 ? 2 : 1);
+      mbar_init(XE(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(AF(i), 1);
+      mbar_init(AE(i), 4);
+    }
+    *abort_s = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&maps.codes[0][0]);
+    prefetch_tmap(&maps.codes[0][1]);
+    if (NMAT == 2) {
+      prefetch_tmap(&maps.codes[1][0]);
+      prefetch_tmap(&maps.codes[1][1]);
+    }
+    if (MODE == 1) prefetch_tmap(&maps.h);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int R = MODE == 0 ? a.F : a.d;   // weight rows (output features of this projection)
+  const int K = MODE == 0 ? a.d : a.F;   // reduction length
+  const int MT = R / kBM;
+  const int KC = K / 64;
+  const int num_units = (*a.num_tiles) * MT;
+  const int4* tiles = reinterpret_cast<const int4*>(a.tiles);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int s = 0, sx = 0;
+      uint32_t ph = 0, phx = 0;
+      for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+        const int4 tl = tiles[u / MT];
+        const int m = u % MT;
+        const int which = tl.x == a.E ? 1 : 0;
+        const int ec = which ? 0 : tl.x;
+        bool ok = true;
+        for (int kc = 0; kc < KC && ok; ++kc) {
+          if (!mbar_wait(RE(s), ph ^ 1u, abort_s, a.err)) { ok = false; break; }
+          mbar_arrive_expect_tx(RF(s), NMAT * kRawBytes);
+#pragma unroll
+          for (int mat = 0; mat < NMAT; ++mat)
+            tma_load_3d(sRaw + (s * NMAT + mat) * kRawBytes, &maps.codes[mat][which], RF(s), kc * 8, m * kBM, ec);
+          if (++s == C::S_RAW) { s = 0; ph ^= 1u; }
+          if (MODE == 1) {
+            if (!mbar_wait(XE(sx), phx ^ 1u, abort_s, a.err)) { ok = false; break; }
+            mbar_arrive_expect_tx(XF(sx), kTileBytes);
+            tma_load_2d(sX + sx * kTileBytes, &maps.h, XF(sx), kc * 64, tl.y);
+            if (++sx == C::S_X) { sx = 0; phx ^= 1u; }
+          }
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int sw = 0, sx = 0;
+      uint32_t phw = 0, phx = 0;
+      int li = 0;
+      for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++li) {
+        const int4 tl = tiles[u / MT];
+        const uint32_t n_inst = (uint32_t)((tl.z + 15) & ~15);
+        const int b = li & 1;
+        if (!mbar_wait(AE(b), ((li >> 1) & 1) ^ 1u, abort_s, a.err)) break;
+        tc_fence_after();
+        const uint32_t idesc = idesc_f16_f32(kBM, n_inst);
+        const uint32_t d0 = tmem + (uint32_t)(b * C::ACC_COLS);
+        bool ok = true;
+        for (int kc = 0; kc < KC; ++kc) {
+          if (!mbar_wait(WF(sw), phw, abort_s, a.err) || !mbar_wait(XF(sx), phx, abort_s, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bdesc = smem_desc_sw128(sX + sx * kTileBytes + kk * 32);
+#pragma unroll
+            for (int mat = 0; mat < NMAT; ++mat) {
+              const uint64_t adesc = smem_desc_sw128(sW + (sw * NMAT + mat) * kTileBytes + kk * 32);
+              tc_mma_f16(d0 + mat * 128, adesc, bdesc, idesc, (kc | kk) != 0 ? 1u : 0u);
+            }
+          }
+          tc_commit(WE(sw));
+          tc_commit(XE(sx));
+          if (++sw == C::S_W) { sw = 0; phw ^= 1u; }
+          if (++sx == C::S_X) { sx = 0; phx ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(AF(b));
+      }
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ x row gather (gate/up)
+    if (MODE == 0) {
+      const int g = threadIdx.x - 64;   // 0..63: rows g and g + 64 of every token tile
+      int issued = 0, arrived = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        const int4 tl = tiles[u / MT];
+        int tok[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = g + 64 * h;
+          tok[h] = -1;
+          if (r < tl.z) tok[h] = (tl.x == a.E) ? (tl.y + r - a.T * a.k) : (a.perm[tl.y + r] / a.k);
+        }
+        for (int kc = 0; kc < KC; ++kc) {
+          const int sx = issued % C::S_X;
+          const uint32_t par = ((uint32_t)(issued / C::S_X) & 1u) ^ 1u;
+          if (!mbar_wait(XE(sx), par, abort_s, a.err)) { ok = false; break; }
+          const uint32_t dst = sX + sx * kTileBytes;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (tok[h] < 0) continue;
+            const int r = g + 64 * h;
+            const uint16_t* src = a.x16p + (size_t)tok[h] * a.d + kc * 64;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) cp_async_16(dst + r * 128 + ((c ^ (r & 7)) << 4), src + c * 8);
+          }
+          cp_async_commit();
+          ++issued;
+          if (issued - arrived > 2) {
+            cp_async_wait<2>();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(XF(arrived % C::S_X));
+            ++arrived;
+          }
+        }
+      }
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      __syncwarp();
+      while (arrived < issued) {
+        if (lane == 0) mbar_arrive(XF(arrived % C::S_X));
+        ++arrived;
+      }
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ dequant: one weight row per thread
+    const int i = threadIdx.x - 128;
+    const uint32_t swz = (uint32_t)(i & 7);
+    int s = 0, sw = 0;
+    uint32_t ph = 0, phw = 0;
+    bool ok = true;
+    bool bad = false;
+    const int G = K / 64;
+    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      const int4 tl = tiles[u / MT];
+      const int m = u % MT;
+      const int which = tl.x == a.E ? 1 : 0;
+      const int ec = which ? 0 : tl.x;
+      const size_t row = (size_t)ec * R + (size_t)m * kBM + i;
+      const uint16_t* srow[NMAT];
+      const uint16_t* brow[NMAT];
+#pragma unroll
+      for (int mat = 0; mat < NMAT; ++mat) {
+        srow[mat] = a.mat[mat][which].scales + row * G;
+        brow[mat] = a.mat[mat][which].biases + row * G;
+      }
+      uint4 ns[NMAT], nb[NMAT];
+#pragma unroll
+      for (int mat = 0; mat < NMAT; ++mat) {
+        ns[mat] = load_group_block(srow[mat], 0, G);
+        nb[mat] = load_group_block(brow[mat], 0, G);
+      }
+      for (int kb = 0; kb < KC && ok; kb += 8) {
+        uint4 cs[NMAT], cb[NMAT];
+#pragma unroll
+        for (int mat = 0; mat < NMAT; ++mat) {
+          cs[mat] = ns[mat];
+          cb[mat] = nb[mat];
+          if (kb + 8 < KC) {
+            ns[mat] = load_group_block(srow[mat], kb + 8, G);
+            nb[mat] = load_group_block(brow[mat], kb + 8, G);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (kb + j >= KC) break;
+          __half2 s2[NMAT], b2[NMAT];
+#pragma unroll
+          for (int mat = 0; mat < NMAT; ++mat) {
+            const float sf = bf16_bits_to_f32(j == 0 ? pick_bf16<0>(cs[mat]) : j == 1 ? pick_bf16<1>(cs[mat])
+                                              : j == 2 ? pick_bf16<2>(cs[mat]) : j == 3 ? pick_bf16<3>(cs[mat])
+                                              : j == 4 ? pick_bf16<4>(cs[mat]) : j == 5 ? pick_bf16<5>(cs[mat])
+                                              : j == 6 ? pick_bf16<6>(cs[mat]) : pick_bf16<7>(cs[mat]));
+            const float bf = bf16_bits_to_f32(j == 0 ? pick_bf16<0>(cb[mat]) : j == 1 ? pick_bf16<1>(cb[mat])
+                                              : j == 2 ? pick_bf16<2>(cb[mat]) : j == 3 ? pick_bf16<3>(cb[mat])
+                                              : j == 4 ? pick_bf16<4>(cb[mat]) : j == 5 ? pick_bf16<5>(cb[mat])
+                                              : j == 6 ? pick_bf16<6>(cb[mat]) : pick_bf16<7>(cb[mat]));
+            bad = bad || !(fmaf(15.0f, fabsf(sf), fabsf(bf)) <= 65504.0f);
+            s2[mat] = __float2half2_rn(sf);
+            b2[mat] = __float2half2_rn(bf);
+          }
+          if (!mbar_wait(RF(s), ph, abort_s, a.err)) { ok = false; break; }
+          uint4 c0[NMAT], c1[NMAT];
+#pragma unroll
+          for (int mat = 0; mat < NMAT; ++mat) {
+            const uint32_t src = sRaw + (s * NMAT + mat) * kRawBytes + i * 32;
+            c0[mat] = ld_shared_v4(src);
+            c1[mat] = ld_shared_v4(src + 16);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(RE(s));
+          if (++s == C::S_RAW) { s = 0; ph ^= 1u; }
+          if (!mbar_wait(WE(sw), phw ^ 1u, abort_s, a.err)) { ok = false; break; }
+#pragma unroll
+          for (int mat = 0; mat < NMAT; ++mat) {
+            const uint32_t dst = sW + (sw * NMAT + mat) * kTileBytes + i * 128;
+            const uint32_t words[8] = {c0[mat].x, c0[mat].y, c0[mat].z, c0[mat].w,
+                                       c1[mat].x, c1[mat].y, c1[mat].z, c1[mat].w};
+#pragma unroll
+            for (int wd = 0; wd < 8; ++wd) {
+              uint32_t o[4];
+              dequant_word(words[wd], s2[mat], b2[mat], o);
+              st_shared_v4(dst + ((((uint32_t)wd) ^ swz) << 4), o[0], o[1], o[2], o[3]);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(WF(sw));
+          if (++sw == C::S_W) { sw = 0; phw ^= 1u; }
+        }
+      }
+    }
+    if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) raise_flag(a.err, kErrFp16Range);
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;   // TMEM lane quarter this warp may access
+    int li = 0;
+    bool bad = false;
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++li) {
+      const int4 tl = tiles[u / MT];
+      const int m = u % MT;
+      const int b = li & 1;
+      if (!mbar_wait(AF(b), (li >> 1) & 1, abort_s, a.err)) break;
+      tc_fence_after();
+      const int rowg = m * kBM + q * 32 + lane;
+      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::ACC_COLS);
+      for (int n0 = 0; n0 < tl.z; n0 += 16) {
+        uint32_t g[16];
+        tmem_ld16(tb + n0, g);
+        if (MODE == 0) {
+          uint32_t uu[16];
+          tmem_ld16(tb + 128 + n0, uu);
+          tmem_ld_wait();
+          const int col = (rowg & ~7) | chunk_pos(rowg & 7);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int n = n0 + i;
+            if (n < tl.z) {
+              const float gv = __uint_as_float(g[i]);
+              const float hv = gv / (1.0f + __expf(-gv)) * __uint_as_float(uu[i]);
+              const __half hh = __float2half_rn(hv);
+              bad = bad || (__hisinf(hh) != 0);
+              reinterpret_cast<__half*>(a.h)[(size_t)(tl.y + n) * a.F + col] = hh;
+            }
+          }
+        } else {
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int n = n0 + i;
+            if (n < tl.z) a.y_perm[(size_t)(tl.y + n) * a.d + rowg] = __uint_as_float(g[i]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(AE(b));
+    }
+    if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) raise_flag(a.err, kErrFp16Range);
+  }
+
+  // Wind down.  After a timeout, give copies that may still be in flight time to land before
+  // the CTA's shared memory and tensor memory are released.
+  if (threadIdx.x == 0 && *abort_s) {
+    const long long t0 = clock64();
+    while (clock64() - t0 < 4000000ll) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+__global__ void combine_kernel(CombineArgs a) {
+  const int t = blockIdx.x;
+  const int d4 = a.d / 4;
+  const float4* yp = reinterpret_cast<const float4*>(a.y_perm);
+  float4* y = reinterpret_cast<float4*>(a.y);
+  for (int c = threadIdx.x; c < d4; c += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < a.k; ++j) {
+      const int p = __ldg(a.inv + (size_t)t * a.k + j);
+      const float wv = __ldg(a.w + (size_t)t * a.k + j);
+      const float4 v = __ldg(yp + (size_t)p * d4 + c);
+      acc.x = fmaf(wv, v.x, acc.x);
+      acc.y = fmaf(wv, v.y, acc.y);
+      acc.z = fmaf(wv, v.z, acc.z);
+      acc.w = fmaf(wv, v.w, acc.w);
+    }
+    if (a.gs != nullptr) {
+      const float gv = __ldg(a.gs + t);
+      const float4 v = __ldg(yp + ((size_t)a.T * a.k + t) * d4 + c);
+      acc.x = fmaf(gv, v.x, acc.x);
+      acc.y = fmaf(gv, v.y, acc.y);
+      acc.z = fmaf(gv, v.z, acc.z);
+      acc.w = fmaf(gv, v.w, acc.w);
+    }
+    y[(size_t)t * d4 + c] = acc;
+  }
+}
+
+__global__ void convert_kernel(ConvertArgs a) {
+  const size_t nch = (size_t)a.T * a.d / 8;
+  bool bad = false;
+  for (size_t ch = (size_t)blockIdx.x * blockDim.x + threadIdx.x; ch < nch; ch += (size_t)gridDim.x * blockDim.x) {
+    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.x) + ch);
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+    float xf[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      xf[2 * i] = bf16_bits_to_f32(xw[i] & 0xFFFFu);
+      xf[2 * i + 1] = bf16_bits_to_f32(xw[i] >> 16);
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const __half lo = __float2half_rn(xf[p]);
+      const __half hi = __float2half_rn(xf[p + 4]);
+      bad = bad || (__hisinf(lo) != 0) || (__hisinf(hi) != 0);
+      o[p] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+    }
+    reinterpret_cast<uint4*>(a.x16p)[ch] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (bad) raise_flag(a.err, kErrFp16Range);
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes(int mode) { return mode == 0 ? Cfg<0>::BYTES : Cfg<1>::BYTES; }
+
+cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmArgs& a, int grid, cudaStream_t st) {
+  static thread_local int configured_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_dev != dev) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Cfg<0>::BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<1>::BYTES);
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+  }
+  if (mode == 0) gemm_kernel<0><<<grid, kThreads, Cfg<0>::BYTES, st>>>(maps, a);
+  else gemm_kernel<1><<<grid, kThreads, Cfg<1>::BYTES, st>>>(maps, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
+  combine_kernel<<<a.T, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_convert(const ConvertArgs& a, cudaStream_t st) {
+  const size_t nch = (size_t)a.T * a.d / 8;
+  const int blocks = (int)((nch + 255) / 256 < 4096 ? (nch + 255) / 256 : 4096);
+  convert_kernel<<<blocks, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

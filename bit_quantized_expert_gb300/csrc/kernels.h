@@ -1,0 +1,94 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.  Plain structs of
+// device pointers and sizes; no allocation happens behind any of these functions.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+// ---------------------------------------------------------------- routing (route.cu)
+struct RouteArgs {
+  const float* logits;   // [T, E]
+  int T, E, k, d;
+  int32_t* idx;          // [T, k]
+  float* w;              // [T, k]
+  const uint16_t* x;     // bf16 [T, d] or null (no fp16 copy / gate)
+  const uint16_t* w_sg;  // bf16 [d] or null
+  uint16_t* x16p;        // fp16 [T, d] in operand chunk order, or null
+  float* gs;             // [T] shared gate, or null
+  uint32_t* err;
+};
+cudaError_t launch_topk(const RouteArgs& a, cudaStream_t st);
+
+struct TablesArgs {
+  const int32_t* idx;
+  int T, E, k, tile_n, has_shared;
+  int32_t *counts, *offsets, *perm, *inv, *tiles, *num_tiles;
+  uint32_t* err;
+};
+size_t tables_smem_bytes(int E);
+cudaError_t launch_tables(const TablesArgs& a, cudaStream_t st);
+
+// ---------------------------------------------------------------- grouped GEMM (gemm.cu)
+struct QPtr {
+  const uint32_t* codes;
+  const uint16_t* scales;
+  const uint16_t* biases;
+};
+
+// Tensor maps of one launch: packed codes of each operand matrix for the routed and the
+// shared expert set, and (down projection) the h operand.
+struct GemmMaps {
+  CUtensorMap codes[2][2];   // [matrix][0 = routed, 1 = shared]
+  CUtensorMap h;             // down projection: h [slots, F] fp16
+};
+
+struct GemmArgs {
+  const int32_t* tiles;      // block map rows (e, row0, rows, 0)
+  const int32_t* num_tiles;
+  const int32_t* perm;       // slot -> assignment (gate/up gathers x rows)
+  const uint16_t* x16p;      // fp16 [T, d] operand copy of x (gate/up)
+  QPtr mat[2][2];            // [matrix][routed/shared]: scales and biases read by the dequant warps
+  int T, k, E, d, F;
+  uint16_t* h;               // gate/up output: fp16 [slots, F], operand chunk order
+  float* y_perm;             // down output: fp32 [slots, d]
+  uint32_t* err;
+};
+size_t gemm_smem_bytes(int mode);
+cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmArgs& a, int grid, cudaStream_t st);
+
+struct CombineArgs {
+  const float* y_perm;    // [T*k + T, d]
+  const int32_t* inv;     // [T*k]
+  const float* w;         // [T, k]
+  const float* gs;        // [T] or null (no shared expert)
+  int T, k, d;
+  float* y;               // [T, d]
+};
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
+
+struct ConvertArgs {
+  const uint16_t* x;      // bf16 [T, d]
+  uint16_t* x16p;         // fp16 [T, d] operand chunk order
+  int T, d;
+  uint32_t* err;
+};
+cudaError_t launch_convert(const ConvertArgs& a, cudaStream_t st);
+
+// ---------------------------------------------------------------- decode T = 1 (decode.cu)
+struct DecodeArgs {
+  const uint16_t* x;       // bf16 [d]
+  const float* logits;     // [E]
+  QPtr gate[2], up[2], down[2];   // [0] routed (stacked over E), [1] shared (may be null)
+  const uint16_t* w_sg;    // bf16 [d] or null
+  int d, E, k, F, has_shared;
+  float* h;                // workspace: fp32 [(k+1), F]
+  float* y;                // fp32 [d]
+  uint32_t* err;
+};
+bool decode_supported(int d, int E, int k, int F);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st, bool pdl);
+
+}  // namespace moe

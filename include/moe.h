@@ -1,0 +1,153 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) mixture-of-experts layer with 4-bit affine experts.
+ *
+ * What the layer computes (sources: four news pages about Perplexity's "Lily" engine):
+ *   - Weights are 4-bit affine codes in groups of 64 with one bf16 scale and one bf16 bias per
+ *     group, w = q * scale + bias; the GPU rebuilds them tile by tile inside the grouped GEMM and
+ *     accumulates in FP32, so the expanded weights never reach memory.  ("Perplexity libera
+ *     Lily: inferencia en Rust y Metal para Mac", section "Prefill: pesos comprimidos y
+ *     enrutamiento en la GPU".)
+ *   - A router scores 256 experts and keeps eight; a shared expert sees every token.  (Same
+ *     page, section "Tres formas de carga en un mismo modelo"; "Perplexity ouvre le code de
+ *     Lily...", article body.)
+ *   - The routing histogram, prefix scan, scatter and block map stay on the GPU with no host
+ *     synchronisation inside the layer.  (Same page and section as the weight format.)
+ *   - At batch 1 the layer is bound by weight bandwidth.  (Same page, section "Decode: mover
+ *     menos bytes por token".)
+ * Readings where the pages are silent: top-k in descending logit order, ties to the lower
+ * expert index; routing weights are the softmax of the k selected logits; SwiGLU experts
+ * h = silu(x Wg^T) * (x Wu^T), y = h Wd^T; shared-expert gate sigmoid(x . w_sg); eight codes
+ * per uint32 with the lowest nibble holding the lowest column.
+ *
+ * Conventions for every call:
+ *   - All array pointers are DEVICE pointers owned by the caller, 16-byte aligned.  The library
+ *     allocates no memory and keeps no per-call state; scratch lives in the caller's workspace.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *     No call synchronises with the host except moe_read_error_flags.
+ *   - Inputs are never written.  Calls are reentrant; two calls may run concurrently only with
+ *     distinct workspaces and outputs.
+ *   - Errors are returned, never thrown.  Argument checks happen on the host before any launch.
+ *     Conditions only the GPU can see (a bounded wait that timed out, a value outside the fp16
+ *     operand range) set bits in the workspace's error word; read them with
+ *     moe_read_error_flags.  Outputs are then invalid.
+ *   - T == 0 is a no-op that returns MOE_OK.
+ *
+ * Dimension limits: 1 <= k <= 32, k <= E <= 1024, d and F multiples of 128, F_shared == 0 (no
+ * shared expert) or F_shared == F, T * (k + 1) < 2^31.
+ */
+#ifndef MOE_GB300_H_
+#define MOE_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* null pointer, k > E, T < 0, tile_n outside 16..128 or not a multiple of 16 */
+  MOE_ERR_UNSUPPORTED = 2, /* dims outside the limits above */
+  MOE_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
+  MOE_ERR_WORKSPACE = 4,   /* workspace null or smaller than moe_workspace_bytes() */
+  MOE_ERR_CUDA = 5         /* a CUDA runtime call or kernel launch failed */
+} moe_status;
+
+/* Layer dimensions.  T tokens, hidden size d, E routed experts, top-k, expert FFN width F,
+ * shared-expert FFN width F_shared (0 or F).  Quantisation group size is fixed at 64. */
+typedef struct moe_dims {
+  int32_t T, d, E, k, F, F_shared;
+} moe_dims;
+
+/* One 4-bit matrix of R output rows and C input columns (a "qmat"), stacked over a leading
+ * expert axis:
+ *   codes  uint32 [n, R, C/8]   column c of row r in bits 4*(c%8)..4*(c%8)+3 of word (r, c/8)
+ *   scales bf16   [n, R, C/64]  (stored as uint16 bit patterns)
+ *   biases bf16   [n, R, C/64]
+ *   w[r, c] = q * scales[r, c/64] + biases[r, c/64]. */
+typedef struct moe_qmat {
+  const uint32_t* codes;
+  const uint16_t* scales;
+  const uint16_t* biases;
+} moe_qmat;
+
+/* An expert set: gate [n, F, d], up [n, F, d], down [n, d, F].  n = E for the routed experts,
+ * n = 1 for the shared expert. */
+typedef struct moe_experts {
+  moe_qmat gate, up, down;
+} moe_experts;
+
+/* Routing tables (all device memory, caller-owned; assignment a = t*k + j routes token t to its
+ * j-th expert):
+ *   idx       int32 [T, k]   experts in descending logit order, ties to the lower index
+ *   w         fp32  [T, k]   softmax of the selected logits
+ *   counts    int32 [E]      assignments per expert (histogram)
+ *   offsets   int32 [E + 1]  exclusive prefix sum of counts; offsets[E] = T*k
+ *   perm      int32 [T*k]    assignment held by slot p; slots sorted by (expert, token)
+ *   inv       int32 [T*k]    slot of assignment a
+ *   tiles     int32 [moe_max_tiles(), 4]  block map rows (e, first slot, rows, 0): for each
+ *             expert with counts[e] > 0 in increasing e, ceil(counts[e]/tile_n) tiles of at
+ *             most tile_n consecutive slots; then the shared expert as group e = E over slots
+ *             T*k .. T*k+T-1 (token order), in tiles of at most tile_n
+ *   num_tiles int32 [1]      number of block-map rows written
+ *   tile_n    rows per tile (16..128, a multiple of 16)
+ * Every field is bit-exact given the same fp32 logits. */
+typedef struct moe_routing {
+  int32_t* idx;
+  float* w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* inv;
+  int32_t* tiles;
+  int32_t* num_tiles;
+  int32_t tile_n;
+} moe_routing;
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(moe_status s);
+
+/* Upper bound on the number of block-map rows for these dims: floor(T*k/tile_n) + min(E, T*k)
+ * + ceil(T/tile_n).  Returns 0 for invalid arguments. */
+size_t moe_max_tiles(const moe_dims* dims, int32_t tile_n);
+
+/* Workspace bytes needed by moe_route, moe_expert_forward and moe_layer_forward for these dims
+ * (one size serves all three).  Returns 0 for invalid dims.  The workspace needs no
+ * initialisation; its first 4 bytes are the error word, cleared by every call. */
+size_t moe_workspace_bytes(const moe_dims* dims);
+
+/* Routing: top-k, weights, histogram, exclusive scan, permutation and block map of fp32
+ * router logits [T, E].  Writes every field of *out (out->tile_n is an input). */
+moe_status moe_route(const moe_dims* dims, const float* logits, const moe_routing* out, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/* Expert outputs per slot: y_perm[p] = FFN_{e(p)}(x[token(p)]) for the T*k routed slots of
+ * `routing`, followed (when `shared` is non-NULL) by the shared expert's outputs for the T
+ * tokens in slots T*k .. T*k+T-1.  x bf16 [T, d]; y_perm fp32 [T*k + T, d] (or [T*k, d] without
+ * a shared expert).  GEMM operands are rounded to fp16 (dequantised weights, x, h), products
+ * accumulate in fp32. */
+moe_status moe_expert_forward(const moe_dims* dims, const uint16_t* x, const moe_routing* routing,
+                              const moe_experts* routed, const moe_experts* shared, float* y_perm,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* The whole layer: y[t] = sum_j w[t,j] FFN_{idx[t,j]}(x_t) + sigmoid(x_t . w_sg) FFN_shared(x_t).
+ * x bf16 [T, d]; logits fp32 [T, E]; w_shared_gate bf16 [d] (ignored when shared is NULL);
+ * y fp32 [T, d].  routing_out may be NULL; when given, its tables are filled as by moe_route.
+ * T == 1 runs the fused decode path (fp32 arithmetic on CUDA cores), T > 1 the grouped-GEMM
+ * path (fp16 tensor-core operands, fp32 accumulation). */
+moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const float* logits,
+                             const moe_experts* routed, const moe_experts* shared, const uint16_t* w_shared_gate,
+                             float* y, const moe_routing* routing_out, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* Synchronises `stream`, copies the workspace's error word to *flags and returns.  Bits:
+ * 1 = a bounded device wait timed out, 2 = a value left the fp16 operand range,
+ * 4 = routing tables inconsistent with the dims.  0 means the last call completed cleanly. */
+moe_status moe_read_error_flags(const void* workspace, size_t workspace_bytes, uint32_t* flags, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H_ */

@@ -136,7 +136,7 @@ def route_topk(logits, k: int):
     return idx, w
 
 
-def routing_tables(idx, E: int, tile_n: int) -> dict:
+def routing_tables(idx, E: int, tile_n: int, with_shared: bool = True) -> dict:
     """Histogram, exclusive scan, permutation and block map of the top-k assignments.
 
     Assignment a = t*k + j routes token t to expert idx[t, j].
@@ -145,8 +145,8 @@ def routing_tables(idx, E: int, tile_n: int) -> dict:
       perm[p]     assignment in slot p; slots sorted by (expert, token)     int32 [T*k]
       inv[a]      slot of assignment a (inv[perm[p]] = p)                   int32 [T*k]
       tiles       [num_tiles, 3] rows (e, first slot, rows): for each non-empty expert in
-                  increasing e, ceil(counts[e]/tile_n) tiles of at most tile_n slots; then the
-                  shared expert as group E over slots T*k .. T*k+T-1 in token order.
+                  increasing e, ceil(counts[e]/tile_n) tiles of at most tile_n slots; then, when
+                  the layer has a shared expert, group E over slots T*k .. T*k+T-1 in token order.
     """
     idx = np.asarray(idx, dtype=np.int64)
     T, k = idx.shape
@@ -164,8 +164,9 @@ def routing_tables(idx, E: int, tile_n: int) -> dict:
         c = int(counts[e])
         for i in range(0, c, tile_n):
             tiles.append((e, int(offsets[e]) + i, min(tile_n, c - i)))
-    for i in range(0, T, tile_n):
-        tiles.append((E, T * k + i, min(tile_n, T - i)))
+    if with_shared:
+        for i in range(0, T, tile_n):
+            tiles.append((E, T * k + i, min(tile_n, T - i)))
     return {
         "counts": counts.astype(np.int32),
         "offsets": offsets.astype(np.int32),
@@ -224,7 +225,7 @@ def moe_layer(x_bits, logits, layer: dict, k: int, tile_n: int = 128, operands=N
     routed = layer["routed"]
     E = routed["gate"]["codes"].shape[0]
     idx, w = route_topk(logits, k)
-    tab = routing_tables(idx, E, tile_n)
+    tab = routing_tables(idx, E, tile_n, with_shared=layer.get("shared") is not None)
     perm, inv, off = tab["perm"], tab["inv"], tab["offsets"]
     n_slots = T * k + (T if layer.get("shared") is not None else 0)
     Y = np.zeros((n_slots, d), dtype=np.float64)

@@ -1,0 +1,97 @@
+"""The C-ABI library: it loads, exports every symbol include/moe.h declares, and its host-side
+argument checks and size queries behave as documented.  No kernel runs here (no GPU needed):
+every call below returns from the host checks before any CUDA work is enqueued."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_quantized_expert_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "moe.h")) as f:
+        src = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\*\s]+?\b(moe_\w+)\s*\(", src, re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(moe.LIB_PATH):
+        from bit_quantized_expert_gb300 import build
+        build.build()
+    return moe.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared()
+    assert set(declared) == set(moe.EXPORTED)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in moe.STATUS.items():
+        assert lib.moe_status_string(code).decode().startswith(name)
+
+
+def test_workspace_and_tile_bounds(lib):
+    dm = moe.dims(4096, 2048, 256, 8, 512, 512)
+    ws = moe.workspace_bytes(dm)
+    T, k, d, F = 4096, 8, 2048, 512
+    slots = T * k + T
+    assert ws >= slots * F * 2 + slots * d * 4 + T * d * 2       # h, expert outputs, fp16 x
+    assert moe.max_tiles(dm, 128) == T * k // 128 + min(256, T * k) + T // 128
+    assert moe.max_tiles(dm, 16) == T * k // 16 + min(256, T * k) + T // 16
+    assert moe.max_tiles(dm, 17) == 0 and moe.max_tiles(dm, 256) == 0
+
+
+@pytest.mark.parametrize("bad", [
+    dict(T=-1), dict(k=0), dict(k=17, E=16), dict(d=200), dict(F=192), dict(F_shared=256),
+    dict(E=2000), dict(k=40, E=64)])
+def test_invalid_dims_rejected(lib, bad):
+    args = dict(T=4, d=256, E=16, k=2, F=128, F_shared=128)
+    args.update(bad)
+    assert lib.moe_workspace_bytes(ctypes.byref(moe.dims(**args))) == 0
+
+
+def test_route_host_checks(lib):
+    dm = moe.dims(4, 256, 16, 2, 128, 128)
+    ws_n = moe.workspace_bytes(dm)
+    good = moe.RoutingC(16, 16, 16, 16, 16, 16, 16, 16, 128)
+    # null logits
+    assert lib.moe_route(ctypes.byref(dm), None, ctypes.byref(good), 16, ws_n, None) == 1
+    # misaligned logits
+    assert lib.moe_route(ctypes.byref(dm), 20, ctypes.byref(good), 16, ws_n, None) == 3
+    # workspace too small / missing
+    assert lib.moe_route(ctypes.byref(dm), 16, ctypes.byref(good), 16, ws_n - 1, None) == 4
+    assert lib.moe_route(ctypes.byref(dm), 16, ctypes.byref(good), None, ws_n, None) == 4
+    # bad tile_n
+    bad = moe.RoutingC(16, 16, 16, 16, 16, 16, 16, 16, 24)
+    assert lib.moe_route(ctypes.byref(dm), 16, ctypes.byref(bad), 16, ws_n, None) == 1
+    # T == 0 is a no-op
+    dm0 = moe.dims(0, 256, 16, 2, 128, 128)
+    assert lib.moe_route(ctypes.byref(dm0), None, ctypes.byref(good), None, 0, None) == 0
+
+
+def test_layer_host_checks(lib):
+    dm = moe.dims(4, 256, 16, 2, 128, 128)
+    ws_n = moe.workspace_bytes(dm)
+    q = moe.QMat(16, 16, 16)
+    ex = moe.ExpertsC(q, q, q)
+    call = lambda **kw: lib.moe_layer_forward(
+        ctypes.byref(kw.get("dm", dm)), kw.get("x", 16), kw.get("lg", 16), ctypes.byref(kw.get("re", ex)),
+        kw.get("se", ctypes.byref(ex)), kw.get("wsg", 16), kw.get("y", 16), None, kw.get("ws", 16),
+        kw.get("wsn", ws_n), None)
+    assert call(x=None) == 1
+    assert call(y=8) == 3
+    assert call(wsg=None) == 1
+    assert call(re=moe.ExpertsC(moe.QMat(16, 16, 0), q, q)) == 1
+    assert call(re=moe.ExpertsC(moe.QMat(16, 24, 16), q, q)) == 3
+    assert call(se=None) == 1                  # dims say there is a shared expert
+    assert call(wsn=ws_n - 256) == 4
+    dm_ns = moe.dims(4, 256, 16, 2, 128, 0)
+    assert call(dm=dm_ns) == 1                 # a shared expert given but dims say none

@@ -1,0 +1,228 @@
+"""CUDA path vs the CPU oracle, through the C ABI, on seeded inputs of every workload shape.
+
+Bars (written here, derived in the design doc):
+  * routing tables (idx, counts, offsets, perm, inv, block map): bit-exact;
+  * routing weights: relative error <= 1e-6 (fp32 expf vs float64);
+  * layer outputs: max over tokens of ||y_t - r_t|| / ||r_t|| <= 2e-3 against the exact oracle,
+    and <= 2e-4 against the oracle with fp16 GEMM operands (the rounding the tensor-core path
+    applies), so accumulation-order error is all that remains;
+  * the decode (T = 1) path computes in fp32 throughout: <= 2e-5 against the exact oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bit_quantized_expert_gb300 as moe
+import synth
+from oracle import moe_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+EXACT_TOL = 2e-3
+EMUL_TOL = 2e-4
+DECODE_TOL = 2e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from bit_quantized_expert_gb300 import build
+    build.build()
+    moe.load_library()
+
+
+def rowwise_err(y, ref):
+    y = np.asarray(y, dtype=np.float64)
+    num = np.linalg.norm(y - ref, axis=1)
+    den = np.maximum(np.linalg.norm(ref, axis=1), 1e-30)
+    return float((num / den).max())
+
+
+def dev(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    elif a.dtype == np.uint32:
+        a = a.view(np.int32)
+    return torch.from_numpy(a).cuda()
+
+
+_LAYERS = {}
+
+
+def layer_for(wl):
+    if wl.name not in _LAYERS:
+        host = synth.make_layer(wl)
+        _LAYERS.clear()
+        _LAYERS[wl.name] = (host, moe.to_device_layer(host))
+    return _LAYERS[wl.name]
+
+
+def run_route(wl, logits, tile_n, T=None):
+    T = wl.T if T is None else T
+    dm = moe.dims(T, wl.d, wl.E, wl.k, wl.F, wl.F_shared)
+    r = moe.alloc_routing(dm, tile_n)
+    ws = moe.alloc_workspace(dm)
+    moe.route(dm, dev(logits), r, ws)
+    assert moe.read_error_flags(ws) == 0
+    return {k: (v.cpu().numpy() if torch.is_tensor(v) else v) for k, v in r.items()}
+
+
+def assert_routing_equal(got, logits, E, k, tile_n, with_shared=True):
+    idx, w = O.route_topk(logits, k)
+    tab = O.routing_tables(idx, E, tile_n, with_shared=with_shared)
+    assert np.array_equal(got["idx"], idx)
+    assert np.allclose(got["w"], w, rtol=1e-6, atol=1e-7, equal_nan=True)
+    for key in ("counts", "offsets", "perm", "inv"):
+        assert np.array_equal(got[key], tab[key]), key
+    nt = int(got["num_tiles"][0])
+    assert nt == tab["num_tiles"]
+    assert np.array_equal(got["tiles"][:nt, :3], tab["tiles"])
+
+
+# ------------------------------------------------------------------------------ routing
+
+@pytest.mark.parametrize("wl,tile_n", [(synth.TINY, 128), (synth.TINY, 16), (synth.DECODE, 128),
+                                       (synth.PREFILL, 128), (synth.PREFILL, 32), (synth.SKEWED, 128),
+                                       (synth.SKEWED, 16), (synth.STACK, 64)])
+def test_route_bit_exact(wl, tile_n):
+    inp = synth.make_inputs(wl)
+    got = run_route(wl, inp["logits"], tile_n)
+    assert_routing_equal(got, inp["logits"], wl.E, wl.k, tile_n)
+
+
+def test_route_ties_zero_signs_nan_and_ragged():
+    wl = synth.Workload("edge", T=37, d=256, E=40, k=5, F=128, F_shared=128)
+    rng = np.random.default_rng(9)
+    lg = rng.integers(-2, 3, size=(wl.T, wl.E)).astype(np.float32)     # heavy ties
+    lg[0] = 0.0
+    lg[1, :] = -0.0
+    lg[1, ::3] = 0.0
+    lg[2, 5] = np.nan
+    lg[2, 7] = -np.inf
+    lg[3, :] = np.nan
+    lg[3, 11] = 1.0
+    got = run_route(wl, lg, 16)
+    assert_routing_equal(got, lg, wl.E, wl.k, 16)
+    assert got["idx"][0].tolist() == [0, 1, 2, 3, 4]
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 16, 1), (5, 8, 8), (300, 1024, 32), (2049, 256, 8), (64, 33, 3)])
+def test_route_shapes(T, E, k):
+    wl = synth.Workload("shape", T=T, d=256, E=E, k=k, F=128, F_shared=128)
+    lg = synth.make_logits(np.random.default_rng(T + E + k), wl, T)
+    got = run_route(wl, lg, 32)
+    assert_routing_equal(got, lg, E, k, 32)
+
+
+# ------------------------------------------------------------------------------ layer
+
+def run_layer(wl, host, dl, inp, tile_n=None, T=None):
+    T = wl.T if T is None else T
+    dm = moe.dims(T, wl.d, wl.E, wl.k, wl.F, wl.F_shared)
+    ws = moe.alloc_workspace(dm)
+    y = torch.empty((T, wl.d), dtype=torch.float32, device="cuda")
+    routing = moe.alloc_routing(dm, tile_n) if tile_n else None
+    moe.layer_forward(dm, dev(inp["x"][:T]), dev(inp["logits"][:T]), dl["routed"], dl["shared"], dl["w_sg"], y,
+                      ws, routing=routing)
+    flags = moe.read_error_flags(ws)
+    assert flags == 0, flags
+    out = {"y": y.cpu().numpy()}
+    if routing:
+        out["routing"] = {k: (v.cpu().numpy() if torch.is_tensor(v) else v) for k, v in routing.items()}
+    return out
+
+
+def test_layer_tiny_exact_and_emulated():
+    wl = synth.TINY
+    host, dl = layer_for(wl)
+    inp = synth.make_inputs(wl)
+    got = run_layer(wl, host, dl, inp)["y"]
+    ref = O.moe_layer(inp["x"], inp["logits"], host, wl.k)["y"]
+    emu = O.moe_layer(inp["x"], inp["logits"], host, wl.k, operands="fp16")["y"]
+    assert rowwise_err(got, ref) <= EXACT_TOL
+    assert rowwise_err(got, emu) <= EMUL_TOL
+
+
+@pytest.mark.parametrize("tile_n", [16, 48, 128])
+def test_layer_tiny_tile_widths_and_routing_out(tile_n):
+    wl = synth.TINY
+    host, dl = layer_for(wl)
+    inp = synth.make_inputs(wl, seed=3)
+    out = run_layer(wl, host, dl, inp, tile_n=tile_n)
+    emu = O.moe_layer(inp["x"], inp["logits"], host, wl.k, tile_n=tile_n, operands="fp16")
+    assert rowwise_err(out["y"], emu["y"]) <= EMUL_TOL
+    assert_routing_equal(out["routing"], inp["logits"], wl.E, wl.k, tile_n)
+
+
+def test_expert_forward_tiny_slots():
+    wl = synth.TINY
+    host, dl = layer_for(wl)
+    inp = synth.make_inputs(wl, seed=5)
+    dm = moe.dims(wl.T, wl.d, wl.E, wl.k, wl.F, wl.F_shared)
+    ws = moe.alloc_workspace(dm)
+    r = moe.alloc_routing(dm, 128)
+    moe.route(dm, dev(inp["logits"]), r, ws)
+    yp = torch.empty((wl.T * wl.k + wl.T, wl.d), dtype=torch.float32, device="cuda")
+    moe.expert_forward(dm, dev(inp["x"]), r, dl["routed"], dl["shared"], yp, ws)
+    assert moe.read_error_flags(ws) == 0
+    emu = O.moe_layer(inp["x"], inp["logits"], host, wl.k, operands="fp16")
+    assert rowwise_err(yp.cpu().numpy(), emu["Y_perm"]) <= EMUL_TOL
+
+
+def test_layer_tiny_small_T_and_ragged():
+    wl = synth.TINY
+    host, dl = layer_for(wl)
+    inp = synth.make_inputs(wl, seed=11)
+    for T in (1, 2, 3, 15):
+        got = run_layer(wl, host, dl, inp, T=T)["y"]
+        ref = O.moe_layer(inp["x"][:T], inp["logits"][:T], host, wl.k)["y"]
+        tol = DECODE_TOL if T == 1 else EXACT_TOL
+        assert rowwise_err(got, ref) <= tol, T
+
+
+def test_layer_deterministic():
+    wl = synth.TINY
+    host, dl = layer_for(wl)
+    inp = synth.make_inputs(wl, seed=2)
+    a = run_layer(wl, host, dl, inp)["y"]
+    b = run_layer(wl, host, dl, inp)["y"]
+    assert np.array_equal(a, b)
+
+
+def test_decode_full_size():
+    wl = synth.DECODE
+    host, dl = layer_for(wl)
+    for seed in range(6):
+        inp = synth.make_inputs(wl, seed=seed)
+        got = run_layer(wl, host, dl, inp)["y"]
+        ref, _, _ = O.moe_token(inp["x"][0], inp["logits"][0], host, wl.k)
+        assert rowwise_err(got, ref[None, :]) <= DECODE_TOL, seed
+
+
+def test_decode_routing_out_matches_oracle():
+    wl = synth.DECODE
+    host, dl = layer_for(wl)
+    inp = synth.make_inputs(wl, seed=1)
+    out = run_layer(wl, host, dl, inp, tile_n=128)
+    assert_routing_equal(out["routing"], inp["logits"], wl.E, wl.k, 128)
+
+
+def test_prefill_full_size():
+    wl = synth.PREFILL
+    host, dl = layer_for(wl)
+    inp = synth.make_inputs(wl)
+    got = run_layer(wl, host, dl, inp)["y"]
+    ref = O.moe_layer(inp["x"], inp["logits"], host, wl.k)["y"]
+    assert rowwise_err(got, ref) <= EXACT_TOL
+    emu = O.moe_layer(inp["x"], inp["logits"], host, wl.k, operands="fp16")["y"]
+    assert rowwise_err(got, emu) <= EMUL_TOL
+
+
+def test_skewed_prefill_full_size():
+    wl = synth.SKEWED
+    host, dl = layer_for(wl)
+    inp = synth.make_inputs(wl)
+    out = run_layer(wl, host, dl, inp, tile_n=128)
+    assert_routing_equal(out["routing"], inp["logits"], wl.E, wl.k, 128)
+    ref = O.moe_layer(inp["x"], inp["logits"], host, wl.k)["y"]
+    assert rowwise_err(out["y"], ref) <= EXACT_TOL
