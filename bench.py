@@ -1,0 +1,436 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 4-bit MoE layer: MoE-layer tokens/s and fraction of roofline.
+
+Headline workload: decode, batch 1 (T = 1, d = 2048, E = 256, top-8, SwiGLU width 512, shared
+expert with sigmoid gate, 4-bit affine group-64 weights).  One step = one decode token through 40
+MoE layers, each with its own seeded weight set (40 x 455 MB = 18.2 GB resident in HBM, cycled, so
+no layer's experts are in L2 when it runs) and its own precomputed input row.  `value` counts
+MoE-layer tokens per second (40 per step per GPU).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-extras]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (independent replicas; the
+layer has no cross-GPU exchange) and rank 0 prints one JSON line with the whole-job rate.
+`--impl reference` times the CPU oracle (float64 numpy) on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (decode T=1, prefill T=512/4096); % of HBM/tensor roofline"
+LAYERS = 40
+NI = 64   # distinct input rows per layer for decode
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-extras", action="store_true", help="skip the prefill T=512 / T=4096 sub-measurements")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=50)
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------------------ algorithmic work
+
+def qmat_bytes(R, C):
+    return R * C // 2 + 2 * R * (C // 64) * 2
+
+
+def expert_bytes(wl):
+    return 2 * qmat_bytes(wl.F, wl.d) + qmat_bytes(wl.d, wl.F)
+
+
+def layer_bytes(wl, T, touched_experts):
+    """Weights of the experts the tokens actually use (+ shared) + x, logits, w_sg, y."""
+    w = (touched_experts + (1 if wl.F_shared else 0)) * expert_bytes(wl)
+    io = T * wl.d * 2 + T * wl.E * 4 + wl.d * 2 + T * wl.d * 4
+    return w + io
+
+
+def layer_flops(wl, T):
+    return 6 * wl.d * wl.F * (T * wl.k + (T if wl.F_shared else 0))
+
+
+# ------------------------------------------------------------------------------ clocks
+
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if self.proc is None:
+            return out
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for ln in f:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return out
+        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        out.update({"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                    "reasons": reasons, "samples": len(rows)})
+        return out
+
+
+# ------------------------------------------------------------------------------ distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(v, world, device):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------------ ours
+
+def make_layers(wl, device, n):
+    import bit_quantized_expert_gb300 as moe
+    layers = []
+    for l in range(n):
+        t = synth.torch_make_layer(wl, seed=l, device=device)
+        layers.append(moe.Layer(t["routed"], t["shared"], t["w_sg"], wl.d, wl.E, wl.k, wl.F))
+    return layers
+
+
+def capture(fn, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def timed_graph_steps(graph_of_g, g_steps, graph_of_1, steps, stream):
+    """Replay graphs so that exactly `steps` steps run; returns elapsed ms (CUDA events on `stream`)."""
+    import torch
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps, rest = divmod(steps, g_steps)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(reps):
+            graph_of_g.replay()
+        for _ in range(rest):
+            graph_of_1.replay()
+        end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end)
+
+
+def decode_bench(args, world, rank, local, device, pk):
+    import torch
+
+    import bit_quantized_expert_gb300 as moe
+    wl = synth.DECODE
+    layers = make_layers(wl, device, LAYERS)
+    ins = [synth.torch_make_inputs(wl, seed=1000 + l, device=device, T=NI) for l in range(LAYERS)]
+    y = torch.empty((LAYERS, NI, wl.d), dtype=torch.float32, device=device)
+    dm = layers[0].dims(1)
+    ws = moe.alloc_workspace(dm, device)
+    stream = torch.cuda.Stream(device=device)
+
+    def step(s):
+        i = s % NI
+        for l in range(LAYERS):
+            layers[l].forward(ins[l]["x"][i:i + 1], ins[l]["logits"][i:i + 1], y[l, i:i + 1], ws)
+
+    with torch.cuda.stream(stream):
+        for s in range(args.warmup):
+            step(s)
+    stream.synchronize()
+    G = 25
+    g_many = capture(lambda: [step(s) for s in range(G)], stream)
+    g_one = capture(lambda: step(0), stream)
+    with torch.cuda.stream(stream):
+        g_many.replay()
+    stream.synchronize()
+    if moe.read_error_flags(ws) != 0:
+        raise RuntimeError("device error flags set during warm-up")
+
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    clocks = Clocks(vis.split(",")[local] if vis else local)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks.start()
+    ms = timed_graph_steps(g_many, G, g_one, args.steps, stream)
+    ck = clocks.stop()
+    torch.cuda.synchronize()
+    barrier(world)
+    flags = moe.read_error_flags(ws)
+    ms_max = max_over_ranks(ms, world, device)
+
+    # Expert touches per layer call: k routed (distinct) + shared; algorithmic bytes of one call.
+    per_call = layer_bytes(wl, 1, wl.k)
+    per_step_bytes = LAYERS * per_call
+    step_s = ms_max / 1e3 / args.steps
+    tokens = LAYERS * args.steps * world
+    res = {
+        "value": tokens / (ms_max / 1e3), "ms_per_step": ms_max / args.steps, "clocks": ck, "flags": flags,
+        "roofline": {"kernel": "decode_gateup_kernel + decode_down_kernel (one MoE layer call, PDL-chained)",
+                     "bound": "hbm", "achieved": per_step_bytes / step_s / 1e9, "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": per_step_bytes / step_s / 1e9 / pk["hbm_gbs"], "traffic": None,
+                     "algorithmic_bytes_per_launch": per_call, "peak_source": pk["source"]},
+        "gpu_launches": 2 * LAYERS * args.steps,
+    }
+
+    # End to end through the C ABI with host buffers: per layer call, copy x and logits from pinned
+    # host memory, run the layer, copy y back to pinned host memory.
+    xh = [ins[l]["x"].cpu().pin_memory() for l in range(LAYERS)]
+    lh = [ins[l]["logits"].cpu().pin_memory() for l in range(LAYERS)]
+    yh = torch.empty((LAYERS, NI, wl.d), dtype=torch.float32).pin_memory()
+    xd = torch.empty((1, wl.d), dtype=torch.int16, device=device)
+    ld = torch.empty((1, wl.E), dtype=torch.float32, device=device)
+    yd = torch.empty((1, wl.d), dtype=torch.float32, device=device)
+
+    def e2e_step(s):
+        i = s % NI
+        for l in range(LAYERS):
+            xd.copy_(xh[l][i:i + 1], non_blocking=True)
+            ld.copy_(lh[l][i:i + 1], non_blocking=True)
+            layers[l].forward(xd, ld, yd, ws)
+            yh[l, i:i + 1].copy_(yd, non_blocking=True)
+
+    n_e2e = max(1, min(args.steps, args.e2e_steps))
+    with torch.cuda.stream(stream):
+        for s in range(2):
+            e2e_step(s)
+        stream.synchronize()
+        barrier(world)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for s in range(n_e2e):
+            e2e_step(s)
+        t1.record(stream)
+    t1.synchronize()
+    e2e_ms = max_over_ranks(t0.elapsed_time(t1), world, device)
+    res["e2e"] = {"value": LAYERS * n_e2e * world / (e2e_ms / 1e3), "unit": "tokens/s",
+                  "h2d_bytes_per_step": LAYERS * (wl.d * 2 + wl.E * 4), "d2h_bytes_per_step": LAYERS * wl.d * 4,
+                  "steps": n_e2e, "launch": "eager per call (2 H2D copies, 2 kernels, 1 D2H copy per layer)"}
+    del layers
+    torch.cuda.empty_cache()
+    return res
+
+
+def prefill_bench(wl, steps, device, pk):
+    """One step = one layer call over T tokens; 40 weight sets cycled; CUDA-graph replay."""
+    import torch
+
+    import bit_quantized_expert_gb300 as moe
+    n_sets = 8 if wl.T >= 4096 else 16
+    layers = make_layers(wl, device, n_sets)
+    ins = [synth.torch_make_inputs(wl, seed=1000 + l, device=device) for l in range(n_sets)]
+    y = torch.empty((wl.T, wl.d), dtype=torch.float32, device=device)
+    dm = layers[0].dims(wl.T)
+    ws = moe.alloc_workspace(dm, device)
+    routing = moe.alloc_routing(dm, 128, device)
+    stream = torch.cuda.Stream(device=device)
+
+    def step(s):
+        l = s % n_sets
+        layers[l].forward(ins[l]["x"], ins[l]["logits"], y, ws)
+
+    with torch.cuda.stream(stream):
+        for s in range(3):
+            step(s)
+    stream.synchronize()
+    g_many = capture(lambda: [step(s) for s in range(n_sets)], stream)
+    g_one = capture(lambda: step(0), stream)
+    with torch.cuda.stream(stream):
+        g_many.replay()
+    stream.synchronize()
+    steps = max(n_sets, steps // n_sets * n_sets)
+    ms = timed_graph_steps(g_many, n_sets, g_one, steps, stream)
+    flags = moe.read_error_flags(ws)
+    # touched experts per weight set (from the routing of that set's inputs)
+    touched = []
+    for l in range(n_sets):
+        with torch.cuda.stream(stream):
+            layers[l].forward(ins[l]["x"], ins[l]["logits"], y, ws, routing=routing)
+        stream.synchronize()
+        touched.append(int((routing["counts"] > 0).sum().item()))
+    step_s = ms / 1e3 / steps
+    bytes_avg = sum(layer_bytes(wl, wl.T, t) for t in touched) / n_sets
+    flops = layer_flops(wl, wl.T)
+    out = {"workload": wl.name, "value": wl.T / step_s, "unit": "tokens/s", "ms_per_step": ms / steps,
+           "steps": steps, "weight_sets": n_sets, "flags": flags,
+           "hbm": {"achieved": bytes_avg / step_s / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                   "frac": bytes_avg / step_s / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": bytes_avg},
+           "tensor": {"achieved": flops / step_s / 1e12, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                      "frac": flops / step_s / 1e12 / pk["bf16_tflops"], "algorithmic_flops": flops,
+                      "note": "fp16 operands; peak is the measured bf16 dense rate (same nominal rate)"},
+           "gpu_launches_per_step": 5}
+    del layers
+    torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+
+def oracle_rate(budget_s: float, max_tokens: int | None = None):
+    """The float64 oracle on decode tokens of one layer (its cost does not depend on the weights)."""
+    from oracle import moe_oracle as O
+    wl = synth.DECODE
+    host = synth.make_layer(wl, seed=0)
+    inp = synth.make_inputs(wl, T=NI)
+    O.moe_token(inp["x"][0], inp["logits"][0], host, wl.k)   # warm
+    n, t0 = 0, time.perf_counter()
+    while True:
+        i = n % NI
+        O.moe_token(inp["x"][i], inp["logits"][i], host, wl.k)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_tokens is not None and n >= max_tokens):
+            break
+    return n, el
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def config(world):
+    return {"workload": synth.DECODE.name, "layers_per_step": LAYERS, "weight_sets": LAYERS,
+            "global_batch": 1 * world, "seq_len": 1,
+            "l2": "not flushed; inputs larger than L2 (40 weight sets, 18.2 GB, cycled per step)",
+            "parallelism": f"replicas{world}" if world > 1 else "single GPU"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    budget = 60.0
+    n, el = oracle_rate(budget, max_tokens=LAYERS * max(1, args.steps))
+    steps = max(1, n // LAYERS)
+    value = n / el
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / max(1, n) * LAYERS,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config(1),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+                             "sample": f"{n} decode layer-tokens (one layer's weights) in {el:.1f} s; "
+                                       f"bounded to {budget:.0f} s"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    world, rank, local = dist_setup()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    import bit_quantized_expert_gb300 as moe
+    moe.load_library()
+    pk = peaks()
+
+    res = decode_bench(args, world, rank, local, device, pk)
+    extras = []
+    if not args.no_extras and rank == 0:
+        extras.append(prefill_bench(synth.PREFILL, 48, device, pk))
+        extras.append(prefill_bench(synth.SKEWED, 24, device, pk))
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n, el = oracle_rate(20.0)
+        cpu = {"value": n / el, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+               "sample": f"{n} decode layer-tokens through one layer in {el:.1f} s (float64 numpy oracle)"}
+    if rank == 0:
+        line = {"metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; random weights)",
+                "config": config(world), "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": res["e2e"],
+                "gpu_launches": res["gpu_launches"], "clocks": res["clocks"], "error_flags": res["flags"],
+                "prefill": extras}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

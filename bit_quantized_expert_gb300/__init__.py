@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(PKG_DIR, "libmoe_gb300.so")
 
 # Symbols declared in include/moe.h.
 EXPORTED = ("moe_status_string", "moe_max_tiles", "moe_workspace_bytes", "moe_route",
-            "moe_expert_forward", "moe_layer_forward", "moe_read_error_flags")
+            "moe_expert_forward", "moe_layer_forward", "moe_clear_error_flags", "moe_read_error_flags")
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_MISALIGNED",
           4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA"}
@@ -77,6 +77,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_expert_forward.argtypes = [P(Dims), VP, P(RoutingC), P(ExpertsC), P(ExpertsC), VP, VP, S, VP]
     lib.moe_layer_forward.restype = ctypes.c_int
     lib.moe_layer_forward.argtypes = [P(Dims), VP, VP, P(ExpertsC), P(ExpertsC), VP, VP, P(RoutingC), VP, S, VP]
+    lib.moe_clear_error_flags.restype = ctypes.c_int
+    lib.moe_clear_error_flags.argtypes = [VP, S, VP]
     lib.moe_read_error_flags.restype = ctypes.c_int
     lib.moe_read_error_flags.argtypes = [VP, S, P(ctypes.c_uint32), VP]
     _lib = lib
@@ -136,8 +138,16 @@ def workspace_bytes(dm: Dims) -> int:
 
 
 def alloc_workspace(dm: Dims, device="cuda"):
+    """Workspace for these dims with its error word cleared."""
     import torch
-    return torch.empty(workspace_bytes(dm), dtype=torch.uint8, device=device)
+    ws = torch.empty(workspace_bytes(dm), dtype=torch.uint8, device=device)
+    ws[:256].zero_()
+    return ws
+
+
+def clear_error_flags(workspace, stream=None):
+    _check(load_library().moe_clear_error_flags(_ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_clear_error_flags")
 
 
 def alloc_routing(dm: Dims, tile_n: int = 128, device="cuda") -> dict:
@@ -178,6 +188,7 @@ def layer_forward(dm: Dims, x, logits, routed: dict, shared: dict | None, w_sg, 
 
 
 def read_error_flags(workspace, stream=None) -> int:
+    """Synchronise, return the sticky error word and clear it."""
     out = ctypes.c_uint32(0)
     _check(load_library().moe_read_error_flags(_ptr(workspace), workspace.numel(), ctypes.byref(out),
                                                _stream(stream)), "moe_read_error_flags")

@@ -283,7 +283,6 @@ moe_status moe_route(const moe_dims* dims, const float* logits, const moe_routin
   if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* err = at<uint32_t>(workspace, L.err);
-  if (cudaMemsetAsync(err, 0, 4, st) != cudaSuccess) return MOE_ERR_CUDA;
   return cuda_status(run_routing(*dims, logits, caller_routing(out), nullptr, nullptr, nullptr, nullptr, err, st));
 }
 
@@ -305,7 +304,6 @@ moe_status moe_expert_forward(const moe_dims* dims, const uint16_t* x, const moe
   if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* err = at<uint32_t>(workspace, L.err);
-  if (cudaMemsetAsync(err, 0, 4, st) != cudaSuccess) return MOE_ERR_CUDA;
   uint16_t* x16p = at<uint16_t>(workspace, L.x16p);
   ConvertArgs ca{x, x16p, dims->T, dims->d, err};
   if (launch_convert(ca, st) != cudaSuccess) return MOE_ERR_CUDA;
@@ -334,7 +332,6 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* err = at<uint32_t>(workspace, L.err);
-  if (cudaMemsetAsync(err, 0, 4, st) != cudaSuccess) return MOE_ERR_CUDA;
   const bool sh = shared != nullptr;
   const moe_dims& d = *dims;
 
@@ -377,12 +374,19 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
   return cuda_status(launch_combine(cb, st));
 }
 
-moe_status moe_read_error_flags(const void* workspace, size_t workspace_bytes, uint32_t* flags, void* stream) {
+moe_status moe_clear_error_flags(void* workspace, size_t workspace_bytes, void* stream) {
+  if (workspace == nullptr) return MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < 4) return MOE_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(workspace, 0, 4, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_read_error_flags(void* workspace, size_t workspace_bytes, uint32_t* flags, void* stream) {
   if (workspace == nullptr || flags == nullptr) return MOE_ERR_INVALID_ARG;
   if (workspace_bytes < 4) return MOE_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemcpy(flags, workspace, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(workspace, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 

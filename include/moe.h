@@ -113,8 +113,9 @@ const char* moe_status_string(moe_status s);
 size_t moe_max_tiles(const moe_dims* dims, int32_t tile_n);
 
 /* Workspace bytes needed by moe_route, moe_expert_forward and moe_layer_forward for these dims
- * (one size serves all three).  Returns 0 for invalid dims.  The workspace needs no
- * initialisation; its first 4 bytes are the error word, cleared by every call. */
+ * (one size serves all three).  Returns 0 for invalid dims.  The first 4 bytes of the workspace are
+ * its error word: kernels only ever set bits in it, so it is sticky across calls.  Clear it once
+ * after allocating the workspace (moe_clear_error_flags); the rest needs no initialisation. */
 size_t moe_workspace_bytes(const moe_dims* dims);
 
 /* Routing: top-k, weights, histogram, exclusive scan, permutation and block map of fp32
@@ -141,10 +142,14 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
                              float* y, const moe_routing* routing_out, void* workspace, size_t workspace_bytes,
                              void* stream);
 
-/* Synchronises `stream`, copies the workspace's error word to *flags and returns.  Bits:
+/* Enqueues the clearing of the workspace's error word on `stream` (no host synchronisation). */
+moe_status moe_clear_error_flags(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, copies the workspace's error word to *flags, then clears it.  Bits:
  * 1 = a bounded device wait timed out, 2 = a value left the fp16 operand range,
- * 4 = routing tables inconsistent with the dims.  0 means the last call completed cleanly. */
-moe_status moe_read_error_flags(const void* workspace, size_t workspace_bytes, uint32_t* flags, void* stream);
+ * 4 = routing tables inconsistent with the dims.  0 means every call since the last clear
+ * completed cleanly. */
+moe_status moe_read_error_flags(void* workspace, size_t workspace_bytes, uint32_t* flags, void* stream);
 
 #ifdef __cplusplus
 }
