@@ -17,7 +17,8 @@ LIB_PATH = os.path.join(PKG_DIR, "libmoe_gb300.so")
 
 # Symbols declared in include/moe.h.
 EXPORTED = ("moe_status_string", "moe_max_tiles", "moe_workspace_bytes", "moe_route",
-            "moe_expert_forward", "moe_layer_forward", "moe_clear_error_flags", "moe_read_error_flags")
+            "moe_expert_forward", "moe_layer_forward", "moe_rmsnorm_router", "moe_clear_error_flags",
+            "moe_read_error_flags")
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_MISALIGNED",
           4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA"}
@@ -77,6 +78,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_expert_forward.argtypes = [P(Dims), VP, P(RoutingC), P(ExpertsC), P(ExpertsC), VP, VP, S, VP]
     lib.moe_layer_forward.restype = ctypes.c_int
     lib.moe_layer_forward.argtypes = [P(Dims), VP, VP, P(ExpertsC), P(ExpertsC), VP, VP, P(RoutingC), VP, S, VP]
+    lib.moe_rmsnorm_router.restype = ctypes.c_int
+    lib.moe_rmsnorm_router.argtypes = [P(Dims), VP, VP, VP, VP, ctypes.c_float, VP, VP, VP, S, VP]
     lib.moe_clear_error_flags.restype = ctypes.c_int
     lib.moe_clear_error_flags.argtypes = [VP, S, VP]
     lib.moe_read_error_flags.restype = ctypes.c_int
@@ -185,6 +188,14 @@ def layer_forward(dm: Dims, x, logits, routed: dict, shared: dict | None, w_sg, 
                                             ctypes.byref(se) if se is not None else None, _ptr(w_sg), _ptr(y),
                                             ctypes.byref(r) if r is not None else None, _ptr(workspace),
                                             workspace.numel(), _stream(stream)), "moe_layer_forward")
+
+
+def rmsnorm_router(dm: Dims, x_resid, y_prev, gamma, w_router, eps: float, h_out, logits_out, workspace,
+                   stream=None):
+    _check(load_library().moe_rmsnorm_router(ctypes.byref(dm), _ptr(x_resid), _ptr(y_prev), _ptr(gamma),
+                                             _ptr(w_router), float(eps), _ptr(h_out), _ptr(logits_out),
+                                             _ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_rmsnorm_router")
 
 
 def read_error_flags(workspace, stream=None) -> int:

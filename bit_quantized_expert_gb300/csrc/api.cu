@@ -144,6 +144,19 @@ bool encode_h(CUtensorMap* m, const uint16_t* h, long long slots, int F) {
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row-major bf16 matrix [rows, cols] with a 64 x 128 box in the 128-byte swizzle.
+bool encode_bf16_rows(CUtensorMap* m, const uint16_t* p, long long rows, int cols) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t es[2] = {1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(p), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
   static int counts[64] = {0};
   int dev = 0;
@@ -372,6 +385,29 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
   if (s != MOE_OK) return s;
   CombineArgs cb{yperm, R.inv, R.w, gs, d.T, d.k, d.d, y};
   return cuda_status(launch_combine(cb, st));
+}
+
+moe_status moe_rmsnorm_router(const moe_dims* dims, float* x_resid, const float* y_prev, const uint16_t* gamma,
+                              const uint16_t* w_router, float eps, uint16_t* h_out, float* logits_out,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  moe_status s = check_dims(dims);
+  if (s != MOE_OK) return s;
+  if (!(eps >= 0.0f)) return MOE_ERR_INVALID_ARG;
+  if (dims->T == 0) return MOE_OK;
+  const void* ps[] = {x_resid, gamma, w_router, h_out, logits_out};
+  for (const void* p : ps)
+    if ((s = check_ptr(p)) != MOE_OK) return s;
+  if (y_prev != nullptr && (s = check_ptr(y_prev)) != MOE_OK) return s;
+  if ((s = check_ptr(workspace)) != MOE_OK) return s == MOE_ERR_INVALID_ARG ? MOE_ERR_WORKSPACE : s;
+  if (workspace_bytes < 4) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  NormArgs na{x_resid, y_prev, gamma, dims->T, dims->d, eps, h_out};
+  if (launch_rmsnorm(na, st) != cudaSuccess) return MOE_ERR_CUDA;
+  RouterMaps maps{};
+  if (!encode_bf16_rows(&maps.w, w_router, dims->E, dims->d) || !encode_bf16_rows(&maps.h, h_out, dims->T, dims->d))
+    return MOE_ERR_CUDA;
+  RouterArgs ra{dims->T, dims->d, dims->E, logits_out, at<uint32_t>(workspace, 0)};
+  return cuda_status(launch_router(maps, ra, st));
 }
 
 moe_status moe_clear_error_flags(void* workspace, size_t workspace_bytes, void* stream) {

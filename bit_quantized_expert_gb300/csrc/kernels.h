@@ -91,4 +91,26 @@ struct DecodeArgs {
 bool decode_supported(int d, int E, int k, int F);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st, bool pdl);
 
+// ---------------------------------------------------------------- pre-norm block (router.cu)
+struct NormArgs {
+  float* x;               // fp32 [T, d] residual stream (updated when y_prev is given)
+  const float* y_prev;    // fp32 [T, d] or null
+  const uint16_t* gamma;  // bf16 [d]
+  int T, d;
+  float eps;
+  uint16_t* h;            // bf16 [T, d]
+};
+cudaError_t launch_rmsnorm(const NormArgs& a, cudaStream_t st);
+
+struct RouterMaps {
+  CUtensorMap w;          // W_r bf16 [E, d], box 64 x 128, 128-byte swizzle
+  CUtensorMap h;          // h bf16 [T, d], box 64 x 128, 128-byte swizzle
+};
+struct RouterArgs {
+  int T, d, E;
+  float* logits;          // fp32 [T, E]
+  uint32_t* err;
+};
+cudaError_t launch_router(const RouterMaps& maps, const RouterArgs& a, cudaStream_t st);
+
 }  // namespace moe

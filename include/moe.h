@@ -142,6 +142,16 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
                              float* y, const moe_routing* routing_out, void* workspace, size_t workspace_bytes,
                              void* stream);
 
+/* Pre-norm block of a stack of MoE layers (the step between two layers, not part of the layer):
+ * when y_prev is non-NULL, x_resid += y_prev (written back); then h = RMSNorm(x_resid) * gamma
+ * = x / sqrt(mean(x^2) + eps) * gamma rounded to bf16, and router logits = h W_r^T with bf16
+ * operands and fp32 accumulation on the tensor cores.  x_resid fp32 [T, d] (in/out); y_prev fp32
+ * [T, d] or NULL; gamma bf16 [d]; w_router bf16 [E, d]; h_out bf16 [T, d]; logits_out fp32 [T, E].
+ * The workspace is only used for its error word (any size >= 4 bytes). */
+moe_status moe_rmsnorm_router(const moe_dims* dims, float* x_resid, const float* y_prev, const uint16_t* gamma,
+                              const uint16_t* w_router, float eps, uint16_t* h_out, float* logits_out,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
 /* Enqueues the clearing of the workspace's error word on `stream` (no host synchronisation). */
 moe_status moe_clear_error_flags(void* workspace, size_t workspace_bytes, void* stream);
 

@@ -4,8 +4,10 @@ Bars (written here, derived in the design doc):
   * routing tables (idx, counts, offsets, perm, inv, block map): bit-exact;
   * routing weights: relative error <= 1e-6 (fp32 expf vs float64);
   * layer outputs: max over tokens of ||y_t - r_t|| / ||r_t|| <= 2e-3 against the exact oracle,
-    and <= 2e-4 against the oracle with fp16 GEMM operands (the rounding the tensor-core path
-    applies), so accumulation-order error is all that remains;
+    and <= 5e-4 against the oracle with fp16 GEMM operands (the rounding the tensor-core path
+    applies).  The second bar is one fp16 ulp of h (2^-11 relative): the kernel rounds h to fp16
+    from an fp32 value and the oracle from a float64 one, so elements of h that sit near a
+    rounding boundary may land one ulp apart; everything else left is accumulation order;
   * the decode (T = 1) path computes in fp32 throughout: <= 2e-5 against the exact oracle.
 """
 import numpy as np
@@ -19,7 +21,7 @@ from oracle import moe_oracle as O
 pytestmark = pytest.mark.gpu
 
 EXACT_TOL = 2e-3
-EMUL_TOL = 2e-4
+EMUL_TOL = 5e-4
 DECODE_TOL = 2e-5
 
 
