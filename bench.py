@@ -43,6 +43,9 @@ def parse():
     p.add_argument("--no-extras", action="store_true", help="skip the prefill T=512 / T=4096 sub-measurements")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=50)
+    p.add_argument("--profile", choices=["decode", "prefill", "skewed", "stack"], default=None,
+                   help="small eager run of one workload for ncu captures (prints a short summary only)")
+    p.add_argument("--profile-sets", type=int, default=4, help="weight sets cycled in --profile mode")
     return p.parse_args()
 
 
@@ -390,8 +393,44 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(args):
+    """Eager launches (no CUDA graph) of one workload over a few weight sets, for ncu: every kernel
+    of the path shows up as its own launch.  Holds at most a few GB on the device."""
+    import torch
+
+    import bit_quantized_expert_gb300 as moe
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    moe.load_library()
+    wl = {"decode": synth.DECODE, "prefill": synth.PREFILL, "skewed": synth.SKEWED, "stack": synth.STACK}[args.profile]
+    n = args.profile_sets
+    layers = make_layers(wl, device, n)
+    T = wl.T
+    ins = [synth.torch_make_inputs(wl, seed=1000 + l, device=device, T=(NI if T == 1 else T)) for l in range(n)]
+    dm = layers[0].dims(T)
+    ws = moe.alloc_workspace(dm, device)
+    y = torch.empty((T, wl.d), dtype=torch.float32, device=device)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    total = args.warmup + args.steps
+    for s in range(total):
+        l = s % n
+        if T == 1:
+            i = s % NI
+            layers[l].forward(ins[l]["x"][i:i + 1], ins[l]["logits"][i:i + 1], y, ws)
+        else:
+            layers[l].forward(ins[l]["x"], ins[l]["logits"], y, ws)
+    torch.cuda.synchronize()
+    flags = moe.read_error_flags(ws)
+    print(json.dumps({"profile": wl.name, "calls": total, "weight_sets": n, "flags": flags,
+                      "wall_s": time.perf_counter() - t0}), flush=True)
+
+
 def main():
     args = parse()
+    if args.profile is not None:
+        run_profile(args)
+        return
     if args.impl == "reference":
         run_reference(args)
         return
