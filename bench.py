@@ -26,6 +26,11 @@ import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
+_T0 = time.perf_counter()
+
+
+def log(msg):
+    print(f"[bench {time.perf_counter() - _T0:7.1f}s] {msg}", file=sys.stderr, flush=True)
 
 import synth  # noqa: E402
 
@@ -197,6 +202,7 @@ def decode_bench(args, world, rank, local, device, pk):
 
     import bit_quantized_expert_gb300 as moe
     wl = synth.DECODE
+    log("decode: generating 40 weight sets on the device")
     layers = make_layers(wl, device, LAYERS)
     ins = [synth.torch_make_inputs(wl, seed=1000 + l, device=device, T=NI) for l in range(LAYERS)]
     y = torch.empty((LAYERS, NI, wl.d), dtype=torch.float32, device=device)
@@ -214,6 +220,7 @@ def decode_bench(args, world, rank, local, device, pk):
             step(s)
     stream.synchronize()
     G = 25
+    log("decode: warm-up done; capturing graphs")
     g_many = capture(lambda: [step(s) for s in range(G)], stream)
     g_one = capture(lambda: step(0), stream)
     with torch.cuda.stream(stream):
@@ -226,9 +233,11 @@ def decode_bench(args, world, rank, local, device, pk):
     clocks = Clocks(vis.split(",")[local] if vis else local)
     torch.cuda.synchronize()
     barrier(world)
+    log(f"decode: timing {args.steps} steps")
     clocks.start()
     ms = timed_graph_steps(g_many, G, g_one, args.steps, stream)
     ck = clocks.stop()
+    log(f"decode: {ms / args.steps * 1e3:.2f} us per step")
     torch.cuda.synchronize()
     barrier(world)
     flags = moe.read_error_flags(ws)
@@ -293,6 +302,7 @@ def prefill_bench(wl, steps, device, pk):
 
     import bit_quantized_expert_gb300 as moe
     n_sets = 8 if wl.T >= 4096 else 16
+    log(f"{wl.name}: generating {n_sets} weight sets")
     layers = make_layers(wl, device, n_sets)
     ins = [synth.torch_make_inputs(wl, seed=1000 + l, device=device) for l in range(n_sets)]
     y = torch.empty((wl.T, wl.d), dtype=torch.float32, device=device)
@@ -316,6 +326,7 @@ def prefill_bench(wl, steps, device, pk):
     stream.synchronize()
     steps = max(n_sets, steps // n_sets * n_sets)
     ms = timed_graph_steps(g_many, n_sets, g_one, steps, stream)
+    log(f"{wl.name}: {ms / steps * 1e3:.1f} us per step")
     flags = moe.read_error_flags(ws)
     # touched experts per weight set (from the routing of that set's inputs)
     touched = []

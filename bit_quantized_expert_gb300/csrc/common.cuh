@@ -79,6 +79,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// The same wait for a whole warp that next executes warp-collective (.sync.aligned)
+// instructions such as tcgen05.ld: mbar_wait is a per-lane polling loop, so lanes may leave it at
+// different iterations; the warp is reconverged and agrees on the outcome before returning.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_s,
+                                               uint32_t* err) {
+  const bool ok = mbar_wait(bar, parity, abort_s, err);
+  __syncwarp();
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
 // ------------------------------------------------------------------------------------------
 // Bulk and tensor copies (TMA)
 // ------------------------------------------------------------------------------------------
@@ -172,17 +182,33 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                : "memory");
 }
 
+// TMEM -> registers.  tcgen05.ld is asynchronous: its destination registers hold valid data
+// only after tcgen05.wait::ld.  Load and wait sit in ONE asm statement, so for the compiler the
+// registers are defined only after the wait and no use of them can be scheduled ahead of it.
 // Each thread of the warp reads 16 consecutive 32-bit columns of its own TMEM lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+__device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
-      "[%16];"
+      "{\n\ttcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+      "[%16];\n\ttcgen05.wait::ld.sync.aligned;\n\t}"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
 }
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Two 16-column loads (TMEM addresses ta, tb) and one wait, in one statement.
+__device__ __forceinline__ void tmem_ld16x2_wait(uint32_t ta, uint32_t tb, uint32_t (&a)[16], uint32_t (&b)[16]) {
+  asm volatile(
+      "{\n\ttcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+      "[%32];\n\ttcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,"
+      "%29,%30,%31}, [%33];\n\ttcgen05.wait::ld.sync.aligned;\n\t}"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
+        "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]),
+        "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]),
+        "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15])
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
 
 // Shared-memory matrix descriptor for a K-major operand stored in the 128-byte swizzled
 // canonical layout: rows of 64 16-bit elements (128 B), 8-row atoms 1024 B apart, the 16-byte

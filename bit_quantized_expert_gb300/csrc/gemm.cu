@@ -380,17 +380,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       const int4 tl = tiles[u / MT];
       const int m = u % MT;
       const int b = li & 1;
-      if (!mbar_wait(AF(b), (li >> 1) & 1, abort_s, a.err)) break;
+      if (!mbar_wait_warp(AF(b), (li >> 1) & 1, abort_s, a.err)) break;
       tc_fence_after();
       const int rowg = m * kBM + q * 32 + lane;
       const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::ACC_COLS);
       for (int n0 = 0; n0 < tl.z; n0 += 16) {
         uint32_t g[16];
-        tmem_ld16(tb + n0, g);
         if (MODE == 0) {
           uint32_t uu[16];
-          tmem_ld16(tb + 128 + n0, uu);
-          tmem_ld_wait();
+          tmem_ld16x2_wait(tb + n0, tb + 128 + n0, g, uu);
           const int col = (rowg & ~7) | chunk_pos(rowg & 7);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -404,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             }
           }
         } else {
-          tmem_ld_wait();
+          tmem_ld16_wait(tb + n0, g);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int n = n0 + i;

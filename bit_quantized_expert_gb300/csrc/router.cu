@@ -130,13 +130,12 @@ __global__ void __launch_bounds__(192, 1) router_kernel(const __grid_constant__ 
     }
   } else {
     const int q = warp & 3;
-    if (mbar_wait(DONE, 0, abort_s, a.err)) {
+    if (mbar_wait_warp(DONE, 0, abort_s, a.err)) {
       tc_fence_after();
       const int e = m0 + q * 32 + lane;
       for (int c0 = 0; c0 < 128; c0 += 16) {
         uint32_t v[16];
-        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
-        tmem_ld_wait();
+        tmem_ld16_wait(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int t = n0 + c0 + i;
