@@ -347,8 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             c0[mat] = ld_shared_v4(src);
             c1[mat] = ld_shared_v4(src + 16);
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(RE(s));
+          const int s_used = s;
           if (++s == C::S_RAW) { s = 0; ph ^= 1u; }
           if (!mbar_wait(WE(sw), phw ^ 1u, abort_s, a.err)) { ok = false; break; }
 #pragma unroll
@@ -365,7 +364,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(WF(sw));
+          // The raw stage is released only now: the stores above consumed the codes loaded from
+          // it, so every lane's shared-memory read of the stage has completed.  Releasing it right
+          // after issuing those reads let the TMA refill land before slow lanes had read it.
+          if (lane == 0) {
+            mbar_arrive(RE(s_used));
+            mbar_arrive(WF(sw));
+          }
           if (++sw == C::S_W) { sw = 0; phw ^= 1u; }
         }
       }

@@ -220,6 +220,19 @@ def test_prefill_full_size():
     assert rowwise_err(got, emu) <= EMUL_TOL
 
 
+def test_skewed_prefill_repeats_bitwise():
+    """Repeated calls give identical outputs.  The skewed workload (long 128-token tiles beside
+    one-token tiles) is the one that exposed an early release of the packed-code ring: slow lanes
+    then read codes of the chunk six stages later, corrupting one K-chunk of a few weight rows in
+    roughly one call in five."""
+    wl = synth.SKEWED
+    host, dl = layer_for(wl)
+    inp = synth.make_inputs(wl, seed=4)
+    first = run_layer(wl, host, dl, inp)["y"]
+    for _ in range(7):
+        assert np.array_equal(run_layer(wl, host, dl, inp)["y"], first)
+
+
 def test_skewed_prefill_full_size():
     wl = synth.SKEWED
     host, dl = layer_for(wl)
