@@ -311,6 +311,9 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a) {
 bool decode_supported(int d, int E, int k, int F) {
   const int k1 = k + 1;
   if (k1 > 32 || E > 1024 || F > 2048 || d > 4096) return false;
+  // The down kernel gives each lane max(8, F/32) consecutive elements of a row and reduces over
+  // F / that many lanes with a butterfly: F must be 128 times a power of two.
+  if (F != 128 && F != 256 && F != 512 && F != 1024 && F != 2048) return false;
   return SmemA::bytes(d) <= 200 * 1024 && SmemB::bytes(k1, F) <= 200 * 1024;
 }
 

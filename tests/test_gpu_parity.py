@@ -201,6 +201,17 @@ def test_decode_full_size():
         assert rowwise_err(got, ref[None, :]) <= DECODE_TOL, seed
 
 
+def test_decode_width_not_power_of_two_uses_gemm_path():
+    """F = 384 (not 128 times a power of two) at T = 1 is served by the grouped-GEMM path."""
+    wl = synth.Workload("t1_f384", T=1, d=256, E=16, k=2, F=384, F_shared=384)
+    host = synth.make_layer(wl)
+    dl = moe.to_device_layer(host)
+    inp = synth.make_inputs(wl, seed=8)
+    got = run_layer(wl, host, dl, inp)["y"]
+    ref = O.moe_layer(inp["x"], inp["logits"], host, wl.k)["y"]
+    assert rowwise_err(got, ref) <= EXACT_TOL
+
+
 def test_decode_routing_out_matches_oracle():
     wl = synth.DECODE
     host, dl = layer_for(wl)
