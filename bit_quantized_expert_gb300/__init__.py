@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(PKG_DIR, "libmoe_gb300.so")
 # Symbols declared in include/moe.h.
 EXPORTED = ("moe_status_string", "moe_max_tiles", "moe_workspace_bytes", "moe_route",
             "moe_expert_forward", "moe_layer_forward", "moe_rmsnorm_router", "moe_clear_error_flags",
-            "moe_read_error_flags")
+            "moe_read_error_flags", "moe_layer_forward_decode_noalloc")
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_MISALIGNED",
           4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA"}
@@ -80,6 +80,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_layer_forward.argtypes = [P(Dims), VP, VP, P(ExpertsC), P(ExpertsC), VP, VP, P(RoutingC), VP, S, VP]
     lib.moe_rmsnorm_router.restype = ctypes.c_int
     lib.moe_rmsnorm_router.argtypes = [P(Dims), VP, VP, VP, VP, ctypes.c_float, VP, VP, VP, S, VP]
+    lib.moe_layer_forward_decode_noalloc.restype = ctypes.c_int
+    lib.moe_layer_forward_decode_noalloc.argtypes = [P(Dims), VP, VP, P(ExpertsC), P(ExpertsC), VP, VP, VP]
     lib.moe_clear_error_flags.restype = ctypes.c_int
     lib.moe_clear_error_flags.argtypes = [VP, S, VP]
     lib.moe_read_error_flags.restype = ctypes.c_int
@@ -196,6 +198,14 @@ def rmsnorm_router(dm: Dims, x_resid, y_prev, gamma, w_router, eps: float, h_out
                                              _ptr(w_router), float(eps), _ptr(h_out), _ptr(logits_out),
                                              _ptr(workspace), workspace.numel(), _stream(stream)),
            "moe_rmsnorm_router")
+
+
+def layer_forward_decode_noalloc(dm: Dims, x, logits, routed: dict, shared: dict | None, w_sg, y, stream=None):
+    """One-token layer call without a workspace (scratch is a library-owned device array)."""
+    re, se = experts_struct(routed), experts_struct(shared)
+    _check(load_library().moe_layer_forward_decode_noalloc(
+        ctypes.byref(dm), _ptr(x), _ptr(logits), ctypes.byref(re), ctypes.byref(se) if se is not None else None,
+        _ptr(w_sg), _ptr(y), _stream(stream)), "moe_layer_forward_decode_noalloc")
 
 
 def read_error_flags(workspace, stream=None) -> int:

@@ -152,6 +152,26 @@ moe_status moe_rmsnorm_router(const moe_dims* dims, float* x_resid, const float*
                               const uint16_t* w_router, float eps, uint16_t* h_out, float* logits_out,
                               void* workspace, size_t workspace_bytes, void* stream);
 
+/* Decode (T == 1) layer forward that allocates nothing and takes no workspace.  The pages have
+ * no counterpart: this entry point exists for callers that cannot allocate device memory when
+ * they run the layer -- an engine whose memory planner hands out all of HBM once at start-up and
+ * forbids later cudaMalloc calls, a latency-critical decode loop that must never enter
+ * cudaMalloc/cudaFree (they may synchronise the device), or a host program that holds only
+ * pointers to weights, inputs and outputs.  Arguments and results are those of
+ * moe_layer_forward with T == 1 (same kernels).
+ *   - Scratch: a library-owned device array of 32 KB (+256 B) that every GPU which loads the
+ *     library keeps until the process exits; it bounds (k + 1) * F <= 8192.  Larger dims, T > 1,
+ *     or dims the decode path does not take return MOE_ERR_UNSUPPORTED; T == 0 returns MOE_OK.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls share the array: calls whose work overlaps on the GPU (different streams, or
+ *     different host threads) race.  Serialise them, e.g. on one stream.
+ *   - Device-side error bits (a timed-out wait) land in the shared array and are not reported;
+ *     use moe_layer_forward with a workspace to read them. */
+moe_status moe_layer_forward_decode_noalloc(const moe_dims* dims, const uint16_t* x, const float* logits,
+                                            const moe_experts* routed, const moe_experts* shared,
+                                            const uint16_t* w_shared_gate, float* y, void* stream);
+
 /* Enqueues the clearing of the workspace's error word on `stream` (no host synchronisation). */
 moe_status moe_clear_error_flags(void* workspace, size_t workspace_bytes, void* stream);
 
