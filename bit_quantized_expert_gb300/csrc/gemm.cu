@@ -167,14 +167,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   const int KC = K / 64;
   const int num_units = (*a.num_tiles) * MT;
   const int4* tiles = reinterpret_cast<const int4*>(a.tiles);
+  // Every role walks units blockIdx.x, +gridDim.x, ...; each loads the descriptor of its next unit
+  // one unit ahead so the global-memory latency of the block map stays off the critical path.
+  auto tile_of = [&](int u) { return u < num_units ? __ldg(tiles + u / MT) : make_int4(0, 0, 0, 0); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int s = 0, sx = 0;
       uint32_t ph = 0, phx = 0;
+      int4 tl_next = tile_of(blockIdx.x);
       for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
-        const int4 tl = tiles[u / MT];
+        const int4 tl = tl_next;
+        tl_next = tile_of(u + gridDim.x);
         const int m = u % MT;
         const int which = tl.x == a.E ? 1 : 0;
         const int ec = which ? 0 : tl.x;
@@ -202,8 +207,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       int sw = 0, sx = 0;
       uint32_t phw = 0, phx = 0;
       int li = 0;
+      int4 tl_next = tile_of(blockIdx.x);
       for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++li) {
-        const int4 tl = tiles[u / MT];
+        const int4 tl = tl_next;
+        tl_next = tile_of(u + gridDim.x);
         const uint32_t n_inst = (uint32_t)((tl.z + 15) & ~15);
         const int b = li & 1;
         if (!mbar_wait(AE(b), ((li >> 1) & 1) ^ 1u, abort_s, a.err)) break;
@@ -241,15 +248,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       const int g = threadIdx.x - 64;   // 0..63: rows g and g + 64 of every token tile
       int issued = 0, arrived = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const int4 tl = tiles[u / MT];
-        int tok[2];
+      auto tokens_of = [&](const int4& t, int (&tk)[2]) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int r = g + 64 * h;
-          tok[h] = -1;
-          if (r < tl.z) tok[h] = (tl.x == a.E) ? (tl.y + r - a.T * a.k) : (a.perm[tl.y + r] / a.k);
+          tk[h] = -1;
+          if (r < t.z) tk[h] = (t.x == a.E) ? (t.y + r - a.T * a.k) : (__ldg(a.perm + t.y + r) / a.k);
         }
+      };
+      int4 tl_next = tile_of(blockIdx.x);
+      int tok_next[2];
+      tokens_of(tl_next, tok_next);
+      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        const int tok[2] = {tok_next[0], tok_next[1]};
+        tl_next = tile_of(u + gridDim.x);
+        tokens_of(tl_next, tok_next);
         for (int kc = 0; kc < KC; ++kc) {
           const int sx = issued % C::S_X;
           const uint32_t par = ((uint32_t)(issued / C::S_X) & 1u) ^ 1u;
@@ -291,25 +304,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     bool ok = true;
     bool bad = false;
     const int G = K / 64;
-    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-      const int4 tl = tiles[u / MT];
-      const int m = u % MT;
-      const int which = tl.x == a.E ? 1 : 0;
-      const int ec = which ? 0 : tl.x;
-      const size_t row = (size_t)ec * R + (size_t)m * kBM + i;
-      const uint16_t* srow[NMAT];
-      const uint16_t* brow[NMAT];
+    // Scale and bias rows of this thread's weight row in a unit; the first 8-group block of the
+    // next unit is loaded during the last block of the current one.
+    auto rows_of = [&](int u, const uint16_t* (&sr)[NMAT], const uint16_t* (&br)[NMAT]) {
+      const int4 t = tile_of(u);
+      const int which = t.x == a.E ? 1 : 0;
+      const size_t row = (size_t)(which ? 0 : t.x) * R + (size_t)(u % MT) * kBM + i;
 #pragma unroll
       for (int mat = 0; mat < NMAT; ++mat) {
-        srow[mat] = a.mat[mat][which].scales + row * G;
-        brow[mat] = a.mat[mat][which].biases + row * G;
+        sr[mat] = a.mat[mat][which].scales + row * G;
+        br[mat] = a.mat[mat][which].biases + row * G;
       }
-      uint4 ns[NMAT], nb[NMAT];
+    };
+    const uint16_t* srow[NMAT];
+    const uint16_t* brow[NMAT];
+    uint4 ns[NMAT], nb[NMAT];
+    if (blockIdx.x < num_units) {
+      rows_of(blockIdx.x, srow, brow);
 #pragma unroll
       for (int mat = 0; mat < NMAT; ++mat) {
         ns[mat] = load_group_block(srow[mat], 0, G);
         nb[mat] = load_group_block(brow[mat], 0, G);
       }
+    }
+    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      const uint16_t* srow_n[NMAT];
+      const uint16_t* brow_n[NMAT];
+      const bool has_next = u + (int)gridDim.x < num_units;
+      if (has_next) rows_of(u + gridDim.x, srow_n, brow_n);
       for (int kb = 0; kb < KC && ok; kb += 8) {
         uint4 cs[NMAT], cb[NMAT];
 #pragma unroll
@@ -319,6 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           if (kb + 8 < KC) {
             ns[mat] = load_group_block(srow[mat], kb + 8, G);
             nb[mat] = load_group_block(brow[mat], kb + 8, G);
+          } else if (has_next) {
+            ns[mat] = load_group_block(srow_n[mat], 0, G);
+            nb[mat] = load_group_block(brow_n[mat], 0, G);
           }
         }
 #pragma unroll
@@ -374,6 +399,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           if (++sw == C::S_W) { sw = 0; phw ^= 1u; }
         }
       }
+      if (has_next) {
+#pragma unroll
+        for (int mat = 0; mat < NMAT; ++mat) {
+          srow[mat] = srow_n[mat];
+          brow[mat] = brow_n[mat];
+        }
+      }
     }
     if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) raise_flag(a.err, kErrFp16Range);
   } else {
@@ -381,8 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int q = warp & 3;   // TMEM lane quarter this warp may access
     int li = 0;
     bool bad = false;
+    int4 tl_next = tile_of(blockIdx.x);
     for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++li) {
-      const int4 tl = tiles[u / MT];
+      const int4 tl = tl_next;
+      tl_next = tile_of(u + gridDim.x);
       const int m = u % MT;
       const int b = li & 1;
       if (!mbar_wait_warp(AF(b), (li >> 1) & 1, abort_s, a.err)) break;

@@ -103,10 +103,26 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* total)
   return incl - v + warp_tot[warp];
 }
 
-constexpr int kTokWarps = 16;   // warps that walk the tokens in kernel 2
+// Warps that walk the tokens in kernel 2: 32 when their per-warp tables (2 x E ints each) fit
+// in 96 KB, fewer for large E.
+__host__ __device__ constexpr int tok_warps(int E) { return (96 * 1024) / (8 * E) >= 32 ? 32 : (96 * 1024) / (8 * E); }
+
+// The k expert ids of token t, loaded together (independent loads, one latency); -1 past T or k.
+__device__ __forceinline__ void load_token_ids(const int32_t* __restrict__ idx, int t, int T, int k, int E,
+                                               int (&ev)[32], uint32_t* err) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) ev[j] = (j < k && t < T) ? __ldg(idx + (size_t)t * k + j) : -1;
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (j < k && t < T && (unsigned)ev[j] >= (unsigned)E) {
+      raise_flag(err, kErrBadRouting);
+      ev[j] = -1;
+    }
+}
 
 __global__ void __launch_bounds__(1024, 1) tables_kernel(TablesArgs a) {
   extern __shared__ int tsm[];
+  const int kTokWarps = tok_warps(a.E);
   int* base = tsm;                                       // [kTokWarps][E]: counts, then running slots
   uint32_t* mask = reinterpret_cast<uint32_t*>(tsm + kTokWarps * a.E);   // [kTokWarps][E]
   __shared__ int warp_tot[32];
@@ -128,13 +144,11 @@ __global__ void __launch_bounds__(1024, 1) tables_kernel(TablesArgs a) {
   if (warp < kTokWarps) {
     int* hw = base + warp * E;
     for (int c = c_lo; c < c_hi; ++c) {
-      const int t = c * 32 + lane;
-      if (t < T)
-        for (int j = 0; j < k; ++j) {
-          const int e = a.idx[(size_t)t * k + j];
-          if ((unsigned)e < (unsigned)E) atomicAdd(&hw[e], 1);
-          else raise_flag(a.err, kErrBadRouting);
-        }
+      int ev[32];
+      load_token_ids(a.idx, c * 32 + lane, T, k, E, ev, a.err);
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (ev[j] >= 0) atomicAdd(&hw[ev[j]], 1);
     }
   }
   __syncthreads();
@@ -190,14 +204,8 @@ __global__ void __launch_bounds__(1024, 1) tables_kernel(TablesArgs a) {
     const uint32_t lt = (1u << lane) - 1u;
     for (int c = c_lo; c < c_hi; ++c) {
       const int t = c * 32 + lane;
-      const bool valid = t < T;
       int ev[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        int e = -1;
-        if (j < k && valid) e = a.idx[(size_t)t * k + j];
-        ev[j] = ((unsigned)e < (unsigned)E) ? e : -1;
-      }
+      load_token_ids(a.idx, t, T, k, E, ev, nullptr);
 #pragma unroll
       for (int j = 0; j < 32; ++j)
         if (ev[j] >= 0) atomicOr(&mk[ev[j]], 1u << lane);
@@ -239,7 +247,7 @@ cudaError_t launch_topk(const RouteArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-size_t tables_smem_bytes(int E) { return (size_t)2 * kTokWarps * E * sizeof(int); }
+size_t tables_smem_bytes(int E) { return (size_t)2 * tok_warps(E) * E * sizeof(int); }
 
 cudaError_t launch_tables(const TablesArgs& a, cudaStream_t st) {
   const size_t smem = tables_smem_bytes(a.E);
@@ -248,7 +256,7 @@ cudaError_t launch_tables(const TablesArgs& a, cudaStream_t st) {
   cudaGetDevice(&dev);
   if (configured_dev != dev) {
     cudaError_t e = cudaFuncSetAttribute(tables_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)tables_smem_bytes(1024));
+                                         (int)(96 * 1024));
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }

@@ -14,54 +14,45 @@ __device__ __forceinline__ uint32_t logit_key(float v) {
 }
 
 // Lane j < k returns the j-th expert in *e_out and its routing weight in *w_out.
-// NI = ceil(E / 32) candidates per lane (compile-time upper bound).
+// NI = ceil(E / 32) candidates per lane (compile-time upper bound), lane l holding l + 32 i.
+// Each round takes the largest key with redux.sync max and, among the lanes holding it, the
+// lowest expert index with redux.sync min; the owning lane then clears that candidate.
 template <int NI>
 __device__ __forceinline__ void warp_topk_softmax(const float* __restrict__ row, int E, int k, int* e_out,
                                                   float* w_out) {
   const int lane = threadIdx.x & 31;
-  uint64_t comb[NI];
+  uint32_t key[NI];
   float val[NI];
 #pragma unroll
   for (int i = 0; i < NI; ++i) {
     const int e = lane + 32 * i;
-    float v = 0.0f;
-    uint64_t c = 0;
-    if (e < E) {
-      v = __ldg(row + e);
-      c = ((uint64_t)logit_key(v) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)e);
-    }
-    comb[i] = c;
+    const float v = e < E ? __ldg(row + e) : 0.0f;
+    key[i] = e < E ? logit_key(v) : 0u;
     val[i] = v;
   }
   int my_e = 0;
   float my_v = 0.0f;
   for (int j = 0; j < k; ++j) {
-    uint64_t best = 0;
+    uint32_t best = 0u, bi = 0xFFFFFFFFu;
     float bestv = 0.0f;
-    int bi = -1;
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
-      if (comb[i] > best) {
-        best = comb[i];
+      if (key[i] > best) {   // strict: this lane's lowest index wins its ties
+        best = key[i];
+        bi = (uint32_t)(lane + 32 * i);
         bestv = val[i];
-        bi = i;
       }
     }
-    uint64_t m = best;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, m, off);
-      m = o > m ? o : m;
-    }
-    const int e_win = (int)(0xFFFFFFFFu - (uint32_t)(m & 0xFFFFFFFFu));
-    const float v_win = __shfl_sync(0xFFFFFFFFu, bestv, e_win & 31);
-    if (best == m && m != 0) {
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, best);
+    const uint32_t win = __reduce_min_sync(0xFFFFFFFFu, best == m ? bi : 0xFFFFFFFFu);
+    const float v_win = __shfl_sync(0xFFFFFFFFu, bestv, (int)(win & 31u));
+    if (lane == (int)(win & 31u)) {
 #pragma unroll
       for (int i = 0; i < NI; ++i)
-        if (i == bi) comb[i] = 0;
+        if (i == (int)(win >> 5)) key[i] = 0u;
     }
     if (lane == j) {
-      my_e = e_win;
+      my_e = (int)win;
       my_v = v_win;
     }
   }
