@@ -19,6 +19,10 @@ struct Layout {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// The first 256 bytes of a workspace: the error word at 0, the decode path's grid-barrier word
+// (64-bit, arrivals in the low half and a generation count in the high half) at kSyncOffset.
+constexpr size_t kSyncOffset = 8;
+
 size_t max_tiles_of(long long T, long long k, long long E, long long tile_n, bool shared) {
   return (size_t)(T * k / tile_n + std::min(E, T * k) + (shared ? (T + tile_n - 1) / tile_n : 0));
 }
@@ -369,6 +373,7 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
     da.h = at<float>(workspace, L.hdec);
     da.y = y;
     da.err = err;
+    da.sync = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + L.err + kSyncOffset);
     if (launch_decode(da, st, true) != cudaSuccess) return MOE_ERR_CUDA;
     if (routing_out != nullptr)
       return cuda_status(run_routing(d, logits, caller_routing(routing_out), nullptr, nullptr, nullptr, nullptr, err, st));
@@ -413,7 +418,9 @@ moe_status moe_rmsnorm_router(const moe_dims* dims, float* x_resid, const float*
 moe_status moe_clear_error_flags(void* workspace, size_t workspace_bytes, void* stream) {
   if (workspace == nullptr) return MOE_ERR_INVALID_ARG;
   if (workspace_bytes < 4) return MOE_ERR_WORKSPACE;
-  return cuda_status(cudaMemsetAsync(workspace, 0, 4, static_cast<cudaStream_t>(stream)));
+  // The error word, and (in workspaces large enough for a layer) the decode grid-barrier word.
+  const size_t n = workspace_bytes >= kSyncOffset + 8 ? kSyncOffset + 8 : 4;
+  return cuda_status(cudaMemsetAsync(workspace, 0, n, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_read_error_flags(void* workspace, size_t workspace_bytes, uint32_t* flags, void* stream) {
@@ -422,7 +429,10 @@ moe_status moe_read_error_flags(void* workspace, size_t workspace_bytes, uint32_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemcpy(flags, workspace, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaMemset(workspace, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
+  // After a timed-out wait the grid-barrier word may hold a partial count: reset it too (the
+  // stream is idle here).
+  const size_t n = ((*flags & 1u) != 0 && workspace_bytes >= kSyncOffset + 8) ? kSyncOffset + 8 : 4;
+  if (cudaMemset(workspace, 0, n) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 

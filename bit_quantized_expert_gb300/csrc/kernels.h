@@ -87,6 +87,7 @@ struct DecodeArgs {
   float* h;                // workspace: fp32 [(k+1), F]
   float* y;                // fp32 [d]
   uint32_t* err;
+  unsigned long long* sync;   // grid-barrier word (8-byte aligned; count low, generation high)
 };
 bool decode_supported(int d, int E, int k, int F);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st, bool pdl);

@@ -90,9 +90,10 @@ extern "C" moe_status moe_layer_forward_decode_noalloc(const moe_dims* dims, con
   if (scratch_for_current_device(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* err = reinterpret_cast<uint32_t*>(scratch);
-  // The array keeps the previous call's contents: the error word must start at zero.  The h
-  // values are fully written by the first kernel before the second reads them.
-  if (cudaMemsetAsync(err, 0, sizeof(uint32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+  // The array keeps the previous call's contents: the error word and the grid-barrier word
+  // (bytes 8..15) start every call at zero.  The h values are fully written by the gate/up
+  // phase before the down phase reads them.
+  if (cudaMemsetAsync(err, 0, 16, st) != cudaSuccess) return MOE_ERR_CUDA;
 
   DecodeArgs da{};
   da.x = x;
@@ -114,5 +115,6 @@ extern "C" moe_status moe_layer_forward_decode_noalloc(const moe_dims* dims, con
   da.h = scratch + kNoAllocHeadFloats;
   da.y = y;
   da.err = err;
+  da.sync = reinterpret_cast<unsigned long long*>(scratch + 2);
   return launch_decode(da, st, true) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -46,11 +46,9 @@ __device__ __forceinline__ void warp_topk_softmax(const float* __restrict__ row,
     const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, best);
     const uint32_t win = __reduce_min_sync(0xFFFFFFFFu, best == m ? bi : 0xFFFFFFFFu);
     const float v_win = __shfl_sync(0xFFFFFFFFu, bestv, (int)(win & 31u));
-    if (lane == (int)(win & 31u)) {
+    const int sel = (lane == (int)(win & 31u)) ? (int)(win >> 5) : -1;
 #pragma unroll
-      for (int i = 0; i < NI; ++i)
-        if (i == (int)(win >> 5)) key[i] = 0u;
-    }
+    for (int i = 0; i < NI; ++i) key[i] = (i == sel) ? 0u : key[i];
     if (lane == j) {
       my_e = (int)win;
       my_v = v_win;

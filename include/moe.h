@@ -114,8 +114,10 @@ size_t moe_max_tiles(const moe_dims* dims, int32_t tile_n);
 
 /* Workspace bytes needed by moe_route, moe_expert_forward and moe_layer_forward for these dims
  * (one size serves all three).  Returns 0 for invalid dims.  The first 4 bytes of the workspace are
- * its error word: kernels only ever set bits in it, so it is sticky across calls.  Clear it once
- * after allocating the workspace (moe_clear_error_flags); the rest needs no initialisation. */
+ * its error word: kernels only ever set bits in it, so it is sticky across calls.  Bytes 8..15
+ * hold the decode path's grid-barrier word (it returns to zero at the end of every T == 1 call).
+ * Clear both once after allocating the workspace (moe_clear_error_flags); the rest needs no
+ * initialisation. */
 size_t moe_workspace_bytes(const moe_dims* dims);
 
 /* Routing: top-k, weights, histogram, exclusive scan, permutation and block map of fp32
@@ -172,10 +174,12 @@ moe_status moe_layer_forward_decode_noalloc(const moe_dims* dims, const uint16_t
                                             const moe_experts* routed, const moe_experts* shared,
                                             const uint16_t* w_shared_gate, float* y, void* stream);
 
-/* Enqueues the clearing of the workspace's error word on `stream` (no host synchronisation). */
+/* Enqueues the clearing of the workspace's error word (and, for workspaces of at least 16 bytes,
+ * the decode grid-barrier word) on `stream` (no host synchronisation). */
 moe_status moe_clear_error_flags(void* workspace, size_t workspace_bytes, void* stream);
 
-/* Synchronises `stream`, copies the workspace's error word to *flags, then clears it.  Bits:
+/* Synchronises `stream`, copies the workspace's error word to *flags, then clears it (and the
+ * decode grid-barrier word when bit 1 was set).  Bits:
  * 1 = a bounded device wait timed out, 2 = a value left the fp16 operand range,
  * 4 = routing tables inconsistent with the dims.  0 means every call since the last clear
  * completed cleanly. */
