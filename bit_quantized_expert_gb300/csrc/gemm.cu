@@ -12,11 +12,12 @@
 //   * Work unit = (block-map tile of <= 128 slots of one expert, 128-row slice of the weight
 //     matrix), iterated over K in chunks of 64 (= one quantisation group).  A persistent grid of
 //     one CTA per SM walks the units; every role walks the same list.
-//   * Warp roles (12 warps): 0 = TMA producer (packed codes; the h operand of the down
+//   * Warp roles (16 warps): 0 = TMA producer (packed codes; the h operand of the down
 //     projection), 1 = MMA issuer (one thread) and TMEM owner, 2-3 = row gather of x for the
-//     gate/up projection (16-byte cp.async into the swizzled operand layout), 4-7 = dequant
-//     (one weight row per thread: 4-bit codes -> fp16 w = q*scale + bias, single rounding),
-//     8-11 = epilogue (TMEM -> registers; SwiGLU -> fp16 h, or fp32 expert outputs).
+//     gate/up projection (16-byte cp.async into the swizzled operand layout), 4-11 = dequant
+//     (two threads per weight row: 4-bit codes -> fp16 w = q*scale + bias, single rounding; two
+//     dequant warps per scheduler so one hides the other's shared-memory and barrier latency),
+//     12-15 = epilogue (TMEM -> registers; SwiGLU -> fp16 h, or fp32 expert outputs).
 //   * Gate/up mode keeps the gate and up accumulators of the same 128 F-rows side by side in
 //     TMEM so the epilogue applies silu(g) * u in registers.  Two accumulator buffers let the
 //     epilogue of one unit overlap the MMAs of the next.
@@ -31,7 +32,7 @@ namespace moe {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr uint32_t kTileBytes = 128 * 128;   // one 128-row x 64-column fp16 operand tile
 constexpr uint32_t kRawBytes = 128 * 32;     // 128 rows x 64 packed 4-bit codes
 
@@ -126,10 +127,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::S_RAW; ++i) {
       mbar_init(RF(i), 1);
-      mbar_init(RE(i), 4);
+      mbar_init(RE(i), 8);
     }
     for (int i = 0; i < C::S_W; ++i) {
-      mbar_init(WF(i), 4);
+      mbar_init(WF(i), 8);
       mbar_init(WE(i), 1);
     }
     for (int i = 0; i < C::S_X; ++i) {
@@ -295,9 +296,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         ++arrived;
       }
     }
-  } else if (warp < 8) {
-    // ------------------------------------------------------------ dequant: one weight row per thread
-    const int i = threadIdx.x - 128;
+  } else if (warp < 12) {
+    // ------------------------------------------------------------ dequant: 8 warps; thread i
+    // handles weight row i % 128 and half i / 128 of every chunk: the gate (0) or up (1) matrix
+    // in gate/up mode, code words 0-3 (0) or 4-7 (1) of the 64-code chunk in down mode.
+    const int i = (threadIdx.x - 128) & 127;
+    const int half = (threadIdx.x - 128) >> 7;
+    const int mat = MODE == 0 ? half : 0;
+    constexpr int NW = MODE == 0 ? 8 : 4;   // code words per thread per chunk
+    const int w0 = MODE == 0 ? 0 : 4 * half;
     const uint32_t swz = (uint32_t)(i & 7);
     int s = 0, sw = 0;
     uint32_t ph = 0, phw = 0;
@@ -306,86 +313,71 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int G = K / 64;
     // Scale and bias rows of this thread's weight row in a unit; the first 8-group block of the
     // next unit is loaded during the last block of the current one.
-    auto rows_of = [&](int u, const uint16_t* (&sr)[NMAT], const uint16_t* (&br)[NMAT]) {
+    auto rows_of = [&](int u, const uint16_t*& sr, const uint16_t*& br) {
       const int4 t = tile_of(u);
       const int which = t.x == a.E ? 1 : 0;
       const size_t row = (size_t)(which ? 0 : t.x) * R + (size_t)(u % MT) * kBM + i;
-#pragma unroll
-      for (int mat = 0; mat < NMAT; ++mat) {
-        sr[mat] = a.mat[mat][which].scales + row * G;
-        br[mat] = a.mat[mat][which].biases + row * G;
-      }
+      sr = a.mat[mat][which].scales + row * G;
+      br = a.mat[mat][which].biases + row * G;
     };
-    const uint16_t* srow[NMAT];
-    const uint16_t* brow[NMAT];
-    uint4 ns[NMAT], nb[NMAT];
+    const uint16_t* srow = nullptr;
+    const uint16_t* brow = nullptr;
+    uint4 ns = make_uint4(0u, 0u, 0u, 0u), nb = make_uint4(0u, 0u, 0u, 0u);
     if (blockIdx.x < num_units) {
       rows_of(blockIdx.x, srow, brow);
-#pragma unroll
-      for (int mat = 0; mat < NMAT; ++mat) {
-        ns[mat] = load_group_block(srow[mat], 0, G);
-        nb[mat] = load_group_block(brow[mat], 0, G);
-      }
+      ns = load_group_block(srow, 0, G);
+      nb = load_group_block(brow, 0, G);
     }
     for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-      const uint16_t* srow_n[NMAT];
-      const uint16_t* brow_n[NMAT];
+      const uint16_t* srow_n = nullptr;
+      const uint16_t* brow_n = nullptr;
       const bool has_next = u + (int)gridDim.x < num_units;
       if (has_next) rows_of(u + gridDim.x, srow_n, brow_n);
       for (int kb = 0; kb < KC && ok; kb += 8) {
-        uint4 cs[NMAT], cb[NMAT];
-#pragma unroll
-        for (int mat = 0; mat < NMAT; ++mat) {
-          cs[mat] = ns[mat];
-          cb[mat] = nb[mat];
-          if (kb + 8 < KC) {
-            ns[mat] = load_group_block(srow[mat], kb + 8, G);
-            nb[mat] = load_group_block(brow[mat], kb + 8, G);
-          } else if (has_next) {
-            ns[mat] = load_group_block(srow_n[mat], 0, G);
-            nb[mat] = load_group_block(brow_n[mat], 0, G);
-          }
+        const uint4 cs = ns, cb = nb;
+        if (kb + 8 < KC) {
+          ns = load_group_block(srow, kb + 8, G);
+          nb = load_group_block(brow, kb + 8, G);
+        } else if (has_next) {
+          ns = load_group_block(srow_n, 0, G);
+          nb = load_group_block(brow_n, 0, G);
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           if (kb + j >= KC) break;
-          __half2 s2[NMAT], b2[NMAT];
-#pragma unroll
-          for (int mat = 0; mat < NMAT; ++mat) {
-            const float sf = bf16_bits_to_f32(j == 0 ? pick_bf16<0>(cs[mat]) : j == 1 ? pick_bf16<1>(cs[mat])
-                                              : j == 2 ? pick_bf16<2>(cs[mat]) : j == 3 ? pick_bf16<3>(cs[mat])
-                                              : j == 4 ? pick_bf16<4>(cs[mat]) : j == 5 ? pick_bf16<5>(cs[mat])
-                                              : j == 6 ? pick_bf16<6>(cs[mat]) : pick_bf16<7>(cs[mat]));
-            const float bf = bf16_bits_to_f32(j == 0 ? pick_bf16<0>(cb[mat]) : j == 1 ? pick_bf16<1>(cb[mat])
-                                              : j == 2 ? pick_bf16<2>(cb[mat]) : j == 3 ? pick_bf16<3>(cb[mat])
-                                              : j == 4 ? pick_bf16<4>(cb[mat]) : j == 5 ? pick_bf16<5>(cb[mat])
-                                              : j == 6 ? pick_bf16<6>(cb[mat]) : pick_bf16<7>(cb[mat]));
-            bad = bad || !(fmaf(15.0f, fabsf(sf), fabsf(bf)) <= 65504.0f);
-            s2[mat] = __float2half2_rn(sf);
-            b2[mat] = __float2half2_rn(bf);
-          }
+          const float sf = bf16_bits_to_f32(j == 0 ? pick_bf16<0>(cs) : j == 1 ? pick_bf16<1>(cs)
+                                            : j == 2 ? pick_bf16<2>(cs) : j == 3 ? pick_bf16<3>(cs)
+                                            : j == 4 ? pick_bf16<4>(cs) : j == 5 ? pick_bf16<5>(cs)
+                                            : j == 6 ? pick_bf16<6>(cs) : pick_bf16<7>(cs));
+          const float bf = bf16_bits_to_f32(j == 0 ? pick_bf16<0>(cb) : j == 1 ? pick_bf16<1>(cb)
+                                            : j == 2 ? pick_bf16<2>(cb) : j == 3 ? pick_bf16<3>(cb)
+                                            : j == 4 ? pick_bf16<4>(cb) : j == 5 ? pick_bf16<5>(cb)
+                                            : j == 6 ? pick_bf16<6>(cb) : pick_bf16<7>(cb));
+          bad = bad || !(fmaf(15.0f, fabsf(sf), fabsf(bf)) <= 65504.0f);
+          const __half2 s2 = __float2half2_rn(sf);
+          const __half2 b2 = __float2half2_rn(bf);
           if (!mbar_wait(RF(s), ph, abort_s, a.err)) { ok = false; break; }
-          uint4 c0[NMAT], c1[NMAT];
-#pragma unroll
-          for (int mat = 0; mat < NMAT; ++mat) {
-            const uint32_t src = sRaw + (s * NMAT + mat) * kRawBytes + i * 32;
-            c0[mat] = ld_shared_v4(src);
-            c1[mat] = ld_shared_v4(src + 16);
+          const uint32_t src = sRaw + (s * NMAT + mat) * kRawBytes + i * 32 + w0 * 4;
+          uint32_t words[8];
+          {
+            const uint4 c0 = ld_shared_v4(src);
+            words[0] = c0.x; words[1] = c0.y; words[2] = c0.z; words[3] = c0.w;
+            if (NW == 8) {
+              const uint4 c1 = ld_shared_v4(src + 16);
+              words[4] = c1.x; words[5] = c1.y; words[6] = c1.z; words[7] = c1.w;
+            } else {
+              words[4] = words[5] = words[6] = words[7] = 0u;
+            }
           }
           const int s_used = s;
           if (++s == C::S_RAW) { s = 0; ph ^= 1u; }
           if (!mbar_wait(WE(sw), phw ^ 1u, abort_s, a.err)) { ok = false; break; }
+          const uint32_t dst = sW + (sw * NMAT + mat) * kTileBytes + i * 128;
 #pragma unroll
-          for (int mat = 0; mat < NMAT; ++mat) {
-            const uint32_t dst = sW + (sw * NMAT + mat) * kTileBytes + i * 128;
-            const uint32_t words[8] = {c0[mat].x, c0[mat].y, c0[mat].z, c0[mat].w,
-                                       c1[mat].x, c1[mat].y, c1[mat].z, c1[mat].w};
-#pragma unroll
-            for (int wd = 0; wd < 8; ++wd) {
-              uint32_t o[4];
-              dequant_word(words[wd], s2[mat], b2[mat], o);
-              st_shared_v4(dst + ((((uint32_t)wd) ^ swz) << 4), o[0], o[1], o[2], o[3]);
-            }
+          for (int wd = 0; wd < NW; ++wd) {
+            uint32_t o[4];
+            dequant_word(words[wd], s2, b2, o);
+            st_shared_v4(dst + ((((uint32_t)(w0 + wd)) ^ swz) << 4), o[0], o[1], o[2], o[3]);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -400,11 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
       }
       if (has_next) {
-#pragma unroll
-        for (int mat = 0; mat < NMAT; ++mat) {
-          srow[mat] = srow_n[mat];
-          brow[mat] = brow_n[mat];
-        }
+        srow = srow_n;
+        brow = brow_n;
       }
     }
     if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) raise_flag(a.err, kErrFp16Range);
