@@ -51,7 +51,7 @@ Layout layout_of(const moe_dims& d) {
   L.num_tiles = take(16);
   L.h = take(slots * F * 2);
   L.yperm = take(slots * D * 4);
-  L.hdec = take(33 * F * 4);
+  L.hdec = take(T == 1 ? decode_scratch_floats((int)D, (int)k, (int)F) * 4 : 0);   // decode partials
   L.total = o;
   return L;
 }
@@ -370,7 +370,7 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
     da.k = d.k;
     da.F = d.F;
     da.has_shared = sh ? 1 : 0;
-    da.h = at<float>(workspace, L.hdec);
+    da.part = at<float>(workspace, L.hdec);
     da.y = y;
     da.err = err;
     da.sync = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + L.err + kSyncOffset);

@@ -6,26 +6,29 @@
 // 0.2% and that matrix ops reached 97.9% of bandwidth ("Perplexity открыла код Lily...",
 // section "Спекулятивное декодирование не взлетело").  On a GB300 one layer's routed weights
 // (~16 MB) stream in ~2.3 us, so the layer is as much a latency chain as a bandwidth problem:
-// the design removes every step of that chain that is not a weight byte in flight.
+// the design keeps that chain short.
 //
-// One cooperative launch per layer, one CTA per SM (grid = max(jobs), all CTAs co-resident):
-//   * before the programmatic-launch wait, every CTA starts the bulk copies of the shared
-//     expert's rows it owns (weights are never written upstream, so they may be read early);
-//   * after it, every CTA redoes the top-k of the token's logits in registers (1 KB from L2;
-//     cheaper than a routing kernel and its launch) and starts the copies of its routed rows:
-//       gate/up job c < (k+1) F / 32: 32 gate rows and the 32 up rows of expert slot c / (F/32),
-//         copied in four quarters with one mbarrier each, so compute starts on the first quarter;
-//       down job c < d / 16: rows 16c .. 16c+15 of the down matrix of all k + 1 experts;
-//   * gate/up jobs write their 32 SwiGLU outputs h (fp32) to global memory, then every CTA
-//     arrives at a grid barrier (one 64-bit word: arrivals in the low half, a generation count
-//     in the high half; the last arrival resets the count and bumps the generation);
-//   * down jobs wait for the generation to move, read all (k + 1) F values of h from L2 into
-//     shared memory and compute y[r] = sum_j w_j (W_down[e_j] h_j)[r] + g_s (W_down_s h_s)[r].
+// One cooperative launch per layer; CTA c (grid = (k+1) F / 32, one per SM, all co-resident)
+// owns rows f0 = 32 (c mod F/32) .. f0+31 of expert slot j = c / (F/32) (k = the shared expert):
+//   * before the programmatic-launch wait, shared-expert CTAs start their weight copies (weights
+//     are never written upstream, so they may be read early);
+//   * after it, warp 0 routes the token in registers (top-k of the 1 KB of logits; cheaper than a
+//     routing kernel and its launch) and starts the bulk copies of the 32 gate rows and 32 up rows
+//     (four quarters, one mbarrier each, so compute starts on the first quarter), while every
+//     thread copies the matching 32-column block of the down matrix (all d rows, 16 B each, plus
+//     the scale and bias of its quantisation group) with cp.async;
+//   * the CTA computes its 32 SwiGLU outputs h, then its share of the down projection,
+//     part_c[r] = w_j * sum_{f in f0..f0+31} W_down[e_j][r][f] h[f] for every output row r
+//     (a split over F: no CTA needs another CTA's h);
+//   * every CTA writes part_c and arrives at a grid barrier (one 64-bit word: arrivals in the low
+//     half, a generation count in the high half; the last arrival resets the count and bumps the
+//     generation), then sums a slice of rows over all CTAs in a fixed order:
+//     y[r] = sum_c part_c[r] -- deterministic, no atomics on data.
 //
 // Arithmetic: codes become exact fp32 values q * 16^e via the 2^23 exponent trick (the nibble
 // stays where it is in the word; the activation carries the matching 16^-e), partial dot
 // products sum_c q_c x_c accumulate in fp32 with packed two-lane FMAs, and w = q*s + b enters as
-// s * sum(q x) + b * sum(x) per quantisation group.
+// s * sum(q x) + b * sum(x) per quantisation group (per half group for the down rows).
 #include <algorithm>
 #include <mutex>
 
@@ -36,9 +39,9 @@
 namespace moe {
 namespace {
 
-constexpr int RF = 32;   // gate/up rows per job
-constexpr int RD = 16;   // down rows per job
+constexpr int RF = 32;   // gate/up rows (and down columns) per CTA
 constexpr int kQuarters = 4;
+constexpr int kRQ = RF / kQuarters;   // gate/up rows per quarter
 constexpr int kMaxE = 1024;
 constexpr float kMagic = 8388608.0f;   // 2^23
 constexpr int kThreadsDec = 256;
@@ -67,29 +70,26 @@ __device__ __forceinline__ float2 word_dot2(uint32_t w, const float2* xs, float2
   return acc;
 }
 
-// Shared-memory plan of one CTA (byte offsets; every region 16-byte aligned).
+// Shared-memory plan of one CTA (byte offsets, 16-byte aligned regions).
 struct DecPlan {
-  int d, F, k1, G, GF, epl, segs;
-  uint32_t gu_codes, gu_sb, dn_codes, dn_sb, h, hsum, bytes;
+  int d, F, k1, G, GF, grid;
+  uint32_t gu_codes, gu_sb, dn_codes, dn_sb, hbuf, bytes;
   __host__ __device__ DecPlan(int d_, int F_, int k1_) : d(d_), F(F_), k1(k1_) {
     G = d / 64;
     GF = F / 64;
-    epl = F / 32 <= 8 ? 8 : F / 32;   // down-row elements per lane
-    segs = F / epl;                   // lanes covering one down row
+    grid = k1 * (F / RF);
     uint32_t o = 0;
-    gu_codes = o;  o += 2u * RF * (d / 2);                 // [gate|up][RF][d/8] u32
-    gu_sb = o;     o += 4u * RF * G * 2;                   // [g.s|g.b|u.s|u.b][RF][G] bf16
+    gu_codes = o;  o += 2u * RF * (d / 2);   // [gate|up][RF][d/8] u32
+    gu_sb = o;     o += 4u * RF * G * 2;     // [g.s|g.b|u.s|u.b][RF][G] bf16
     o = (o + 15u) & ~15u;
-    dn_codes = o;  o += (uint32_t)k1 * RD * (F / 2);       // [k1][RD][F/8] u32
-    dn_sb = o;     o += 2u * k1 * RD * GF * 2;             // [s|b][k1][RD][GF] bf16
-    o = (o + 15u) & ~15u;
-    h = o;         o += (uint32_t)k1 * segs * (epl + 4) * 4;   // [k1][segs][epl + 4] fp32, padded
-    hsum = o;      o += (uint32_t)k1 * segs * 4;               // [k1][segs] fp32
+    dn_codes = o;  o += 16u * d;             // [d][4] u32: code words f0/8 .. f0/8+3 of every row
+    dn_sb = o;     o += 8u * d;              // [s|b][d] u32: the bf16 pair holding group f0/64
+    hbuf = o;      o += 4u * RF;             // h of rows f0 .. f0+31, fp32
     bytes = (o + 15u) & ~15u;
   }
 };
 
-// One warp: top-k of logits[0..E) and the softmax of the selected logits, with the candidates
+// Warp-wide top-k of logits[0..E) and the softmax of the selected logits, with the candidates
 // held in registers (8 per lane up to E = 256, else 32); lane j < k returns expert j and its weight.
 __device__ __forceinline__ void reg_topk(const float* __restrict__ logits, int E, int k, int* e_out, float* w_out) {
   if (E <= 256) warp_topk_softmax<8>(logits, E, k, e_out, w_out);
@@ -107,8 +107,6 @@ __device__ __forceinline__ unsigned long long ld_acquire(const unsigned long lon
   return v;
 }
 
-// EPL: elements of one down row per lane, max(8, F / 32); F / EPL lanes cover one row.
-template <int EPL>
 __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t sm[];
   const int d = a.d, F = a.F, k = a.k;
@@ -117,85 +115,90 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
   const int G = P.G, GF = P.GF;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x;
-  const int jobs_per_expert = F / RF;
-  const bool has_gu = cta < k1 * jobs_per_expert;
-  const bool has_dn = cta < d / RD;
-  const int j = has_gu ? cta / jobs_per_expert : 0;   // expert slot: 0..k-1 routed, k shared
-  const int f0 = has_gu ? (cta % jobs_per_expert) * RF : 0;
-  const int r0 = cta * RD;
+  const int jobs = F / RF;
+  const int j = cta / jobs;            // expert slot: 0..k-1 routed, k shared
+  const int f0 = (cta % jobs) * RF;    // first gate/up row = first down column
+  const bool shared_cta = (j == k);
+  const int wset = shared_cta ? 1 : 0;
 
   uint32_t* gcodes = reinterpret_cast<uint32_t*>(sm + P.gu_codes);   // gate [RF][d/8], then up
   uint16_t* gsb = reinterpret_cast<uint16_t*>(sm + P.gu_sb);         // [g.s | g.b | u.s | u.b][RF][G]
-  uint32_t* dcodes = reinterpret_cast<uint32_t*>(sm + P.dn_codes);   // [k1][RD][F/8]
-  uint16_t* dsb = reinterpret_cast<uint16_t*>(sm + P.dn_sb);         // [s | b][k1][RD][GF]
-  float* hs = reinterpret_cast<float*>(sm + P.h);                    // [k1][segs][EPL + 4]
-  float* hsum_s = reinterpret_cast<float*>(sm + P.hsum);             // [k1][segs]
-  __shared__ __align__(8) uint64_t bars[kQuarters + 1];
-  __shared__ int e_s[32];
-  __shared__ float w_s[33];   // routing weights, then the shared-expert gate at [k]
+  uint32_t* dcodes = reinterpret_cast<uint32_t*>(sm + P.dn_codes);   // [d][4]
+  uint32_t* dsb = reinterpret_cast<uint32_t*>(sm + P.dn_sb);         // [s | b][d]
+  float* hbuf = reinterpret_cast<float*>(sm + P.hbuf);               // [RF]
+  __shared__ __align__(8) uint64_t bars[kQuarters];
+  __shared__ int e_s;
+  __shared__ float wgt_s;    // w_j (routed) or the shared-expert gate
   __shared__ int abort_s;
-  __shared__ unsigned long long gen_s;
 
   if (tid == 0) {
-    for (int i = 0; i <= kQuarters; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    for (int i = 0; i < kQuarters; ++i) mbar_init(smem_u32(&bars[i]), 1);
     abort_s = 0;
     mbar_fence_init();
   }
   __syncthreads();
-  const uint32_t bar_dn = smem_u32(&bars[kQuarters]);
 
-  // Gate and up rows f0 .. f0+31 of expert e of weight set `which`, in quarters of 8 rows.
-  auto issue_gu = [&](int which, int e) {
-    const QPtr& g = a.gate[which];
-    const QPtr& u = a.up[which];
-    constexpr int rq = RF / kQuarters;
-    const uint32_t cb = rq * (d / 2), sb = rq * G * 2;
+  // Gate and up rows f0 .. f0+31 of expert e (code words by quarter; scales and biases with the
+  // first quarter).
+  auto issue_gu = [&](int e) {
+    const QPtr& g = a.gate[wset];
+    const QPtr& u = a.up[wset];
+    const uint32_t cb = kRQ * (d / 2), sb = RF * G * 2;
+    const size_t rowb = (size_t)e * F + f0;
     for (int q = 0; q < kQuarters; ++q) {
       const uint32_t bar = smem_u32(&bars[q]);
-      const size_t row0 = (size_t)e * F + f0 + q * rq;
-      mbar_arrive_expect_tx(bar, 2 * cb + 4 * sb);
-      bulk_g2s(smem_u32(gcodes + (q * rq) * (d / 8)), g.codes + row0 * (d / 8), cb, bar);
-      bulk_g2s(smem_u32(gcodes + (RF + q * rq) * (d / 8)), u.codes + row0 * (d / 8), cb, bar);
-      bulk_g2s(smem_u32(gsb + (0 * RF + q * rq) * G), g.scales + row0 * G, sb, bar);
-      bulk_g2s(smem_u32(gsb + (1 * RF + q * rq) * G), g.biases + row0 * G, sb, bar);
-      bulk_g2s(smem_u32(gsb + (2 * RF + q * rq) * G), u.scales + row0 * G, sb, bar);
-      bulk_g2s(smem_u32(gsb + (3 * RF + q * rq) * G), u.biases + row0 * G, sb, bar);
+      const size_t row0 = rowb + q * kRQ;
+      mbar_arrive_expect_tx(bar, 2 * cb + (q == 0 ? 4 * sb : 0));
+      if (q == 0) {
+        bulk_g2s(smem_u32(gsb + 0 * RF * G), g.scales + rowb * G, sb, bar);
+        bulk_g2s(smem_u32(gsb + 1 * RF * G), g.biases + rowb * G, sb, bar);
+        bulk_g2s(smem_u32(gsb + 2 * RF * G), u.scales + rowb * G, sb, bar);
+        bulk_g2s(smem_u32(gsb + 3 * RF * G), u.biases + rowb * G, sb, bar);
+      }
+      bulk_g2s(smem_u32(gcodes + (q * kRQ) * (d / 8)), g.codes + row0 * (d / 8), cb, bar);
+      bulk_g2s(smem_u32(gcodes + (RF + q * kRQ) * (d / 8)), u.codes + row0 * (d / 8), cb, bar);
     }
   };
-  // Down rows r0 .. r0+15 of expert e of weight set `which` into expert slot `slot`.
-  auto issue_dn = [&](int slot, int which, int e) {
-    const QPtr& q = a.down[which];
-    const size_t row0 = (size_t)e * d + r0;
-    const uint32_t cb = RD * (F / 2), sb = RD * GF * 2;
-    bulk_g2s(smem_u32(dcodes + slot * RD * (F / 8)), q.codes + row0 * (F / 8), cb, bar_dn);
-    bulk_g2s(smem_u32(dsb + (slot * RD) * GF), q.scales + row0 * GF, sb, bar_dn);
-    bulk_g2s(smem_u32(dsb + ((k1 + slot) * RD) * GF), q.biases + row0 * GF, sb, bar_dn);
+  // Columns f0 .. f0+31 of every row of the down matrix of expert e: 16 code bytes per row, and
+  // the 4-byte aligned bf16 pairs holding the row's scale and bias of group f0/64.
+  auto copy_dn = [&](int e) {
+    const QPtr& q = a.down[wset];
+    const int g2 = (f0 / 64) & ~1;
+    for (int r = tid; r < d; r += kThreadsDec) {
+      const size_t row = (size_t)e * d + r;
+      cp_async_16(smem_u32(dcodes + 4 * r), q.codes + row * (F / 8) + f0 / 8);
+      cp_async_4(smem_u32(dsb + r), q.scales + row * GF + g2);
+      cp_async_4(smem_u32(dsb + d + r), q.biases + row * GF + g2);
+    }
+    cp_async_commit();
   };
 
   // Weights are never written upstream: the shared expert's copies start before the wait.
-  if (tid == 0) {
-    if (has_dn) mbar_arrive_expect_tx(bar_dn, (uint32_t)k1 * (RD * (F / 2) + 2 * RD * GF * 2));
-    if (a.has_shared) {
-      if (has_gu && j == k) issue_gu(1, 0);
-      if (has_dn) issue_dn(k, 1, 0);
-    }
+  if (shared_cta) {
+    if (tid == 0) issue_gu(0);
+    copy_dn(0);
   }
   pdl_wait();   // x and logits from upstream kernels are complete and visible past this point
-  if (warp == 0) {
+
+  // x: lane l owns quantisation group l (64 inputs); the loads go out before routing.
+  const bool active = lane < G;
+  uint4 xr[8];
+#pragma unroll
+  for (int c8 = 0; c8 < 8; ++c8)
+    xr[c8] = active ? __ldg(reinterpret_cast<const uint4*>(a.x) + lane * 8 + c8) : make_uint4(0u, 0u, 0u, 0u);
+
+  if (warp == 0 && !shared_cta) {
     int e;
     float w;
     reg_topk(a.logits, a.E, k, &e, &w);
-    if (lane < k) {
-      e_s[lane] = e;
-      w_s[lane] = w;
-    }
-    __syncwarp();
+    const int ej = __shfl_sync(0xFFFFFFFFu, e, j);
+    const float wj = __shfl_sync(0xFFFFFFFFu, w, j);
     if (lane == 0) {
-      if (has_gu && j < k) issue_gu(0, e_s[j]);
-      if (has_dn)
-        for (int jj = 0; jj < k; ++jj) issue_dn(jj, 0, e_s[jj]);
+      e_s = ej;
+      wgt_s = wj;
+      issue_gu(ej);
     }
-  } else if (warp == 1 && has_dn && a.has_shared) {
+  } else if (warp == 1 && shared_cta) {
     float dot = 0.0f;
     const uint4* xv = reinterpret_cast<const uint4*>(a.x);
     const uint4* gv = reinterpret_cast<const uint4*>(a.w_sg);
@@ -210,69 +213,62 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, off);
-    if (lane == 0) w_s[k] = 1.0f / (1.0f + expf(-dot));
+    if (lane == 0) wgt_s = 1.0f / (1.0f + expf(-dot));
   }
   pdl_launch_dependents();
+  __syncthreads();   // e_s and wgt_s
+  if (!shared_cta) copy_dn(e_s);
 
-  // ---- gate/up job: lane l owns quantisation group l (64 inputs) of every row; warp w computes
-  // gate and up of rows q*8 + w (q = 0..3) as slots s = 2q + mat, then a reduce-scatter leaves
-  // slot s fully summed in lane 4s.
-  if (has_gu) {
-    const bool active = lane < G;
-    float2 xs[32];
-    float xsum = 0.0f;
+  // ---- gate/up: warp w computes gate and up of rows q*8 + w (q = 0..3) as slots s = 2q + mat;
+  // a reduce-scatter leaves slot s fully summed in lane 4s.
+  float2 xs[32];
+  float xsum = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) xs[i] = make_float2(0.0f, 0.0f);
-    if (active) {
-      const uint4* xv = reinterpret_cast<const uint4*>(a.x) + lane * 8;
+  for (int c8 = 0; c8 < 8; ++c8) {
+    const uint32_t wv[4] = {xr[c8].x, xr[c8].y, xr[c8].z, xr[c8].w};
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        const uint4 v = __ldg(xv + c8);
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float lo = bf16_bits_to_f32(wv[i] & 0xFFFFu), hi = bf16_bits_to_f32(wv[i] >> 16);
-          xsum += lo + hi;
-          xs[c8 * 4 + i] = make_float2(lo * act_prescale(2 * i), hi * act_prescale(2 * i + 1));
-        }
-      }
+    for (int i = 0; i < 4; ++i) {
+      const float lo = bf16_bits_to_f32(wv[i] & 0xFFFFu), hi = bf16_bits_to_f32(wv[i] >> 16);
+      xsum += lo + hi;
+      xs[c8 * 4 + i] = make_float2(lo * act_prescale(2 * i), hi * act_prescale(2 * i + 1));
     }
-    float v8[8];
+  }
+  float v8[8];
 #pragma unroll
-    for (int s = 0; s < 8; ++s) v8[s] = 0.0f;
-    bool ok_all = true;
+  for (int sl = 0; sl < 8; ++sl) v8[sl] = 0.0f;
+  bool ok_all = true;
 #pragma unroll 1
-    for (int q = 0; q < kQuarters; ++q) {
-      const bool ok = mbar_wait_warp(smem_u32(&bars[q]), 0, &abort_s, a.err);
-      ok_all = ok_all && ok;
+  for (int q = 0; q < kQuarters; ++q) {
+    const bool ok = mbar_wait_warp(smem_u32(&bars[q]), 0, &abort_s, a.err);
+    ok_all = ok_all && ok;
 #pragma unroll
-      for (int mat = 0; mat < 2; ++mat) {
-        const int row = q * (RF / kQuarters) + warp;
-        float v = 0.0f;
-        if (active && ok) {
-          const uint32_t* cw = gcodes + (mat * RF + row) * (d / 8) + lane * 8;
-          const uint4 c0 = *reinterpret_cast<const uint4*>(cw);
-          const uint4 c1 = *reinterpret_cast<const uint4*>(cw + 4);
-          float2 p0 = make_float2(0.0f, 0.0f), p1 = make_float2(0.0f, 0.0f);
-          p0 = word_dot2(c0.x, xs + 0, p0);
-          p1 = word_dot2(c0.y, xs + 4, p1);
-          p0 = word_dot2(c0.z, xs + 8, p0);
-          p1 = word_dot2(c0.w, xs + 12, p1);
-          p0 = word_dot2(c1.x, xs + 16, p0);
-          p1 = word_dot2(c1.y, xs + 20, p1);
-          p0 = word_dot2(c1.z, xs + 24, p0);
-          p1 = word_dot2(c1.w, xs + 28, p1);
-          const float p = (p0.x + p0.y) + (p1.x + p1.y);
-          const float s = bf16_bits_to_f32(gsb[((2 * mat) * RF + row) * G + lane]);
-          const float b = bf16_bits_to_f32(gsb[((2 * mat + 1) * RF + row) * G + lane]);
-          v = fmaf(s, p, b * xsum);
-        }
-#pragma unroll
-        for (int s = 0; s < 8; ++s) v8[s] = (s == 2 * q + mat) ? v : v8[s];
+    for (int mat = 0; mat < 2; ++mat) {
+      const int row = q * kRQ + warp;
+      float v = 0.0f;
+      if (active && ok) {
+        const uint32_t* cw = gcodes + (mat * RF + row) * (d / 8) + lane * 8;
+        const uint4 c0 = *reinterpret_cast<const uint4*>(cw);
+        const uint4 c1 = *reinterpret_cast<const uint4*>(cw + 4);
+        float2 p0 = make_float2(0.0f, 0.0f), p1 = make_float2(0.0f, 0.0f);
+        p0 = word_dot2(c0.x, xs + 0, p0);
+        p1 = word_dot2(c0.y, xs + 4, p1);
+        p0 = word_dot2(c0.z, xs + 8, p0);
+        p1 = word_dot2(c0.w, xs + 12, p1);
+        p0 = word_dot2(c1.x, xs + 16, p0);
+        p1 = word_dot2(c1.y, xs + 20, p1);
+        p0 = word_dot2(c1.z, xs + 24, p0);
+        p1 = word_dot2(c1.w, xs + 28, p1);
+        const float p = (p0.x + p0.y) + (p1.x + p1.y);
+        const float s = bf16_bits_to_f32(gsb[((2 * mat) * RF + row) * G + lane]);
+        const float b = bf16_bits_to_f32(gsb[((2 * mat + 1) * RF + row) * G + lane]);
+        v = fmaf(s, p, b * xsum);
       }
+      const int sl = 2 * q + mat;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) v8[t] = (t == sl) ? v : v8[t];
     }
-    // Reduce-scatter of 8 values over 32 lanes: after the xor-16, -8 and -4 steps lane l holds
-    // a partial of slot ((l >> 2) & 7); the xor-2 and -1 steps finish the sum.
+  }
+  {
     float t4[4], t2[2];
     const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0, b2 = (lane & 4) != 0;
 #pragma unroll
@@ -285,136 +281,88 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
     t1 += __shfl_xor_sync(0xFFFFFFFFu, t1, 2);
     t1 += __shfl_xor_sync(0xFFFFFFFFu, t1, 1);
     const float upv = __shfl_down_sync(0xFFFFFFFFu, t1, 4);   // slot 2q+1 (lane 8q+4) -> lane 8q
-    if ((lane & 7) == 0 && ok_all) {
+    if ((lane & 7) == 0) {
       const float gv = t1;
-      a.h[(size_t)j * F + f0 + (lane >> 3) * (RF / kQuarters) + warp] = gv / (1.0f + expf(-gv)) * upv;
+      hbuf[(lane >> 3) * kRQ + warp] = gv / (1.0f + expf(-gv)) * upv;
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();   // h and this thread's down copies -> visible to the whole CTA
+
+  // ---- down share: part_c[r] = wgt * (s * sum_f q h_f + b * sum_f h_f) over f0 .. f0+31.
+  {
+    float2 hv[16];
+    float hsum = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float hx = hbuf[2 * i], hy = hbuf[2 * i + 1];
+      hsum += hx + hy;
+      hv[i] = make_float2(hx * act_prescale(2 * i), hy * act_prescale(2 * i + 1));
+    }
+    const float wgt = wgt_s;
+    const bool hi_half = ((f0 / 64) & 1) != 0;   // group f0/64 is the upper bf16 of its pair
+    for (int r = tid; r < d; r += kThreadsDec) {
+      const uint4 c = *reinterpret_cast<const uint4*>(dcodes + 4 * r);
+      float2 p0 = make_float2(0.0f, 0.0f), p1 = make_float2(0.0f, 0.0f);
+      p0 = word_dot2(c.x, hv + 0, p0);
+      p1 = word_dot2(c.y, hv + 4, p1);
+      p0 = word_dot2(c.z, hv + 8, p0);
+      p1 = word_dot2(c.w, hv + 12, p1);
+      const float p = (p0.x + p0.y) + (p1.x + p1.y);
+      const uint32_t sp = dsb[r], bp = dsb[d + r];
+      const float s = bf16_bits_to_f32(hi_half ? (sp >> 16) : (sp & 0xFFFFu));
+      const float b = bf16_bits_to_f32(hi_half ? (bp >> 16) : (bp & 0xFFFFu));
+      a.part[(size_t)cta * d + r] = wgt * fmaf(s, p, b * hsum);
     }
   }
 
   // ---- grid barrier: every CTA arrives once; the last arrival resets the count and bumps the
-  // generation in one atomic.  The h stores above are ordered before the arrival by the block
-  // barrier and the fence.
+  // generation in one atomic.  The partial stores are ordered before the arrival by the block
+  // barrier and the fence; the acquire load and fence order the reads below after it.
   __syncthreads();
   if (tid == 0) {
     __threadfence();
     const unsigned long long n = gridDim.x;
     const unsigned long long old = atom_add_release(a.sync, 1ull);
     if ((old & 0xFFFFFFFFull) == n - 1ull) atom_add_release(a.sync, (1ull << 32) - n);
-    gen_s = old >> 32;
+    const unsigned long long g0 = old >> 32;
+    const long long t0 = clock64();
+    while ((ld_acquire(a.sync) >> 32) == g0) {
+      if (clock64() - t0 > kWaitTimeoutCycles) {
+        abort_s = 1;
+        raise_flag(a.err, kErrWaitTimeout);
+        break;
+      }
+    }
+    __threadfence();
   }
+  __syncthreads();
 
-  // ---- down job: rows r0 .. r0+15; warp w owns rows 2w and 2w+1.
-  if (has_dn) {
-    if (tid == 0) {
-      const unsigned long long g0 = gen_s;
-      const long long t0 = clock64();
-      while ((ld_acquire(a.sync) >> 32) == g0) {
-        if (abort_s || clock64() - t0 > kWaitTimeoutCycles) {
-          abort_s = 1;
-          raise_flag(a.err, kErrWaitTimeout);
-          break;
-        }
+  // ---- y rows of this CTA: sum of all CTAs' partials in a fixed order (16 lanes per row, each
+  // summing every 16th CTA, then a fixed butterfly).
+  if (!abort_s) {
+    const int n = gridDim.x;
+    const int rpc = (d + n - 1) / n;
+    const int r_lo = cta * rpc, r_hi = min(d, r_lo + rpc);
+    const int sub = tid & 15;
+    for (int rb = r_lo; rb < r_hi; rb += kThreadsDec / 16) {
+      const int r = rb + (tid >> 4);
+      float acc = 0.0f;
+      if (r < r_hi) {
+#pragma unroll 4
+        for (int c = sub; c < n; c += 16) acc += __ldcg(a.part + (size_t)c * d + r);
       }
-      __threadfence();
-    }
-    __syncthreads();
-    const int segs = P.segs;   // lanes covering one row (F / EPL)
-    if (!abort_s) {
-      // h (fp32, from L2) -> shared memory, pre-scaled per code position and padded per lane
-      // segment so that the segment loads below are conflict-free; segment sums of unscaled h.
-      const float4* h4 = reinterpret_cast<const float4*>(a.h);
-      const int n4 = k1 * F / 4;
-      for (int base = 0; base < n4; base += kThreadsDec) {
-        const int i = base + tid;
-        const bool valid = i < n4;
-        float4 v = valid ? __ldcg(h4 + i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        float part = (v.x + v.y) + (v.z + v.w);
-#pragma unroll
-        for (int off = 1; off < EPL / 4; off <<= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, off);
-        if (valid) {
-          const int e = 4 * i, jj = e / F, c = e % F;
-          const int n0 = c & 7;   // 0 or 4
-          v.x *= n0 ? act_prescale(4) : act_prescale(0);
-          v.y *= n0 ? act_prescale(5) : act_prescale(1);
-          v.z *= n0 ? act_prescale(6) : act_prescale(2);
-          v.w *= n0 ? act_prescale(7) : act_prescale(3);
-          const int sg = jj * segs + c / EPL;
-          *reinterpret_cast<float4*>(hs + sg * (EPL + 4) + c % EPL) = v;
-          if ((c % EPL) == 0) hsum_s[sg] = part;
-        }
-      }
-    }
-    __syncthreads();
-    const bool ok = mbar_wait_warp(bar_dn, 0, &abort_s, a.err) && !abort_s;
-    constexpr int EPW = EPL / 8;   // code words per lane segment
-    const int rpw = 32 / segs;     // rows a warp covers at once (1 or 2)
-    const int npass = 2 / rpw;
-    const int sub = lane / segs, l = lane % segs;
-    const int grp = (l * EPL) / 64;
-    float acc[2] = {0.0f, 0.0f};
-    if (ok) {
-#pragma unroll 1
-      for (int jj = 0; jj < k1; ++jj) {
-        float2 hv[EPL / 2];
-        const float4* hp = reinterpret_cast<const float4*>(hs + (jj * segs + l) * (EPL + 4));
-#pragma unroll
-        for (int c4 = 0; c4 < EPL / 4; ++c4) {
-          const float4 t = hp[c4];
-          hv[2 * c4] = make_float2(t.x, t.y);
-          hv[2 * c4 + 1] = make_float2(t.z, t.w);
-        }
-        const float hsm = hsum_s[jj * segs + l];
-        const float wj = w_s[jj];
-#pragma unroll
-        for (int it = 0; it < 2; ++it) {
-          if (it < npass) {
-            const int r = 2 * warp + it * rpw + sub;
-            const uint32_t* cw = dcodes + (jj * RD + r) * (F / 8) + l * EPW;
-            uint32_t wd[EPW];
-            if (EPW == 1) {
-              wd[0] = cw[0];
-            } else if (EPW == 2) {
-              const uint2 t = *reinterpret_cast<const uint2*>(cw);
-              wd[0] = t.x;
-              wd[EPW > 1 ? 1 : 0] = t.y;
-            } else {
-#pragma unroll
-              for (int q4 = 0; q4 < EPW / 4; ++q4) {
-                const uint4 t = *reinterpret_cast<const uint4*>(cw + 4 * q4);
-                wd[(4 * q4) % EPW] = t.x;
-                wd[(4 * q4 + 1) % EPW] = t.y;
-                wd[(4 * q4 + 2) % EPW] = t.z;
-                wd[(4 * q4 + 3) % EPW] = t.w;
-              }
-            }
-            float2 p0 = make_float2(0.0f, 0.0f), p1 = make_float2(0.0f, 0.0f);
-#pragma unroll
-            for (int w8 = 0; w8 < EPW; ++w8) {
-              if (w8 & 1) p1 = word_dot2(wd[w8], hv + 4 * w8, p1);
-              else p0 = word_dot2(wd[w8], hv + 4 * w8, p0);
-            }
-            const float p = (p0.x + p0.y) + (p1.x + p1.y);
-            const float s = bf16_bits_to_f32(dsb[(jj * RD + r) * GF + grp]);
-            const float b = bf16_bits_to_f32(dsb[((k1 + jj) * RD + r) * GF + grp]);
-            acc[it] = fmaf(wj, fmaf(s, p, b * hsm), acc[it]);
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int it = 0; it < 2; ++it) {
-      float v = acc[it];
-      for (int off = segs / 2; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-      if (it < npass && l == 0 && ok) a.y[r0 + 2 * warp + it * rpw + sub] = v;
+      acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 8);
+      acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 4);
+      acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 2);
+      acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
+      if (sub == 0 && r < r_hi) a.y[r] = acc;
     }
   }
 
   // ---- wind down: after a timeout, copies still in flight must land before the CTA exits.
-  __syncthreads();
   if (tid == 0 && abort_s) {
-    for (int i = 0; i <= kQuarters; ++i) {
-      const bool used = (i < kQuarters) ? has_gu : has_dn;
-      if (!used) continue;
+    for (int i = 0; i < kQuarters; ++i) {
       const long long t0 = clock64();
       while (!mbar_try_wait(smem_u32(&bars[i]), 0) && clock64() - t0 < 4000000ll) {
       }
@@ -422,19 +370,6 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
   }
 }
 
-int dec_epl(int F) { return F / 32 <= 8 ? 8 : F / 32; }
-int dec_grid(int d, int k1, int F) { return std::max(k1 * (F / RF), d / RD); }
-
-template <int EPL>
-cudaError_t configure(size_t smem) {
-  cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel<EPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_layer_kernel<EPL>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-  return e;
-}
-
-// Per device: SM count and CTAs per SM of each instantiation at the largest plan (checked at
-// every call against the actual plan's grid).
 struct DevInfo {
   int sms = 0;
   bool ready = false;
@@ -442,7 +377,6 @@ struct DevInfo {
 constexpr int kMaxDev = 64;
 DevInfo g_dev[kMaxDev];
 std::mutex g_dev_mu;
-
 constexpr size_t kDecSmemMax = 200 * 1024;
 
 cudaError_t dev_info(DevInfo** out) {
@@ -454,10 +388,10 @@ cudaError_t dev_info(DevInfo** out) {
   DevInfo& di = g_dev[dev];
   if (!di.ready) {
     if ((e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = configure<8>(kDecSmemMax)) != cudaSuccess) return e;
-    if ((e = configure<16>(kDecSmemMax)) != cudaSuccess) return e;
-    if ((e = configure<32>(kDecSmemMax)) != cudaSuccess) return e;
-    if ((e = configure<64>(kDecSmemMax)) != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecSmemMax);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
     di.ready = true;
   }
   *out = &di;
@@ -466,17 +400,20 @@ cudaError_t dev_info(DevInfo** out) {
 
 }  // namespace
 
+size_t decode_scratch_floats(int d, int k, int F) { return (size_t)(k + 1) * (F / RF) * d; }
+
 bool decode_supported(int d, int E, int k, int F) {
   const int k1 = k + 1;
-  // One quantisation group per lane in the gate/up rows: d <= 2048, at most 32 experts per token.
-  if (k1 > 32 || E > kMaxE || F > 2048 || d > 2048 || d % RD != 0) return false;
-  // A down row is covered by F / max(8, F/32) lanes with a butterfly: F = 128 * 2^n.
-  if (F != 128 && F != 256 && F != 512 && F != 1024 && F != 2048) return false;
-  if (DecPlan(d, F, k1).bytes > kDecSmemMax) return false;
+  // One quantisation group per lane in the gate/up rows: d <= 2048 (and d a multiple of 64).
+  // F a multiple of 128: the down columns f0 .. f0+31 of a CTA lie in one bf16 pair of
+  // scale (bias) values that starts on a 4-byte boundary (F / 64 even).
+  if (k1 > 32 || E > kMaxE || d > 2048 || d % 64 != 0 || F % 128 != 0) return false;
+  const DecPlan P(d, F, k1);
+  if (P.bytes > kDecSmemMax) return false;
   // Every CTA must be resident at once (one per SM): the grid barrier waits on all of them.
   DevInfo* di = nullptr;
   if (dev_info(&di) != cudaSuccess) return false;
-  return dec_grid(d, k1, F) <= di->sms;
+  return P.grid <= di->sms;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st, bool pdl) {
@@ -485,27 +422,20 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st, bool pdl) {
   cudaError_t e = dev_info(&di);
   if (e != cudaSuccess) return e;
   const DecPlan P(a.d, a.F, k1);
-  const int grid = dec_grid(a.d, k1, a.F);
-  if (grid > di->sms || P.bytes > kDecSmemMax) return cudaErrorInvalidConfiguration;
-
+  if (P.grid > di->sms || P.bytes > kDecSmemMax) return cudaErrorInvalidConfiguration;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = dim3(P.grid);
   cfg.blockDim = dim3(kThreadsDec);
   cfg.dynamicSmemBytes = P.bytes;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  switch (dec_epl(a.F)) {
-    case 8: e = cudaLaunchKernelEx(&cfg, decode_layer_kernel<8>, a); break;
-    case 16: e = cudaLaunchKernelEx(&cfg, decode_layer_kernel<16>, a); break;
-    case 32: e = cudaLaunchKernelEx(&cfg, decode_layer_kernel<32>, a); break;
-    default: e = cudaLaunchKernelEx(&cfg, decode_layer_kernel<64>, a); break;
-  }
+  e = cudaLaunchKernelEx(&cfg, decode_layer_kernel, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

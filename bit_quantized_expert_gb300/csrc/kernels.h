@@ -84,12 +84,13 @@ struct DecodeArgs {
   QPtr gate[2], up[2], down[2];   // [0] routed (stacked over E), [1] shared (may be null)
   const uint16_t* w_sg;    // bf16 [d] or null
   int d, E, k, F, has_shared;
-  float* h;                // workspace: fp32 [(k+1), F]
+  float* part;             // scratch: fp32 [(k+1) F / 32][d] per-CTA partial outputs
   float* y;                // fp32 [d]
   uint32_t* err;
   unsigned long long* sync;   // grid-barrier word (8-byte aligned; count low, generation high)
 };
 bool decode_supported(int d, int E, int k, int F);
+size_t decode_scratch_floats(int d, int k, int F);   // floats of DecodeArgs::part
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st, bool pdl);
 
 // ---------------------------------------------------------------- pre-norm block (router.cu)

@@ -6,8 +6,8 @@
 // latency-critical decode loop that must never enter cudaMalloc or cudaFree, which may
 // synchronise the whole device; or a host program that only holds pointers to weights, inputs
 // and outputs and has no allocator of its own.  moe_layer_forward_decode_noalloc serves them: the
-// only scratch it needs (an error word and the fp32 SwiGLU outputs of the k + 1 experts of one
-// token) lives in the file-scope device array below, which every GPU that loads this library
+// only scratch it needs (an error word, a grid-barrier word and the decode kernel's per-CTA
+// partial outputs) lives in the file-scope device array below, which every GPU that loads this library
 // holds until the process exits.
 #include <mutex>
 
@@ -17,10 +17,11 @@
 namespace moe {
 namespace {
 
-// The first 64 floats (256 bytes) hold the error word; then (k + 1) * F fp32 values.
+// The first 64 floats (256 bytes) hold the error word and the grid-barrier word; then the
+// decode kernel's per-CTA partial outputs, (k + 1) F / 32 rows of d fp32 values.
 constexpr int kNoAllocHeadFloats = 64;
-constexpr int kNoAllocMaxH = 8192;    // upper bound on (k + 1) * F: 32 KB
-static __device__ __align__(256) float g_noalloc_scratch[kNoAllocHeadFloats + kNoAllocMaxH];
+constexpr size_t kNoAllocMaxPart = 327680;   // upper bound on (k + 1) (F / 32) d: 1.25 MB
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocHeadFloats + kNoAllocMaxPart];
 
 constexpr int kMaxDevices = 64;
 float* g_scratch_addr[kMaxDevices] = {nullptr};
@@ -76,7 +77,7 @@ extern "C" moe_status moe_layer_forward_decode_noalloc(const moe_dims* dims, con
   const bool sh = shared != nullptr;
   if (sh != (dims->F_shared > 0)) return MOE_ERR_INVALID_ARG;
   if (!decode_supported(dims->d, dims->E, dims->k, dims->F)) return MOE_ERR_UNSUPPORTED;
-  if ((long long)(dims->k + 1) * dims->F > kNoAllocMaxH) return MOE_ERR_UNSUPPORTED;
+  if (decode_scratch_floats(dims->d, dims->k, dims->F) > kNoAllocMaxPart) return MOE_ERR_UNSUPPORTED;
   moe_status s;
   if ((s = check_expert_ptrs(*routed)) != MOE_OK) return s;
   if (sh && (s = check_expert_ptrs(*shared)) != MOE_OK) return s;
@@ -91,8 +92,8 @@ extern "C" moe_status moe_layer_forward_decode_noalloc(const moe_dims* dims, con
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* err = reinterpret_cast<uint32_t*>(scratch);
   // The array keeps the previous call's contents: the error word and the grid-barrier word
-  // (bytes 8..15) start every call at zero.  The h values are fully written by the gate/up
-  // phase before the down phase reads them.
+  // (bytes 8..15) start every call at zero.  Every partial is written before the grid barrier
+  // and read after it.
   if (cudaMemsetAsync(err, 0, 16, st) != cudaSuccess) return MOE_ERR_CUDA;
 
   DecodeArgs da{};
@@ -112,7 +113,7 @@ extern "C" moe_status moe_layer_forward_decode_noalloc(const moe_dims* dims, con
   da.k = dims->k;
   da.F = dims->F;
   da.has_shared = sh ? 1 : 0;
-  da.h = scratch + kNoAllocHeadFloats;
+  da.part = scratch + kNoAllocHeadFloats;
   da.y = y;
   da.err = err;
   da.sync = reinterpret_cast<unsigned long long*>(scratch + 2);

@@ -137,8 +137,9 @@ moe_status moe_expert_forward(const moe_dims* dims, const uint16_t* x, const moe
 /* The whole layer: y[t] = sum_j w[t,j] FFN_{idx[t,j]}(x_t) + sigmoid(x_t . w_sg) FFN_shared(x_t).
  * x bf16 [T, d]; logits fp32 [T, E]; w_shared_gate bf16 [d] (ignored when shared is NULL);
  * y fp32 [T, d].  routing_out may be NULL; when given, its tables are filled as by moe_route.
- * T == 1 runs the fused decode path (fp32 arithmetic on CUDA cores), T > 1 the grouped-GEMM
- * path (fp16 tensor-core operands, fp32 accumulation). */
+ * T == 1 runs the fused decode path (fp32 arithmetic on CUDA cores) when d <= 2048, d % 64 == 0,
+ * F % 128 == 0, k < 32, E <= 1024 and (k + 1) * F / 32 CTAs fit one per SM; otherwise, and for
+ * T > 1, the grouped-GEMM path (fp16 tensor-core operands, fp32 accumulation). */
 moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const float* logits,
                              const moe_experts* routed, const moe_experts* shared, const uint16_t* w_shared_gate,
                              float* y, const moe_routing* routing_out, void* workspace, size_t workspace_bytes,
@@ -161,9 +162,10 @@ moe_status moe_rmsnorm_router(const moe_dims* dims, float* x_resid, const float*
  * cudaMalloc/cudaFree (they may synchronise the device), or a host program that holds only
  * pointers to weights, inputs and outputs.  Arguments and results are those of
  * moe_layer_forward with T == 1 (same kernels).
- *   - Scratch: a library-owned device array of 32 KB (+256 B) that every GPU which loads the
- *     library keeps until the process exits; it bounds (k + 1) * F <= 8192.  Larger dims, T > 1,
- *     or dims the decode path does not take return MOE_ERR_UNSUPPORTED; T == 0 returns MOE_OK.
+ *   - Scratch: a library-owned device array of 1.25 MB (+256 B) that every GPU which loads the
+ *     library keeps until the process exits; it bounds (k + 1) * (F / 32) * d <= 327680.  Larger
+ *     dims, T > 1, or dims the decode path does not take return MOE_ERR_UNSUPPORTED; T == 0
+ *     returns MOE_OK.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
  *     that device current; make that first call before any stream capture.
  *   - All calls share the array: calls whose work overlaps on the GPU (different streams, or

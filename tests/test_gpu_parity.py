@@ -201,15 +201,18 @@ def test_decode_full_size():
         assert rowwise_err(got, ref[None, :]) <= DECODE_TOL, seed
 
 
-def test_decode_width_not_power_of_two_uses_gemm_path():
-    """F = 384 (not 128 times a power of two) at T = 1 is served by the grouped-GEMM path."""
-    wl = synth.Workload("t1_f384", T=1, d=256, E=16, k=2, F=384, F_shared=384)
+@pytest.mark.parametrize("d,F,tol", [(256, 384, DECODE_TOL),    # decode path, 3 column blocks of 128
+                                       (4096, 128, EXACT_TOL)])   # d > 2048: grouped-GEMM path at T = 1
+def test_decode_shapes_and_gemm_fallback_at_t1(d, F, tol):
+    """T = 1 at an F that is not a power of two (decode kernel) and at a width the decode kernel
+    does not take (served by the grouped-GEMM path)."""
+    wl = synth.Workload(f"t1_d{d}_f{F}", T=1, d=d, E=16, k=2, F=F, F_shared=F)
     host = synth.make_layer(wl)
     dl = moe.to_device_layer(host)
     inp = synth.make_inputs(wl, seed=8)
     got = run_layer(wl, host, dl, inp)["y"]
     ref = O.moe_layer(inp["x"], inp["logits"], host, wl.k)["y"]
-    assert rowwise_err(got, ref) <= EXACT_TOL
+    assert rowwise_err(got, ref) <= tol
 
 
 def test_decode_routing_out_matches_oracle():

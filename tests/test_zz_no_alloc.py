@@ -79,5 +79,5 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(decode_layer):
 
     unsupported = 2
     assert call(moe.dims(2, wl.d, wl.E, wl.k, wl.F, wl.F_shared)) == unsupported       # more than one token
-    assert call(moe.dims(1, wl.d, wl.E, 8, 1024, 1024)) == unsupported                 # (k+1)*F = 9216 > 8192
+    assert call(moe.dims(1, wl.d, wl.E, 8, 1024, 1024)) == unsupported                 # (k+1) F/32 = 288 CTAs > SMs
     assert call(moe.dims(0, wl.d, wl.E, wl.k, wl.F, wl.F_shared)) == 0                  # no token: no-op
