@@ -148,6 +148,20 @@ bool encode_h(CUtensorMap* m, const uint16_t* h, long long slots, int F) {
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// x [T, d] fp16 (operand chunk order) for row gathers: a 64 x 1 box (one 128-byte row piece)
+// in the 128-byte swizzle, so four gathered rows land as four rows of the MMA operand tile.
+bool encode_x_rows(CUtensorMap* m, const uint16_t* x16p, long long T, int d) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)T};
+  const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  const cuuint32_t box[2] = {64, 1};
+  const cuuint32_t es[2] = {1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(x16p), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Row-major bf16 matrix [rows, cols] with a 64 x 128 box in the 128-byte swizzle.
 bool encode_bf16_rows(CUtensorMap* m, const uint16_t* p, long long rows, int cols) {
   EncodeTiledFn f = encode_fn();
@@ -222,7 +236,7 @@ moe_status run_experts(const moe_dims& d, const RoutingPtrs& R, const moe_expert
             encode_codes(&m0.codes[1][1], s_or_r->up.codes, ns, d.F, d.d) &&
             encode_codes(&m1.codes[0][0], routed->down.codes, d.E, d.d, d.F) &&
             encode_codes(&m1.codes[0][1], s_or_r->down.codes, ns, d.d, d.F) &&
-            encode_h(&m1.h, h, slots, d.F);
+            encode_h(&m1.h, h, slots, d.F) && encode_x_rows(&m0.x, x16p, d.T, d.d);
   if (!ok) return MOE_ERR_CUDA;
   m0.h = m1.h;
   m1.codes[1][0] = m1.codes[0][0];

@@ -13,8 +13,9 @@
 //     matrix), iterated over K in chunks of 64 (= one quantisation group).  A persistent grid of
 //     one CTA per SM walks the units; every role walks the same list.
 //   * Warp roles (16 warps): 0 = TMA producer (packed codes; the h operand of the down
-//     projection), 1 = MMA issuer (one thread) and TMEM owner, 2-3 = row gather of x for the
-//     gate/up projection (16-byte cp.async into the swizzled operand layout), 4-11 = dequant
+//     projection), 1 = MMA issuer (one thread) and TMEM owner, 2 = row gather of x for the
+//     gate/up projection (TMA gather4: four token rows per instruction into the swizzled operand
+//     layout), 3 = idle, 4-11 = dequant
 //     (two threads per weight row: 4-bit codes -> fp16 w = q*scale + bias, single rounding; two
 //     dequant warps per scheduler so one hides the other's shared-memory and barrier latency),
 //     12-15 = epilogue (TMEM -> registers; SwiGLU -> fp16 h, or fp32 expert outputs).
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       mbar_init(WE(i), 1);
     }
     for (int i = 0; i < C::S_X; ++i) {
-      mbar_init(XF(i), MODE == 0 ? 2 : 1);
+      mbar_init(XF(i), 1);
       mbar_init(XE(i), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -152,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       prefetch_tmap(&maps.codes[1][1]);
     }
     if (MODE == 1) prefetch_tmap(&maps.h);
+    if (MODE == 0) prefetch_tmap(&maps.x);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -243,59 +245,49 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         tc_commit(AF(b));
       }
     }
-  } else if (warp < 4) {
+  } else if (warp == 2) {
     // ------------------------------------------------------------ x row gather (gate/up)
+    // Lane l fetches tile rows 4l .. 4l+3 of every K chunk with one TMA gather4 (four token rows
+    // of 64 fp16 -> four 128-byte rows of the swizzled operand tile).  Rows past the tile's end
+    // repeat the lane's first row; the MMA columns they feed are never stored.
     if (MODE == 0) {
-      const int g = threadIdx.x - 64;   // 0..63: rows g and g + 64 of every token tile
-      int issued = 0, arrived = 0;
-      bool ok = true;
-      auto tokens_of = [&](const int4& t, int (&tk)[2]) {
+      auto tokens_of = [&](const int4& t, int (&tk)[4]) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int r = g + 64 * h;
-          tk[h] = -1;
-          if (r < t.z) tk[h] = (t.x == a.E) ? (t.y + r - a.T * a.k) : (__ldg(a.perm + t.y + r) / a.k);
+        for (int i = 0; i < 4; ++i) {
+          const int r = min(4 * lane + i, t.z - 1);
+          tk[i] = r < 0 ? 0 : (t.x == a.E) ? (t.y + r - a.T * a.k) : (__ldg(a.perm + t.y + r) / a.k);
+        }
+        if (4 * lane >= t.z) tk[0] = tk[1] = tk[2] = tk[3] = 0;
+        if (4 * lane < t.z) {
+#pragma unroll
+          for (int i = 1; i < 4; ++i)
+            if (4 * lane + i >= t.z) tk[i] = tk[0];
         }
       };
+      int sx = 0;
+      uint32_t phx = 0;
+      bool ok = true;
       int4 tl_next = tile_of(blockIdx.x);
-      int tok_next[2];
+      int tok_next[4];
       tokens_of(tl_next, tok_next);
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const int tok[2] = {tok_next[0], tok_next[1]};
+        const int4 tl = tl_next;
+        const int tok[4] = {tok_next[0], tok_next[1], tok_next[2], tok_next[3]};
         tl_next = tile_of(u + gridDim.x);
         tokens_of(tl_next, tok_next);
+        const int ng = (tl.z + 3) / 4;   // gather4 groups of this tile
         for (int kc = 0; kc < KC; ++kc) {
-          const int sx = issued % C::S_X;
-          const uint32_t par = ((uint32_t)(issued / C::S_X) & 1u) ^ 1u;
-          if (!mbar_wait(XE(sx), par, abort_s, a.err)) { ok = false; break; }
-          const uint32_t dst = sX + sx * kTileBytes;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (tok[h] < 0) continue;
-            const int r = g + 64 * h;
-            const uint16_t* src = a.x16p + (size_t)tok[h] * a.d + kc * 64;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) cp_async_16(dst + r * 128 + ((c ^ (r & 7)) << 4), src + c * 8);
-          }
-          cp_async_commit();
-          ++issued;
-          if (issued - arrived > 2) {
-            cp_async_wait<2>();
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(XF(arrived % C::S_X));
-            ++arrived;
-          }
+          if (!mbar_wait_warp(XE(sx), phx ^ 1u, abort_s, a.err)) { ok = false; break; }
+          if (lane == 0) mbar_arrive_expect_tx(XF(sx), (uint32_t)ng * 512u);
+          __syncwarp();
+          if (lane < ng)
+            tma_gather4(sX + sx * kTileBytes + lane * 512, &maps.x, XF(sx), kc * 64, tok[0], tok[1], tok[2], tok[3]);
+          if (++sx == C::S_X) { sx = 0; phx ^= 1u; }
         }
       }
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      __syncwarp();
-      while (arrived < issued) {
-        if (lane == 0) mbar_arrive(XF(arrived % C::S_X));
-        ++arrived;
-      }
     }
+  } else if (warp == 3) {
+    // idle (keeps the dequant warps at 4..11 and the epilogue warps at 12..15)
   } else if (warp < 12) {
     // ------------------------------------------------------------ dequant: 8 warps; thread i
     // handles weight row i % 128 and half i / 128 of every chunk: the gate (0) or up (1) matrix

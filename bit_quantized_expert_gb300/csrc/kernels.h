@@ -43,6 +43,7 @@ struct QPtr {
 struct GemmMaps {
   CUtensorMap codes[2][2];   // [matrix][0 = routed, 1 = shared]
   CUtensorMap h;             // down projection: h [slots, F] fp16
+  CUtensorMap x;             // gate/up projection: x [T, d] fp16 (operand chunk order), 64 x 1 box
 };
 
 struct GemmArgs {
