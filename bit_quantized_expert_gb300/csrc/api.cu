@@ -14,7 +14,7 @@ namespace {
 constexpr int kTileN = 128;   // block-map tile of the layer call (token rows per MMA tile)
 
 struct Layout {
-  size_t err, x16p, gs, idx, w, counts, offsets, perm, inv, tiles, num_tiles, h, yperm, hdec, total;
+  size_t err, xperm, gs, idx, w, counts, offsets, perm, inv, tiles, num_tiles, h, yperm, hdec, total;
 };
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -39,7 +39,7 @@ Layout layout_of(const moe_dims& d) {
   const bool sh = d.F_shared > 0;
   const size_t slots = T * k + (sh ? T : 0);
   L.err = take(256);
-  L.x16p = take(T * D * 2);
+  L.xperm = take(slots * D * 2);
   L.gs = take(T * 4);
   L.idx = take(T * k * 4);
   L.w = take(T * k * 4);
@@ -135,29 +135,16 @@ bool encode_codes(CUtensorMap* m, const uint32_t* codes, int n, int R, int C) {
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// h [slots, F] fp16 with a 64 x 128 box in the 128-byte swizzle (the MMA operand layout).
-bool encode_h(CUtensorMap* m, const uint16_t* h, long long slots, int F) {
+// Row-major fp16 matrix [rows, cols] (h, or x in slot order) with a 64 x 128 box in the 128-byte
+// swizzle (the MMA operand layout).
+bool encode_f16_rows(CUtensorMap* m, const uint16_t* p, long long rows, int cols) {
   EncodeTiledFn f = encode_fn();
   if (!f) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)F, (cuuint64_t)slots};
-  const cuuint64_t strides[1] = {(cuuint64_t)F * 2};
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
   const cuuint32_t box[2] = {64, 128};
   const cuuint32_t es[2] = {1, 1};
-  return f(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(h), dims, strides, box, es,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// x [T, d] fp16 (operand chunk order) for row gathers: a 64 x 1 box (one 128-byte row piece)
-// in the 128-byte swizzle, so four gathered rows land as four rows of the MMA operand tile.
-bool encode_x_rows(CUtensorMap* m, const uint16_t* x16p, long long T, int d) {
-  EncodeTiledFn f = encode_fn();
-  if (!f) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)T};
-  const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
-  const cuuint32_t box[2] = {64, 1};
-  const cuuint32_t es[2] = {1, 1};
-  return f(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(x16p), dims, strides, box, es,
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(p), dims, strides, box, es,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -210,8 +197,8 @@ RoutingPtrs caller_routing(const moe_routing* r) {
 }
 
 cudaError_t run_routing(const moe_dims& d, const float* logits, const RoutingPtrs& R, const uint16_t* x,
-                        const uint16_t* w_sg, uint16_t* x16p, float* gs, uint32_t* err, cudaStream_t st) {
-  RouteArgs ra{logits, d.T, d.E, d.k, d.d, R.idx, R.w, x, w_sg, x16p, gs, err};
+                        const uint16_t* w_sg, float* gs, uint32_t* err, cudaStream_t st) {
+  RouteArgs ra{logits, d.T, d.E, d.k, d.d, R.idx, R.w, x, w_sg, gs, err};
   cudaError_t e = launch_topk(ra, st);
   if (e != cudaSuccess) return e;
   TablesArgs ta{R.idx, d.T, d.E, d.k, R.tile_n, d.F_shared > 0 ? 1 : 0, R.counts, R.offsets, R.perm, R.inv,
@@ -221,9 +208,10 @@ cudaError_t run_routing(const moe_dims& d, const float* logits, const RoutingPtr
 
 QPtr qptr(const moe_qmat& q) { return QPtr{q.codes, q.scales, q.biases}; }
 
-// Gate/up GEMM (h) then down GEMM (y_perm) over the block map in R.
+// x rows in slot order (fp16), gate/up GEMM (h), then down GEMM (y_perm) over the block map in R.
 moe_status run_experts(const moe_dims& d, const RoutingPtrs& R, const moe_experts* routed, const moe_experts* shared,
-                       const uint16_t* x16p, uint16_t* h, float* y_perm, uint32_t* err, cudaStream_t st) {
+                       const uint16_t* x, uint16_t* xperm, uint16_t* h, float* y_perm, uint32_t* err,
+                       cudaStream_t st) {
   const bool sh = shared != nullptr && d.F_shared > 0;
   const long long slots = (long long)d.T * d.k + (sh ? d.T : 0);
   const moe_experts* s_or_r = sh ? shared : routed;
@@ -236,8 +224,10 @@ moe_status run_experts(const moe_dims& d, const RoutingPtrs& R, const moe_expert
             encode_codes(&m0.codes[1][1], s_or_r->up.codes, ns, d.F, d.d) &&
             encode_codes(&m1.codes[0][0], routed->down.codes, d.E, d.d, d.F) &&
             encode_codes(&m1.codes[0][1], s_or_r->down.codes, ns, d.d, d.F) &&
-            encode_h(&m1.h, h, slots, d.F) && encode_x_rows(&m0.x, x16p, d.T, d.d);
+            encode_f16_rows(&m1.h, h, slots, d.F) && encode_f16_rows(&m0.x, xperm, slots, d.d);
   if (!ok) return MOE_ERR_CUDA;
+  PermuteArgs pa{x, R.perm, d.T, d.k, d.d, (int)slots, xperm, err};
+  if (launch_permute_x(pa, st) != cudaSuccess) return MOE_ERR_CUDA;
   m0.h = m1.h;
   m1.codes[1][0] = m1.codes[0][0];
   m1.codes[1][1] = m1.codes[0][1];
@@ -247,7 +237,6 @@ moe_status run_experts(const moe_dims& d, const RoutingPtrs& R, const moe_expert
   a.tiles = R.tiles;
   a.num_tiles = R.num_tiles;
   a.perm = R.perm;
-  a.x16p = x16p;
   a.T = d.T;
   a.k = d.k;
   a.E = d.E;
@@ -314,7 +303,7 @@ moe_status moe_route(const moe_dims* dims, const float* logits, const moe_routin
   if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* err = at<uint32_t>(workspace, L.err);
-  return cuda_status(run_routing(*dims, logits, caller_routing(out), nullptr, nullptr, nullptr, nullptr, err, st));
+  return cuda_status(run_routing(*dims, logits, caller_routing(out), nullptr, nullptr, nullptr, err, st));
 }
 
 moe_status moe_expert_forward(const moe_dims* dims, const uint16_t* x, const moe_routing* routing,
@@ -335,10 +324,8 @@ moe_status moe_expert_forward(const moe_dims* dims, const uint16_t* x, const moe
   if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* err = at<uint32_t>(workspace, L.err);
-  uint16_t* x16p = at<uint16_t>(workspace, L.x16p);
-  ConvertArgs ca{x, x16p, dims->T, dims->d, err};
-  if (launch_convert(ca, st) != cudaSuccess) return MOE_ERR_CUDA;
-  return run_experts(*dims, caller_routing(routing), routed, shared, x16p, at<uint16_t>(workspace, L.h), y_perm, err,
+  return run_experts(*dims, caller_routing(routing), routed, shared, x, at<uint16_t>(workspace, L.xperm),
+                     at<uint16_t>(workspace, L.h), y_perm, err,
                      st);
 }
 
@@ -390,17 +377,17 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
     da.sync = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + L.err + kSyncOffset);
     if (launch_decode(da, st, true) != cudaSuccess) return MOE_ERR_CUDA;
     if (routing_out != nullptr)
-      return cuda_status(run_routing(d, logits, caller_routing(routing_out), nullptr, nullptr, nullptr, nullptr, err, st));
+      return cuda_status(run_routing(d, logits, caller_routing(routing_out), nullptr, nullptr, nullptr, err, st));
     return MOE_OK;
   }
 
   const RoutingPtrs R = routing_out ? caller_routing(routing_out) : internal_routing(workspace, L);
-  uint16_t* x16p = at<uint16_t>(workspace, L.x16p);
+  uint16_t* xperm = at<uint16_t>(workspace, L.xperm);
   float* gs = sh ? at<float>(workspace, L.gs) : nullptr;
-  cudaError_t e = run_routing(d, logits, R, x, sh ? w_shared_gate : nullptr, x16p, gs, err, st);
+  cudaError_t e = run_routing(d, logits, R, x, sh ? w_shared_gate : nullptr, gs, err, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   float* yperm = at<float>(workspace, L.yperm);
-  s = run_experts(d, R, routed, sh ? shared : nullptr, x16p, at<uint16_t>(workspace, L.h), yperm, err, st);
+  s = run_experts(d, R, routed, sh ? shared : nullptr, x, xperm, at<uint16_t>(workspace, L.h), yperm, err, st);
   if (s != MOE_OK) return s;
   CombineArgs cb{yperm, R.inv, R.w, gs, d.T, d.k, d.d, y};
   return cuda_status(launch_combine(cb, st));

@@ -12,10 +12,9 @@
 //   * Work unit = (block-map tile of <= 128 slots of one expert, 128-row slice of the weight
 //     matrix), iterated over K in chunks of 64 (= one quantisation group).  A persistent grid of
 //     one CTA per SM walks the units; every role walks the same list.
-//   * Warp roles (16 warps): 0 = TMA producer (packed codes; the h operand of the down
-//     projection), 1 = MMA issuer (one thread) and TMEM owner, 2 = row gather of x for the
-//     gate/up projection (TMA gather4: four token rows per instruction into the swizzled operand
-//     layout), 3 = idle, 4-11 = dequant
+//   * Warp roles (16 warps): 0 = TMA producer (packed codes, and the activation tiles of both
+//     projections: x rows in slot order, or h), 1 = MMA issuer (one thread) and TMEM owner,
+//     2-3 = idle, 4-11 = dequant
 //     (two threads per weight row: 4-bit codes -> fp16 w = q*scale + bias, single rounding; two
 //     dequant warps per scheduler so one hides the other's shared-memory and barrier latency),
 //     12-15 = epilogue (TMEM -> registers; SwiGLU -> fp16 h, or fp32 expert outputs).
@@ -194,12 +193,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           for (int mat = 0; mat < NMAT; ++mat)
             tma_load_3d(sRaw + (s * NMAT + mat) * kRawBytes, &maps.codes[mat][which], RF(s), kc * 8, m * kBM, ec);
           if (++s == C::S_RAW) { s = 0; ph ^= 1u; }
-          if (MODE == 1) {
-            if (!mbar_wait(XE(sx), phx ^ 1u, abort_s, a.err)) { ok = false; break; }
-            mbar_arrive_expect_tx(XF(sx), kTileBytes);
-            tma_load_2d(sX + sx * kTileBytes, &maps.h, XF(sx), kc * 64, tl.y);
-            if (++sx == C::S_X) { sx = 0; phx ^= 1u; }
-          }
+          // activation tile: 128 slot rows x 64 columns (x in slot order, or h); rows past the
+          // tile's end belong to the next tile or lie outside the tensor (zero-filled), and the
+          // MMA columns they feed are never stored
+          if (!mbar_wait(XE(sx), phx ^ 1u, abort_s, a.err)) { ok = false; break; }
+          mbar_arrive_expect_tx(XF(sx), kTileBytes);
+          tma_load_2d(sX + sx * kTileBytes, MODE == 0 ? &maps.x : &maps.h, XF(sx), kc * 64, tl.y);
+          if (++sx == C::S_X) { sx = 0; phx ^= 1u; }
         }
         if (!ok) break;
       }
@@ -245,49 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         tc_commit(AF(b));
       }
     }
-  } else if (warp == 2) {
-    // ------------------------------------------------------------ x row gather (gate/up)
-    // Lane l fetches tile rows 4l .. 4l+3 of every K chunk with one TMA gather4 (four token rows
-    // of 64 fp16 -> four 128-byte rows of the swizzled operand tile).  Rows past the tile's end
-    // repeat the lane's first row; the MMA columns they feed are never stored.
-    if (MODE == 0) {
-      auto tokens_of = [&](const int4& t, int (&tk)[4]) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = min(4 * lane + i, t.z - 1);
-          tk[i] = r < 0 ? 0 : (t.x == a.E) ? (t.y + r - a.T * a.k) : (__ldg(a.perm + t.y + r) / a.k);
-        }
-        if (4 * lane >= t.z) tk[0] = tk[1] = tk[2] = tk[3] = 0;
-        if (4 * lane < t.z) {
-#pragma unroll
-          for (int i = 1; i < 4; ++i)
-            if (4 * lane + i >= t.z) tk[i] = tk[0];
-        }
-      };
-      int sx = 0;
-      uint32_t phx = 0;
-      bool ok = true;
-      int4 tl_next = tile_of(blockIdx.x);
-      int tok_next[4];
-      tokens_of(tl_next, tok_next);
-      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const int4 tl = tl_next;
-        const int tok[4] = {tok_next[0], tok_next[1], tok_next[2], tok_next[3]};
-        tl_next = tile_of(u + gridDim.x);
-        tokens_of(tl_next, tok_next);
-        const int ng = (tl.z + 3) / 4;   // gather4 groups of this tile
-        for (int kc = 0; kc < KC; ++kc) {
-          if (!mbar_wait_warp(XE(sx), phx ^ 1u, abort_s, a.err)) { ok = false; break; }
-          if (lane == 0) mbar_arrive_expect_tx(XF(sx), (uint32_t)ng * 512u);
-          __syncwarp();
-          if (lane < ng)
-            tma_gather4(sX + sx * kTileBytes + lane * 512, &maps.x, XF(sx), kc * 64, tok[0], tok[1], tok[2], tok[3]);
-          if (++sx == C::S_X) { sx = 0; phx ^= 1u; }
-        }
-      }
-    }
-  } else if (warp == 3) {
-    // idle (keeps the dequant warps at 4..11 and the epilogue warps at 12..15)
+  } else if (warp < 4) {
+    // warps 2-3 idle (keeps the dequant warps at 4..11 and the epilogue warps at 12..15)
   } else if (warp < 12) {
     // ------------------------------------------------------------ dequant: 8 warps; thread i
     // handles weight row i % 128 and half i / 128 of every chunk: the gate (0) or up (1) matrix
@@ -480,27 +439,38 @@ __global__ void combine_kernel(CombineArgs a) {
   }
 }
 
-__global__ void convert_kernel(ConvertArgs a) {
-  const size_t nch = (size_t)a.T * a.d / 8;
+// Row s of the gate/up activation operand: x of the token routed to slot s (slots below T*k
+// through the permutation, the shared expert's slots T*k + t are token t), converted to fp16 in
+// the operand chunk order.  Writing the rows in slot order lets the GEMM fetch every activation
+// tile with one TMA box load.
+__global__ void __launch_bounds__(256) permute_x_kernel(PermuteArgs a) {
+  const int nch = a.d / 8;
+  const int Tk = a.T * a.k;
   bool bad = false;
-  for (size_t ch = (size_t)blockIdx.x * blockDim.x + threadIdx.x; ch < nch; ch += (size_t)gridDim.x * blockDim.x) {
-    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.x) + ch);
-    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-    float xf[8];
+  for (int s = blockIdx.x; s < a.slots; s += gridDim.x) {
+    const int t = s < Tk ? __ldg(a.perm + s) / a.k : s - Tk;
+    const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)t * a.d);
+    uint4* out = reinterpret_cast<uint4*>(a.xperm + (size_t)s * a.d);
+    for (int ch = threadIdx.x; ch < nch; ch += blockDim.x) {
+      const uint4 xv = __ldg(xr + ch);
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+      float xf[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      xf[2 * i] = bf16_bits_to_f32(xw[i] & 0xFFFFu);
-      xf[2 * i + 1] = bf16_bits_to_f32(xw[i] >> 16);
-    }
-    uint32_t o[4];
+      for (int i = 0; i < 4; ++i) {
+        xf[2 * i] = bf16_bits_to_f32(xw[i] & 0xFFFFu);
+        xf[2 * i + 1] = bf16_bits_to_f32(xw[i] >> 16);
+      }
+      // stored order (0,4,1,5,2,6,3,7): word p holds logical elements (p, p+4)
+      uint32_t o[4];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      const __half lo = __float2half_rn(xf[p]);
-      const __half hi = __float2half_rn(xf[p + 4]);
-      bad = bad || (__hisinf(lo) != 0) || (__hisinf(hi) != 0);
-      o[p] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+      for (int p = 0; p < 4; ++p) {
+        const __half lo = __float2half_rn(xf[p]);
+        const __half hi = __float2half_rn(xf[p + 4]);
+        bad = bad || (__hisinf(lo) != 0) || (__hisinf(hi) != 0);
+        o[p] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+      }
+      out[ch] = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    reinterpret_cast<uint4*>(a.x16p)[ch] = make_uint4(o[0], o[1], o[2], o[3]);
   }
   if (bad) raise_flag(a.err, kErrFp16Range);
 }
@@ -531,10 +501,10 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_convert(const ConvertArgs& a, cudaStream_t st) {
-  const size_t nch = (size_t)a.T * a.d / 8;
-  const int blocks = (int)((nch + 255) / 256 < 4096 ? (nch + 255) / 256 : 4096);
-  convert_kernel<<<blocks, 256, 0, st>>>(a);
+cudaError_t launch_permute_x(const PermuteArgs& a, cudaStream_t st) {
+  if (a.slots <= 0) return cudaSuccess;
+  const int grid = a.slots < 152 * 16 ? a.slots : 152 * 16;
+  permute_x_kernel<<<grid, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 

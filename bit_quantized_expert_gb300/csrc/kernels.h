@@ -16,7 +16,6 @@ struct RouteArgs {
   float* w;              // [T, k]
   const uint16_t* x;     // bf16 [T, d] or null (no fp16 copy / gate)
   const uint16_t* w_sg;  // bf16 [d] or null
-  uint16_t* x16p;        // fp16 [T, d] in operand chunk order, or null
   float* gs;             // [T] shared gate, or null
   uint32_t* err;
 };
@@ -43,14 +42,13 @@ struct QPtr {
 struct GemmMaps {
   CUtensorMap codes[2][2];   // [matrix][0 = routed, 1 = shared]
   CUtensorMap h;             // down projection: h [slots, F] fp16
-  CUtensorMap x;             // gate/up projection: x [T, d] fp16 (operand chunk order), 64 x 1 box
+  CUtensorMap x;             // gate/up projection: x rows in slot order [slots, d] fp16
 };
 
 struct GemmArgs {
   const int32_t* tiles;      // block map rows (e, row0, rows, 0)
   const int32_t* num_tiles;
   const int32_t* perm;       // slot -> assignment (gate/up gathers x rows)
-  const uint16_t* x16p;      // fp16 [T, d] operand copy of x (gate/up)
   QPtr mat[2][2];            // [matrix][routed/shared]: scales and biases read by the dequant warps
   int T, k, E, d, F;
   uint16_t* h;               // gate/up output: fp16 [slots, F], operand chunk order
@@ -70,13 +68,14 @@ struct CombineArgs {
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
 
-struct ConvertArgs {
+struct PermuteArgs {
   const uint16_t* x;      // bf16 [T, d]
-  uint16_t* x16p;         // fp16 [T, d] operand chunk order
-  int T, d;
+  const int32_t* perm;    // [T*k] slot -> assignment t*k + j
+  int T, k, d, slots;     // slots = T*k (+ T with a shared expert)
+  uint16_t* xperm;        // fp16 [slots, d] operand chunk order: row s = x[token(s)]
   uint32_t* err;
 };
-cudaError_t launch_convert(const ConvertArgs& a, cudaStream_t st);
+cudaError_t launch_permute_x(const PermuteArgs& a, cudaStream_t st);
 
 // ---------------------------------------------------------------- decode T = 1 (decode.cu)
 struct DecodeArgs {

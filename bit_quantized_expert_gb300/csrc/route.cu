@@ -5,8 +5,7 @@
 // histogram, prefix scan, scatter and block map stay in one GPU command stream).
 //
 // Kernel 1 (one warp per token): top-k over fp32 logits with ties to the lower expert index,
-// softmax over the selected logits, and two by-products of reading the token once: the shared
-// expert gate sigmoid(x . w_sg) and the fp16 copy of x in the tensor-core operand order.
+// softmax over the selected logits, and the shared expert gate sigmoid(x . w_sg).
 // Kernel 2 (one CTA): per-expert counts, exclusive offsets, a permutation sorted by
 // (expert, token) that depends only on the counts (never on atomic arrival order), its
 // inverse and the tile block map.
@@ -29,50 +28,23 @@ __global__ void __launch_bounds__(256) topk_kernel(RouteArgs a) {
     a.w[(size_t)t * a.k + lane] = my_w;
   }
 
-  // One pass over the token row: shared-expert gate logit and the fp16 operand copy of x.
-  if (a.x != nullptr && (a.x16p != nullptr || a.gs != nullptr)) {
+  // Shared-expert gate logit x . w_sg (one pass over the token row).
+  if (a.x != nullptr && a.gs != nullptr && a.w_sg != nullptr) {
     const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)t * a.d);
     const uint4* wr = reinterpret_cast<const uint4*>(a.w_sg);
-    uint4* outr = a.x16p ? reinterpret_cast<uint4*>(a.x16p + (size_t)t * a.d) : nullptr;
     float dot = 0.0f;
-    bool bad = false;
     for (int ch = lane; ch < a.d / 8; ch += 32) {
-      const uint4 xv = __ldg(xr + ch);
-      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-      float xf[8];
+      const uint4 xv = __ldg(xr + ch), wv = __ldg(wr + ch);
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        xf[2 * i] = bf16_bits_to_f32(xw[i] & 0xFFFFu);
-        xf[2 * i + 1] = bf16_bits_to_f32(xw[i] >> 16);
-      }
-      if (a.gs != nullptr && wr != nullptr) {
-        const uint4 wv = __ldg(wr + ch);
-        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          dot = fmaf(xf[2 * i], bf16_bits_to_f32(ww[i] & 0xFFFFu), dot);
-          dot = fmaf(xf[2 * i + 1], bf16_bits_to_f32(ww[i] >> 16), dot);
-        }
-      }
-      if (outr != nullptr) {
-        // stored order (0,4,1,5,2,6,3,7): word p holds logical elements (p, p+4)
-        uint32_t o[4];
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const __half lo = __float2half_rn(xf[p]);
-          const __half hi = __float2half_rn(xf[p + 4]);
-          bad = bad || (__hisinf(lo) != 0) || (__hisinf(hi) != 0);
-          o[p] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
-        }
-        outr[ch] = make_uint4(o[0], o[1], o[2], o[3]);
+        dot = fmaf(bf16_bits_to_f32(xw[i] & 0xFFFFu), bf16_bits_to_f32(ww[i] & 0xFFFFu), dot);
+        dot = fmaf(bf16_bits_to_f32(xw[i] >> 16), bf16_bits_to_f32(ww[i] >> 16), dot);
       }
     }
-    if (a.gs != nullptr && wr != nullptr) {
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, off);
-      if (lane == 0) a.gs[t] = 1.0f / (1.0f + expf(-dot));
-    }
-    if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) raise_flag(a.err, kErrFp16Range);
+    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, off);
+    if (lane == 0) a.gs[t] = 1.0f / (1.0f + expf(-dot));
   }
 }
 
