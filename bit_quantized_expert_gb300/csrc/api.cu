@@ -50,7 +50,7 @@ Layout layout_of(const moe_dims& d) {
   L.tiles = take(max_tiles_of(d.T, d.k, d.E, kTileN, sh) * 16);
   L.num_tiles = take(16);
   L.h = take(slots * F * 2);
-  L.yperm = take(slots * D * 4);
+  L.yperm = take(slots * D * 2);   // fp16 expert outputs of the layer path
   L.hdec = take(T == 1 ? decode_scratch_floats((int)D, (int)k, (int)F) * 4 : 0);   // decode partials
   L.total = o;
   return L;
@@ -208,10 +208,11 @@ cudaError_t run_routing(const moe_dims& d, const float* logits, const RoutingPtr
 
 QPtr qptr(const moe_qmat& q) { return QPtr{q.codes, q.scales, q.biases}; }
 
-// x rows in slot order (fp16), gate/up GEMM (h), then down GEMM (y_perm) over the block map in R.
+// x rows in slot order (fp16), gate/up GEMM (h), then down GEMM (expert outputs: fp32 y_perm, or
+// fp16 y16 when y16 is non-null) over the block map in R.
 moe_status run_experts(const moe_dims& d, const RoutingPtrs& R, const moe_experts* routed, const moe_experts* shared,
-                       const uint16_t* x, uint16_t* xperm, uint16_t* h, float* y_perm, uint32_t* err,
-                       cudaStream_t st) {
+                       const uint16_t* x, uint16_t* xperm, uint16_t* h, float* y_perm, uint16_t* y16,
+                       uint32_t* err, cudaStream_t st) {
   const bool sh = shared != nullptr && d.F_shared > 0;
   const long long slots = (long long)d.T * d.k + (sh ? d.T : 0);
   const moe_experts* s_or_r = sh ? shared : routed;
@@ -244,6 +245,7 @@ moe_status run_experts(const moe_dims& d, const RoutingPtrs& R, const moe_expert
   a.F = d.F;
   a.h = h;
   a.y_perm = y_perm;
+  a.y16 = y16;
   a.err = err;
   a.mat[0][0] = qptr(routed->gate);
   a.mat[0][1] = qptr(s_or_r->gate);
@@ -325,8 +327,7 @@ moe_status moe_expert_forward(const moe_dims* dims, const uint16_t* x, const moe
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* err = at<uint32_t>(workspace, L.err);
   return run_experts(*dims, caller_routing(routing), routed, shared, x, at<uint16_t>(workspace, L.xperm),
-                     at<uint16_t>(workspace, L.h), y_perm, err,
-                     st);
+                     at<uint16_t>(workspace, L.h), y_perm, nullptr, err, st);
 }
 
 moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const float* logits, const moe_experts* routed,
@@ -386,10 +387,11 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
   float* gs = sh ? at<float>(workspace, L.gs) : nullptr;
   cudaError_t e = run_routing(d, logits, R, x, sh ? w_shared_gate : nullptr, gs, err, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  float* yperm = at<float>(workspace, L.yperm);
-  s = run_experts(d, R, routed, sh ? shared : nullptr, x, xperm, at<uint16_t>(workspace, L.h), yperm, err, st);
+  uint16_t* y16 = at<uint16_t>(workspace, L.yperm);
+  s = run_experts(d, R, routed, sh ? shared : nullptr, x, xperm, at<uint16_t>(workspace, L.h), nullptr, y16, err,
+                  st);
   if (s != MOE_OK) return s;
-  CombineArgs cb{yperm, R.inv, R.w, gs, d.T, d.k, d.d, y};
+  CombineArgs cb{nullptr, y16, R.inv, R.w, gs, d.T, d.k, d.d, y};
   return cuda_status(launch_combine(cb, st));
 }
 

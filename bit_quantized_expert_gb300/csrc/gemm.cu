@@ -48,7 +48,8 @@ struct Cfg {
   static constexpr uint32_t OFF_RAW = OFF_X + S_X * kTileBytes;
   static constexpr uint32_t OFF_BAR = OFF_RAW + S_RAW * NMAT * kRawBytes;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
+  static constexpr uint32_t OFF_STG = (OFF_MISC + 16 + 15) & ~15u;   // epilogue staging, 2 KB per warp
+  static constexpr uint32_t BYTES = OFF_STG + 4 * 2048 + 1024;        // + alignment slack
   static constexpr uint32_t ACC_COLS = NMAT * 128;          // TMEM columns of one accumulator buffer
 };
 
@@ -63,6 +64,12 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                : "r"(addr)
                : "memory");
   return v;
+}
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 v;
@@ -227,14 +234,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             break;
           }
           tc_fence_after();
+          // Descriptors of the stage's tiles; each 16-element K step advances the start address
+          // by 32 bytes (2 in the descriptor's address field, which cannot carry: stages lie
+          // below 256 KB).
+          const uint64_t bdesc0 = smem_desc_sw128(sX + sx * kTileBytes);
+          uint64_t adesc0[NMAT];
+#pragma unroll
+          for (int mat = 0; mat < NMAT; ++mat) adesc0[mat] = smem_desc_sw128(sW + (sw * NMAT + mat) * kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bdesc = smem_desc_sw128(sX + sx * kTileBytes + kk * 32);
 #pragma unroll
-            for (int mat = 0; mat < NMAT; ++mat) {
-              const uint64_t adesc = smem_desc_sw128(sW + (sw * NMAT + mat) * kTileBytes + kk * 32);
-              tc_mma_f16(d0 + mat * 128, adesc, bdesc, idesc, (kc | kk) != 0 ? 1u : 0u);
-            }
+            for (int mat = 0; mat < NMAT; ++mat)
+              tc_mma_f16(d0 + mat * 128, adesc0[mat] + 2u * kk, bdesc0 + 2u * kk, idesc, (kc | kk) != 0 ? 1u : 0u);
           }
           tc_commit(WE(sw));
           tc_commit(XE(sx));
@@ -351,6 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;   // TMEM lane quarter this warp may access
+    const uint32_t stg = sbase + C::OFF_STG + (uint32_t)q * 2048u;
     int li = 0;
     bool bad = false;
     int4 tl_next = tile_of(blockIdx.x);
@@ -363,30 +375,65 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       tc_fence_after();
       const int rowg = m * kBM + q * 32 + lane;
       const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::ACC_COLS);
+      // Per 16-token block: TMEM -> registers -> this warp's staging buffer ([token][32 rows]) ->
+      // 16-byte stores of each token's 32 contiguous output columns.
+      const int col0 = m * kBM + q * 32;   // first output column of this warp's rows
       for (int n0 = 0; n0 < tl.z; n0 += 16) {
         uint32_t g[16];
         if (MODE == 0) {
           uint32_t uu[16];
           tmem_ld16x2_wait(tb + n0, tb + 128 + n0, g, uu);
-          const int col = (rowg & ~7) | chunk_pos(rowg & 7);
+          const int pos = (lane & ~7) | chunk_pos(lane & 7);   // stored operand order of h
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const int n = n0 + i;
-            if (n < tl.z) {
-              const float gv = __uint_as_float(g[i]);
-              const float hv = gv / (1.0f + __expf(-gv)) * __uint_as_float(uu[i]);
-              const __half hh = __float2half_rn(hv);
-              bad = bad || (__hisinf(hh) != 0);
-              reinterpret_cast<__half*>(a.h)[(size_t)(tl.y + n) * a.F + col] = hh;
+            const float gv = __uint_as_float(g[i]);
+            const float hv = gv * __frcp_rn(1.0f + __expf(-gv)) * __uint_as_float(uu[i]);
+            const __half hh = __float2half_rn(hv);
+            if (n0 + i < tl.z) bad = bad || (__hisinf(hh) != 0);
+            st_shared_u16(stg + (uint32_t)(i * 32 + pos) * 2, __half_as_ushort(hh));
+          }
+          __syncwarp();
+#pragma unroll
+          for (int c = lane; c < 64; c += 32) {
+            const int n = c >> 2, p = c & 3;
+            if (n0 + n < tl.z) {
+              const uint4 v = ld_shared_v4(stg + (uint32_t)(n * 32 + p * 8) * 2);
+              *reinterpret_cast<uint4*>(a.h + (size_t)(tl.y + n0 + n) * a.F + col0 + p * 8) = v;
             }
           }
-        } else {
+          __syncwarp();
+        } else if (a.y16 != nullptr) {
           tmem_ld16_wait(tb + n0, g);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const int n = n0 + i;
-            if (n < tl.z) a.y_perm[(size_t)(tl.y + n) * a.d + rowg] = __uint_as_float(g[i]);
+            const __half yh = __float2half_rn(__uint_as_float(g[i]));
+            if (n0 + i < tl.z) bad = bad || (__hisinf(yh) != 0);
+            st_shared_u16(stg + (uint32_t)(i * 32 + lane) * 2, __half_as_ushort(yh));
           }
+          __syncwarp();
+#pragma unroll
+          for (int c = lane; c < 64; c += 32) {
+            const int n = c >> 2, p = c & 3;
+            if (n0 + n < tl.z) {
+              const uint4 v = ld_shared_v4(stg + (uint32_t)(n * 32 + p * 8) * 2);
+              *reinterpret_cast<uint4*>(a.y16 + (size_t)(tl.y + n0 + n) * a.d + col0 + p * 8) = v;
+            }
+          }
+          __syncwarp();
+        } else {
+          tmem_ld16_wait(tb + n0, g);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) st_shared_u32(stg + (uint32_t)(i * 32 + lane) * 4, g[i]);
+          __syncwarp();
+#pragma unroll
+          for (int c = lane; c < 128; c += 32) {
+            const int n = c >> 3, p = c & 7;
+            if (n0 + n < tl.z) {
+              const uint4 v = ld_shared_v4(stg + (uint32_t)(n * 32 + p * 4) * 4);
+              *reinterpret_cast<uint4*>(a.y_perm + (size_t)(tl.y + n0 + n) * a.d + col0 + p * 4) = v;
+            }
+          }
+          __syncwarp();
         }
       }
       tc_fence_before();
@@ -411,31 +458,44 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   }
 }
 
+// y[t] = sum_j w[t,j] Y[inv[t,j]] + gs[t] Y[T*k + t], fp32 accumulation in j order.  Y is read as
+// fp16 (the layer path) or fp32 (expert outputs handed in by a caller), 8 or 4 values per load.
+template <bool HALF>
 __global__ void combine_kernel(CombineArgs a) {
+  constexpr int V = HALF ? 8 : 4;
   const int t = blockIdx.x;
-  const int d4 = a.d / 4;
-  const float4* yp = reinterpret_cast<const float4*>(a.y_perm);
-  float4* y = reinterpret_cast<float4*>(a.y);
-  for (int c = threadIdx.x; c < d4; c += blockDim.x) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < a.k; ++j) {
-      const int p = __ldg(a.inv + (size_t)t * a.k + j);
-      const float wv = __ldg(a.w + (size_t)t * a.k + j);
-      const float4 v = __ldg(yp + (size_t)p * d4 + c);
-      acc.x = fmaf(wv, v.x, acc.x);
-      acc.y = fmaf(wv, v.y, acc.y);
-      acc.z = fmaf(wv, v.z, acc.z);
-      acc.w = fmaf(wv, v.w, acc.w);
-    }
-    if (a.gs != nullptr) {
-      const float gv = __ldg(a.gs + t);
-      const float4 v = __ldg(yp + ((size_t)a.T * a.k + t) * d4 + c);
-      acc.x = fmaf(gv, v.x, acc.x);
-      acc.y = fmaf(gv, v.y, acc.y);
-      acc.z = fmaf(gv, v.z, acc.z);
-      acc.w = fmaf(gv, v.w, acc.w);
-    }
-    y[(size_t)t * d4 + c] = acc;
+  const int nv = a.d / V;
+  for (int c = threadIdx.x; c < nv; c += blockDim.x) {
+    float acc[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = 0.0f;
+    auto add_row = [&](size_t row, float wv) {
+      float v[V];
+      if (HALF) {
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(a.y16 + row * a.d) + c);
+        const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&qw[i]));
+          v[2 * i] = f.x;
+          v[2 * i + 1] = f.y;
+        }
+      } else {
+        const float4 q = __ldg(reinterpret_cast<const float4*>(a.y_perm + row * a.d) + c);
+        v[0] = q.x;
+        v[1] = q.y;
+        v[2 % V] = q.z;
+        v[3 % V] = q.w;
+      }
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] = fmaf(wv, v[i], acc[i]);
+    };
+    for (int j = 0; j < a.k; ++j)
+      add_row((size_t)__ldg(a.inv + (size_t)t * a.k + j), __ldg(a.w + (size_t)t * a.k + j));
+    if (a.gs != nullptr) add_row((size_t)a.T * a.k + t, __ldg(a.gs + t));
+    float4* yo = reinterpret_cast<float4*>(a.y + (size_t)t * a.d + (size_t)c * V);
+    yo[0] = make_float4(acc[0], acc[1], acc[2 % V], acc[3 % V]);
+    if (HALF) yo[1] = make_float4(acc[4 % V], acc[5 % V], acc[6 % V], acc[7 % V]);
   }
 }
 
@@ -443,33 +503,46 @@ __global__ void combine_kernel(CombineArgs a) {
 // through the permutation, the shared expert's slots T*k + t are token t), converted to fp16 in
 // the operand chunk order.  Writing the rows in slot order lets the GEMM fetch every activation
 // tile with one TMA box load.
+constexpr int kPermRows = 8;   // rows per CTA step: eight independent loads in flight per thread
+
 __global__ void __launch_bounds__(256) permute_x_kernel(PermuteArgs a) {
   const int nch = a.d / 8;
   const int Tk = a.T * a.k;
   bool bad = false;
-  for (int s = blockIdx.x; s < a.slots; s += gridDim.x) {
-    const int t = s < Tk ? __ldg(a.perm + s) / a.k : s - Tk;
-    const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)t * a.d);
-    uint4* out = reinterpret_cast<uint4*>(a.xperm + (size_t)s * a.d);
+  for (int s0 = blockIdx.x * kPermRows; s0 < a.slots; s0 += gridDim.x * kPermRows) {
+    int tok[kPermRows];
+#pragma unroll
+    for (int i = 0; i < kPermRows; ++i) {
+      const int s = s0 + i;
+      tok[i] = s >= a.slots ? -1 : s < Tk ? __ldg(a.perm + s) / a.k : s - Tk;
+    }
     for (int ch = threadIdx.x; ch < nch; ch += blockDim.x) {
-      const uint4 xv = __ldg(xr + ch);
-      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-      float xf[8];
+      uint4 xv[kPermRows];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        xf[2 * i] = bf16_bits_to_f32(xw[i] & 0xFFFFu);
-        xf[2 * i + 1] = bf16_bits_to_f32(xw[i] >> 16);
-      }
-      // stored order (0,4,1,5,2,6,3,7): word p holds logical elements (p, p+4)
-      uint32_t o[4];
+      for (int i = 0; i < kPermRows; ++i)
+        xv[i] = tok[i] >= 0 ? __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)tok[i] * a.d) + ch)
+                            : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const __half lo = __float2half_rn(xf[p]);
-        const __half hi = __float2half_rn(xf[p + 4]);
-        bad = bad || (__hisinf(lo) != 0) || (__hisinf(hi) != 0);
-        o[p] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+      for (int i = 0; i < kPermRows; ++i) {
+        if (tok[i] < 0) continue;
+        const uint32_t xw[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+        float xf[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          xf[2 * e] = bf16_bits_to_f32(xw[e] & 0xFFFFu);
+          xf[2 * e + 1] = bf16_bits_to_f32(xw[e] >> 16);
+        }
+        // stored order (0,4,1,5,2,6,3,7): word p holds logical elements (p, p+4)
+        uint32_t o[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const __half lo = __float2half_rn(xf[p]);
+          const __half hi = __float2half_rn(xf[p + 4]);
+          bad = bad || (__hisinf(lo) != 0) || (__hisinf(hi) != 0);
+          o[p] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+        }
+        reinterpret_cast<uint4*>(a.xperm + (size_t)(s0 + i) * a.d)[ch] = make_uint4(o[0], o[1], o[2], o[3]);
       }
-      out[ch] = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
   if (bad) raise_flag(a.err, kErrFp16Range);
@@ -497,13 +570,15 @@ cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmArgs& a, int g
 }
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
-  combine_kernel<<<a.T, 256, 0, st>>>(a);
+  if (a.y16 != nullptr) combine_kernel<true><<<a.T, 256, 0, st>>>(a);
+  else combine_kernel<false><<<a.T, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_permute_x(const PermuteArgs& a, cudaStream_t st) {
   if (a.slots <= 0) return cudaSuccess;
-  const int grid = a.slots < 152 * 16 ? a.slots : 152 * 16;
+  const int steps = (a.slots + kPermRows - 1) / kPermRows;
+  const int grid = steps < 152 * 8 ? steps : 152 * 8;
   permute_x_kernel<<<grid, 256, 0, st>>>(a);
   return cudaGetLastError();
 }

@@ -52,14 +52,16 @@ struct GemmArgs {
   QPtr mat[2][2];            // [matrix][routed/shared]: scales and biases read by the dequant warps
   int T, k, E, d, F;
   uint16_t* h;               // gate/up output: fp16 [slots, F], operand chunk order
-  float* y_perm;             // down output: fp32 [slots, d]
+  float* y_perm;             // down output: fp32 [slots, d] (when y16 is null)
+  uint16_t* y16;             // down output: fp16 [slots, d], or null
   uint32_t* err;
 };
 size_t gemm_smem_bytes(int mode);
 cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmArgs& a, int grid, cudaStream_t st);
 
 struct CombineArgs {
-  const float* y_perm;    // [T*k + T, d]
+  const float* y_perm;    // [T*k + T, d] fp32, or null
+  const uint16_t* y16;    // [T*k + T, d] fp16 (used when non-null)
   const int32_t* inv;     // [T*k]
   const float* w;         // [T, k]
   const float* gs;        // [T] or null (no shared expert)

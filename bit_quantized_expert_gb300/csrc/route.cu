@@ -80,18 +80,21 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* total)
 __host__ __device__ constexpr int tok_warps(int E) { return (96 * 1024) / (8 * E) >= 32 ? 32 : (96 * 1024) / (8 * E); }
 
 // The k expert ids of token t, loaded together (independent loads, one latency); -1 past T or k.
+template <int KMAX>
 __device__ __forceinline__ void load_token_ids(const int32_t* __restrict__ idx, int t, int T, int k, int E,
-                                               int (&ev)[32], uint32_t* err) {
+                                               int (&ev)[KMAX], uint32_t* err) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) ev[j] = (j < k && t < T) ? __ldg(idx + (size_t)t * k + j) : -1;
+  for (int j = 0; j < KMAX; ++j) ev[j] = (j < k && t < T) ? __ldg(idx + (size_t)t * k + j) : -1;
 #pragma unroll
-  for (int j = 0; j < 32; ++j)
+  for (int j = 0; j < KMAX; ++j)
     if (j < k && t < T && (unsigned)ev[j] >= (unsigned)E) {
       raise_flag(err, kErrBadRouting);
       ev[j] = -1;
     }
 }
 
+// KMAX: upper bound on k held in registers per token (8 or 32).
+template <int KMAX>
 __global__ void __launch_bounds__(1024, 1) tables_kernel(TablesArgs a) {
   extern __shared__ int tsm[];
   const int kTokWarps = tok_warps(a.E);
@@ -116,11 +119,17 @@ __global__ void __launch_bounds__(1024, 1) tables_kernel(TablesArgs a) {
   if (warp < kTokWarps) {
     int* hw = base + warp * E;
     for (int c = c_lo; c < c_hi; ++c) {
-      int ev[32];
-      load_token_ids(a.idx, c * 32 + lane, T, k, E, ev, a.err);
+      int ev[KMAX];
+      load_token_ids<KMAX>(a.idx, c * 32 + lane, T, k, E, ev, a.err);
+      // lanes routing to the same expert in round j add their count once (hot experts would
+      // otherwise serialise 32 atomics on one word)
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (ev[j] >= 0) atomicAdd(&hw[ev[j]], 1);
+      for (int j = 0; j < KMAX; ++j) {
+        if (j < k) {
+          const uint32_t m = __match_any_sync(0xFFFFFFFFu, ev[j]);
+          if (ev[j] >= 0 && lane == __ffs(m) - 1) atomicAdd(&hw[ev[j]], __popc(m));
+        }
+      }
     }
   }
   __syncthreads();
@@ -176,14 +185,18 @@ __global__ void __launch_bounds__(1024, 1) tables_kernel(TablesArgs a) {
     const uint32_t lt = (1u << lane) - 1u;
     for (int c = c_lo; c < c_hi; ++c) {
       const int t = c * 32 + lane;
-      int ev[32];
-      load_token_ids(a.idx, t, T, k, E, ev, nullptr);
+      int ev[KMAX];
+      load_token_ids<KMAX>(a.idx, t, T, k, E, ev, nullptr);
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (ev[j] >= 0) atomicOr(&mk[ev[j]], 1u << lane);
+      for (int j = 0; j < KMAX; ++j) {
+        if (j < k) {
+          const uint32_t m = __match_any_sync(0xFFFFFFFFu, ev[j]);
+          if (ev[j] >= 0 && lane == __ffs(m) - 1) atomicOr(&mk[ev[j]], m);
+        }
+      }
       __syncwarp();
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
+      for (int j = 0; j < KMAX; ++j)
         if (ev[j] >= 0) {
           const uint32_t m = mk[ev[j]];
           const int slot = run[ev[j]] + __popc(m & lt);
@@ -192,14 +205,14 @@ __global__ void __launch_bounds__(1024, 1) tables_kernel(TablesArgs a) {
         }
       __syncwarp();
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
+      for (int j = 0; j < KMAX; ++j)
         if (ev[j] >= 0) {
           const uint32_t m = mk[ev[j]];
           if (lane == 31 - __clz(m)) run[ev[j]] += __popc(m);   // last token of the chunk for e
         }
       __syncwarp();
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
+      for (int j = 0; j < KMAX; ++j)
         if (ev[j] >= 0) mk[ev[j]] = 0u;
       __syncwarp();
     }
@@ -227,12 +240,15 @@ cudaError_t launch_tables(const TablesArgs& a, cudaStream_t st) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(tables_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(tables_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)(96 * 1024));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tables_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(96 * 1024));
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
-  tables_kernel<<<1, 1024, smem, st>>>(a);
+  if (a.k <= 8) tables_kernel<8><<<1, 1024, smem, st>>>(a);
+  else tables_kernel<32><<<1, 1024, smem, st>>>(a);
   return cudaGetLastError();
 }
 

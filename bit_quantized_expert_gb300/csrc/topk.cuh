@@ -63,4 +63,72 @@ __device__ __forceinline__ void warp_topk_softmax(const float* __restrict__ row,
   *w_out = ex / s;
 }
 
+
+// E <= 256 variant with shorter rounds: every lane first sorts its 8 candidates (a 19-comparator
+// sorting network on (key, lower index first)), so a round only compares the lanes' heads:
+// redux.sync max, a ballot for ties (a second reduction, over expert indices, only when several
+// lanes hold the maximum) and a shift of the winning lane's list.
+__device__ __forceinline__ void warp_topk_softmax_sorted8(const float* __restrict__ row, int E, int k, int* e_out,
+                                                          float* w_out) {
+  const int lane = threadIdx.x & 31;
+  uint64_t rk[8];   // key << 8 | (7 - i): larger first, equal keys -> lower i first
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    const float x = e < E ? __ldg(row + e) : 0.0f;
+    rk[i] = ((uint64_t)(e < E ? logit_key(x) : 0u) << 8) | (uint64_t)(7 - i);
+    v[i] = x;
+  }
+  auto cas = [&](int a, int b) {
+    const bool sw = rk[a] < rk[b];
+    const uint64_t ra = rk[a], rb = rk[b];
+    const float va = v[a], vb = v[b];
+    rk[a] = sw ? rb : ra;
+    rk[b] = sw ? ra : rb;
+    v[a] = sw ? vb : va;
+    v[b] = sw ? va : vb;
+  };
+  cas(0, 1); cas(2, 3); cas(4, 5); cas(6, 7);
+  cas(0, 2); cas(1, 3); cas(4, 6); cas(5, 7);
+  cas(1, 2); cas(5, 6);
+  cas(0, 4); cas(1, 5); cas(2, 6); cas(3, 7);
+  cas(2, 4); cas(3, 5);
+  cas(1, 2); cas(3, 4); cas(5, 6);
+  int my_e = 0;
+  float my_v = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    const uint32_t hk = (uint32_t)(rk[0] >> 8);
+    const int hidx = lane + 32 * (7 - (int)(rk[0] & 0xFFu));
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, hk);
+    const uint32_t tie = __ballot_sync(0xFFFFFFFFu, hk == m);
+    int wl;
+    if (__popc(tie) == 1) {
+      wl = __ffs(tie) - 1;
+    } else {
+      wl = (int)(__reduce_min_sync(0xFFFFFFFFu, hk == m ? (uint32_t)hidx : 0xFFFFFFFFu) & 31u);
+    }
+    const int widx = __shfl_sync(0xFFFFFFFFu, hidx, wl);
+    const float wv = __shfl_sync(0xFFFFFFFFu, v[0], wl);
+    if (lane == j) {
+      my_e = widx;
+      my_v = wv;
+    }
+    const bool me = lane == wl;
+#pragma unroll
+    for (int i = 0; i < 7; ++i) {
+      rk[i] = me ? rk[i + 1] : rk[i];
+      v[i] = me ? v[i + 1] : v[i];
+    }
+    rk[7] = me ? 0ull : rk[7];
+  }
+  const float vmax = __shfl_sync(0xFFFFFFFFu, my_v, 0);
+  const float ex = (lane < k) ? expf(my_v - vmax) : 0.0f;
+  float s = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+  *e_out = my_e;
+  *w_out = ex / s;
+}
+
 }  // namespace moe

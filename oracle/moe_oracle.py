@@ -194,11 +194,14 @@ def sigmoid(a):
 _ROUNDERS = {None: None, "fp16": round_fp16, "bf16": round_bf16}
 
 
-def expert_ffn(xe, Wg, Wu, Wd, operands=None):
+def expert_ffn(xe, Wg, Wu, Wd, operands=None, out16=False):
     """SwiGLU expert: h = silu(xe Wg^T) * (xe Wu^T); returns h Wd^T.  float64 accumulation.
 
     operands: None for the exact path, or "fp16"/"bf16" to round the GEMM operands
     (weights, activations and h) to that type first, as the tensor-core path does.
+    out16: also round the expert's output rows to fp16, as the layer path of the tensor-core
+    kernels stores them before the weighted combine (an emulation choice only: the pages fix
+    no intermediate precision; the exact oracle never rounds).
     """
     rnd = _ROUNDERS[operands]
     if rnd is not None:
@@ -208,7 +211,8 @@ def expert_ffn(xe, Wg, Wu, Wd, operands=None):
     h = silu(g) * u
     if rnd is not None:
         h = rnd(h)
-    return h @ Wd.T
+    out = h @ Wd.T
+    return round_fp16(out) if out16 else out
 
 
 def shared_gate(x, w_sg_bits):
@@ -216,7 +220,7 @@ def shared_gate(x, w_sg_bits):
     return sigmoid(np.asarray(x, dtype=np.float64) @ bf16_to_f64(w_sg_bits))
 
 
-def moe_layer(x_bits, logits, layer: dict, k: int, tile_n: int = 128, operands=None) -> dict:
+def moe_layer(x_bits, logits, layer: dict, k: int, tile_n: int = 128, operands=None, out16=False) -> dict:
     """One MoE layer: route, run every expert on its tokens (grouped by the permutation),
     run the shared expert on all tokens, and combine.  Returns y (float64 [T,d]) and the
     routing tables."""
@@ -234,13 +238,13 @@ def moe_layer(x_bits, logits, layer: dict, k: int, tile_n: int = 128, operands=N
         if hi == lo:
             continue
         tokens = perm[lo:hi] // k
-        Y[lo:hi] = expert_ffn(x[tokens], *expert_weights(routed, e), operands=operands)
+        Y[lo:hi] = expert_ffn(x[tokens], *expert_weights(routed, e), operands=operands, out16=out16)
     y = np.zeros((T, d), dtype=np.float64)
     for j in range(k):
         y += w[:, j:j + 1] * Y[inv[np.arange(T) * k + j]]
     gs = None
     if layer.get("shared") is not None:
-        Y[T * k:] = expert_ffn(x, *expert_weights(layer["shared"], 0), operands=operands)
+        Y[T * k:] = expert_ffn(x, *expert_weights(layer["shared"], 0), operands=operands, out16=out16)
         gs = shared_gate(x, layer["w_sg"])
         y += gs[:, None] * Y[T * k:]
     out = dict(tab)
@@ -248,7 +252,7 @@ def moe_layer(x_bits, logits, layer: dict, k: int, tile_n: int = 128, operands=N
     return out
 
 
-def moe_token(x_bits_row, logits_row, layer: dict, k: int, operands=None):
+def moe_token(x_bits_row, logits_row, layer: dict, k: int, operands=None, out16=False):
     """The layer for one token (float64 [d]); the same definition, without routing tables.
     Used to check sampled tokens of large workloads one by one."""
     x = bf16_to_f64(np.asarray(x_bits_row)[None, :])
@@ -256,10 +260,10 @@ def moe_token(x_bits_row, logits_row, layer: dict, k: int, operands=None):
     y = np.zeros(x.shape[1], dtype=np.float64)
     for j in range(k):
         e = int(idx[0, j])
-        y += w[0, j] * expert_ffn(x, *expert_weights(layer["routed"], e), operands=operands)[0]
+        y += w[0, j] * expert_ffn(x, *expert_weights(layer["routed"], e), operands=operands, out16=out16)[0]
     if layer.get("shared") is not None:
         gs = shared_gate(x, layer["w_sg"])[0]
-        y += gs * expert_ffn(x, *expert_weights(layer["shared"], 0), operands=operands)[0]
+        y += gs * expert_ffn(x, *expert_weights(layer["shared"], 0), operands=operands, out16=out16)[0]
     return y, idx[0], w[0]
 
 
@@ -283,7 +287,7 @@ def router_logits(h, w_router_bits):
 
 
 def stack_tokens(x0_rows, layers: list, routers: list, k: int, eps: float = 1e-6, operands=None,
-                 forced_logits: list | None = None):
+                 forced_logits: list | None = None, out16=False):
     """The residual stack for a few independent tokens: for each layer,
     h = RMSNorm(x)*gamma (bf16), logits = h W_r^T, x <- x + MoE(h).  Tokens are independent,
     so any subset of rows can be checked alone.  `forced_logits[l]` (optional, [n, E]) replaces
@@ -296,7 +300,7 @@ def stack_tokens(x0_rows, layers: list, routers: list, k: int, eps: float = 1e-6
         lg = router_logits(h, rt["w_router"]) if forced_logits is None else forced_logits[li]
         ys, ids = [], []
         for i in range(x.shape[0]):
-            y, idx, _ = moe_token(hbits[i], lg[i], layer, k, operands=operands)
+            y, idx, _ = moe_token(hbits[i], lg[i], layer, k, operands=operands, out16=out16)
             ys.append(y)
             ids.append(idx)
         x = x + np.stack(ys)

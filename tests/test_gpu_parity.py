@@ -140,7 +140,7 @@ def test_layer_tiny_exact_and_emulated():
     inp = synth.make_inputs(wl)
     got = run_layer(wl, host, dl, inp)["y"]
     ref = O.moe_layer(inp["x"], inp["logits"], host, wl.k)["y"]
-    emu = O.moe_layer(inp["x"], inp["logits"], host, wl.k, operands="fp16")["y"]
+    emu = O.moe_layer(inp["x"], inp["logits"], host, wl.k, operands="fp16", out16=True)["y"]
     assert rowwise_err(got, ref) <= EXACT_TOL
     assert rowwise_err(got, emu) <= EMUL_TOL
 
@@ -151,7 +151,7 @@ def test_layer_tiny_tile_widths_and_routing_out(tile_n):
     host, dl = layer_for(wl)
     inp = synth.make_inputs(wl, seed=3)
     out = run_layer(wl, host, dl, inp, tile_n=tile_n)
-    emu = O.moe_layer(inp["x"], inp["logits"], host, wl.k, tile_n=tile_n, operands="fp16")
+    emu = O.moe_layer(inp["x"], inp["logits"], host, wl.k, tile_n=tile_n, operands="fp16", out16=True)
     assert rowwise_err(out["y"], emu["y"]) <= EMUL_TOL
     assert_routing_equal(out["routing"], inp["logits"], wl.E, wl.k, tile_n)
 
@@ -230,7 +230,7 @@ def test_prefill_full_size():
     got = run_layer(wl, host, dl, inp)["y"]
     ref = O.moe_layer(inp["x"], inp["logits"], host, wl.k)["y"]
     assert rowwise_err(got, ref) <= EXACT_TOL
-    emu = O.moe_layer(inp["x"], inp["logits"], host, wl.k, operands="fp16")["y"]
+    emu = O.moe_layer(inp["x"], inp["logits"], host, wl.k, operands="fp16", out16=True)["y"]
     assert rowwise_err(got, emu) <= EMUL_TOL
 
 
@@ -319,7 +319,7 @@ def test_stack_of_layers_tiny():
     # so the stack is compared with the oracle that applies the same operand rounding; what is
     # left is accumulation order and one-ulp rounding flips of h (bf16 after the norm, fp16 after
     # SwiGLU), which checks the composition: residual add, norm, router, layer.
-    ref, ref_picks = O.stack_tokens(x0, hosts, routers, wl.k, operands="fp16")
+    ref, ref_picks = O.stack_tokens(x0, hosts, routers, wl.k, operands="fp16", out16=True)
     same = np.ones(wl.T, bool)
     for l in range(L):
         same &= np.all(np.sort(picks[l], axis=1) == np.sort(ref_picks[l], axis=1), axis=1)
