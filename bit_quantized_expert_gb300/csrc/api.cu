@@ -14,7 +14,7 @@ namespace {
 constexpr int kTileN = 128;   // block-map tile of the layer call (token rows per MMA tile)
 
 struct Layout {
-  size_t err, xperm, gs, idx, w, counts, offsets, perm, inv, tiles, num_tiles, h, yperm, hdec, total;
+  size_t err, xperm, gs, idx, w, counts, offsets, perm, inv, tiles, num_tiles, chunk, h, yperm, hdec, total;
 };
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -49,6 +49,7 @@ Layout layout_of(const moe_dims& d) {
   L.inv = take(T * k * 4);
   L.tiles = take(max_tiles_of(d.T, d.k, d.E, kTileN, sh) * 16);
   L.num_tiles = take(16);
+  L.chunk = take(tables_scratch_bytes((int)T, (int)E));   // routing-table scratch
   L.h = take(slots * F * 2);
   L.yperm = take(slots * D * 2);   // fp16 expert outputs of the layer path
   L.hdec = take(T == 1 ? decode_scratch_floats((int)D, (int)k, (int)F) * 4 : 0);   // decode partials
@@ -197,12 +198,12 @@ RoutingPtrs caller_routing(const moe_routing* r) {
 }
 
 cudaError_t run_routing(const moe_dims& d, const float* logits, const RoutingPtrs& R, const uint16_t* x,
-                        const uint16_t* w_sg, float* gs, uint32_t* err, cudaStream_t st) {
+                        const uint16_t* w_sg, float* gs, int32_t* chunk, uint32_t* err, cudaStream_t st) {
   RouteArgs ra{logits, d.T, d.E, d.k, d.d, R.idx, R.w, x, w_sg, gs, err};
   cudaError_t e = launch_topk(ra, st);
   if (e != cudaSuccess) return e;
   TablesArgs ta{R.idx, d.T, d.E, d.k, R.tile_n, d.F_shared > 0 ? 1 : 0, R.counts, R.offsets, R.perm, R.inv,
-                R.tiles, R.num_tiles, err};
+                R.tiles, R.num_tiles, chunk, err};
   return launch_tables(ta, st);
 }
 
@@ -305,7 +306,8 @@ moe_status moe_route(const moe_dims* dims, const float* logits, const moe_routin
   if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* err = at<uint32_t>(workspace, L.err);
-  return cuda_status(run_routing(*dims, logits, caller_routing(out), nullptr, nullptr, nullptr, err, st));
+  return cuda_status(run_routing(*dims, logits, caller_routing(out), nullptr, nullptr, nullptr,
+                                 at<int32_t>(workspace, L.chunk), err, st));
 }
 
 moe_status moe_expert_forward(const moe_dims* dims, const uint16_t* x, const moe_routing* routing,
@@ -378,14 +380,15 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
     da.sync = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + L.err + kSyncOffset);
     if (launch_decode(da, st, true) != cudaSuccess) return MOE_ERR_CUDA;
     if (routing_out != nullptr)
-      return cuda_status(run_routing(d, logits, caller_routing(routing_out), nullptr, nullptr, nullptr, err, st));
+      return cuda_status(run_routing(d, logits, caller_routing(routing_out), nullptr, nullptr, nullptr,
+                                     at<int32_t>(workspace, L.chunk), err, st));
     return MOE_OK;
   }
 
   const RoutingPtrs R = routing_out ? caller_routing(routing_out) : internal_routing(workspace, L);
   uint16_t* xperm = at<uint16_t>(workspace, L.xperm);
   float* gs = sh ? at<float>(workspace, L.gs) : nullptr;
-  cudaError_t e = run_routing(d, logits, R, x, sh ? w_shared_gate : nullptr, gs, err, st);
+  cudaError_t e = run_routing(d, logits, R, x, sh ? w_shared_gate : nullptr, gs, at<int32_t>(workspace, L.chunk), err, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   uint16_t* y16 = at<uint16_t>(workspace, L.yperm);
   s = run_experts(d, R, routed, sh ? shared : nullptr, x, xperm, at<uint16_t>(workspace, L.h), nullptr, y16, err,

@@ -25,9 +25,10 @@ struct TablesArgs {
   const int32_t* idx;
   int T, E, k, tile_n, has_shared;
   int32_t *counts, *offsets, *perm, *inv, *tiles, *num_tiles;
+  int32_t* chunk;          // scratch [ceil(T/32)][E]: per-chunk counts, then per-chunk bases
   uint32_t* err;
 };
-size_t tables_smem_bytes(int E);
+size_t tables_scratch_bytes(int T, int E);
 cudaError_t launch_tables(const TablesArgs& a, cudaStream_t st);
 
 // ---------------------------------------------------------------- grouped GEMM (gemm.cu)

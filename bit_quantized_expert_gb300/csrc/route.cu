@@ -6,9 +6,9 @@
 //
 // Kernel 1 (one warp per token): top-k over fp32 logits with ties to the lower expert index,
 // softmax over the selected logits, and the shared expert gate sigmoid(x . w_sg).
-// Kernel 2 (one CTA): per-expert counts, exclusive offsets, a permutation sorted by
-// (expert, token) that depends only on the counts (never on atomic arrival order), its
-// inverse and the tile block map.
+// Kernels 2-4 (over 32-token chunks, plus one scan CTA): per-expert counts, exclusive offsets, a
+// permutation sorted by (expert, token) that depends only on the counts (never on atomic arrival
+// order), its inverse and the tile block map.
 #include "common.cuh"
 #include "kernels.h"
 #include "topk.cuh"
@@ -75,10 +75,6 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* total)
   return incl - v + warp_tot[warp];
 }
 
-// Warps that walk the tokens in kernel 2: 32 when their per-warp tables (2 x E ints each) fit
-// in 96 KB, fewer for large E.
-__host__ __device__ constexpr int tok_warps(int E) { return (96 * 1024) / (8 * E) >= 32 ? 32 : (96 * 1024) / (8 * E); }
-
 // The k expert ids of token t, loaded together (independent loads, one latency); -1 past T or k.
 template <int KMAX>
 __device__ __forceinline__ void load_token_ids(const int32_t* __restrict__ idx, int t, int T, int k, int E,
@@ -93,64 +89,62 @@ __device__ __forceinline__ void load_token_ids(const int32_t* __restrict__ idx, 
     }
 }
 
+// Routing tables in three kernels over 32-token chunks (one warp each), so the token passes use
+// the whole GPU:
+//   chunk_hist_kernel   per-chunk expert counts -> chunk[c][e];
+//   chunk_scan_kernel   one CTA: per expert, exclusive prefix over chunks (in place), counts,
+//                       offsets (exclusive scan over experts) and the block map;
+//   chunk_scatter_kernel  slot of assignment (t, j) = offsets[e] + chunk[c][e] + (earlier tokens of
+//                       the chunk routed to e), from a per-chunk bit mask per expert.
+// Slots inside an expert are in token order; they follow from the counts alone.
 // KMAX: upper bound on k held in registers per token (8 or 32).
 template <int KMAX>
-__global__ void __launch_bounds__(1024, 1) tables_kernel(TablesArgs a) {
-  extern __shared__ int tsm[];
-  const int kTokWarps = tok_warps(a.E);
-  int* base = tsm;                                       // [kTokWarps][E]: counts, then running slots
-  uint32_t* mask = reinterpret_cast<uint32_t*>(tsm + kTokWarps * a.E);   // [kTokWarps][E]
-  __shared__ int warp_tot[32];
-  __shared__ int total_s;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__global__ void __launch_bounds__(256) chunk_hist_kernel(TablesArgs a) {
+  extern __shared__ int hsm[];   // [8 warps][E]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int E = a.E, k = a.k, T = a.T;
-
-  for (int i = tid; i < kTokWarps * E; i += blockDim.x) {
-    base[i] = 0;
-    mask[i] = 0u;
-  }
-  __syncthreads();
-
-  const int nchunks = (T + 31) / 32;
-  const int c_lo = (int)((long long)warp * nchunks / kTokWarps);
-  const int c_hi = (int)((long long)(warp + 1) * nchunks / kTokWarps);
-
-  // Pass A: per-warp histogram of the warp's contiguous token range.
-  if (warp < kTokWarps) {
-    int* hw = base + warp * E;
-    for (int c = c_lo; c < c_hi; ++c) {
-      int ev[KMAX];
-      load_token_ids<KMAX>(a.idx, c * 32 + lane, T, k, E, ev, a.err);
-      // lanes routing to the same expert in round j add their count once (hot experts would
-      // otherwise serialise 32 atomics on one word)
+  const int nc = (T + 31) / 32;
+  const int c = blockIdx.x * 8 + warp;
+  int* hw = hsm + warp * E;
+  for (int i = lane; i < E; i += 32) hw[i] = 0;
+  __syncwarp();
+  if (c < nc) {
+    int ev[KMAX];
+    load_token_ids<KMAX>(a.idx, c * 32 + lane, T, k, E, ev, a.err);
+    // lanes routing to the same expert in round j add their count once
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j) {
-        if (j < k) {
-          const uint32_t m = __match_any_sync(0xFFFFFFFFu, ev[j]);
-          if (ev[j] >= 0 && lane == __ffs(m) - 1) atomicAdd(&hw[ev[j]], __popc(m));
-        }
+    for (int j = 0; j < KMAX; ++j) {
+      if (j < k) {
+        const uint32_t m = __match_any_sync(0xFFFFFFFFu, ev[j]);
+        if (ev[j] >= 0 && lane == __ffs(m) - 1) atomicAdd(&hw[ev[j]], __popc(m));
       }
     }
+    __syncwarp();
+    for (int i = lane; i < E; i += 32) a.chunk[(size_t)c * E + i] = hw[i];
   }
-  __syncthreads();
+}
 
-  // Pass B: per expert, exclusive prefix over warps (warp order = token order) and the total.
+__global__ void __launch_bounds__(1024, 1) chunk_scan_kernel(TablesArgs a) {
+  __shared__ int warp_tot[32];
+  __shared__ int total_s;
+  const int tid = threadIdx.x;
+  const int E = a.E, k = a.k, T = a.T;
+  const int nc = (T + 31) / 32;
   int cnt = 0;
   if (tid < E) {
     int run = 0;
-    for (int w = 0; w < kTokWarps; ++w) {
-      const int c = base[w * E + tid];
-      base[w * E + tid] = run;
-      run += c;
+#pragma unroll 8
+    for (int c = 0; c < nc; ++c) {
+      const size_t o = (size_t)c * E + tid;
+      const int v = a.chunk[o];
+      a.chunk[o] = run;
+      run += v;
     }
     cnt = run;
     a.counts[tid] = run;
   }
   const int off = block_excl_scan(cnt, warp_tot, &total_s);
-  if (tid < E) {
-    a.offsets[tid] = off;
-    for (int w = 0; w < kTokWarps; ++w) base[w * E + tid] += off;   // absolute first slot
-  }
+  if (tid < E) a.offsets[tid] = off;
   if (tid == 0) a.offsets[E] = total_s;
   // Block map: ceil(count / tile_n) tiles per non-empty expert, then the shared expert.
   const int nt = (tid < E) ? (cnt + a.tile_n - 1) / a.tile_n : 0;
@@ -174,49 +168,39 @@ __global__ void __launch_bounds__(1024, 1) tables_kernel(TablesArgs a) {
     reinterpret_cast<int4*>(a.tiles)[routed_tiles + i] = r;
   }
   if (tid == 0) *a.num_tiles = routed_tiles + shared_tiles;
-  __syncthreads();
+}
 
-  // Pass C: slots.  Within a 32-token chunk, a bit mask per expert gives each assignment the
-  // number of earlier tokens of the chunk routed to the same expert; the warp's running slot
-  // per expert carries the count across chunks.  Every slot follows from the counts alone.
-  if (warp < kTokWarps) {
-    int* run = base + warp * E;
-    uint32_t* mk = mask + warp * E;
-    const uint32_t lt = (1u << lane) - 1u;
-    for (int c = c_lo; c < c_hi; ++c) {
-      const int t = c * 32 + lane;
-      int ev[KMAX];
-      load_token_ids<KMAX>(a.idx, t, T, k, E, ev, nullptr);
+template <int KMAX>
+__global__ void __launch_bounds__(256) chunk_scatter_kernel(TablesArgs a) {
+  extern __shared__ uint32_t msm[];   // [8 warps][E] bit masks
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int E = a.E, k = a.k, T = a.T;
+  const int nc = (T + 31) / 32;
+  const int c = blockIdx.x * 8 + warp;
+  if (c >= nc) return;   // whole warps leave; no block barrier below
+  uint32_t* mk = msm + warp * E;
+  for (int i = lane; i < E; i += 32) mk[i] = 0u;
+  __syncwarp();
+  const int t = c * 32 + lane;
+  int ev[KMAX];
+  load_token_ids<KMAX>(a.idx, t, T, k, E, ev, nullptr);
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j) {
-        if (j < k) {
-          const uint32_t m = __match_any_sync(0xFFFFFFFFu, ev[j]);
-          if (ev[j] >= 0 && lane == __ffs(m) - 1) atomicOr(&mk[ev[j]], m);
-        }
-      }
-      __syncwarp();
-#pragma unroll
-      for (int j = 0; j < KMAX; ++j)
-        if (ev[j] >= 0) {
-          const uint32_t m = mk[ev[j]];
-          const int slot = run[ev[j]] + __popc(m & lt);
-          a.perm[slot] = t * k + j;
-          a.inv[(size_t)t * k + j] = slot;
-        }
-      __syncwarp();
-#pragma unroll
-      for (int j = 0; j < KMAX; ++j)
-        if (ev[j] >= 0) {
-          const uint32_t m = mk[ev[j]];
-          if (lane == 31 - __clz(m)) run[ev[j]] += __popc(m);   // last token of the chunk for e
-        }
-      __syncwarp();
-#pragma unroll
-      for (int j = 0; j < KMAX; ++j)
-        if (ev[j] >= 0) mk[ev[j]] = 0u;
-      __syncwarp();
+  for (int j = 0; j < KMAX; ++j) {
+    if (j < k) {
+      const uint32_t m = __match_any_sync(0xFFFFFFFFu, ev[j]);
+      if (ev[j] >= 0 && lane == __ffs(m) - 1) atomicOr(&mk[ev[j]], m);
     }
   }
+  __syncwarp();
+  const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j)
+    if (ev[j] >= 0) {
+      const int e = ev[j];
+      const int slot = __ldg(a.offsets + e) + a.chunk[(size_t)c * E + e] + __popc(mk[e] & lt);
+      a.perm[slot] = t * k + j;
+      a.inv[(size_t)t * k + j] = slot;
+    }
 }
 
 cudaError_t launch_topk(const RouteArgs& a, cudaStream_t st) {
@@ -232,23 +216,22 @@ cudaError_t launch_topk(const RouteArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-size_t tables_smem_bytes(int E) { return (size_t)2 * tok_warps(E) * E * sizeof(int); }
+size_t tables_scratch_bytes(int T, int E) { return (size_t)((T + 31) / 32) * E * sizeof(int); }
 
 cudaError_t launch_tables(const TablesArgs& a, cudaStream_t st) {
-  const size_t smem = tables_smem_bytes(a.E);
-  static thread_local int configured_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(tables_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(96 * 1024));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tables_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(96 * 1024));
-    if (e != cudaSuccess) return e;
-    configured_dev = dev;
+  if (a.T <= 0) {
+    // no tokens: empty tables (counts and offsets zero, no tiles)
+    chunk_scan_kernel<<<1, 1024, 0, st>>>(a);
+    return cudaGetLastError();
   }
-  if (a.k <= 8) tables_kernel<8><<<1, 1024, smem, st>>>(a);
-  else tables_kernel<32><<<1, 1024, smem, st>>>(a);
+  const int nc = (a.T + 31) / 32;
+  const int grid = (nc + 7) / 8;
+  const size_t smem = (size_t)8 * a.E * sizeof(int);   // <= 32 KB (E <= 1024)
+  if (a.k <= 8) chunk_hist_kernel<8><<<grid, 256, smem, st>>>(a);
+  else chunk_hist_kernel<32><<<grid, 256, smem, st>>>(a);
+  chunk_scan_kernel<<<1, 1024, 0, st>>>(a);
+  if (a.k <= 8) chunk_scatter_kernel<8><<<grid, 256, smem, st>>>(a);
+  else chunk_scatter_kernel<32><<<grid, 256, smem, st>>>(a);
   return cudaGetLastError();
 }
 
