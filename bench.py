@@ -250,11 +250,11 @@ def decode_bench(args, world, rank, local, device, pk):
     tokens = LAYERS * args.steps * world
     res = {
         "value": tokens / (ms_max / 1e3), "ms_per_step": ms_max / args.steps, "clocks": ck, "flags": flags,
-        "roofline": {"kernel": "decode_gateup_kernel + decode_down_kernel (one MoE layer call, PDL-chained)",
+        "roofline": {"kernel": "decode_layer_kernel (one cooperative launch per layer call)",
                      "bound": "hbm", "achieved": per_step_bytes / step_s / 1e9, "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": per_step_bytes / step_s / 1e9 / pk["hbm_gbs"], "traffic": None,
                      "algorithmic_bytes_per_launch": per_call, "peak_source": pk["source"]},
-        "gpu_launches": 2 * LAYERS * args.steps,
+        "gpu_launches": LAYERS * args.steps,   # one decode_layer_kernel per layer call
     }
 
     # End to end through the C ABI with host buffers: per layer call, copy x and logits from pinned
@@ -290,7 +290,7 @@ def decode_bench(args, world, rank, local, device, pk):
     e2e_ms = max_over_ranks(t0.elapsed_time(t1), world, device)
     res["e2e"] = {"value": LAYERS * n_e2e * world / (e2e_ms / 1e3), "unit": "tokens/s",
                   "h2d_bytes_per_step": LAYERS * (wl.d * 2 + wl.E * 4), "d2h_bytes_per_step": LAYERS * wl.d * 4,
-                  "steps": n_e2e, "launch": "eager per call (2 H2D copies, 2 kernels, 1 D2H copy per layer)"}
+                  "steps": n_e2e, "launch": "eager per call (2 H2D copies, 1 kernel, 1 D2H copy per layer)"}
     del layers
     torch.cuda.empty_cache()
     return res
@@ -345,7 +345,8 @@ def prefill_bench(wl, steps, device, pk):
            "tensor": {"achieved": flops / step_s / 1e12, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                       "frac": flops / step_s / 1e12 / pk["bf16_tflops"], "algorithmic_flops": flops,
                       "note": "fp16 operands; peak is the measured bf16 dense rate (same nominal rate)"},
-           "gpu_launches_per_step": 5}
+           # top-k, chunk histogram, chunk scan, chunk scatter, x permute, gate/up GEMM, down GEMM, combine
+           "gpu_launches_per_step": 8}
     del layers
     torch.cuda.empty_cache()
     return out

@@ -127,21 +127,44 @@ __global__ void __launch_bounds__(256) chunk_hist_kernel(TablesArgs a) {
 __global__ void __launch_bounds__(1024, 1) chunk_scan_kernel(TablesArgs a) {
   __shared__ int warp_tot[32];
   __shared__ int total_s;
+  __shared__ int part_s[1024];   // [part][expert] chunk sums
   const int tid = threadIdx.x;
   const int E = a.E, k = a.k, T = a.T;
   const int nc = (T + 31) / 32;
-  int cnt = 0;
-  if (tid < E) {
-    int run = 0;
-#pragma unroll 8
-    for (int c = 0; c < nc; ++c) {
-      const size_t o = (size_t)c * E + tid;
-      const int v = a.chunk[o];
-      a.chunk[o] = run;
-      run += v;
+  // tpe threads per expert, each owning a contiguous range of chunks; loads go out 16 at a time
+  const int tpe = E <= 256 ? 4 : E <= 512 ? 2 : 1;
+  const int e = tid % E, p = tid / E;
+  const bool owner = tid < E * tpe;
+  const int per = (nc + tpe - 1) / tpe;
+  const int c_lo = owner ? min(nc, p * per) : 0, c_hi = owner ? min(nc, (p + 1) * per) : 0;
+  int sum = 0;
+  for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+    int v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = c0 + i < c_hi ? __ldcg(a.chunk + (size_t)(c0 + i) * E + e) : 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sum += v[i];
+  }
+  if (owner) part_s[p * E + e] = sum;
+  __syncthreads();
+  int run = 0, cnt = 0;
+  if (owner) {
+    for (int q = 0; q < p; ++q) run += part_s[q * E + e];
+    for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+      int v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = c0 + i < c_hi ? __ldcg(a.chunk + (size_t)(c0 + i) * E + e) : 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (c0 + i < c_hi) {
+          a.chunk[(size_t)(c0 + i) * E + e] = run;
+          run += v[i];
+        }
     }
-    cnt = run;
-    a.counts[tid] = run;
+  }
+  if (tid < E) {
+    for (int q = 0; q < tpe; ++q) cnt += part_s[q * E + tid];
+    a.counts[tid] = cnt;
   }
   const int off = block_excl_scan(cnt, warp_tot, &total_s);
   if (tid < E) a.offsets[tid] = off;
