@@ -40,9 +40,9 @@ template <int MODE>
 struct Cfg {
   static constexpr int NMAT = MODE == 0 ? 2 : 1;
   static constexpr int S_RAW = MODE == 0 ? 6 : 8;
-  static constexpr int S_W = MODE == 0 ? 3 : 4;
-  static constexpr int S_X = MODE == 0 ? 3 : 4;
-  static constexpr int NBAR = 2 * S_RAW + 2 * S_W + 2 * S_X + 4;
+  static constexpr int S_W = MODE == 0 ? 3 : 4;   // operand stages: W (dequantised) and X together
+  static constexpr int S_X = S_W;
+  static constexpr int NBAR = 2 * S_RAW + 2 * S_W + 4;
   static constexpr uint32_t OFF_W = 0;
   static constexpr uint32_t OFF_X = OFF_W + S_W * NMAT * kTileBytes;
   static constexpr uint32_t OFF_RAW = OFF_X + S_X * kTileBytes;
@@ -123,12 +123,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
   auto RF = [&](int i) { return sBar + 8u * i; };
   auto RE = [&](int i) { return sBar + 8u * (C::S_RAW + i); };
+  // Operand stage s holds the dequantised W tile(s) and the activation tile X of one K chunk:
+  // WF(s) completes when the 8 dequant warps have arrived and the X bytes have landed; WE(s) when
+  // the MMAs reading the stage have completed.
   auto WF = [&](int i) { return sBar + 8u * (2 * C::S_RAW + i); };
   auto WE = [&](int i) { return sBar + 8u * (2 * C::S_RAW + C::S_W + i); };
-  auto XF = [&](int i) { return sBar + 8u * (2 * C::S_RAW + 2 * C::S_W + i); };
-  auto XE = [&](int i) { return sBar + 8u * (2 * C::S_RAW + 2 * C::S_W + C::S_X + i); };
-  auto AF = [&](int i) { return sBar + 8u * (2 * C::S_RAW + 2 * C::S_W + 2 * C::S_X + i); };
-  auto AE = [&](int i) { return sBar + 8u * (2 * C::S_RAW + 2 * C::S_W + 2 * C::S_X + 2 + i); };
+  auto AF = [&](int i) { return sBar + 8u * (2 * C::S_RAW + 2 * C::S_W + i); };
+  auto AE = [&](int i) { return sBar + 8u * (2 * C::S_RAW + 2 * C::S_W + 2 + i); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -137,12 +138,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       mbar_init(RE(i), 8);
     }
     for (int i = 0; i < C::S_W; ++i) {
-      mbar_init(WF(i), 8);
+      mbar_init(WF(i), 8 + 1);   // dequant warps + the producer's expect_tx arrival
       mbar_init(WE(i), 1);
-    }
-    for (int i = 0; i < C::S_X; ++i) {
-      mbar_init(XF(i), 1);
-      mbar_init(XE(i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(AF(i), 1);
@@ -203,9 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           // activation tile: 128 slot rows x 64 columns (x in slot order, or h); rows past the
           // tile's end belong to the next tile or lie outside the tensor (zero-filled), and the
           // MMA columns they feed are never stored
-          if (!mbar_wait(XE(sx), phx ^ 1u, abort_s, a.err)) { ok = false; break; }
-          mbar_arrive_expect_tx(XF(sx), kTileBytes);
-          tma_load_2d(sX + sx * kTileBytes, MODE == 0 ? &maps.x : &maps.h, XF(sx), kc * 64, tl.y);
+          if (!mbar_wait(WE(sx), phx ^ 1u, abort_s, a.err)) { ok = false; break; }
+          mbar_arrive_expect_tx(WF(sx), kTileBytes);
+          tma_load_2d(sX + sx * kTileBytes, MODE == 0 ? &maps.x : &maps.h, WF(sx), kc * 64, tl.y);
           if (++sx == C::S_X) { sx = 0; phx ^= 1u; }
         }
         if (!ok) break;
@@ -214,8 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int sw = 0, sx = 0;
-      uint32_t phw = 0, phx = 0;
+      int sw = 0;
+      uint32_t phw = 0;
       int li = 0;
       int4 tl_next = tile_of(blockIdx.x);
       for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++li) {
@@ -229,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const uint32_t d0 = tmem + (uint32_t)(b * C::ACC_COLS);
         bool ok = true;
         for (int kc = 0; kc < KC; ++kc) {
-          if (!mbar_wait(WF(sw), phw, abort_s, a.err) || !mbar_wait(XF(sx), phx, abort_s, a.err)) {
+          if (!mbar_wait(WF(sw), phw, abort_s, a.err)) {
             ok = false;
             break;
           }
@@ -237,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           // Descriptors of the stage's tiles; each 16-element K step advances the start address
           // by 32 bytes (2 in the descriptor's address field, which cannot carry: stages lie
           // below 256 KB).
-          const uint64_t bdesc0 = smem_desc_sw128(sX + sx * kTileBytes);
+          const uint64_t bdesc0 = smem_desc_sw128(sX + sw * kTileBytes);
           uint64_t adesc0[NMAT];
 #pragma unroll
           for (int mat = 0; mat < NMAT; ++mat) adesc0[mat] = smem_desc_sw128(sW + (sw * NMAT + mat) * kTileBytes);
@@ -248,9 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
               tc_mma_f16(d0 + mat * 128, adesc0[mat] + 2u * kk, bdesc0 + 2u * kk, idesc, (kc | kk) != 0 ? 1u : 0u);
           }
           tc_commit(WE(sw));
-          tc_commit(XE(sx));
           if (++sw == C::S_W) { sw = 0; phw ^= 1u; }
-          if (++sx == C::S_X) { sx = 0; phx ^= 1u; }
         }
         if (!ok) break;
         tc_commit(AF(b));
