@@ -122,17 +122,18 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Packed codes of n stacked [R, C] matrices as a 3-D uint32 tensor {C/8, R, n}; box 8 x 128 x 1
-// (64 codes of 128 rows = one 4 KB quantisation-group column of a tile).
+// Packed codes of n stacked [R, C] matrices as a 3-D uint32 tensor {C/8, R, n}; box 16 x 128 x 1
+// (128 codes of 128 rows = two quantisation groups of a tile, 64 bytes per row) in the 64-byte
+// swizzle.
 bool encode_codes(CUtensorMap* m, const uint32_t* codes, int n, int R, int C) {
   EncodeTiledFn f = encode_fn();
   if (!f) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)(C / 8), (cuuint64_t)R, (cuuint64_t)n};
   const cuuint64_t strides[2] = {(cuuint64_t)(C / 8) * 4, (cuuint64_t)R * (C / 8) * 4};
-  const cuuint32_t box[3] = {8, 128, 1};
+  const cuuint32_t box[3] = {16, 128, 1};
   const cuuint32_t es[3] = {1, 1, 1};
   return f(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(codes), dims, strides, box, es,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

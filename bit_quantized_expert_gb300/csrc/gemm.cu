@@ -34,12 +34,12 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kThreads = 512;
 constexpr uint32_t kTileBytes = 128 * 128;   // one 128-row x 64-column fp16 operand tile
-constexpr uint32_t kRawBytes = 128 * 32;     // 128 rows x 64 packed 4-bit codes
+constexpr uint32_t kRawBytes = 128 * 64;     // 128 rows x 128 packed 4-bit codes: two K chunks
 
 template <int MODE>
 struct Cfg {
   static constexpr int NMAT = MODE == 0 ? 2 : 1;
-  static constexpr int S_RAW = MODE == 0 ? 6 : 8;
+  static constexpr int S_RAW = MODE == 0 ? 3 : 4;   // packed-code stages of two K chunks each
   static constexpr int S_W = MODE == 0 ? 3 : 4;   // operand stages: W (dequantised) and X together
   static constexpr int S_X = S_W;
   static constexpr int NBAR = 2 * S_RAW + 2 * S_W + 4;
@@ -191,12 +191,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const int ec = which ? 0 : tl.x;
         bool ok = true;
         for (int kc = 0; kc < KC && ok; ++kc) {
-          if (!mbar_wait(RE(s), ph ^ 1u, abort_s, a.err)) { ok = false; break; }
-          mbar_arrive_expect_tx(RF(s), NMAT * kRawBytes);
+          if ((kc & 1) == 0) {   // packed codes of chunks kc and kc+1 (K is a multiple of 128)
+            if (!mbar_wait(RE(s), ph ^ 1u, abort_s, a.err)) { ok = false; break; }
+            mbar_arrive_expect_tx(RF(s), NMAT * kRawBytes);
 #pragma unroll
-          for (int mat = 0; mat < NMAT; ++mat)
-            tma_load_3d(sRaw + (s * NMAT + mat) * kRawBytes, &maps.codes[mat][which], RF(s), kc * 8, m * kBM, ec);
-          if (++s == C::S_RAW) { s = 0; ph ^= 1u; }
+            for (int mat = 0; mat < NMAT; ++mat)
+              tma_load_3d(sRaw + (s * NMAT + mat) * kRawBytes, &maps.codes[mat][which], RF(s), kc * 8, m * kBM, ec);
+            if (++s == C::S_RAW) { s = 0; ph ^= 1u; }
+          }
           // activation tile: 128 slot rows x 64 columns (x in slot order, or h); rows past the
           // tile's end belong to the next tile or lie outside the tensor (zero-filled), and the
           // MMA columns they feed are never stored
@@ -313,21 +315,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           bad = bad || !(fmaf(15.0f, fabsf(sf), fabsf(bf)) <= 65504.0f);
           const __half2 s2 = __float2half2_rn(sf);
           const __half2 b2 = __float2half2_rn(bf);
-          if (!mbar_wait(RF(s), ph, abort_s, a.err)) { ok = false; break; }
-          const uint32_t src = sRaw + (s * NMAT + mat) * kRawBytes + i * 32 + w0 * 4;
+          // codes of this chunk: half (j & 1) of the two-chunk stage s (kb is a multiple of 8).
+          // The stage holds 64-byte rows in the 64-byte swizzle: 16-byte piece c of row i sits at
+          // piece c ^ ((i >> 1) & 3), which keeps the lanes' loads free of bank conflicts.
+          if ((j & 1) == 0 && !mbar_wait(RF(s), ph, abort_s, a.err)) { ok = false; break; }
+          const uint32_t row_base = sRaw + (s * NMAT + mat) * kRawBytes + i * 64;
+          const uint32_t sx64 = (uint32_t)((i >> 1) & 3);
+          const uint32_t piece0 = (uint32_t)((j & 1) * 2 + (w0 >> 2));
           uint32_t words[8];
           {
-            const uint4 c0 = ld_shared_v4(src);
+            const uint4 c0 = ld_shared_v4(row_base + ((piece0 ^ sx64) << 4));
             words[0] = c0.x; words[1] = c0.y; words[2] = c0.z; words[3] = c0.w;
             if (NW == 8) {
-              const uint4 c1 = ld_shared_v4(src + 16);
+              const uint4 c1 = ld_shared_v4(row_base + (((piece0 + 1) ^ sx64) << 4));
               words[4] = c1.x; words[5] = c1.y; words[6] = c1.z; words[7] = c1.w;
             } else {
               words[4] = words[5] = words[6] = words[7] = 0u;
             }
           }
           const int s_used = s;
-          if (++s == C::S_RAW) { s = 0; ph ^= 1u; }
+          const bool stage_done = (j & 1) == 1;
+          if (stage_done && ++s == C::S_RAW) { s = 0; ph ^= 1u; }
           if (!mbar_wait(WE(sw), phw ^ 1u, abort_s, a.err)) { ok = false; break; }
           const uint32_t dst = sW + (sw * NMAT + mat) * kTileBytes + i * 128;
 #pragma unroll
@@ -342,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           // it, so every lane's shared-memory read of the stage has completed.  Releasing it right
           // after issuing those reads let the TMA refill land before slow lanes had read it.
           if (lane == 0) {
-            mbar_arrive(RE(s_used));
+            if (stage_done) mbar_arrive(RE(s_used));
             mbar_arrive(WF(sw));
           }
           if (++sw == C::S_W) { sw = 0; phw ^= 1u; }
