@@ -215,6 +215,8 @@ QPtr qptr(const moe_qmat& q) { return QPtr{q.codes, q.scales, q.biases}; }
 moe_status run_experts(const moe_dims& d, const RoutingPtrs& R, const moe_experts* routed, const moe_experts* shared,
                        const uint16_t* x, uint16_t* xperm, uint16_t* h, float* y_perm, uint16_t* y16,
                        uint32_t* err, cudaStream_t st) {
+  // the down GEMM pairs 128-row blocks of the output dimension
+  if (d.d % 256 != 0) return MOE_ERR_UNSUPPORTED;
   const bool sh = shared != nullptr && d.F_shared > 0;
   const long long slots = (long long)d.T * d.k + (sh ? d.T : 0);
   const moe_experts* s_or_r = sh ? shared : routed;
@@ -261,7 +263,7 @@ moe_status run_experts(const moe_dims& d, const RoutingPtrs& R, const moe_expert
   a.mat[0][1] = qptr(s_or_r->down);
   a.mat[1][0] = a.mat[0][0];
   a.mat[1][1] = a.mat[0][1];
-  const int g1 = (int)std::max<size_t>(1, std::min<size_t>((size_t)sms, maxt * (d.d / 128)));
+  const int g1 = (int)std::max<size_t>(1, std::min<size_t>((size_t)sms, maxt * (d.d / 256)));
   e = launch_gemm(1, m1, a, g1, st);
   return cuda_status(e);
 }
@@ -322,6 +324,7 @@ moe_status moe_expert_forward(const moe_dims* dims, const uint16_t* x, const moe
   if (shared != nullptr && dims->F_shared == 0) return MOE_ERR_INVALID_ARG;
   if (shared == nullptr && dims->F_shared != 0) return MOE_ERR_INVALID_ARG;
   if (dims->T == 0) return MOE_OK;
+  if (dims->d % 256 != 0) return MOE_ERR_UNSUPPORTED;   // grouped-GEMM path
   if ((s = check_ptr(x)) != MOE_OK) return s;
   if ((s = check_ptr(y_perm)) != MOE_OK) return s;
   if ((s = check_ptr(workspace)) != MOE_OK) return s == MOE_ERR_INVALID_ARG ? MOE_ERR_WORKSPACE : s;
@@ -386,6 +389,7 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
     return MOE_OK;
   }
 
+  if (d.d % 256 != 0) return MOE_ERR_UNSUPPORTED;   // grouped-GEMM path
   const RoutingPtrs R = routing_out ? caller_routing(routing_out) : internal_routing(workspace, L);
   uint16_t* xperm = at<uint16_t>(workspace, L.xperm);
   float* gs = sh ? at<float>(workspace, L.gs) : nullptr;

@@ -38,9 +38,11 @@ constexpr uint32_t kRawBytes = 128 * 64;     // 128 rows x 128 packed 4-bit code
 
 template <int MODE>
 struct Cfg {
-  static constexpr int NMAT = MODE == 0 ? 2 : 1;
-  static constexpr int S_RAW = MODE == 0 ? 3 : 4;   // packed-code stages of two K chunks each
-  static constexpr int S_W = MODE == 0 ? 3 : 4;   // operand stages: W (dequantised) and X together
+  // Two weight tiles per unit: gate and up rows f .. f+127 (gate/up mode), or the down rows of two
+  // adjacent 128-row blocks (down mode); both share the unit's activation tile.
+  static constexpr int NMAT = 2;
+  static constexpr int S_RAW = 3;   // packed-code stages of two K chunks each
+  static constexpr int S_W = 3;     // operand stages: W (dequantised) and X together
   static constexpr int S_X = S_W;
   static constexpr int NBAR = 2 * S_RAW + 2 * S_W + 4;
   static constexpr uint32_t OFF_W = 0;
@@ -169,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
   const int R = MODE == 0 ? a.F : a.d;   // weight rows (output features of this projection)
   const int K = MODE == 0 ? a.d : a.F;   // reduction length
-  const int MT = R / kBM;
+  const int MT = R / (MODE == 0 ? kBM : 2 * kBM);   // units per block-map tile
   const int KC = K / 64;
   const int num_units = (*a.num_tiles) * MT;
   const int4* tiles = reinterpret_cast<const int4*>(a.tiles);
@@ -196,7 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             mbar_arrive_expect_tx(RF(s), NMAT * kRawBytes);
 #pragma unroll
             for (int mat = 0; mat < NMAT; ++mat)
-              tma_load_3d(sRaw + (s * NMAT + mat) * kRawBytes, &maps.codes[mat][which], RF(s), kc * 8, m * kBM, ec);
+              tma_load_3d(sRaw + (s * NMAT + mat) * kRawBytes, &maps.codes[MODE == 0 ? mat : 0][which], RF(s), kc * 8,
+                          (MODE == 0 ? m : 2 * m + mat) * kBM, ec);
             if (++s == C::S_RAW) { s = 0; ph ^= 1u; }
           }
           // activation tile: 128 slot rows x 64 columns (x in slot order, or h); rows past the
@@ -257,13 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     // warps 2-3 idle (keeps the dequant warps at 4..11 and the epilogue warps at 12..15)
   } else if (warp < 12) {
     // ------------------------------------------------------------ dequant: 8 warps; thread i
-    // handles weight row i % 128 and half i / 128 of every chunk: the gate (0) or up (1) matrix
-    // in gate/up mode, code words 0-3 (0) or 4-7 (1) of the 64-code chunk in down mode.
+    // handles row i % 128 of weight tile i / 128 of every chunk: the gate (0) or up (1) matrix in
+    // gate/up mode, the first or second 128-row block of the unit in down mode.
     const int i = (threadIdx.x - 128) & 127;
-    const int half = (threadIdx.x - 128) >> 7;
-    const int mat = MODE == 0 ? half : 0;
-    constexpr int NW = MODE == 0 ? 8 : 4;   // code words per thread per chunk
-    const int w0 = MODE == 0 ? 0 : 4 * half;
+    const int mat = (threadIdx.x - 128) >> 7;
+    constexpr int NW = 8;   // code words per thread per chunk
+    const int w0 = 0;
     const uint32_t swz = (uint32_t)(i & 7);
     int s = 0, sw = 0;
     uint32_t ph = 0, phw = 0;
@@ -275,9 +277,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     auto rows_of = [&](int u, const uint16_t*& sr, const uint16_t*& br) {
       const int4 t = tile_of(u);
       const int which = t.x == a.E ? 1 : 0;
-      const size_t row = (size_t)(which ? 0 : t.x) * R + (size_t)(u % MT) * kBM + i;
-      sr = a.mat[mat][which].scales + row * G;
-      br = a.mat[mat][which].biases + row * G;
+      const int blk = MODE == 0 ? (u % MT) : 2 * (u % MT) + mat;   // 128-row block of the matrix
+      const size_t row = (size_t)(which ? 0 : t.x) * R + (size_t)blk * kBM + i;
+      const QPtr& qm = a.mat[MODE == 0 ? mat : 0][which];
+      sr = qm.scales + row * G;
+      br = qm.biases + row * G;
     };
     const uint16_t* srow = nullptr;
     const uint16_t* brow = nullptr;
@@ -376,11 +380,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       const int b = li & 1;
       if (!mbar_wait_warp(AF(b), (li >> 1) & 1, abort_s, a.err)) break;
       tc_fence_after();
-      const int rowg = m * kBM + q * 32 + lane;
       const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::ACC_COLS);
       // Per 16-token block: TMEM -> registers -> this warp's staging buffer ([token][32 rows]) ->
       // 16-byte stores of each token's 32 contiguous output columns.
-      const int col0 = m * kBM + q * 32;   // first output column of this warp's rows
+      const int col0 = m * kBM + q * 32;   // gate/up mode: first output column of this warp's rows
       for (int n0 = 0; n0 < tl.z; n0 += 16) {
         uint32_t g[16];
         if (MODE == 0) {
@@ -405,38 +408,43 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             }
           }
           __syncwarp();
-        } else if (a.y16 != nullptr) {
-          tmem_ld16_wait(tb + n0, g);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const __half yh = __float2half_rn(__uint_as_float(g[i]));
-            if (n0 + i < tl.z) bad = bad || (__hisinf(yh) != 0);
-            st_shared_u16(stg + (uint32_t)(i * 32 + lane) * 2, __half_as_ushort(yh));
-          }
-          __syncwarp();
-#pragma unroll
-          for (int c = lane; c < 64; c += 32) {
-            const int n = c >> 2, p = c & 3;
-            if (n0 + n < tl.z) {
-              const uint4 v = ld_shared_v4(stg + (uint32_t)(n * 32 + p * 8) * 2);
-              *reinterpret_cast<uint4*>(a.y16 + (size_t)(tl.y + n0 + n) * a.d + col0 + p * 8) = v;
-            }
-          }
-          __syncwarp();
         } else {
-          tmem_ld16_wait(tb + n0, g);
+          // down mode: the unit's two 128-row blocks sit in TMEM columns 0..127 and 128..255
+#pragma unroll 1
+          for (int mat = 0; mat < 2; ++mat) {
+            const int colm = (2 * m + mat) * kBM + q * 32;
+            tmem_ld16_wait(tb + (uint32_t)(mat * 128) + n0, g);
+            if (a.y16 != nullptr) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) st_shared_u32(stg + (uint32_t)(i * 32 + lane) * 4, g[i]);
-          __syncwarp();
+              for (int i = 0; i < 16; ++i) {
+                const __half yh = __float2half_rn(__uint_as_float(g[i]));
+                if (n0 + i < tl.z) bad = bad || (__hisinf(yh) != 0);
+                st_shared_u16(stg + (uint32_t)(i * 32 + lane) * 2, __half_as_ushort(yh));
+              }
+              __syncwarp();
 #pragma unroll
-          for (int c = lane; c < 128; c += 32) {
-            const int n = c >> 3, p = c & 7;
-            if (n0 + n < tl.z) {
-              const uint4 v = ld_shared_v4(stg + (uint32_t)(n * 32 + p * 4) * 4);
-              *reinterpret_cast<uint4*>(a.y_perm + (size_t)(tl.y + n0 + n) * a.d + col0 + p * 4) = v;
+              for (int c = lane; c < 64; c += 32) {
+                const int n = c >> 2, p = c & 3;
+                if (n0 + n < tl.z) {
+                  const uint4 v = ld_shared_v4(stg + (uint32_t)(n * 32 + p * 8) * 2);
+                  *reinterpret_cast<uint4*>(a.y16 + (size_t)(tl.y + n0 + n) * a.d + colm + p * 8) = v;
+                }
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) st_shared_u32(stg + (uint32_t)(i * 32 + lane) * 4, g[i]);
+              __syncwarp();
+#pragma unroll
+              for (int c = lane; c < 128; c += 32) {
+                const int n = c >> 3, p = c & 7;
+                if (n0 + n < tl.z) {
+                  const uint4 v = ld_shared_v4(stg + (uint32_t)(n * 32 + p * 4) * 4);
+                  *reinterpret_cast<uint4*>(a.y_perm + (size_t)(tl.y + n0 + n) * a.d + colm + p * 4) = v;
+                }
+              }
             }
+            __syncwarp();
           }
-          __syncwarp();
         }
       }
       tc_fence_before();

@@ -215,6 +215,21 @@ def test_decode_shapes_and_gemm_fallback_at_t1(d, F, tol):
     assert rowwise_err(got, ref) <= tol
 
 
+def test_gemm_path_needs_d_multiple_of_256():
+    """The grouped-GEMM path pairs 128-row blocks of d: d = 384 at T > 1 is refused up front."""
+    wl = synth.Workload("d384", T=8, d=384, E=16, k=2, F=128, F_shared=128)
+    host = synth.make_layer(wl)
+    dl = moe.to_device_layer(host)
+    inp = synth.make_inputs(wl, seed=9)
+    dm = moe.dims(wl.T, wl.d, wl.E, wl.k, wl.F, wl.F_shared)
+    ws = moe.alloc_workspace(dm)
+    y = torch.zeros((wl.T, wl.d), dtype=torch.float32, device="cuda")
+    x, lg = dev(inp["x"]), dev(inp["logits"])
+    with pytest.raises(moe.MoeError) as ei:
+        moe.layer_forward(dm, x, lg, dl["routed"], dl["shared"], dl["w_sg"], y, ws)
+    assert ei.value.status == 2   # MOE_ERR_UNSUPPORTED
+
+
 def test_decode_routing_out_matches_oracle():
     wl = synth.DECODE
     host, dl = layer_for(wl)
