@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int q = warp & 3;   // TMEM lane quarter this warp may access
     const uint32_t stg = sbase + C::OFF_STG + (uint32_t)q * 2048u;
     int li = 0;
-    bool bad = false;
+    float amax = 0.0f;   // largest |value| rounded to fp16 (above 65504 it does not fit)
     int4 tl_next = tile_of(blockIdx.x);
     for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++li) {
       const int4 tl = tl_next;
@@ -384,7 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       // Per 16-token block: TMEM -> registers -> this warp's staging buffer ([token][32 rows]) ->
       // 16-byte stores of each token's 32 contiguous output columns.
       const int col0 = m * kBM + q * 32;   // gate/up mode: first output column of this warp's rows
-      for (int n0 = 0; n0 < tl.z; n0 += 16) {
+      const int nstep = (MODE == 1 && a.y16 != nullptr) ? 32 : 16;   // fp16 down outputs: 32 per round
+      for (int n0 = 0; n0 < tl.z; n0 += nstep) {
         uint32_t g[16];
         if (MODE == 0) {
           uint32_t uu[16];
@@ -394,9 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           for (int i = 0; i < 16; ++i) {
             const float gv = __uint_as_float(g[i]);
             const float hv = gv * __frcp_rn(1.0f + __expf(-gv)) * __uint_as_float(uu[i]);
-            const __half hh = __float2half_rn(hv);
-            if (n0 + i < tl.z) bad = bad || (__hisinf(hh) != 0);
-            st_shared_u16(stg + (uint32_t)(i * 32 + pos) * 2, __half_as_ushort(hh));
+            if (n0 + i < tl.z) amax = fmaxf(amax, fabsf(hv));
+            st_shared_u16(stg + (uint32_t)(i * 32 + pos) * 2, __half_as_ushort(__float2half_rn(hv)));
           }
           __syncwarp();
 #pragma unroll
@@ -413,17 +413,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll 1
           for (int mat = 0; mat < 2; ++mat) {
             const int colm = (2 * m + mat) * kBM + q * 32;
-            tmem_ld16_wait(tb + (uint32_t)(mat * 128) + n0, g);
             if (a.y16 != nullptr) {
+              // 32 tokens: two 16-column loads and one wait, then [token][32 rows] staging (2 KB)
+              uint32_t g1[16];
+              tmem_ld16x2_wait(tb + (uint32_t)(mat * 128) + n0, tb + (uint32_t)(mat * 128) + n0 + 16, g, g1);
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
-                const __half yh = __float2half_rn(__uint_as_float(g[i]));
-                if (n0 + i < tl.z) bad = bad || (__hisinf(yh) != 0);
-                st_shared_u16(stg + (uint32_t)(i * 32 + lane) * 2, __half_as_ushort(yh));
+                const float v0 = __uint_as_float(g[i]), v1 = __uint_as_float(g1[i]);
+                if (n0 + i < tl.z) amax = fmaxf(amax, fabsf(v0));
+                if (n0 + 16 + i < tl.z) amax = fmaxf(amax, fabsf(v1));
+                st_shared_u16(stg + (uint32_t)(i * 32 + lane) * 2, __half_as_ushort(__float2half_rn(v0)));
+                st_shared_u16(stg + (uint32_t)((i + 16) * 32 + lane) * 2, __half_as_ushort(__float2half_rn(v1)));
               }
               __syncwarp();
 #pragma unroll
-              for (int c = lane; c < 64; c += 32) {
+              for (int c = lane; c < 128; c += 32) {
                 const int n = c >> 2, p = c & 3;
                 if (n0 + n < tl.z) {
                   const uint4 v = ld_shared_v4(stg + (uint32_t)(n * 32 + p * 8) * 2);
@@ -431,6 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 }
               }
             } else {
+              tmem_ld16_wait(tb + (uint32_t)(mat * 128) + n0, g);
 #pragma unroll
               for (int i = 0; i < 16; ++i) st_shared_u32(stg + (uint32_t)(i * 32 + lane) * 4, g[i]);
               __syncwarp();
@@ -451,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       __syncwarp();
       if (lane == 0) mbar_arrive(AE(b));
     }
-    if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) raise_flag(a.err, kErrFp16Range);
+    if (__any_sync(0xFFFFFFFFu, !(amax <= 65504.0f)) && lane == 0) raise_flag(a.err, kErrFp16Range);
   }
 
   // Wind down.  After a timeout, give copies that may still be in flight time to land before
