@@ -14,7 +14,7 @@ namespace {
 constexpr int kTileN = 128;   // block-map tile of the layer call (token rows per MMA tile)
 
 struct Layout {
-  size_t err, xperm, gs, idx, w, counts, offsets, perm, inv, tiles, num_tiles, chunk, h, yperm, hdec, total;
+  size_t err, xperm, gs, idx, w, counts, offsets, perm, inv, tiles, num_tiles, sched, chunk, h, yperm, hdec, total;
 };
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -49,6 +49,7 @@ Layout layout_of(const moe_dims& d) {
   L.inv = take(T * k * 4);
   L.tiles = take(max_tiles_of(d.T, d.k, d.E, kTileN, sh) * 16);
   L.num_tiles = take(16);
+  L.sched = take(max_tiles_of(d.T, d.k, d.E, 16, sh) * 4);   // GEMM walk order (any tile_n >= 16)
   L.chunk = take(tables_scratch_bytes((int)T, (int)E));   // routing-table scratch
   L.h = take(slots * F * 2);
   L.yperm = take(slots * D * 2);   // fp16 expert outputs of the layer path
@@ -214,7 +215,7 @@ QPtr qptr(const moe_qmat& q) { return QPtr{q.codes, q.scales, q.biases}; }
 // fp16 y16 when y16 is non-null) over the block map in R.
 moe_status run_experts(const moe_dims& d, const RoutingPtrs& R, const moe_experts* routed, const moe_experts* shared,
                        const uint16_t* x, uint16_t* xperm, uint16_t* h, float* y_perm, uint16_t* y16,
-                       uint32_t* err, cudaStream_t st) {
+                       int32_t* sched, uint32_t* err, cudaStream_t st) {
   // the down GEMM pairs 128-row blocks of the output dimension
   if (d.d % 256 != 0) return MOE_ERR_UNSUPPORTED;
   const bool sh = shared != nullptr && d.F_shared > 0;
@@ -233,6 +234,8 @@ moe_status run_experts(const moe_dims& d, const RoutingPtrs& R, const moe_expert
   if (!ok) return MOE_ERR_CUDA;
   PermuteArgs pa{x, R.perm, d.T, d.k, d.d, (int)slots, xperm, err};
   if (launch_permute_x(pa, st) != cudaSuccess) return MOE_ERR_CUDA;
+  ScheduleArgs sa{R.tiles, R.num_tiles, R.tile_n, sched, err};
+  if (launch_schedule(sa, st) != cudaSuccess) return MOE_ERR_CUDA;
   m0.h = m1.h;
   m1.codes[1][0] = m1.codes[0][0];
   m1.codes[1][1] = m1.codes[0][1];
@@ -241,6 +244,7 @@ moe_status run_experts(const moe_dims& d, const RoutingPtrs& R, const moe_expert
   GemmArgs a{};
   a.tiles = R.tiles;
   a.num_tiles = R.num_tiles;
+  a.sched = sched;
   a.perm = R.perm;
   a.T = d.T;
   a.k = d.k;
@@ -333,7 +337,7 @@ moe_status moe_expert_forward(const moe_dims* dims, const uint16_t* x, const moe
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* err = at<uint32_t>(workspace, L.err);
   return run_experts(*dims, caller_routing(routing), routed, shared, x, at<uint16_t>(workspace, L.xperm),
-                     at<uint16_t>(workspace, L.h), y_perm, nullptr, err, st);
+                     at<uint16_t>(workspace, L.h), y_perm, nullptr, at<int32_t>(workspace, L.sched), err, st);
 }
 
 moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const float* logits, const moe_experts* routed,
@@ -396,8 +400,8 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
   cudaError_t e = run_routing(d, logits, R, x, sh ? w_shared_gate : nullptr, gs, at<int32_t>(workspace, L.chunk), err, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   uint16_t* y16 = at<uint16_t>(workspace, L.yperm);
-  s = run_experts(d, R, routed, sh ? shared : nullptr, x, xperm, at<uint16_t>(workspace, L.h), nullptr, y16, err,
-                  st);
+  s = run_experts(d, R, routed, sh ? shared : nullptr, x, xperm, at<uint16_t>(workspace, L.h), nullptr, y16,
+                  at<int32_t>(workspace, L.sched), err, st);
   if (s != MOE_OK) return s;
   CombineArgs cb{nullptr, y16, R.inv, R.w, gs, d.T, d.k, d.d, y};
   return cuda_status(launch_combine(cb, st));

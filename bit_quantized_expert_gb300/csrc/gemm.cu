@@ -175,9 +175,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   const int KC = K / 64;
   const int num_units = (*a.num_tiles) * MT;
   const int4* tiles = reinterpret_cast<const int4*>(a.tiles);
-  // Every role walks units blockIdx.x, +gridDim.x, ...; each loads the descriptor of its next unit
-  // one unit ahead so the global-memory latency of the block map stays off the critical path.
-  auto tile_of = [&](int u) { return u < num_units ? __ldg(tiles + u / MT) : make_int4(0, 0, 0, 0); };
+  // Every role walks units blockIdx.x, +gridDim.x, ... of the scheduled tile order (wide tiles
+  // first, so the round-robin split is balanced); each loads the descriptor of its next unit one
+  // unit ahead so the global-memory latency of the block map stays off the critical path.
+  auto tile_of = [&](int u) {
+    return u < num_units ? __ldg(tiles + __ldg(a.sched + u / MT)) : make_int4(0, 0, 0, 0);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer

@@ -29,6 +29,18 @@ struct TablesArgs {
   uint32_t* err;
 };
 size_t tables_scratch_bytes(int T, int E);
+
+// Order in which the grouped GEMM walks the block map: full tiles first (in block-map order), then
+// the partial tiles by decreasing width (ties in block-map order), so that the round-robin split
+// of units over the persistent CTAs gives every CTA a similar amount of work.
+struct ScheduleArgs {
+  const int32_t* tiles;     // block map rows (e, row0, rows, 0)
+  const int32_t* num_tiles;
+  int tile_n;
+  int32_t* sched;           // [>= num_tiles] tile index of the u-th scheduled tile
+  uint32_t* err;
+};
+cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t st);
 cudaError_t launch_tables(const TablesArgs& a, cudaStream_t st);
 
 // ---------------------------------------------------------------- grouped GEMM (gemm.cu)
@@ -49,6 +61,7 @@ struct GemmMaps {
 struct GemmArgs {
   const int32_t* tiles;      // block map rows (e, row0, rows, 0)
   const int32_t* num_tiles;
+  const int32_t* sched;      // walk order of the block map (launch_schedule)
   const int32_t* perm;       // slot -> assignment (gate/up gathers x rows)
   QPtr mat[2][2];            // [matrix][routed/shared]: scales and biases read by the dequant warps
   int T, k, E, d, F;

@@ -239,6 +239,52 @@ cudaError_t launch_topk(const RouteArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+constexpr int kMaxPartialTiles = 1088;   // one partial tile per expert (E <= 1024) + the shared expert
+
+__global__ void __launch_bounds__(1024, 1) schedule_kernel(ScheduleArgs a) {
+  __shared__ int pw[kMaxPartialTiles];
+  __shared__ int pidx[kMaxPartialTiles];
+  __shared__ int warp_tot[32];
+  __shared__ int total_s;
+  const int tid = threadIdx.x;
+  const int n = *a.num_tiles;
+  int full_base = 0, part_base = 0;
+  for (int i0 = 0; i0 < n; i0 += 1024) {
+    const int i = i0 + tid;
+    const int w = i < n ? __ldg(a.tiles + 4 * (size_t)i + 2) : 0;
+    const bool part = i < n && w < a.tile_n;
+    const bool full = i < n && !part;
+    const int fpos = block_excl_scan(full ? 1 : 0, warp_tot, &total_s);
+    const int ftot = total_s;
+    const int ppos = block_excl_scan(part ? 1 : 0, warp_tot, &total_s);
+    const int ptot = total_s;
+    if (full) a.sched[full_base + fpos] = i;
+    if (part) {
+      if (part_base + ppos < kMaxPartialTiles) {
+        pw[part_base + ppos] = w;
+        pidx[part_base + ppos] = i;
+      } else {
+        raise_flag(a.err, kErrBadRouting);   // more partial tiles than a block map can hold
+      }
+    }
+    full_base += ftot;
+    part_base += ptot;
+  }
+  __syncthreads();
+  const int np = min(part_base, kMaxPartialTiles);
+  for (int p = tid; p < np; p += 1024) {
+    const int w = pw[p];
+    int before = 0;
+    for (int q = 0; q < np; ++q) before += (pw[q] > w || (pw[q] == w && q < p)) ? 1 : 0;
+    a.sched[full_base + before] = pidx[p];
+  }
+}
+
+cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t st) {
+  schedule_kernel<<<1, 1024, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
 size_t tables_scratch_bytes(int T, int E) { return (size_t)((T + 31) / 32) * E * sizeof(int); }
 
 cudaError_t launch_tables(const TablesArgs& a, cudaStream_t st) {
