@@ -12,9 +12,9 @@
 //   * Work unit = (block-map tile of <= 128 slots of one expert, 128-row slice of the weight
 //     matrix), iterated over K in chunks of 64 (= one quantisation group).  A persistent grid of
 //     one CTA per SM walks the units; every role walks the same list.
-//   * Warp roles (16 warps): 0 = TMA producer (packed codes, and the activation tiles of both
-//     projections: x rows in slot order, or h), 1 = MMA issuer (one thread) and TMEM owner,
-//     2-3 = idle, 4-11 = dequant
+//   * Warp roles (16 warps): 0 = TMA producer of the activation tiles (x rows in slot order, or
+//     h), 1 = MMA issuer (one thread) and TMEM owner, 2 = TMA producer of the packed codes,
+//     3 = idle, 4-11 = dequant
 //     (two threads per weight row: 4-bit codes -> fp16 w = q*scale + bias, single rounding; two
 //     dequant warps per scheduler so one hides the other's shared-memory and barrier latency),
 //     12-15 = epilogue (TMEM -> registers; SwiGLU -> fp16 h, or fp32 expert outputs).
@@ -41,7 +41,7 @@ struct Cfg {
   // Two weight tiles per unit: gate and up rows f .. f+127 (gate/up mode), or the down rows of two
   // adjacent 128-row blocks (down mode); both share the unit's activation tile.
   static constexpr int NMAT = 2;
-  static constexpr int S_RAW = 3;   // packed-code stages of two K chunks each
+  static constexpr int S_RAW = 4;   // packed-code stages of two K chunks each
   static constexpr int S_W = 3;     // operand stages: W (dequantised) and X together
   static constexpr int S_X = S_W;
   static constexpr int NBAR = 2 * S_RAW + 2 * S_W + 4;
@@ -53,6 +53,7 @@ struct Cfg {
   static constexpr uint32_t OFF_STG = (OFF_MISC + 16 + 15) & ~15u;   // epilogue staging, 2 KB per warp
   static constexpr uint32_t BYTES = OFF_STG + 4 * 2048 + 1024;        // + alignment slack
   static constexpr uint32_t ACC_COLS = NMAT * 128;          // TMEM columns of one accumulator buffer
+  static_assert(BYTES <= 227u * 1024u, "shared memory of one CTA");
 };
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -98,13 +99,21 @@ __device__ __forceinline__ uint32_t pick_bf16(const uint4& v) {
 }
 
 // One packed word (8 codes, logical columns 0..7) -> four fp16x2 words holding
-// (w0,w4), (w1,w5), (w2,w6), (w3,w7) with w = q * s + b rounded once to fp16.
+// (w0,w4), (w1,w5), (w2,w6), (w3,w7) with w = q * s + b rounded once to fp16.  A code pair is put
+// into the mantissa of 1024.0 (bits 0-3: 1024 + q exactly) or one nibble higher (bits 4-7:
+// 1024 + 16 q) and brought back to q exactly, by subtracting 1024 or by (1024 + 16 q) / 16 - 64,
+// so only one shift per word is needed.
 __device__ __forceinline__ void dequant_word(uint32_t q, __half2 s2, __half2 b2, uint32_t (&o)[4]) {
-  const __half2 magic = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));   // 1024
+  const __half2 k1024 = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));    // 1024
+  const __half2 k16th = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));    // 1/16
+  const __half2 km64 = __halves2half2(__ushort_as_half(0xD400), __ushort_as_half(0xD400));     // -64
+  const uint32_t r = q >> 8;
+  const uint32_t t[4] = {(q & 0x000F000Fu) | 0x64006400u, (q & 0x00F000F0u) | 0x64006400u,
+                         (r & 0x000F000Fu) | 0x64006400u, (r & 0x00F000F0u) | 0x64006400u};
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
-    const uint32_t t = ((q >> (4 * p)) & 0x000F000Fu) | 0x64006400u;   // (1024 + q_p, 1024 + q_{p+4})
-    __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&t), magic);   // exact codes
+    const __half2 h = *reinterpret_cast<const __half2*>(&t[p]);
+    __half2 v = (p & 1) ? __hfma2(h, k16th, km64) : __hsub2(h, k1024);   // exact codes
     v = __hfma2(v, s2, b2);
     o[p] = *reinterpret_cast<uint32_t*>(&v);
   }
@@ -183,10 +192,35 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   };
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer: activation tiles
+    // (one 128-row x 64-column box per K chunk: x rows in slot order, or h; rows past the tile's
+    // end belong to the next tile or lie outside the tensor (zero-filled), and the MMA columns
+    // they feed are never stored).  The packed codes have their own producer (warp 2), so their
+    // loads run up to S_RAW stages ahead of the dequant instead of waiting behind the operand
+    // ring, which only advances as fast as the MMAs retire.
     if (lane == 0) {
-      int s = 0, sx = 0;
-      uint32_t ph = 0, phx = 0;
+      int sx = 0;
+      uint32_t phx = 0;
+      int4 tl_next = tile_of(blockIdx.x);
+      for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+        const int4 tl = tl_next;
+        tl_next = tile_of(u + gridDim.x);
+        bool ok = true;
+        for (int kc = 0; kc < KC; ++kc) {
+          if (!mbar_wait(WE(sx), phx ^ 1u, abort_s, a.err)) { ok = false; break; }
+          mbar_arrive_expect_tx(WF(sx), kTileBytes);
+          tma_load_2d(sX + sx * kTileBytes, MODE == 0 ? &maps.x : &maps.h, WF(sx), kc * 64, tl.y);
+          if (++sx == C::S_X) { sx = 0; phx ^= 1u; }
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ TMA producer: packed codes of
+    // chunks kc and kc+1 (K is a multiple of 128) of the unit's weight tiles
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
       int4 tl_next = tile_of(blockIdx.x);
       for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
         const int4 tl = tl_next;
@@ -195,23 +229,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const int which = tl.x == a.E ? 1 : 0;
         const int ec = which ? 0 : tl.x;
         bool ok = true;
-        for (int kc = 0; kc < KC && ok; ++kc) {
-          if ((kc & 1) == 0) {   // packed codes of chunks kc and kc+1 (K is a multiple of 128)
-            if (!mbar_wait(RE(s), ph ^ 1u, abort_s, a.err)) { ok = false; break; }
-            mbar_arrive_expect_tx(RF(s), NMAT * kRawBytes);
+        for (int kc = 0; kc < KC; kc += 2) {
+          if (!mbar_wait(RE(s), ph ^ 1u, abort_s, a.err)) { ok = false; break; }
+          mbar_arrive_expect_tx(RF(s), NMAT * kRawBytes);
 #pragma unroll
-            for (int mat = 0; mat < NMAT; ++mat)
-              tma_load_3d(sRaw + (s * NMAT + mat) * kRawBytes, &maps.codes[MODE == 0 ? mat : 0][which], RF(s), kc * 8,
-                          (MODE == 0 ? m : 2 * m + mat) * kBM, ec);
-            if (++s == C::S_RAW) { s = 0; ph ^= 1u; }
-          }
-          // activation tile: 128 slot rows x 64 columns (x in slot order, or h); rows past the
-          // tile's end belong to the next tile or lie outside the tensor (zero-filled), and the
-          // MMA columns they feed are never stored
-          if (!mbar_wait(WE(sx), phx ^ 1u, abort_s, a.err)) { ok = false; break; }
-          mbar_arrive_expect_tx(WF(sx), kTileBytes);
-          tma_load_2d(sX + sx * kTileBytes, MODE == 0 ? &maps.x : &maps.h, WF(sx), kc * 64, tl.y);
-          if (++sx == C::S_X) { sx = 0; phx ^= 1u; }
+          for (int mat = 0; mat < NMAT; ++mat)
+            tma_load_3d(sRaw + (s * NMAT + mat) * kRawBytes, &maps.codes[MODE == 0 ? mat : 0][which], RF(s), kc * 8,
+                        (MODE == 0 ? m : 2 * m + mat) * kBM, ec);
+          if (++s == C::S_RAW) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
       }
@@ -259,8 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         tc_commit(AF(b));
       }
     }
-  } else if (warp < 4) {
-    // warps 2-3 idle (keeps the dequant warps at 4..11 and the epilogue warps at 12..15)
+  } else if (warp == 3) {
+    // idle (keeps the dequant warps at 4..11 and the epilogue warps at 12..15)
   } else if (warp < 12) {
     // ------------------------------------------------------------ dequant: 8 warps; thread i
     // handles row i % 128 of weight tile i / 128 of every chunk: the gate (0) or up (1) matrix in
