@@ -138,14 +138,14 @@ bool encode_codes(CUtensorMap* m, const uint32_t* codes, int n, int R, int C) {
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Row-major fp16 matrix [rows, cols] (h, or x in slot order) with a 64 x 128 box in the 128-byte
-// swizzle (the MMA operand layout).
-bool encode_f16_rows(CUtensorMap* m, const uint16_t* p, long long rows, int cols) {
+// Row-major fp16 matrix [rows, cols] (h, or x in slot order) with a box of 64 columns x box_rows
+// rows in the 128-byte swizzle (the MMA operand layout).
+bool encode_f16_rows(CUtensorMap* m, const uint16_t* p, long long rows, int cols, int box_rows) {
   EncodeTiledFn f = encode_fn();
   if (!f) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   const cuuint32_t es[2] = {1, 1};
   return f(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(p), dims, strides, box, es,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -230,13 +230,15 @@ moe_status run_experts(const moe_dims& d, const RoutingPtrs& R, const moe_expert
             encode_codes(&m0.codes[1][1], s_or_r->up.codes, ns, d.F, d.d) &&
             encode_codes(&m1.codes[0][0], routed->down.codes, d.E, d.d, d.F) &&
             encode_codes(&m1.codes[0][1], s_or_r->down.codes, ns, d.d, d.F) &&
-            encode_f16_rows(&m1.h, h, slots, d.F) && encode_f16_rows(&m0.x, xperm, slots, d.d);
+            encode_f16_rows(&m1.h, h, slots, d.F, 128) && encode_f16_rows(&m0.x, xperm, slots, d.d, 128) &&
+            encode_f16_rows(&m1.h16, h, slots, d.F, 16) && encode_f16_rows(&m0.x16, xperm, slots, d.d, 16);
   if (!ok) return MOE_ERR_CUDA;
   PermuteArgs pa{x, R.perm, d.T, d.k, d.d, (int)slots, xperm, err};
   if (launch_permute_x(pa, st) != cudaSuccess) return MOE_ERR_CUDA;
   ScheduleArgs sa{R.tiles, R.num_tiles, R.tile_n, sched, err};
   if (launch_schedule(sa, st) != cudaSuccess) return MOE_ERR_CUDA;
   m0.h = m1.h;
+  m0.h16 = m1.h16;
   m1.codes[1][0] = m1.codes[0][0];
   m1.codes[1][1] = m1.codes[0][1];
 

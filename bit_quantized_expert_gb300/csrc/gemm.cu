@@ -166,8 +166,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       prefetch_tmap(&maps.codes[1][0]);
       prefetch_tmap(&maps.codes[1][1]);
     }
-    if (MODE == 1) prefetch_tmap(&maps.h);
-    if (MODE == 0) prefetch_tmap(&maps.x);
+    if (MODE == 1) {
+      prefetch_tmap(&maps.h);
+      prefetch_tmap(&maps.h16);
+    }
+    if (MODE == 0) {
+      prefetch_tmap(&maps.x);
+      prefetch_tmap(&maps.x16);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -193,11 +199,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer: activation tiles
-    // (one 128-row x 64-column box per K chunk: x rows in slot order, or h; rows past the tile's
-    // end belong to the next tile or lie outside the tensor (zero-filled), and the MMA columns
-    // they feed are never stored).  The packed codes have their own producer (warp 2), so their
-    // loads run up to S_RAW stages ahead of the dequant instead of waiting behind the operand
-    // ring, which only advances as fast as the MMAs retire.
+    // (x rows in slot order, or h; per K chunk the tile's rows rounded up to 16 -- the MMA's N --
+    // by 64 columns: one 128-row box for a full tile, else 16-row boxes, so narrow tiles do not
+    // pull unused rows through L2 and shared memory; rows past the tile's end belong to the next
+    // tile or lie outside the tensor (zero-filled), and the MMA columns they feed are never
+    // stored).  The packed codes have their own producer (warp 2), so their loads run up to
+    // S_RAW stages ahead of the dequant instead of waiting behind the operand ring, which only
+    // advances as fast as the MMAs retire.
     if (lane == 0) {
       int sx = 0;
       uint32_t phx = 0;
@@ -205,11 +213,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
         const int4 tl = tl_next;
         tl_next = tile_of(u + gridDim.x);
+        const int n16 = (tl.z + 15) >> 4;   // 16-row groups of the tile (1..8)
         bool ok = true;
         for (int kc = 0; kc < KC; ++kc) {
           if (!mbar_wait(WE(sx), phx ^ 1u, abort_s, a.err)) { ok = false; break; }
-          mbar_arrive_expect_tx(WF(sx), kTileBytes);
-          tma_load_2d(sX + sx * kTileBytes, MODE == 0 ? &maps.x : &maps.h, WF(sx), kc * 64, tl.y);
+          mbar_arrive_expect_tx(WF(sx), (uint32_t)n16 * 16u * 128u);
+          if (n16 == 8) {
+            tma_load_2d(sX + sx * kTileBytes, MODE == 0 ? &maps.x : &maps.h, WF(sx), kc * 64, tl.y);
+          } else {
+            for (int r = 0; r < n16; ++r)
+              tma_load_2d(sX + sx * kTileBytes + (uint32_t)r * 2048u, MODE == 0 ? &maps.x16 : &maps.h16, WF(sx),
+                          kc * 64, tl.y + 16 * r);
+          }
           if (++sx == C::S_X) { sx = 0; phx ^= 1u; }
         }
         if (!ok) break;

@@ -54,8 +54,10 @@ struct QPtr {
 // shared expert set, and (down projection) the h operand.
 struct GemmMaps {
   CUtensorMap codes[2][2];   // [matrix][0 = routed, 1 = shared]
-  CUtensorMap h;             // down projection: h [slots, F] fp16
-  CUtensorMap x;             // gate/up projection: x rows in slot order [slots, d] fp16
+  CUtensorMap h;             // down projection: h [slots, F] fp16, 128-row boxes
+  CUtensorMap x;             // gate/up projection: x rows in slot order [slots, d] fp16, 128-row boxes
+  CUtensorMap h16;           // the same two tensors with 16-row boxes (tiles narrower than 128)
+  CUtensorMap x16;
 };
 
 struct GemmArgs {
