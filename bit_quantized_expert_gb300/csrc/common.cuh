@@ -180,6 +180,32 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
       : "memory");
 }
 
+// The eight MMAs of one 64-wide K chunk for two weight tiles that share one activation tile:
+// for K step kk = 0..3 and tile j = 0..1, D_j (+)= A_j[kk] B[kk], where the operand of step kk
+// starts 32 bytes (2 in the descriptor's address field) after that of step kk-1 and the first
+// step accumulates only if `accumulate` is non-zero.  One asm statement, so every descriptor is
+// in a register before the first MMA and the eight instructions issue back to back: an issuing
+// warp that shares its scheduler with busy warps then waits for one issue slot per MMA, not for
+// the several an MMA and its descriptor arithmetic would need.
+__device__ __forceinline__ void tc_mma_f16_chunk2(uint32_t d0, uint32_t d1, uint64_t a0, uint64_t a1, uint64_t b,
+                                                  uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t"
+      "setp.ne.b32 p, %15, 0;\n\t"
+      "setp.ne.b32 t, %16, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %14, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], %6, %10, %14, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %14, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], %7, %11, %14, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %14, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], %8, %12, %14, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %14, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], %9, %13, %14, t;\n\t}" ::"r"(d0),
+      "r"(d1), "l"(a0), "l"(a0 + 2u), "l"(a0 + 4u), "l"(a0 + 6u), "l"(a1), "l"(a1 + 2u), "l"(a1 + 4u), "l"(a1 + 6u),
+      "l"(b), "l"(b + 2u), "l"(b + 4u), "l"(b + 6u), "r"(idesc), "r"(accumulate), "r"(1u)
+      : "memory");
+}
+
 // Arrive (once) on an mbarrier when all tcgen05 operations issued so far by this thread complete.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)

@@ -282,16 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           // Descriptors of the stage's tiles; each 16-element K step advances the start address
           // by 32 bytes (2 in the descriptor's address field, which cannot carry: stages lie
           // below 256 KB).
-          const uint64_t bdesc0 = smem_desc_sw128(sX + sw * kTileBytes);
-          uint64_t adesc0[NMAT];
-#pragma unroll
-          for (int mat = 0; mat < NMAT; ++mat) adesc0[mat] = smem_desc_sw128(sW + (sw * NMAT + mat) * kTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-            for (int mat = 0; mat < NMAT; ++mat)
-              tc_mma_f16(d0 + mat * 128, adesc0[mat] + 2u * kk, bdesc0 + 2u * kk, idesc, (kc | kk) != 0 ? 1u : 0u);
-          }
+          static_assert(NMAT == 2, "two weight tiles per unit");
+          tc_mma_f16_chunk2(d0, d0 + 128u, smem_desc_sw128(sW + (sw * NMAT + 0) * kTileBytes),
+                            smem_desc_sw128(sW + (sw * NMAT + 1) * kTileBytes), smem_desc_sw128(sX + sw * kTileBytes),
+                            idesc, kc != 0 ? 1u : 0u);
           tc_commit(WE(sw));
           if (++sw == C::S_W) { sw = 0; phw ^= 1u; }
         }
