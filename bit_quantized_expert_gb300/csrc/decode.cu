@@ -90,9 +90,11 @@ struct DecPlan {
 };
 
 // Warp-wide top-k of logits[0..E) and the softmax of the selected logits, with the candidates
-// held in registers (8 per lane up to E = 256, else 32); lane j < k returns expert j and its weight.
+// held in registers (8 per lane up to E = 256, else 32); lane j < k returns expert j and its
+// weight.  Up to 8 of 256 the merge form (no sequential rounds) is used.
 __device__ __forceinline__ void reg_topk(const float* __restrict__ logits, int E, int k, int* e_out, float* w_out) {
-  if (E <= 256) warp_topk_softmax<8>(logits, E, k, e_out, w_out);
+  if (E <= 256 && k <= 8) warp_top8_softmax(logits, E, k, e_out, w_out);
+  else if (E <= 256) warp_topk_softmax<8>(logits, E, k, e_out, w_out);
   else warp_topk_softmax<32>(logits, E, k, e_out, w_out);
 }
 
@@ -180,13 +182,6 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
   }
   pdl_wait();   // x and logits from upstream kernels are complete and visible past this point
 
-  // x: lane l owns quantisation group l (64 inputs); the loads go out before routing.
-  const bool active = lane < G;
-  uint4 xr[8];
-#pragma unroll
-  for (int c8 = 0; c8 < 8; ++c8)
-    xr[c8] = active ? __ldg(reinterpret_cast<const uint4*>(a.x) + lane * 8 + c8) : make_uint4(0u, 0u, 0u, 0u);
-
   if (warp == 0 && !shared_cta) {
     int e;
     float w;
@@ -217,6 +212,14 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
   }
   pdl_launch_dependents();
   __syncthreads();   // e_s and wgt_s
+  // x: lane l owns quantisation group l (64 inputs).  The loads go out after routing, so the
+  // logits are the first reads behind the dependency wait, and before the down copies; the
+  // gate/up products wait for the weights, which arrive later.
+  const bool active = lane < G;
+  uint4 xr[8];
+#pragma unroll
+  for (int c8 = 0; c8 < 8; ++c8)
+    xr[c8] = active ? __ldg(reinterpret_cast<const uint4*>(a.x) + lane * 8 + c8) : make_uint4(0u, 0u, 0u, 0u);
   if (!shared_cta) copy_dn(e_s);
 
   // ---- gate/up: warp w computes gate and up of rows q*8 + w (q = 0..3) as slots s = 2q + mat;
@@ -339,7 +342,8 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
   __syncthreads();
 
   // ---- y rows of this CTA: sum of all CTAs' partials in a fixed order (16 lanes per row, each
-  // summing every 16th CTA, then a fixed butterfly).
+  // summing every 16th CTA in increasing order, then a fixed butterfly).  The first ten loads of
+  // a lane go out together (one L2 round trip for grids up to 160 CTAs).
   if (!abort_s) {
     const int n = gridDim.x;
     const int rpc = (d + n - 1) / n;
@@ -349,8 +353,15 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
       const int r = rb + (tid >> 4);
       float acc = 0.0f;
       if (r < r_hi) {
-#pragma unroll 4
-        for (int c = sub; c < n; c += 16) acc += __ldcg(a.part + (size_t)c * d + r);
+        float v[10];
+#pragma unroll
+        for (int i = 0; i < 10; ++i) {
+          const int c = sub + 16 * i;
+          v[i] = c < n ? __ldcg(a.part + (size_t)c * d + r) : 0.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < 10; ++i) acc += v[i];
+        for (int c = sub + 160; c < n; c += 16) acc += __ldcg(a.part + (size_t)c * d + r);
       }
       acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 8);
       acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 4);

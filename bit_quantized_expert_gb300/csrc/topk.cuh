@@ -64,30 +64,27 @@ __device__ __forceinline__ void warp_topk_softmax(const float* __restrict__ row,
 }
 
 
-// E <= 256 variant with shorter rounds: every lane first sorts its 8 candidates (a 19-comparator
-// sorting network on (key, lower index first)), so a round only compares the lanes' heads:
-// redux.sync max, a ballot for ties (a second reduction, over expert indices, only when several
-// lanes hold the maximum) and a shift of the winning lane's list.
-__device__ __forceinline__ void warp_topk_softmax_sorted8(const float* __restrict__ row, int E, int k, int* e_out,
-                                                          float* w_out) {
+// E <= 256 and k <= 8, without sequential selection rounds: every lane sorts its 8 candidates
+// (Batcher's 19-comparator network), then five butterfly levels merge the lane's sorted top-8
+// with that of lane ^ m: the elementwise maximum of one list and the other reversed is a bitonic
+// sequence holding the 8 largest of both, which a 12-comparator bitonic merge sorts.  Partners
+// compute the same list, so after the last level every lane holds the row's sorted top-8.  A
+// candidate is (key << 32 | ~index): equal logits go to the lower expert index, and padding (0)
+// sorts below every logit.  Lane j < k returns the j-th expert and its routing weight.
+__device__ __forceinline__ void warp_top8_softmax(const float* __restrict__ row, int E, int k, int* e_out,
+                                                  float* w_out) {
   const int lane = threadIdx.x & 31;
-  uint64_t rk[8];   // key << 8 | (7 - i): larger first, equal keys -> lower i first
-  float v[8];
+  uint64_t c[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int e = lane + 32 * i;
-    const float x = e < E ? __ldg(row + e) : 0.0f;
-    rk[i] = ((uint64_t)(e < E ? logit_key(x) : 0u) << 8) | (uint64_t)(7 - i);
-    v[i] = x;
+    c[i] = e < E ? ((uint64_t)logit_key(__ldg(row + e)) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)e) : 0ull;
   }
-  auto cas = [&](int a, int b) {
-    const bool sw = rk[a] < rk[b];
-    const uint64_t ra = rk[a], rb = rk[b];
-    const float va = v[a], vb = v[b];
-    rk[a] = sw ? rb : ra;
-    rk[b] = sw ? ra : rb;
-    v[a] = sw ? vb : va;
-    v[b] = sw ? va : vb;
+  auto cas = [&](int a, int b) {   // c[a] >= c[b] afterwards
+    const uint64_t x = c[a], y = c[b];
+    const bool sw = x < y;
+    c[a] = sw ? y : x;
+    c[b] = sw ? x : y;
   };
   cas(0, 1); cas(2, 3); cas(4, 5); cas(6, 7);
   cas(0, 2); cas(1, 3); cas(4, 6); cas(5, 7);
@@ -95,33 +92,22 @@ __device__ __forceinline__ void warp_topk_softmax_sorted8(const float* __restric
   cas(0, 4); cas(1, 5); cas(2, 6); cas(3, 7);
   cas(2, 4); cas(3, 5);
   cas(1, 2); cas(3, 4); cas(5, 6);
-  int my_e = 0;
-  float my_v = 0.0f;
-  for (int j = 0; j < k; ++j) {
-    const uint32_t hk = (uint32_t)(rk[0] >> 8);
-    const int hidx = lane + 32 * (7 - (int)(rk[0] & 0xFFu));
-    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, hk);
-    const uint32_t tie = __ballot_sync(0xFFFFFFFFu, hk == m);
-    int wl;
-    if (__popc(tie) == 1) {
-      wl = __ffs(tie) - 1;
-    } else {
-      wl = (int)(__reduce_min_sync(0xFFFFFFFFu, hk == m ? (uint32_t)hidx : 0xFFFFFFFFu) & 31u);
-    }
-    const int widx = __shfl_sync(0xFFFFFFFFu, hidx, wl);
-    const float wv = __shfl_sync(0xFFFFFFFFu, v[0], wl);
-    if (lane == j) {
-      my_e = widx;
-      my_v = wv;
-    }
-    const bool me = lane == wl;
 #pragma unroll
-    for (int i = 0; i < 7; ++i) {
-      rk[i] = me ? rk[i + 1] : rk[i];
-      v[i] = me ? v[i + 1] : v[i];
-    }
-    rk[7] = me ? 0ull : rk[7];
+  for (int m = 1; m < 32; m <<= 1) {
+    uint64_t p[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) p[i] = __shfl_xor_sync(0xFFFFFFFFu, c[i], m);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = c[i] > p[7 - i] ? c[i] : p[7 - i];
+    cas(0, 4); cas(1, 5); cas(2, 6); cas(3, 7);
+    cas(0, 2); cas(1, 3); cas(4, 6); cas(5, 7);
+    cas(0, 1); cas(2, 3); cas(4, 5); cas(6, 7);
   }
+  uint64_t mine = 0ull;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mine = (lane == i) ? c[i] : mine;
+  const int my_e = lane < k ? (int)(0xFFFFFFFFu - (uint32_t)mine) : 0;
+  const float my_v = lane < k ? __ldg(row + my_e) : 0.0f;
   const float vmax = __shfl_sync(0xFFFFFFFFu, my_v, 0);
   const float ex = (lane < k) ? expf(my_v - vmax) : 0.0f;
   float s = ex;

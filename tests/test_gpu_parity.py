@@ -108,6 +108,26 @@ def test_route_ties_zero_signs_nan_and_ragged():
     assert got["idx"][0].tolist() == [0, 1, 2, 3, 4]
 
 
+def test_route_ties_zero_signs_nan_wide_rows():
+    # 129..256 experts with k <= 8 take the merge form of the warp top-k
+    for E, k in ((256, 8), (200, 6), (129, 1)):
+        wl = synth.Workload("edge", T=41, d=256, E=E, k=k, F=128, F_shared=128)
+        rng = np.random.default_rng(E + k)
+        lg = rng.integers(-1, 2, size=(wl.T, wl.E)).astype(np.float32)    # heavy ties
+        lg[0] = 0.0
+        lg[1, :] = -0.0
+        lg[1, ::3] = 0.0
+        lg[2, 5] = np.nan
+        lg[2, 7] = -np.inf
+        lg[3, :] = np.nan
+        lg[3, E - 1] = 1.0
+        lg[4, :] = -np.inf
+        lg[5, ::7] = np.inf
+        got = run_route(wl, lg, 16)
+        assert_routing_equal(got, lg, wl.E, wl.k, 16)
+        assert got["idx"][0].tolist() == list(range(k))
+
+
 @pytest.mark.parametrize("T,E,k", [(1, 16, 1), (5, 8, 8), (300, 1024, 32), (2049, 256, 8), (64, 33, 3)])
 def test_route_shapes(T, E, k):
     wl = synth.Workload("shape", T=T, d=256, E=E, k=k, F=128, F_shared=128)
