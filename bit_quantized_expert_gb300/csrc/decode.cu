@@ -91,10 +91,9 @@ struct DecPlan {
 
 // Warp-wide top-k of logits[0..E) and the softmax of the selected logits, with the candidates
 // held in registers (8 per lane up to E = 256, else 32); lane j < k returns expert j and its
-// weight.  Up to 8 of 256 the merge form (no sequential rounds) is used.
+// weight.
 __device__ __forceinline__ void reg_topk(const float* __restrict__ logits, int E, int k, int* e_out, float* w_out) {
-  if (E <= 256 && k <= 8) warp_top8_softmax(logits, E, k, e_out, w_out);
-  else if (E <= 256) warp_topk_softmax<8>(logits, E, k, e_out, w_out);
+  if (E <= 256) warp_topk_softmax<8>(logits, E, k, e_out, w_out);
   else warp_topk_softmax<32>(logits, E, k, e_out, w_out);
 }
 

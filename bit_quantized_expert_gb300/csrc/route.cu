@@ -22,8 +22,7 @@ __global__ void __launch_bounds__(256) topk_kernel(RouteArgs a) {
   if (t >= a.T) return;
   int my_e;
   float my_w;
-  if (NI == 8 && a.k <= 8) warp_top8_softmax(a.logits + (size_t)t * a.E, a.E, a.k, &my_e, &my_w);
-  else warp_topk_softmax<NI>(a.logits + (size_t)t * a.E, a.E, a.k, &my_e, &my_w);
+  warp_topk_softmax<NI>(a.logits + (size_t)t * a.E, a.E, a.k, &my_e, &my_w);
   if (lane < a.k) {
     a.idx[(size_t)t * a.k + lane] = my_e;
     a.w[(size_t)t * a.k + lane] = my_w;

@@ -13,108 +13,68 @@ __device__ __forceinline__ uint32_t logit_key(float v) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Inverse of logit_key for keys of real logits: -0.0 comes back as +0.0 and every NaN as one
+// NaN, which leaves the softmax below unchanged.
+__device__ __forceinline__ float key_logit(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
 // Lane j < k returns the j-th expert in *e_out and its routing weight in *w_out.
 // NI = ceil(E / 32) candidates per lane (compile-time upper bound), lane l holding l + 32 i.
-// Each round takes the largest key with redux.sync max and, among the lanes holding it, the
-// lowest expert index with redux.sync min; the owning lane then clears that candidate.
+// Each round takes the lane's best candidate by a tree (the lower index wins a tie), the largest
+// key over the warp with redux.sync max and, among the lanes holding it, the lowest expert index
+// with redux.sync min; the owning lane then clears that candidate.  The winner's logit is the
+// inverse of its key (no broadcast); no lane branches inside a round.
 template <int NI>
 __device__ __forceinline__ void warp_topk_softmax(const float* __restrict__ row, int E, int k, int* e_out,
                                                   float* w_out) {
   const int lane = threadIdx.x & 31;
   uint32_t key[NI];
-  float val[NI];
 #pragma unroll
   for (int i = 0; i < NI; ++i) {
     const int e = lane + 32 * i;
-    const float v = e < E ? __ldg(row + e) : 0.0f;
-    key[i] = e < E ? logit_key(v) : 0u;
-    val[i] = v;
+    key[i] = e < E ? logit_key(__ldg(row + e)) : 0u;
   }
   int my_e = 0;
-  float my_v = 0.0f;
+  float my_v = 0.0f, vmax = 0.0f;
   for (int j = 0; j < k; ++j) {
-    uint32_t best = 0u, bi = 0xFFFFFFFFu;
-    float bestv = 0.0f;
+    uint32_t tk[NI], ti[NI];
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
-      if (key[i] > best) {   // strict: this lane's lowest index wins its ties
-        best = key[i];
-        bi = (uint32_t)(lane + 32 * i);
-        bestv = val[i];
+      tk[i] = key[i];
+      ti[i] = (uint32_t)i;
+    }
+#pragma unroll
+    for (int w = 1; w < NI; w <<= 1) {
+#pragma unroll
+      for (int i = 0; i + w < NI; i += 2 * w) {
+        const bool r = tk[i + w] > tk[i];   // strict: the left (lower index) wins a tie
+        tk[i] = r ? tk[i + w] : tk[i];
+        ti[i] = r ? ti[i + w] : ti[i];
       }
     }
+    const uint32_t best = tk[0];
     const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, best);
-    const uint32_t win = __reduce_min_sync(0xFFFFFFFFu, best == m ? bi : 0xFFFFFFFFu);
-    const float v_win = __shfl_sync(0xFFFFFFFFu, bestv, (int)(win & 31u));
+    const uint32_t win = __reduce_min_sync(0xFFFFFFFFu, best == m ? (uint32_t)lane + 32u * ti[0] : 0xFFFFFFFFu);
     const int sel = (lane == (int)(win & 31u)) ? (int)(win >> 5) : -1;
 #pragma unroll
     for (int i = 0; i < NI; ++i) key[i] = (i == sel) ? 0u : key[i];
-    if (lane == j) {
-      my_e = (int)win;
-      my_v = v_win;
-    }
+    const float v = key_logit(m);
+    vmax = j == 0 ? v : vmax;
+    my_e = lane == j ? (int)win : my_e;
+    my_v = lane == j ? v : my_v;
   }
-  const float vmax = __shfl_sync(0xFFFFFFFFu, my_v, 0);
-  const float ex = (lane < k) ? expf(my_v - vmax) : 0.0f;
-  float s = ex;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+  const float my_ex = lane < k ? expf(my_v - vmax) : 0.0f;
+  float s = my_ex;   // lanes >= k hold 0
+  if (k > 8) {
+    s += __shfl_xor_sync(0xFFFFFFFFu, s, 16);
+    s += __shfl_xor_sync(0xFFFFFFFFu, s, 8);
+  }
+  s += __shfl_xor_sync(0xFFFFFFFFu, s, 4);
+  s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
+  s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
   *e_out = my_e;
-  *w_out = ex / s;
-}
-
-
-// E <= 256 and k <= 8, without sequential selection rounds: every lane sorts its 8 candidates
-// (Batcher's 19-comparator network), then five butterfly levels merge the lane's sorted top-8
-// with that of lane ^ m: the elementwise maximum of one list and the other reversed is a bitonic
-// sequence holding the 8 largest of both, which a 12-comparator bitonic merge sorts.  Partners
-// compute the same list, so after the last level every lane holds the row's sorted top-8.  A
-// candidate is (key << 32 | ~index): equal logits go to the lower expert index, and padding (0)
-// sorts below every logit.  Lane j < k returns the j-th expert and its routing weight.
-__device__ __forceinline__ void warp_top8_softmax(const float* __restrict__ row, int E, int k, int* e_out,
-                                                  float* w_out) {
-  const int lane = threadIdx.x & 31;
-  uint64_t c[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int e = lane + 32 * i;
-    c[i] = e < E ? ((uint64_t)logit_key(__ldg(row + e)) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)e) : 0ull;
-  }
-  auto cas = [&](int a, int b) {   // c[a] >= c[b] afterwards
-    const uint64_t x = c[a], y = c[b];
-    const bool sw = x < y;
-    c[a] = sw ? y : x;
-    c[b] = sw ? x : y;
-  };
-  cas(0, 1); cas(2, 3); cas(4, 5); cas(6, 7);
-  cas(0, 2); cas(1, 3); cas(4, 6); cas(5, 7);
-  cas(1, 2); cas(5, 6);
-  cas(0, 4); cas(1, 5); cas(2, 6); cas(3, 7);
-  cas(2, 4); cas(3, 5);
-  cas(1, 2); cas(3, 4); cas(5, 6);
-#pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {
-    uint64_t p[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) p[i] = __shfl_xor_sync(0xFFFFFFFFu, c[i], m);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = c[i] > p[7 - i] ? c[i] : p[7 - i];
-    cas(0, 4); cas(1, 5); cas(2, 6); cas(3, 7);
-    cas(0, 2); cas(1, 3); cas(4, 6); cas(5, 7);
-    cas(0, 1); cas(2, 3); cas(4, 5); cas(6, 7);
-  }
-  uint64_t mine = 0ull;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) mine = (lane == i) ? c[i] : mine;
-  const int my_e = lane < k ? (int)(0xFFFFFFFFu - (uint32_t)mine) : 0;
-  const float my_v = lane < k ? __ldg(row + my_e) : 0.0f;
-  const float vmax = __shfl_sync(0xFFFFFFFFu, my_v, 0);
-  const float ex = (lane < k) ? expf(my_v - vmax) : 0.0f;
-  float s = ex;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
-  *e_out = my_e;
-  *w_out = ex / s;
+  *w_out = my_ex / s;
 }
 
 }  // namespace moe

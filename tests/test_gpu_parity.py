@@ -109,7 +109,7 @@ def test_route_ties_zero_signs_nan_and_ragged():
 
 
 def test_route_ties_zero_signs_nan_wide_rows():
-    # 129..256 experts with k <= 8 take the merge form of the warp top-k
+    # 129..256 experts: eight candidates per lane in the warp top-k
     for E, k in ((256, 8), (200, 6), (129, 1)):
         wl = synth.Workload("edge", T=41, d=256, E=E, k=k, F=128, F_shared=128)
         rng = np.random.default_rng(E + k)
