@@ -15,8 +15,9 @@
 //   * after it, warp 0 routes the token in registers (top-k of the 1 KB of logits; cheaper than a
 //     routing kernel and its launch) and starts the bulk copies of the 32 gate rows and 32 up rows
 //     (four quarters, one mbarrier each, so compute starts on the first quarter), while every
-//     thread copies the matching 32-column block of the down matrix (all d rows, 16 B each, plus
-//     the scale and bias of its quantisation group) with cp.async;
+//     thread copies the matching 32-column block of the down matrix (all d rows, 16 B each) with
+//     cp.async, and one thread bulk-copies the expert's down scales and biases whole (contiguous,
+//     so two large requests replace two small ones per row);
 //   * the CTA computes its 32 SwiGLU outputs h, then its share of the down projection,
 //     part_c[r] = w_j * sum_{f in f0..f0+31} W_down[e_j][r][f] h[f] for every output row r
 //     (a split over F: no CTA needs another CTA's h);
@@ -73,17 +74,20 @@ __device__ __forceinline__ float2 word_dot2(uint32_t w, const float2* xs, float2
 // Shared-memory plan of one CTA (byte offsets, 16-byte aligned regions).
 struct DecPlan {
   int d, F, k1, G, GF, grid;
+  bool bulk_sb;   // the down scales and biases of the expert copied whole (two bulk copies)
   uint32_t gu_codes, gu_sb, dn_codes, dn_sb, hbuf, bytes;
   __host__ __device__ DecPlan(int d_, int F_, int k1_) : d(d_), F(F_), k1(k1_) {
     G = d / 64;
     GF = F / 64;
     grid = k1 * (F / RF);
+    bulk_sb = 4u * (uint32_t)d * (uint32_t)GF <= 64u * 1024u;
     uint32_t o = 0;
     gu_codes = o;  o += 2u * RF * (d / 2);   // [gate|up][RF][d/8] u32
     gu_sb = o;     o += 4u * RF * G * 2;     // [g.s|g.b|u.s|u.b][RF][G] bf16
     o = (o + 15u) & ~15u;
     dn_codes = o;  o += 16u * d;             // [d][4] u32: code words f0/8 .. f0/8+3 of every row
-    dn_sb = o;     o += 8u * d;              // [s|b][d] u32: the bf16 pair holding group f0/64
+    dn_sb = o;                               // [s|b][d][GF] bf16 (whole matrices), or
+    o += bulk_sb ? 4u * d * GF : 8u * d;     // [s|b][d] u32: the bf16 pair holding group f0/64
     hbuf = o;      o += 4u * RF;             // h of rows f0 .. f0+31, fp32
     bytes = (o + 15u) & ~15u;
   }
@@ -125,15 +129,16 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
   uint32_t* gcodes = reinterpret_cast<uint32_t*>(sm + P.gu_codes);   // gate [RF][d/8], then up
   uint16_t* gsb = reinterpret_cast<uint16_t*>(sm + P.gu_sb);         // [g.s | g.b | u.s | u.b][RF][G]
   uint32_t* dcodes = reinterpret_cast<uint32_t*>(sm + P.dn_codes);   // [d][4]
-  uint32_t* dsb = reinterpret_cast<uint32_t*>(sm + P.dn_sb);         // [s | b][d]
+  uint32_t* dsb = reinterpret_cast<uint32_t*>(sm + P.dn_sb);         // [s | b][d] (pairs), or
+  uint16_t* dsb16 = reinterpret_cast<uint16_t*>(sm + P.dn_sb);       // [s | b][d][GF] (whole)
   float* hbuf = reinterpret_cast<float*>(sm + P.hbuf);               // [RF]
-  __shared__ __align__(8) uint64_t bars[kQuarters];
+  __shared__ __align__(8) uint64_t bars[kQuarters + 1];   // gate/up quarters, then the down scales
   __shared__ int e_s;
   __shared__ float wgt_s;    // w_j (routed) or the shared-expert gate
   __shared__ int abort_s;
 
   if (tid == 0) {
-    for (int i = 0; i < kQuarters; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    for (int i = 0; i <= kQuarters; ++i) mbar_init(smem_u32(&bars[i]), 1);
     abort_s = 0;
     mbar_fence_init();
   }
@@ -161,15 +166,28 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
     }
   };
   // Columns f0 .. f0+31 of every row of the down matrix of expert e: 16 code bytes per row, and
-  // the 4-byte aligned bf16 pairs holding the row's scale and bias of group f0/64.
+  // the row's scale and bias of group f0/64 -- where they fit, as the expert's whole scale and
+  // bias matrices (two contiguous bulk copies instead of two small requests per row), else as the
+  // 4-byte aligned bf16 pairs holding the group.
   auto copy_dn = [&](int e) {
     const QPtr& q = a.down[wset];
+    if (P.bulk_sb) {
+      if (tid == 0) {
+        const uint32_t bar = smem_u32(&bars[kQuarters]);
+        const uint32_t nb = 2u * d * GF;
+        mbar_arrive_expect_tx(bar, 2u * nb);
+        bulk_g2s(smem_u32(dsb16), q.scales + (size_t)e * d * GF, nb, bar);
+        bulk_g2s(smem_u32(dsb16 + d * GF), q.biases + (size_t)e * d * GF, nb, bar);
+      }
+    }
     const int g2 = (f0 / 64) & ~1;
     for (int r = tid; r < d; r += kThreadsDec) {
       const size_t row = (size_t)e * d + r;
       cp_async_16(smem_u32(dcodes + 4 * r), q.codes + row * (F / 8) + f0 / 8);
-      cp_async_4(smem_u32(dsb + r), q.scales + row * GF + g2);
-      cp_async_4(smem_u32(dsb + d + r), q.biases + row * GF + g2);
+      if (!P.bulk_sb) {
+        cp_async_4(smem_u32(dsb + r), q.scales + row * GF + g2);
+        cp_async_4(smem_u32(dsb + d + r), q.biases + row * GF + g2);
+      }
     }
     cp_async_commit();
   };
@@ -289,6 +307,7 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
     }
   }
   cp_async_wait<0>();
+  const bool ok_dn = !P.bulk_sb || mbar_wait_warp(smem_u32(&bars[kQuarters]), 0, &abort_s, a.err);
   __syncthreads();   // h and this thread's down copies -> visible to the whole CTA
 
   // ---- down share: part_c[r] = wgt * (s * sum_f q h_f + b * sum_f h_f) over f0 .. f0+31.
@@ -303,7 +322,8 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
     }
     const float wgt = wgt_s;
     const bool hi_half = ((f0 / 64) & 1) != 0;   // group f0/64 is the upper bf16 of its pair
-    for (int r = tid; r < d; r += kThreadsDec) {
+    const int g = f0 / 64;
+    for (int r = tid; r < d && ok_dn; r += kThreadsDec) {
       const uint4 c = *reinterpret_cast<const uint4*>(dcodes + 4 * r);
       float2 p0 = make_float2(0.0f, 0.0f), p1 = make_float2(0.0f, 0.0f);
       p0 = word_dot2(c.x, hv + 0, p0);
@@ -311,9 +331,15 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
       p0 = word_dot2(c.z, hv + 8, p0);
       p1 = word_dot2(c.w, hv + 12, p1);
       const float p = (p0.x + p0.y) + (p1.x + p1.y);
-      const uint32_t sp = dsb[r], bp = dsb[d + r];
-      const float s = bf16_bits_to_f32(hi_half ? (sp >> 16) : (sp & 0xFFFFu));
-      const float b = bf16_bits_to_f32(hi_half ? (bp >> 16) : (bp & 0xFFFFu));
+      float s, b;
+      if (P.bulk_sb) {
+        s = bf16_bits_to_f32(dsb16[r * GF + g]);
+        b = bf16_bits_to_f32(dsb16[(d + r) * GF + g]);
+      } else {
+        const uint32_t sp = dsb[r], bp = dsb[d + r];
+        s = bf16_bits_to_f32(hi_half ? (sp >> 16) : (sp & 0xFFFFu));
+        b = bf16_bits_to_f32(hi_half ? (bp >> 16) : (bp & 0xFFFFu));
+      }
       a.part[(size_t)cta * d + r] = wgt * fmaf(s, p, b * hsum);
     }
   }
@@ -372,7 +398,7 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
 
   // ---- wind down: after a timeout, copies still in flight must land before the CTA exits.
   if (tid == 0 && abort_s) {
-    for (int i = 0; i < kQuarters; ++i) {
+    for (int i = 0; i <= kQuarters; ++i) {
       const long long t0 = clock64();
       while (!mbar_try_wait(smem_u32(&bars[i]), 0) && clock64() - t0 < 4000000ll) {
       }
