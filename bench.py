@@ -40,7 +40,7 @@ NI = 64   # distinct input rows per layer for decode
 # dram__bytes_read.sum + dram__bytes_write.sum of one decode_layer_kernel launch at the decode
 # shape (ncu capture summarised in profiles/decode_layer_kernel_decode_T1.md); reset to None
 # whenever that kernel changes until it is captured again.
-DECODE_NCU_TRAFFIC = 15998080
+DECODE_NCU_TRAFFIC = 16000640
 
 
 def parse():
@@ -350,8 +350,9 @@ def prefill_bench(wl, steps, device, pk):
            "tensor": {"achieved": flops / step_s / 1e12, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                       "frac": flops / step_s / 1e12 / pk["bf16_tflops"], "algorithmic_flops": flops,
                       "note": "fp16 operands; peak is the measured bf16 dense rate (same nominal rate)"},
-           # top-k, chunk histogram, chunk scan, chunk scatter, x permute, gate/up GEMM, down GEMM, combine
-           "gpu_launches_per_step": 8}
+           # top-k, chunk histogram, chunk scan, chunk scatter, x permute, schedule, gate/up GEMM,
+           # down GEMM, combine
+           "gpu_launches_per_step": 9}
     del layers
     torch.cuda.empty_cache()
     return out
