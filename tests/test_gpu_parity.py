@@ -222,10 +222,13 @@ def test_decode_full_size():
 
 
 @pytest.mark.parametrize("d,F,tol", [(256, 384, DECODE_TOL),    # decode path, 3 column blocks of 128
+                                       (2048, 1024, DECODE_TOL),  # decode path, down scales per row
                                        (4096, 128, EXACT_TOL)])   # d > 2048: grouped-GEMM path at T = 1
 def test_decode_shapes_and_gemm_fallback_at_t1(d, F, tol):
-    """T = 1 at an F that is not a power of two (decode kernel) and at a width the decode kernel
-    does not take (served by the grouped-GEMM path)."""
+    """T = 1 at an F that is not a power of two (decode kernel), at a shape whose down scales and
+    biases are too large to copy whole (the decode kernel copies each row's group instead), and at
+    a width the decode kernel does not take (served by the grouped-GEMM path).  (k+1) F / 32 CTAs
+    must fit the SMs: 96 at F = 1024."""
     wl = synth.Workload(f"t1_d{d}_f{F}", T=1, d=d, E=16, k=2, F=F, F_shared=F)
     host = synth.make_layer(wl)
     dl = moe.to_device_layer(host)
