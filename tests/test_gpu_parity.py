@@ -238,6 +238,27 @@ def test_decode_shapes_and_gemm_fallback_at_t1(d, F, tol):
     assert rowwise_err(got, ref) <= tol
 
 
+def test_decode_in_kernel_routing_ties_and_wide_rows():
+    """The decode kernel routes the token itself: tied logits (ties to the lower expert index),
+    zero rows of both signs, and rows of more than 256 experts (32 candidates per lane) must pick
+    the oracle's experts, which shows in the output (other experts give other rows)."""
+    for E, k in ((256, 8), (512, 4)):
+        wl = synth.Workload(f"t1_e{E}", T=1, d=512, E=E, k=k, F=256, F_shared=256)
+        host = synth.make_layer(wl)
+        dl = moe.to_device_layer(host)
+        rng = np.random.default_rng(E)
+        cases = [rng.integers(-1, 2, size=E).astype(np.float32),     # heavy ties
+                 np.zeros(E, np.float32),                            # all equal: experts 0..k-1
+                 np.where(np.arange(E) % 3 == 0, 0.0, -0.0).astype(np.float32),
+                 synth.make_logits(rng, wl, 1)[0]]
+        for ci, lg in enumerate(cases):
+            inp = synth.make_inputs(wl, seed=20 + ci)
+            inp["logits"] = lg[None, :].astype(np.float32)
+            got = run_layer(wl, host, dl, inp)["y"]
+            ref, _, _ = O.moe_token(inp["x"][0], inp["logits"][0], host, wl.k)
+            assert rowwise_err(got, ref[None, :]) <= DECODE_TOL, (E, ci)
+
+
 def test_gemm_path_needs_d_multiple_of_256():
     """The grouped-GEMM path pairs 128-row blocks of d: d = 384 at T > 1 is refused up front."""
     wl = synth.Workload("d384", T=8, d=384, E=16, k=2, F=128, F_shared=128)
