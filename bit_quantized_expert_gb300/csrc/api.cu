@@ -200,12 +200,13 @@ RoutingPtrs caller_routing(const moe_routing* r) {
 }
 
 cudaError_t run_routing(const moe_dims& d, const float* logits, const RoutingPtrs& R, const uint16_t* x,
-                        const uint16_t* w_sg, float* gs, int32_t* chunk, uint32_t* err, cudaStream_t st) {
+                        const uint16_t* w_sg, float* gs, int32_t* chunk, uint32_t* err, cudaStream_t st,
+                        int32_t* sched = nullptr) {
   RouteArgs ra{logits, d.T, d.E, d.k, d.d, R.idx, R.w, x, w_sg, gs, err};
   cudaError_t e = launch_topk(ra, st);
   if (e != cudaSuccess) return e;
   TablesArgs ta{R.idx, d.T, d.E, d.k, R.tile_n, d.F_shared > 0 ? 1 : 0, R.counts, R.offsets, R.perm, R.inv,
-                R.tiles, R.num_tiles, chunk, err};
+                R.tiles, R.num_tiles, chunk, err, sched};
   return launch_tables(ta, st);
 }
 
@@ -215,7 +216,7 @@ QPtr qptr(const moe_qmat& q) { return QPtr{q.codes, q.scales, q.biases}; }
 // fp16 y16 when y16 is non-null) over the block map in R.
 moe_status run_experts(const moe_dims& d, const RoutingPtrs& R, const moe_experts* routed, const moe_experts* shared,
                        const uint16_t* x, uint16_t* xperm, uint16_t* h, float* y_perm, uint16_t* y16,
-                       int32_t* sched, uint32_t* err, cudaStream_t st) {
+                       int32_t* sched, uint32_t* err, cudaStream_t st, bool sched_ready = false) {
   // the down GEMM pairs 128-row blocks of the output dimension
   if (d.d % 256 != 0) return MOE_ERR_UNSUPPORTED;
   const bool sh = shared != nullptr && d.F_shared > 0;
@@ -235,8 +236,10 @@ moe_status run_experts(const moe_dims& d, const RoutingPtrs& R, const moe_expert
   if (!ok) return MOE_ERR_CUDA;
   PermuteArgs pa{x, R.perm, d.T, d.k, d.d, (int)slots, xperm, err};
   if (launch_permute_x(pa, st) != cudaSuccess) return MOE_ERR_CUDA;
-  ScheduleArgs sa{R.tiles, R.num_tiles, R.tile_n, sched, err};
-  if (launch_schedule(sa, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!sched_ready) {   // the layer path's routing already wrote it
+    ScheduleArgs sa{R.tiles, R.num_tiles, R.tile_n, sched, err};
+    if (launch_schedule(sa, st) != cudaSuccess) return MOE_ERR_CUDA;
+  }
   m0.h = m1.h;
   m0.h16 = m1.h16;
   m1.codes[1][0] = m1.codes[0][0];
@@ -399,11 +402,12 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
   const RoutingPtrs R = routing_out ? caller_routing(routing_out) : internal_routing(workspace, L);
   uint16_t* xperm = at<uint16_t>(workspace, L.xperm);
   float* gs = sh ? at<float>(workspace, L.gs) : nullptr;
-  cudaError_t e = run_routing(d, logits, R, x, sh ? w_shared_gate : nullptr, gs, at<int32_t>(workspace, L.chunk), err, st);
+  cudaError_t e = run_routing(d, logits, R, x, sh ? w_shared_gate : nullptr, gs, at<int32_t>(workspace, L.chunk), err, st,
+                              at<int32_t>(workspace, L.sched));
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   uint16_t* y16 = at<uint16_t>(workspace, L.yperm);
   s = run_experts(d, R, routed, sh ? shared : nullptr, x, xperm, at<uint16_t>(workspace, L.h), nullptr, y16,
-                  at<int32_t>(workspace, L.sched), err, st);
+                  at<int32_t>(workspace, L.sched), err, st, true);
   if (s != MOE_OK) return s;
   CombineArgs cb{nullptr, y16, R.inv, R.w, gs, d.T, d.k, d.d, y};
   return cuda_status(launch_combine(cb, st));

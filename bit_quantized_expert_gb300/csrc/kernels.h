@@ -27,6 +27,7 @@ struct TablesArgs {
   int32_t *counts, *offsets, *perm, *inv, *tiles, *num_tiles;
   int32_t* chunk;          // scratch [ceil(T/32)][E]: per-chunk counts, then per-chunk bases
   uint32_t* err;
+  int32_t* sched;          // or null: also write the grouped GEMM's walk order (launch_schedule's)
 };
 size_t tables_scratch_bytes(int T, int E);
 

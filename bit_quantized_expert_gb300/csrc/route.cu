@@ -124,6 +124,8 @@ __global__ void __launch_bounds__(256) chunk_hist_kernel(TablesArgs a) {
   }
 }
 
+constexpr int kMaxPartialTiles = 1088;   // one partial tile per expert (E <= 1024) + the shared expert
+
 __global__ void __launch_bounds__(1024, 1) chunk_scan_kernel(TablesArgs a) {
   __shared__ int warp_tot[32];
   __shared__ int total_s;
@@ -191,6 +193,41 @@ __global__ void __launch_bounds__(1024, 1) chunk_scan_kernel(TablesArgs a) {
     reinterpret_cast<int4*>(a.tiles)[routed_tiles + i] = r;
   }
   if (tid == 0) *a.num_tiles = routed_tiles + shared_tiles;
+
+  // The grouped GEMM's walk order, by the rule of schedule_kernel (full tiles in block-map order,
+  // then partial tiles by decreasing width, ties in block-map order), from the counts at hand: an
+  // expert's full tiles are its first cnt / tile_n, its partial tile (if any) its last.
+  if (a.sched != nullptr) {
+    __shared__ int pw[kMaxPartialTiles];
+    __shared__ int pidx[kMaxPartialTiles];
+    const int nfull = (tid < E) ? cnt / a.tile_n : 0;
+    const bool part = (tid < E) && (cnt % a.tile_n) != 0;
+    const int fpos = block_excl_scan(nfull, warp_tot, &total_s);
+    const int routed_full = total_s;
+    const int ppos = block_excl_scan(part ? 1 : 0, warp_tot, &total_s);
+    const int routed_part = total_s;
+    for (int i = 0; i < nfull; ++i) a.sched[fpos + i] = tile0 + i;
+    const int sh_full = a.has_shared ? T / a.tile_n : 0;
+    const bool sh_part = a.has_shared && (T % a.tile_n) != 0;
+    for (int i = tid; i < sh_full; i += blockDim.x) a.sched[routed_full + i] = routed_tiles + i;
+    if (part) {
+      pw[ppos] = cnt % a.tile_n;
+      pidx[ppos] = tile0 + nfull;
+    }
+    if (tid == 0 && sh_part) {
+      pw[routed_part] = T % a.tile_n;
+      pidx[routed_part] = routed_tiles + sh_full;
+    }
+    __syncthreads();
+    const int np = routed_part + (sh_part ? 1 : 0);   // <= E + 1 <= kMaxPartialTiles
+    const int base = routed_full + sh_full;
+    for (int p = tid; p < np; p += blockDim.x) {
+      const int w = pw[p];
+      int before = 0;
+      for (int q = 0; q < np; ++q) before += (pw[q] > w || (pw[q] == w && q < p)) ? 1 : 0;
+      a.sched[base + before] = pidx[p];
+    }
+  }
 }
 
 template <int KMAX>
@@ -238,8 +275,6 @@ cudaError_t launch_topk(const RouteArgs& a, cudaStream_t st) {
   else topk_kernel<32><<<grid, block, 0, st>>>(a);
   return cudaGetLastError();
 }
-
-constexpr int kMaxPartialTiles = 1088;   // one partial tile per expert (E <= 1024) + the shared expert
 
 __global__ void __launch_bounds__(1024, 1) schedule_kernel(ScheduleArgs a) {
   __shared__ int pw[kMaxPartialTiles];
