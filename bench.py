@@ -262,22 +262,23 @@ def decode_bench(args, world, rank, local, device, pk):
         "gpu_launches": LAYERS * args.steps,   # one decode_layer_kernel per layer call
     }
 
-    # End to end through the C ABI with host buffers: per layer call, copy x and logits from pinned
-    # host memory, run the layer, copy y back to pinned host memory.
+    # End to end through the C ABI with host buffers: one moe_layer_forward_host call per layer,
+    # which queues the copies of x and logits from pinned host memory, the layer, and the copy of
+    # y back to pinned host memory on the stream.
     xh = [ins[l]["x"].cpu().pin_memory() for l in range(LAYERS)]
     lh = [ins[l]["logits"].cpu().pin_memory() for l in range(LAYERS)]
     yh = torch.empty((LAYERS, NI, wl.d), dtype=torch.float32).pin_memory()
-    xd = torch.empty((1, wl.d), dtype=torch.int16, device=device)
-    ld = torch.empty((1, wl.E), dtype=torch.float32, device=device)
-    yd = torch.empty((1, wl.d), dtype=torch.float32, device=device)
+    ws_h = moe.alloc_workspace_host(layers[0].dims(1), device)
+
+    sh = stream.cuda_stream
+    xs = [[xh[l][i:i + 1] for i in range(NI)] for l in range(LAYERS)]   # host views, made once
+    ls = [[lh[l][i:i + 1] for i in range(NI)] for l in range(LAYERS)]
+    ys = [[yh[l, i:i + 1] for i in range(NI)] for l in range(LAYERS)]
 
     def e2e_step(s):
         i = s % NI
         for l in range(LAYERS):
-            xd.copy_(xh[l][i:i + 1], non_blocking=True)
-            ld.copy_(lh[l][i:i + 1], non_blocking=True)
-            layers[l].forward(xd, ld, yd, ws)
-            yh[l, i:i + 1].copy_(yd, non_blocking=True)
+            layers[l].forward_host(xs[l][i], ls[l][i], ys[l][i], ws_h, sh)
 
     n_e2e = max(1, min(args.steps, args.e2e_steps))
     with torch.cuda.stream(stream):
@@ -295,7 +296,8 @@ def decode_bench(args, world, rank, local, device, pk):
     e2e_ms = max_over_ranks(t0.elapsed_time(t1), world, device)
     res["e2e"] = {"value": LAYERS * n_e2e * world / (e2e_ms / 1e3), "unit": "tokens/s",
                   "h2d_bytes_per_step": LAYERS * (wl.d * 2 + wl.E * 4), "d2h_bytes_per_step": LAYERS * wl.d * 4,
-                  "steps": n_e2e, "launch": "eager per call (2 H2D copies, 1 kernel, 1 D2H copy per layer)"}
+                  "steps": n_e2e,
+                  "launch": "one moe_layer_forward_host call per layer (2 H2D copies, 1 kernel, 1 D2H copy)"}
     del layers
     torch.cuda.empty_cache()
     return res

@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(PKG_DIR, "libmoe_gb300.so")
 # Symbols declared in include/moe.h.
 EXPORTED = ("moe_status_string", "moe_max_tiles", "moe_workspace_bytes", "moe_route",
             "moe_expert_forward", "moe_layer_forward", "moe_rmsnorm_router", "moe_clear_error_flags",
-            "moe_read_error_flags", "moe_layer_forward_decode_noalloc")
+            "moe_read_error_flags", "moe_layer_forward_decode_noalloc", "moe_workspace_bytes_host",
+            "moe_layer_forward_host")
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_MISALIGNED",
           4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA"}
@@ -80,6 +81,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_layer_forward.argtypes = [P(Dims), VP, VP, P(ExpertsC), P(ExpertsC), VP, VP, P(RoutingC), VP, S, VP]
     lib.moe_rmsnorm_router.restype = ctypes.c_int
     lib.moe_rmsnorm_router.argtypes = [P(Dims), VP, VP, VP, VP, ctypes.c_float, VP, VP, VP, S, VP]
+    lib.moe_workspace_bytes_host.restype = S
+    lib.moe_workspace_bytes_host.argtypes = [P(Dims)]
+    lib.moe_layer_forward_host.restype = ctypes.c_int
+    lib.moe_layer_forward_host.argtypes = [P(Dims), VP, VP, P(ExpertsC), P(ExpertsC), VP, VP, VP, S, VP]
     lib.moe_layer_forward_decode_noalloc.restype = ctypes.c_int
     lib.moe_layer_forward_decode_noalloc.argtypes = [P(Dims), VP, VP, P(ExpertsC), P(ExpertsC), VP, VP, VP]
     lib.moe_clear_error_flags.restype = ctypes.c_int
@@ -106,6 +111,9 @@ def _ptr(t) -> int | None:
 
 
 def _stream(stream) -> int:
+    """A torch stream, a raw cudaStream_t handle (int), or None for torch's current stream."""
+    if isinstance(stream, int):
+        return stream
     import torch
     s = torch.cuda.current_stream() if stream is None else stream
     return s.cuda_stream
@@ -148,6 +156,29 @@ def alloc_workspace(dm: Dims, device="cuda"):
     ws = torch.empty(workspace_bytes(dm), dtype=torch.uint8, device=device)
     ws[:256].zero_()
     return ws
+
+
+def workspace_bytes_host(dm: Dims) -> int:
+    n = load_library().moe_workspace_bytes_host(ctypes.byref(dm))
+    if n == 0:
+        raise MoeError(1, "moe_workspace_bytes_host")
+    return n
+
+
+def alloc_workspace_host(dm: Dims, device="cuda"):
+    """Workspace (with the host-call staging area) for these dims, its error word cleared."""
+    import torch
+    ws = torch.empty(workspace_bytes_host(dm), dtype=torch.uint8, device=device)
+    ws[:256].zero_()
+    return ws
+
+
+def _host_ptr(t) -> int:
+    if t.is_cuda:
+        raise ValueError("expected a host tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
 
 
 def clear_error_flags(workspace, stream=None):
@@ -224,9 +255,23 @@ class Layer:
         self.d, self.E, self.k, self.F = d, E, k, F
         self._re = experts_struct(routed)
         self._se = experts_struct(shared)
+        self._se_ref = ctypes.byref(self._se) if self._se is not None else None
+        self._dims = {}   # T -> Dims, reused by forward_host
 
     def dims(self, T: int) -> Dims:
         return dims(T, self.d, self.E, self.k, self.F, self.F if self.shared is not None else 0)
+
+    def forward_host(self, x_host, logits_host, y_host, workspace, stream=None):
+        """The layer on host tensors (pinned for asynchronous copies); queued on the stream
+        (a torch stream, a raw handle, or None for the current one)."""
+        T = x_host.shape[0]
+        dm = self._dims.get(T)
+        if dm is None:
+            dm = self._dims[T] = self.dims(T)
+        _check(load_library().moe_layer_forward_host(
+            ctypes.byref(dm), _host_ptr(x_host), _host_ptr(logits_host), ctypes.byref(self._re), self._se_ref,
+            _ptr(self.w_sg), _host_ptr(y_host), _ptr(workspace), workspace.numel(), _stream(stream)),
+            "moe_layer_forward_host")
 
     def forward(self, x, logits, y, workspace, routing: dict | None = None, stream=None):
         dm = self.dims(x.shape[0])

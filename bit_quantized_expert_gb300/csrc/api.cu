@@ -413,6 +413,50 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
   return cuda_status(launch_combine(cb, st));
 }
 
+static size_t host_staging_at(const moe_dims& d, size_t* x_off, size_t* lg_off, size_t* y_off) {
+  const size_t base = (layout_of(d).total + 255) & ~(size_t)255;
+  const size_t xb = ((size_t)d.T * d.d * 2 + 255) & ~(size_t)255;
+  const size_t lb = ((size_t)d.T * d.E * 4 + 255) & ~(size_t)255;
+  const size_t yb = ((size_t)d.T * d.d * 4 + 255) & ~(size_t)255;
+  *x_off = base;
+  *lg_off = base + xb;
+  *y_off = base + xb + lb;
+  return base + xb + lb + yb;
+}
+
+size_t moe_workspace_bytes_host(const moe_dims* dims) {
+  if (check_dims(dims) != MOE_OK) return 0;
+  size_t xo, lo, yo;
+  return host_staging_at(*dims, &xo, &lo, &yo);
+}
+
+moe_status moe_layer_forward_host(const moe_dims* dims, const uint16_t* x_host, const float* logits_host,
+                                  const moe_experts* routed, const moe_experts* shared,
+                                  const uint16_t* w_shared_gate, float* y_host, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  moe_status s = check_dims(dims);
+  if (s != MOE_OK) return s;
+  if (dims->T == 0) return MOE_OK;
+  if (x_host == nullptr || logits_host == nullptr || y_host == nullptr) return MOE_ERR_INVALID_ARG;
+  if ((s = check_ptr(workspace)) != MOE_OK) return s == MOE_ERR_INVALID_ARG ? MOE_ERR_WORKSPACE : s;
+  size_t xo, lo, yo;
+  if (workspace_bytes < host_staging_at(*dims, &xo, &lo, &yo)) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint16_t* x = reinterpret_cast<uint16_t*>(ws + xo);
+  float* logits = reinterpret_cast<float*>(ws + lo);
+  float* y = reinterpret_cast<float*>(ws + yo);
+  const size_t T = (size_t)dims->T;
+  if (cudaMemcpyAsync(x, x_host, T * dims->d * 2, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(logits, logits_host, T * dims->E * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  s = moe_layer_forward(dims, x, logits, routed, shared, w_shared_gate, y, nullptr, workspace, layout_of(*dims).total,
+                        stream);
+  if (s != MOE_OK) return s;
+  return cudaMemcpyAsync(y_host, y, T * dims->d * 4, cudaMemcpyDeviceToHost, st) == cudaSuccess ? MOE_OK
+                                                                                               : MOE_ERR_CUDA;
+}
+
 moe_status moe_rmsnorm_router(const moe_dims* dims, float* x_resid, const float* y_prev, const uint16_t* gamma,
                               const uint16_t* w_router, float eps, uint16_t* h_out, float* logits_out,
                               void* workspace, size_t workspace_bytes, void* stream) {

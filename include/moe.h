@@ -147,6 +147,20 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
                              float* y, const moe_routing* routing_out, void* workspace, size_t workspace_bytes,
                              void* stream);
 
+/* moe_layer_forward with the input and output in host memory: copies x_host (bf16 [T, d]) and
+ * logits_host (fp32 [T, E]) to a staging area at the end of the workspace, runs the layer, and
+ * copies y (fp32 [T, d]) back to y_host -- the copies and the kernels queued on `stream` in that
+ * order; the call returns before they finish, so synchronise the stream before reading y_host.
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for the copies to be
+ * asynchronous; pageable buffers work but the runtime may stage them synchronously.  The
+ * workspace must hold moe_workspace_bytes_host(dims) bytes (the first moe_workspace_bytes(dims)
+ * of it serve as the layer's workspace, error word included).  No routing tables are returned. */
+size_t moe_workspace_bytes_host(const moe_dims* dims);
+moe_status moe_layer_forward_host(const moe_dims* dims, const uint16_t* x_host, const float* logits_host,
+                                  const moe_experts* routed, const moe_experts* shared,
+                                  const uint16_t* w_shared_gate, float* y_host, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
 /* Pre-norm block of a stack of MoE layers (the step between two layers, not part of the layer):
  * when y_prev is non-NULL, x_resid += y_prev (written back); then h = RMSNorm(x_resid) * gamma
  * = x / sqrt(mean(x^2) + eps) * gamma rounded to bf16, and router logits = h W_r^T with bf16

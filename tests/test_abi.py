@@ -95,3 +95,23 @@ def test_layer_host_checks(lib):
     assert call(wsn=ws_n - 256) == 4
     dm_ns = moe.dims(4, 256, 16, 2, 128, 0)
     assert call(dm=dm_ns) == 1                 # a shared expert given but dims say none
+
+
+def test_layer_host_entry_checks(lib):
+    """The host-buffer entry point refuses what it must before touching the GPU."""
+    dm = moe.dims(4, 256, 16, 2, 128, 128)
+    ws_n, ws_h = moe.workspace_bytes(dm), moe.workspace_bytes_host(dm)
+    # staging for x (bf16), logits (fp32) and y (fp32), each padded to 256 bytes
+    assert ws_h >= ws_n + 4 * 256 * 2 + 4 * 16 * 4 + 4 * 256 * 4
+    q = moe.QMat(16, 16, 16)
+    ex = moe.ExpertsC(q, q, q)
+    call = lambda **kw: lib.moe_layer_forward_host(
+        ctypes.byref(kw.get("dm", dm)), kw.get("x", 16), kw.get("lg", 16), ctypes.byref(ex), ctypes.byref(ex),
+        16, kw.get("y", 16), kw.get("ws", 16), kw.get("wsn", ws_h), None)
+    assert call(x=None) == 1
+    assert call(lg=None) == 1
+    assert call(y=None) == 1
+    assert call(ws=None) == 4
+    assert call(wsn=ws_h - 1) == 4
+    assert call(wsn=ws_n) == 4
+    assert call(dm=moe.dims(0, 256, 16, 2, 128, 128)) == 0   # T == 0: nothing to do

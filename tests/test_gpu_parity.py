@@ -259,6 +259,26 @@ def test_decode_in_kernel_routing_ties_and_wide_rows():
             assert rowwise_err(got, ref[None, :]) <= DECODE_TOL, (E, ci)
 
 
+def test_layer_host_entry_matches_device_entry():
+    """moe_layer_forward_host (copies in and out on the stream) gives the device call's y, bit
+    for bit, on the decode path (T = 1) and the grouped-GEMM path (T = 37)."""
+    wl = synth.TINY
+    host, dl = layer_for(wl)
+    layer = moe.Layer(dl["routed"], dl["shared"], dl["w_sg"], wl.d, wl.E, wl.k, wl.F)
+    for T in (1, 37):
+        inp = synth.make_inputs(wl, seed=30 + T, T=T)
+        dm = layer.dims(T)
+        ws = moe.alloc_workspace_host(dm)
+        xh = torch.from_numpy(np.ascontiguousarray(inp["x"][:T]).view(np.int16)).pin_memory()
+        lh = torch.from_numpy(inp["logits"][:T]).pin_memory()
+        yh = torch.zeros((T, wl.d), dtype=torch.float32).pin_memory()
+        layer.forward_host(xh, lh, yh, ws)
+        torch.cuda.synchronize()
+        assert moe.read_error_flags(ws) == 0
+        ref = run_layer(wl, host, dl, inp, T=T)["y"]
+        assert np.array_equal(yh.numpy(), ref), T
+
+
 def test_gemm_path_needs_d_multiple_of_256():
     """The grouped-GEMM path pairs 128-row blocks of d: d = 384 at T > 1 is refused up front."""
     wl = synth.Workload("d384", T=8, d=384, E=16, k=2, F=128, F_shared=128)
