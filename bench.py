@@ -338,7 +338,7 @@ def prefill_bench(wl, steps, device, pk):
     y = torch.empty((wl.T, wl.d), dtype=torch.float32, device=device)
     dm = layers[0].dims(wl.T)
     ws = moe.alloc_workspace(dm, device)
-    routing = moe.alloc_routing(dm, 128, device)
+    routing = moe.alloc_routing(dm, 112, device)
     stream = torch.cuda.Stream(device=device)
 
     def step(s):

@@ -11,7 +11,7 @@
 namespace moe {
 namespace {
 
-constexpr int kTileN = 128;   // block-map tile of the layer call (token rows per MMA tile)
+constexpr int kTileN = kGemmMaxTileN;   // block-map tile of the layer call (token rows per MMA tile)
 
 struct Layout {
   size_t err, xperm, gs, idx, w, counts, offsets, perm, inv, tiles, num_tiles, sched, chunk, h, yperm, hdec, total;
@@ -217,8 +217,8 @@ QPtr qptr(const moe_qmat& q) { return QPtr{q.codes, q.scales, q.biases}; }
 moe_status run_experts(const moe_dims& d, const RoutingPtrs& R, const moe_experts* routed, const moe_experts* shared,
                        const uint16_t* x, uint16_t* xperm, uint16_t* h, float* y_perm, uint16_t* y16,
                        int32_t* sched, uint32_t* err, cudaStream_t st, bool sched_ready = false) {
-  // the down GEMM pairs 128-row blocks of the output dimension
-  if (d.d % 256 != 0) return MOE_ERR_UNSUPPORTED;
+  // the down GEMM pairs 128-row blocks of the output dimension; activation stages hold 112 rows
+  if (d.d % 256 != 0 || R.tile_n > kGemmMaxTileN) return MOE_ERR_UNSUPPORTED;
   const bool sh = shared != nullptr && d.F_shared > 0;
   const long long slots = (long long)d.T * d.k + (sh ? d.T : 0);
   const moe_experts* s_or_r = sh ? shared : routed;
@@ -231,7 +231,8 @@ moe_status run_experts(const moe_dims& d, const RoutingPtrs& R, const moe_expert
             encode_codes(&m0.codes[1][1], s_or_r->up.codes, ns, d.F, d.d) &&
             encode_codes(&m1.codes[0][0], routed->down.codes, d.E, d.d, d.F) &&
             encode_codes(&m1.codes[0][1], s_or_r->down.codes, ns, d.d, d.F) &&
-            encode_f16_rows(&m1.h, h, slots, d.F, 128) && encode_f16_rows(&m0.x, xperm, slots, d.d, 128) &&
+            encode_f16_rows(&m1.h, h, slots, d.F, kGemmMaxTileN) &&
+            encode_f16_rows(&m0.x, xperm, slots, d.d, kGemmMaxTileN) &&
             encode_f16_rows(&m1.h16, h, slots, d.F, 16) && encode_f16_rows(&m0.x16, xperm, slots, d.d, 16);
   if (!ok) return MOE_ERR_CUDA;
   PermuteArgs pa{x, R.perm, d.T, d.k, d.d, (int)slots, xperm, err};

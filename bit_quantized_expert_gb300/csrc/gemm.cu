@@ -33,7 +33,8 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kThreads = 512;
-constexpr uint32_t kTileBytes = 128 * 128;   // one 128-row x 64-column fp16 operand tile
+constexpr uint32_t kTileBytes = 128 * 128;   // one 128-row x 64-column fp16 weight tile
+constexpr uint32_t kXBytes = kGemmMaxTileN * 128;   // one activation tile: <= 112 rows x 64 columns
 constexpr uint32_t kRawBytes = 128 * 64;     // 128 rows x 128 packed 4-bit codes: two K chunks
 
 template <int MODE>
@@ -41,19 +42,24 @@ struct Cfg {
   // Two weight tiles per unit: gate and up rows f .. f+127 (gate/up mode), or the down rows of two
   // adjacent 128-row blocks (down mode); both share the unit's activation tile.
   static constexpr int NMAT = 2;
-  static constexpr int S_RAW = 4;   // packed-code stages of two K chunks each
-  static constexpr int S_W = 3;     // operand stages: W (dequantised) and X together
+  static constexpr int S_RAW = 2;   // packed-code stages of two K chunks each
+  // Operand stages of two K chunks: the W tiles (NMAT x 2 chunks, dequantised) and the X tiles
+  // (2 chunks) together, so the MMA thread waits and commits once per 16 MMAs.
+  static constexpr int S_W = 2;
   static constexpr int S_X = S_W;
+  static constexpr uint32_t W_STAGE = NMAT * 2 * kTileBytes;   // 64 KB
+  static constexpr uint32_t X_STAGE = 2 * kXBytes;             // 28 KB
   static constexpr int NBAR = 2 * S_RAW + 2 * S_W + 4;
   static constexpr uint32_t OFF_W = 0;
-  static constexpr uint32_t OFF_X = OFF_W + S_W * NMAT * kTileBytes;
-  static constexpr uint32_t OFF_RAW = OFF_X + S_X * kTileBytes;
+  static constexpr uint32_t OFF_X = OFF_W + S_W * W_STAGE;
+  static constexpr uint32_t OFF_RAW = OFF_X + S_X * X_STAGE;
   static constexpr uint32_t OFF_BAR = OFF_RAW + S_RAW * NMAT * kRawBytes;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t OFF_STG = (OFF_MISC + 16 + 15) & ~15u;   // epilogue staging, 2 KB per warp
   static constexpr uint32_t BYTES = OFF_STG + 4 * 2048 + 1024;        // + alignment slack
   static constexpr uint32_t ACC_COLS = NMAT * 128;          // TMEM columns of one accumulator buffer
   static_assert(BYTES <= 227u * 1024u, "shared memory of one CTA");
+  static_assert(kXBytes % 1024 == 0 && X_STAGE % 1024 == 0 && OFF_X % 1024 == 0, "128-byte swizzle atoms");
 };
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -191,16 +197,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   const int num_units = (*a.num_tiles) * MT;
   const int4* tiles = reinterpret_cast<const int4*>(a.tiles);
   // Every role walks units blockIdx.x, +gridDim.x, ... of the scheduled tile order (wide tiles
-  // first, so the round-robin split is balanced); each loads the descriptor of its next unit one
-  // unit ahead so the global-memory latency of the block map stays off the critical path.
-  auto tile_of = [&](int u) {
-    return u < num_units ? __ldg(tiles + __ldg(a.sched + u / MT)) : make_int4(0, 0, 0, 0);
+  // first, so the round-robin split is balanced).  A unit's tile is a dependent pair of loads
+  // (schedule entry, then block-map row): the walk reads the entry two units ahead and the row one
+  // unit ahead, so no role stalls on the pair at a unit boundary.
+  const int grid_u = (int)gridDim.x;
+  auto sched_at = [&](int u) { return u < num_units ? __ldg(a.sched + u / MT) : 0; };
+  auto tile_at = [&](int u, int si) { return u < num_units ? __ldg(tiles + si) : make_int4(0, 0, 0, 0); };
+  struct Walk {
+    int4 next;   // tile of the next unit
+    int s2;      // schedule entry of the unit after it
+  };
+  auto walk_init = [&](Walk& w) {
+    w.next = tile_at((int)blockIdx.x, sched_at((int)blockIdx.x));
+    w.s2 = sched_at((int)blockIdx.x + grid_u);
+  };
+  auto walk_step = [&](Walk& w, int u) {   // returns the tile of unit u
+    const int4 cur = w.next;
+    w.next = tile_at(u + grid_u, w.s2);
+    w.s2 = sched_at(u + 2 * grid_u);
+    return cur;
   };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer: activation tiles
     // (x rows in slot order, or h; per K chunk the tile's rows rounded up to 16 -- the MMA's N --
-    // by 64 columns: one 128-row box for a full tile, else 16-row boxes, so narrow tiles do not
+    // by 64 columns: one 112-row box for a full tile, else 16-row boxes, so narrow tiles do not
     // pull unused rows through L2 and shared memory; rows past the tile's end belong to the next
     // tile or lie outside the tensor (zero-filled), and the MMA columns they feed are never
     // stored).  The packed codes have their own producer (warp 2), so their loads run up to
@@ -209,21 +230,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     if (lane == 0) {
       int sx = 0;
       uint32_t phx = 0;
-      int4 tl_next = tile_of(blockIdx.x);
+      Walk wk;
+      walk_init(wk);
       for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
-        const int4 tl = tl_next;
-        tl_next = tile_of(u + gridDim.x);
-        const int n16 = (tl.z + 15) >> 4;   // 16-row groups of the tile (1..8)
+        const int4 tl = walk_step(wk, u);
+        const int n16 = (tl.z + 15) >> 4;   // 16-row groups of the tile (1..7)
         bool ok = true;
-        for (int kc = 0; kc < KC; ++kc) {
+        for (int kc = 0; kc < KC; kc += 2) {   // K chunks kc and kc+1 (K is a multiple of 128)
           if (!mbar_wait(WE(sx), phx ^ 1u, abort_s, a.err)) { ok = false; break; }
-          mbar_arrive_expect_tx(WF(sx), (uint32_t)n16 * 16u * 128u);
-          if (n16 == 8) {
-            tma_load_2d(sX + sx * kTileBytes, MODE == 0 ? &maps.x : &maps.h, WF(sx), kc * 64, tl.y);
-          } else {
-            for (int r = 0; r < n16; ++r)
-              tma_load_2d(sX + sx * kTileBytes + (uint32_t)r * 2048u, MODE == 0 ? &maps.x16 : &maps.h16, WF(sx),
-                          kc * 64, tl.y + 16 * r);
+          mbar_arrive_expect_tx(WF(sx), 2u * (uint32_t)n16 * 16u * 128u);
+#pragma unroll
+          for (int hc = 0; hc < 2; ++hc) {
+            const uint32_t dst = sX + sx * C::X_STAGE + (uint32_t)hc * kXBytes;
+            if (n16 * 16 == kGemmMaxTileN) {
+              tma_load_2d(dst, MODE == 0 ? &maps.x : &maps.h, WF(sx), (kc + hc) * 64, tl.y);
+            } else {
+              for (int r = 0; r < n16; ++r)
+                tma_load_2d(dst + (uint32_t)r * 2048u, MODE == 0 ? &maps.x16 : &maps.h16, WF(sx), (kc + hc) * 64,
+                            tl.y + 16 * r);
+            }
           }
           if (++sx == C::S_X) { sx = 0; phx ^= 1u; }
         }
@@ -236,10 +261,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
-      int4 tl_next = tile_of(blockIdx.x);
+      Walk wk;
+      walk_init(wk);
       for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
-        const int4 tl = tl_next;
-        tl_next = tile_of(u + gridDim.x);
+        const int4 tl = walk_step(wk, u);
         const int m = u % MT;
         const int which = tl.x == a.E ? 1 : 0;
         const int ec = which ? 0 : tl.x;
@@ -262,10 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       int sw = 0;
       uint32_t phw = 0;
       int li = 0;
-      int4 tl_next = tile_of(blockIdx.x);
+      Walk wk;
+      walk_init(wk);
       for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++li) {
-        const int4 tl = tl_next;
-        tl_next = tile_of(u + gridDim.x);
+        const int4 tl = walk_step(wk, u);
         const uint32_t n_inst = (uint32_t)((tl.z + 15) & ~15);
         const int b = li & 1;
         if (!mbar_wait(AE(b), ((li >> 1) & 1) ^ 1u, abort_s, a.err)) break;
@@ -273,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const uint32_t idesc = idesc_f16_f32(kBM, n_inst);
         const uint32_t d0 = tmem + (uint32_t)(b * C::ACC_COLS);
         bool ok = true;
-        for (int kc = 0; kc < KC; ++kc) {
+        for (int kc = 0; kc < KC; kc += 2) {
           if (!mbar_wait(WF(sw), phw, abort_s, a.err)) {
             ok = false;
             break;
@@ -283,9 +308,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           // by 32 bytes (2 in the descriptor's address field, which cannot carry: stages lie
           // below 256 KB).
           static_assert(NMAT == 2, "two weight tiles per unit");
-          tc_mma_f16_chunk2(d0, d0 + 128u, smem_desc_sw128(sW + (sw * NMAT + 0) * kTileBytes),
-                            smem_desc_sw128(sW + (sw * NMAT + 1) * kTileBytes), smem_desc_sw128(sX + sw * kTileBytes),
-                            idesc, kc != 0 ? 1u : 0u);
+#pragma unroll
+          for (int hc = 0; hc < 2; ++hc)
+            tc_mma_f16_chunk2(d0, d0 + 128u, smem_desc_sw128(sW + sw * C::W_STAGE + (0 * 2 + hc) * kTileBytes),
+                              smem_desc_sw128(sW + sw * C::W_STAGE + (1 * 2 + hc) * kTileBytes),
+                              smem_desc_sw128(sX + sw * C::X_STAGE + (uint32_t)hc * kXBytes), idesc,
+                              (kc + hc) != 0 ? 1u : 0u);
           tc_commit(WE(sw));
           if (++sw == C::S_W) { sw = 0; phw ^= 1u; }
         }
@@ -311,8 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int G = K / 64;
     // Scale and bias rows of this thread's weight row in a unit; the first 8-group block of the
     // next unit is loaded during the last block of the current one.
-    auto rows_of = [&](int u, const uint16_t*& sr, const uint16_t*& br) {
-      const int4 t = tile_of(u);
+    auto rows_of = [&](const int4& t, int u, const uint16_t*& sr, const uint16_t*& br) {
       const int which = t.x == a.E ? 1 : 0;
       const int blk = MODE == 0 ? (u % MT) : 2 * (u % MT) + mat;   // 128-row block of the matrix
       const size_t row = (size_t)(which ? 0 : t.x) * R + (size_t)blk * kBM + i;
@@ -323,67 +350,67 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const uint16_t* srow = nullptr;
     const uint16_t* brow = nullptr;
     uint4 ns = make_uint4(0u, 0u, 0u, 0u), nb = make_uint4(0u, 0u, 0u, 0u);
+    Walk wk;
+    walk_init(wk);
     if (blockIdx.x < num_units) {
-      rows_of(blockIdx.x, srow, brow);
+      rows_of(wk.next, blockIdx.x, srow, brow);
       ns = load_group_block(srow, 0, G);
       nb = load_group_block(brow, 0, G);
     }
     for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      walk_step(wk, u);   // wk.next: the tile of the next unit, needed at this unit's last block
       const uint16_t* srow_n = nullptr;
       const uint16_t* brow_n = nullptr;
       const bool has_next = u + (int)gridDim.x < num_units;
-      if (has_next) rows_of(u + gridDim.x, srow_n, brow_n);
       for (int kb = 0; kb < KC && ok; kb += 8) {
         const uint4 cs = ns, cb = nb;
         if (kb + 8 < KC) {
           ns = load_group_block(srow, kb + 8, G);
           nb = load_group_block(brow, kb + 8, G);
         } else if (has_next) {
+          rows_of(wk.next, u + (int)gridDim.x, srow_n, brow_n);
           ns = load_group_block(srow_n, 0, G);
           nb = load_group_block(brow_n, 0, G);
         }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 8; j += 2) {   // K chunks kb+j and kb+j+1: one operand stage
           if (kb + j >= KC) break;
-          const float sf = bf16_bits_to_f32(j == 0 ? pick_bf16<0>(cs) : j == 1 ? pick_bf16<1>(cs)
-                                            : j == 2 ? pick_bf16<2>(cs) : j == 3 ? pick_bf16<3>(cs)
-                                            : j == 4 ? pick_bf16<4>(cs) : j == 5 ? pick_bf16<5>(cs)
-                                            : j == 6 ? pick_bf16<6>(cs) : pick_bf16<7>(cs));
-          const float bf = bf16_bits_to_f32(j == 0 ? pick_bf16<0>(cb) : j == 1 ? pick_bf16<1>(cb)
-                                            : j == 2 ? pick_bf16<2>(cb) : j == 3 ? pick_bf16<3>(cb)
-                                            : j == 4 ? pick_bf16<4>(cb) : j == 5 ? pick_bf16<5>(cb)
-                                            : j == 6 ? pick_bf16<6>(cb) : pick_bf16<7>(cb));
-          bad = bad || !(fmaf(15.0f, fabsf(sf), fabsf(bf)) <= 65504.0f);
-          const __half2 s2 = __float2half2_rn(sf);
-          const __half2 b2 = __float2half2_rn(bf);
-          // codes of this chunk: half (j & 1) of the two-chunk stage s (kb is a multiple of 8).
-          // The stage holds 64-byte rows in the 64-byte swizzle: 16-byte piece c of row i sits at
-          // piece c ^ ((i >> 1) & 3), which keeps the lanes' loads free of bank conflicts.
-          if ((j & 1) == 0 && !mbar_wait(RF(s), ph, abort_s, a.err)) { ok = false; break; }
+          const float sf0 = bf16_bits_to_f32(j == 0 ? pick_bf16<0>(cs) : j == 2 ? pick_bf16<2>(cs)
+                                             : j == 4 ? pick_bf16<4>(cs) : pick_bf16<6>(cs));
+          const float sf1 = bf16_bits_to_f32(j == 0 ? pick_bf16<1>(cs) : j == 2 ? pick_bf16<3>(cs)
+                                             : j == 4 ? pick_bf16<5>(cs) : pick_bf16<7>(cs));
+          const float bf0 = bf16_bits_to_f32(j == 0 ? pick_bf16<0>(cb) : j == 2 ? pick_bf16<2>(cb)
+                                             : j == 4 ? pick_bf16<4>(cb) : pick_bf16<6>(cb));
+          const float bf1 = bf16_bits_to_f32(j == 0 ? pick_bf16<1>(cb) : j == 2 ? pick_bf16<3>(cb)
+                                             : j == 4 ? pick_bf16<5>(cb) : pick_bf16<7>(cb));
+          bad = bad || !(fmaf(15.0f, fabsf(sf0), fabsf(bf0)) <= 65504.0f) ||
+                !(fmaf(15.0f, fabsf(sf1), fabsf(bf1)) <= 65504.0f);
+          const __half2 s2[2] = {__float2half2_rn(sf0), __float2half2_rn(sf1)};
+          const __half2 b2[2] = {__float2half2_rn(bf0), __float2half2_rn(bf1)};
+          // codes of both chunks: the two-chunk stage s.  It holds 64-byte rows in the 64-byte
+          // swizzle: 16-byte piece c of row i sits at piece c ^ ((i >> 1) & 3), which keeps the
+          // lanes' loads free of bank conflicts; chunk hc is pieces 2 hc and 2 hc + 1.
+          if (!mbar_wait(RF(s), ph, abort_s, a.err)) { ok = false; break; }
           const uint32_t row_base = sRaw + (s * NMAT + mat) * kRawBytes + i * 64;
           const uint32_t sx64 = (uint32_t)((i >> 1) & 3);
-          const uint32_t piece0 = (uint32_t)((j & 1) * 2 + (w0 >> 2));
-          uint32_t words[8];
-          {
-            const uint4 c0 = ld_shared_v4(row_base + ((piece0 ^ sx64) << 4));
-            words[0] = c0.x; words[1] = c0.y; words[2] = c0.z; words[3] = c0.w;
-            if (NW == 8) {
-              const uint4 c1 = ld_shared_v4(row_base + (((piece0 + 1) ^ sx64) << 4));
-              words[4] = c1.x; words[5] = c1.y; words[6] = c1.z; words[7] = c1.w;
-            } else {
-              words[4] = words[5] = words[6] = words[7] = 0u;
-            }
+          uint32_t words[16];
+#pragma unroll
+          for (int pc = 0; pc < 4; ++pc) {
+            const uint4 c4 = ld_shared_v4(row_base + ((((uint32_t)pc) ^ sx64) << 4));
+            words[4 * pc] = c4.x; words[4 * pc + 1] = c4.y; words[4 * pc + 2] = c4.z; words[4 * pc + 3] = c4.w;
           }
           const int s_used = s;
-          const bool stage_done = (j & 1) == 1;
-          if (stage_done && ++s == C::S_RAW) { s = 0; ph ^= 1u; }
+          if (++s == C::S_RAW) { s = 0; ph ^= 1u; }
           if (!mbar_wait(WE(sw), phw ^ 1u, abort_s, a.err)) { ok = false; break; }
-          const uint32_t dst = sW + (sw * NMAT + mat) * kTileBytes + i * 128;
 #pragma unroll
-          for (int wd = 0; wd < NW; ++wd) {
-            uint32_t o[4];
-            dequant_word(words[wd], s2, b2, o);
-            st_shared_v4(dst + ((((uint32_t)(w0 + wd)) ^ swz) << 4), o[0], o[1], o[2], o[3]);
+          for (int hc = 0; hc < 2; ++hc) {
+            const uint32_t dst = sW + sw * C::W_STAGE + (mat * 2 + hc) * kTileBytes + i * 128;
+#pragma unroll
+            for (int wd = 0; wd < NW; ++wd) {
+              uint32_t o[4];
+              dequant_word(words[NW * hc + wd], s2[hc], b2[hc], o);
+              st_shared_v4(dst + ((((uint32_t)(w0 + wd)) ^ swz) << 4), o[0], o[1], o[2], o[3]);
+            }
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -391,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           // it, so every lane's shared-memory read of the stage has completed.  Releasing it right
           // after issuing those reads let the TMA refill land before slow lanes had read it.
           if (lane == 0) {
-            if (stage_done) mbar_arrive(RE(s_used));
+            mbar_arrive(RE(s_used));
             mbar_arrive(WF(sw));
           }
           if (++sw == C::S_W) { sw = 0; phw ^= 1u; }
@@ -409,10 +436,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const uint32_t stg = sbase + C::OFF_STG + (uint32_t)q * 2048u;
     int li = 0;
     float amax = 0.0f;   // largest |value| rounded to fp16 (above 65504 it does not fit)
-    int4 tl_next = tile_of(blockIdx.x);
+    Walk wk;
+    walk_init(wk);
     for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++li) {
-      const int4 tl = tl_next;
-      tl_next = tile_of(u + gridDim.x);
+      const int4 tl = walk_step(wk, u);
       const int m = u % MT;
       const int b = li & 1;
       if (!mbar_wait_warp(AF(b), (li >> 1) & 1, abort_s, a.err)) break;

@@ -53,6 +53,9 @@ struct QPtr {
 
 // Tensor maps of one launch: packed codes of each operand matrix for the routed and the
 // shared expert set, and (down projection) the h operand.
+// Widest block-map tile the grouped GEMM takes (its activation stages hold this many rows).
+constexpr int kGemmMaxTileN = 112;
+
 struct GemmMaps {
   CUtensorMap codes[2][2];   // [matrix][0 = routed, 1 = shared]
   CUtensorMap h;             // down projection: h [slots, F] fp16, 128-row boxes

@@ -125,7 +125,8 @@ size_t moe_workspace_bytes(const moe_dims* dims);
 moe_status moe_route(const moe_dims* dims, const float* logits, const moe_routing* out, void* workspace,
                      size_t workspace_bytes, void* stream);
 
-/* Expert outputs per slot (needs d % 256 == 0; MOE_ERR_UNSUPPORTED otherwise):
+/* Expert outputs per slot (needs d % 256 == 0 and routing->tile_n <= 112; MOE_ERR_UNSUPPORTED
+ * otherwise):
  * y_perm[p] = FFN_{e(p)}(x[token(p)]) for the T*k routed slots of
  * `routing`, followed (when `shared` is non-NULL) by the shared expert's outputs for the T
  * tokens in slots T*k .. T*k+T-1.  x bf16 [T, d]; y_perm fp32 [T*k + T, d] (or [T*k, d] without
@@ -141,7 +142,8 @@ moe_status moe_expert_forward(const moe_dims* dims, const uint16_t* x, const moe
  * T == 1 runs the fused decode path (fp32 arithmetic on CUDA cores) when d <= 2048, d % 64 == 0,
  * F % 128 == 0, k < 32, E <= 1024 and (k + 1) * F / 32 CTAs fit one per SM; otherwise, and for
  * T > 1, the grouped-GEMM path (fp16 tensor-core operands, fp32 accumulation; needs
- * d % 256 == 0, MOE_ERR_UNSUPPORTED otherwise). */
+ * d % 256 == 0, and routing_out->tile_n <= 112 when routing_out is given; MOE_ERR_UNSUPPORTED
+ * otherwise).  Its own block map uses tiles of 112 rows. */
 moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const float* logits,
                              const moe_experts* routed, const moe_experts* shared, const uint16_t* w_shared_gate,
                              float* y, const moe_routing* routing_out, void* workspace, size_t workspace_bytes,

@@ -165,7 +165,7 @@ def test_layer_tiny_exact_and_emulated():
     assert rowwise_err(got, emu) <= EMUL_TOL
 
 
-@pytest.mark.parametrize("tile_n", [16, 48, 128])
+@pytest.mark.parametrize("tile_n", [16, 48, 112])
 def test_layer_tiny_tile_widths_and_routing_out(tile_n):
     wl = synth.TINY
     host, dl = layer_for(wl)
@@ -182,7 +182,7 @@ def test_expert_forward_tiny_slots():
     inp = synth.make_inputs(wl, seed=5)
     dm = moe.dims(wl.T, wl.d, wl.E, wl.k, wl.F, wl.F_shared)
     ws = moe.alloc_workspace(dm)
-    r = moe.alloc_routing(dm, 128)
+    r = moe.alloc_routing(dm, 112)
     moe.route(dm, dev(inp["logits"]), r, ws)
     yp = torch.empty((wl.T * wl.k + wl.T, wl.d), dtype=torch.float32, device="cuda")
     moe.expert_forward(dm, dev(inp["x"]), r, dl["routed"], dl["shared"], yp, ws)
@@ -279,6 +279,22 @@ def test_layer_host_entry_matches_device_entry():
         assert np.array_equal(yh.numpy(), ref), T
 
 
+def test_gemm_path_refuses_tiles_wider_than_112():
+    """The grouped GEMM's activation stages hold 112 rows: caller tables with wider tiles are
+    refused up front (routing itself takes tiles of up to 128)."""
+    wl = synth.TINY
+    host, dl = layer_for(wl)
+    inp = synth.make_inputs(wl, seed=11)
+    dm = moe.dims(wl.T, wl.d, wl.E, wl.k, wl.F, wl.F_shared)
+    ws = moe.alloc_workspace(dm)
+    y = torch.zeros((wl.T, wl.d), dtype=torch.float32, device="cuda")
+    r = moe.alloc_routing(dm, 128)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.layer_forward(dm, dev(inp["x"]), dev(inp["logits"]), dl["routed"], dl["shared"], dl["w_sg"], y, ws,
+                          routing=r)
+    assert ei.value.status == 2   # MOE_ERR_UNSUPPORTED
+
+
 def test_gemm_path_needs_d_multiple_of_256():
     """The grouped-GEMM path pairs 128-row blocks of d: d = 384 at T > 1 is refused up front."""
     wl = synth.Workload("d384", T=8, d=384, E=16, k=2, F=128, F_shared=128)
@@ -298,8 +314,8 @@ def test_decode_routing_out_matches_oracle():
     wl = synth.DECODE
     host, dl = layer_for(wl)
     inp = synth.make_inputs(wl, seed=1)
-    out = run_layer(wl, host, dl, inp, tile_n=128)
-    assert_routing_equal(out["routing"], inp["logits"], wl.E, wl.k, 128)
+    out = run_layer(wl, host, dl, inp, tile_n=112)
+    assert_routing_equal(out["routing"], inp["logits"], wl.E, wl.k, 112)
 
 
 def test_prefill_full_size():
@@ -330,8 +346,8 @@ def test_skewed_prefill_full_size():
     wl = synth.SKEWED
     host, dl = layer_for(wl)
     inp = synth.make_inputs(wl)
-    out = run_layer(wl, host, dl, inp, tile_n=128)
-    assert_routing_equal(out["routing"], inp["logits"], wl.E, wl.k, 128)
+    out = run_layer(wl, host, dl, inp, tile_n=112)
+    assert_routing_equal(out["routing"], inp["logits"], wl.E, wl.k, 112)
     ref = O.moe_layer(inp["x"], inp["logits"], host, wl.k)["y"]
     assert rowwise_err(out["y"], ref) <= EXACT_TOL
 
@@ -389,7 +405,7 @@ def test_stack_of_layers_tiny():
     for l in range(L):
         moe.rmsnorm_router(dm, x, y if l > 0 else None, dev(routers[l]["gamma"]), dev(routers[l]["w_router"]),
                            1e-6, h, lg, ws)
-        r = moe.alloc_routing(dm, 128)
+        r = moe.alloc_routing(dm, 112)
         moe.layer_forward(dm, h, lg, dls[l]["routed"], dls[l]["shared"], dls[l]["w_sg"], y, ws, routing=r)
         picks.append(r["idx"].cpu().numpy())
     xf = x.cpu().numpy().astype(np.float64) + y.cpu().numpy()
