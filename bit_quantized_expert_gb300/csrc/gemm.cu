@@ -7,16 +7,18 @@
 // la GPU").  This kernel is that design re-thought for GB300:
 //
 //   * Swap-AB: the weight rows of one expert form the MMA's M = 128 side, the (few, uneven)
-//     tokens routed to the expert form N (16..128, rounded up to 16).  D[m, n] = sum_k W[m, k]
+//     tokens routed to the expert form N (16..112, rounded up to 16).  D[m, n] = sum_k W[m, k]
 //     X[n, k] lands in TMEM (fp32), lane m, column n.
-//   * Work unit = (block-map tile of <= 128 slots of one expert, 128-row slice of the weight
-//     matrix), iterated over K in chunks of 64 (= one quantisation group).  A persistent grid of
-//     one CTA per SM walks the units; every role walks the same list.
+//   * Work unit = (block-map tile of <= 112 slots of one expert, two 128-row weight tiles),
+//     iterated over K in operand stages of two 64-wide chunks (a chunk = one quantisation group):
+//     every hand-off between roles happens once per 16 MMAs.  A persistent grid of one CTA per SM
+//     walks the units; every role walks the same list.
 //   * Warp roles (16 warps): 0 = TMA producer of the activation tiles (x rows in slot order, or
 //     h), 1 = MMA issuer (one thread) and TMEM owner, 2 = TMA producer of the packed codes,
 //     3 = idle, 4-11 = dequant
-//     (two threads per weight row: 4-bit codes -> fp16 w = q*scale + bias, single rounding; two
-//     dequant warps per scheduler so one hides the other's shared-memory and barrier latency),
+//     (one thread per weight row of one of the unit's two tiles: 4-bit codes -> fp16
+//     w = q*scale + bias, single rounding; two dequant warps per scheduler so one hides the
+//     other's shared-memory and barrier latency),
 //     12-15 = epilogue (TMEM -> registers; SwiGLU -> fp16 h, or fp32 expert outputs).
 //   * Gate/up mode keeps the gate and up accumulators of the same 128 F-rows side by side in
 //     TMEM so the epilogue applies silu(g) * u in registers.  Two accumulator buffers let the

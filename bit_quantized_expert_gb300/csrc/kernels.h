@@ -58,8 +58,8 @@ constexpr int kGemmMaxTileN = 112;
 
 struct GemmMaps {
   CUtensorMap codes[2][2];   // [matrix][0 = routed, 1 = shared]
-  CUtensorMap h;             // down projection: h [slots, F] fp16, 128-row boxes
-  CUtensorMap x;             // gate/up projection: x rows in slot order [slots, d] fp16, 128-row boxes
+  CUtensorMap h;             // down projection: h [slots, F] fp16, 112-row boxes
+  CUtensorMap x;             // gate/up projection: x rows in slot order [slots, d] fp16, 112-row boxes
   CUtensorMap h16;           // the same two tensors with 16-row boxes (tiles narrower than 128)
   CUtensorMap x16;
 };
