@@ -262,8 +262,10 @@ class Layer:
         return dims(T, self.d, self.E, self.k, self.F, self.F if self.shared is not None else 0)
 
     def forward_host(self, x_host, logits_host, y_host, workspace, stream=None):
-        """The layer on host tensors (pinned for asynchronous copies); queued on the stream
-        (a torch stream, a raw handle, or None for the current one)."""
+        """The layer on host tensors, queued on the stream (a torch stream, a raw handle, or None
+        for the current one).  Pinned, 16-byte-aligned tensors at T = 1 are read and written by
+        the decode kernel in place; otherwise the library stages them with copies (asynchronous
+        for pinned memory)."""
         T = x_host.shape[0]
         dm = self._dims.get(T)
         if dm is None:

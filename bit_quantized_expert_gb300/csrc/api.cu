@@ -414,6 +414,19 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
   return cuda_status(launch_combine(cb, st));
 }
 
+// Device address of page-locked host memory registered with CUDA and mapped into the device's
+// address space, 16-byte aligned; null for anything else (pageable memory included).
+static void* mapped_host(const void* p) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();   // clear the sticky-free error of an unknown pointer
+    return nullptr;
+  }
+  if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) return nullptr;
+  if ((reinterpret_cast<uintptr_t>(attr.devicePointer) & 15u) != 0) return nullptr;
+  return attr.devicePointer;
+}
+
 static size_t host_staging_at(const moe_dims& d, size_t* x_off, size_t* lg_off, size_t* y_off) {
   const size_t base = (layout_of(d).total + 255) & ~(size_t)255;
   const size_t xb = ((size_t)d.T * d.d * 2 + 255) & ~(size_t)255;
@@ -448,6 +461,28 @@ moe_status moe_layer_forward_host(const moe_dims* dims, const uint16_t* x_host, 
   float* logits = reinterpret_cast<float*>(ws + lo);
   float* y = reinterpret_cast<float*>(ws + yo);
   const size_t T = (size_t)dims->T;
+  // One token on the fused decode kernel: when all three buffers are page-locked host memory
+  // mapped into the device's address space, one small kernel reads x and logits across the
+  // CPU-GPU link into the workspace (once, instead of once per CTA of the decode kernel), and the
+  // decode kernel writes y into host memory itself -- no copy-engine transfers on the stream.
+  // Anything else (pageable memory, unaligned pointers, T > 1) takes the copies.
+  if (T == 1 && decode_supported(dims->d, dims->E, dims->k, dims->F)) {
+    void* xm = mapped_host(x_host);
+    void* lm = mapped_host(logits_host);
+    void* ym = mapped_host(y_host);
+    if (xm != nullptr && lm != nullptr && ym != nullptr) {
+      StageArgs sa{};
+      sa.x_src = static_cast<const uint4*>(xm);
+      sa.x_dst = reinterpret_cast<uint4*>(x);
+      sa.lg_src = static_cast<const float*>(lm);
+      sa.lg_dst = logits;
+      sa.x_units = dims->d * 2 / 16;
+      sa.lg_n = dims->E;
+      if (launch_stage_in(sa, st) != cudaSuccess) return MOE_ERR_CUDA;
+      return moe_layer_forward(dims, x, logits, routed, shared, w_shared_gate, static_cast<float*>(ym), nullptr,
+                               workspace, layout_of(*dims).total, stream);
+    }
+  }
   if (cudaMemcpyAsync(x, x_host, T * dims->d * 2, cudaMemcpyHostToDevice, st) != cudaSuccess ||
       cudaMemcpyAsync(logits, logits_host, T * dims->E * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return MOE_ERR_CUDA;

@@ -452,6 +452,56 @@ bool decode_supported(int d, int E, int k, int F) {
   return P.grid <= di->sms;
 }
 
+constexpr int kStageThreads = 256;
+constexpr int kStageIn = 4;   // loads in flight per thread per round
+
+__global__ void __launch_bounds__(kStageThreads) stage_in_kernel(const StageArgs a) {
+  pdl_wait();   // the previous kernel, the last reader of the destination buffers, is complete
+  pdl_launch_dependents();
+  const int tid = threadIdx.x;
+  for (int base = 0; base < a.x_units; base += kStageThreads * kStageIn) {
+    uint4 v[kStageIn];
+#pragma unroll
+    for (int c = 0; c < kStageIn; ++c) {
+      const int i = base + c * kStageThreads + tid;
+      if (i < a.x_units) v[c] = a.x_src[i];
+    }
+#pragma unroll
+    for (int c = 0; c < kStageIn; ++c) {
+      const int i = base + c * kStageThreads + tid;
+      if (i < a.x_units) a.x_dst[i] = v[c];
+    }
+  }
+  for (int base = 0; base < a.lg_n; base += kStageThreads * kStageIn) {
+    float v[kStageIn];
+#pragma unroll
+    for (int c = 0; c < kStageIn; ++c) {
+      const int i = base + c * kStageThreads + tid;
+      if (i < a.lg_n) v[c] = a.lg_src[i];
+    }
+#pragma unroll
+    for (int c = 0; c < kStageIn; ++c) {
+      const int i = base + c * kStageThreads + tid;
+      if (i < a.lg_n) a.lg_dst[i] = v[c];
+    }
+  }
+}
+
+cudaError_t launch_stage_in(const StageArgs& a, cudaStream_t st) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kStageThreads);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, stage_in_kernel, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st, bool pdl) {
   const int k1 = a.k + (a.has_shared ? 1 : 0);
   DevInfo* di = nullptr;

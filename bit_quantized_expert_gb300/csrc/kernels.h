@@ -114,6 +114,19 @@ struct DecodeArgs {
 bool decode_supported(int d, int E, int k, int F);
 size_t decode_scratch_floats(int d, int k, int F);   // floats of DecodeArgs::part
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st, bool pdl);
+// One CTA copies a token's x (x_bytes, a multiple of 16) and logits (lg_bytes, a multiple of 4)
+// from page-locked, mapped host memory (16-byte aligned) into device buffers, once, so that the
+// decode kernel's many readers hit device memory; launched with programmatic serialisation, it
+// waits for the previous kernel on the stream before writing.
+struct StageArgs {
+  const uint4* x_src;
+  uint4* x_dst;
+  const float* lg_src;
+  float* lg_dst;
+  int x_units;   // 16-byte units of x
+  int lg_n;      // floats of logits
+};
+cudaError_t launch_stage_in(const StageArgs& a, cudaStream_t st);
 
 // ---------------------------------------------------------------- pre-norm block (router.cu)
 struct NormArgs {

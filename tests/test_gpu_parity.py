@@ -259,24 +259,37 @@ def test_decode_in_kernel_routing_ties_and_wide_rows():
             assert rowwise_err(got, ref[None, :]) <= DECODE_TOL, (E, ci)
 
 
-def test_layer_host_entry_matches_device_entry():
-    """moe_layer_forward_host (copies in and out on the stream) gives the device call's y, bit
-    for bit, on the decode path (T = 1) and the grouped-GEMM path (T = 37)."""
+@pytest.mark.parametrize("memory", ["pinned", "pageable", "pinned_unaligned"])
+def test_layer_host_entry_matches_device_entry(memory):
+    """moe_layer_forward_host gives the device call's y, bit for bit, on the decode path (T = 1)
+    and the grouped-GEMM path (T = 37): with pinned, mapped, aligned buffers at T = 1 the decode
+    kernel reads and writes host memory itself; pageable or unaligned buffers, and T > 1, take
+    the copies."""
     wl = synth.TINY
     host, dl = layer_for(wl)
     layer = moe.Layer(dl["routed"], dl["shared"], dl["w_sg"], wl.d, wl.E, wl.k, wl.F)
+    pin = memory != "pageable"
+    off = 1 if memory == "pinned_unaligned" else 0   # one element past a 16-byte boundary
+
+    def host_buf(a):
+        b = torch.zeros((a.shape[0] * a.shape[1] + off,), dtype=a.dtype)
+        b = b.pin_memory() if pin else b
+        v = b[off:].view(a.shape)
+        v.copy_(a)
+        return v
+
     for T in (1, 37):
         inp = synth.make_inputs(wl, seed=30 + T, T=T)
         dm = layer.dims(T)
         ws = moe.alloc_workspace_host(dm)
-        xh = torch.from_numpy(np.ascontiguousarray(inp["x"][:T]).view(np.int16)).pin_memory()
-        lh = torch.from_numpy(inp["logits"][:T]).pin_memory()
-        yh = torch.zeros((T, wl.d), dtype=torch.float32).pin_memory()
+        xh = host_buf(torch.from_numpy(np.ascontiguousarray(inp["x"][:T]).view(np.int16)))
+        lh = host_buf(torch.from_numpy(np.ascontiguousarray(inp["logits"][:T])))
+        yh = host_buf(torch.full((T, wl.d), float("nan"), dtype=torch.float32))
         layer.forward_host(xh, lh, yh, ws)
         torch.cuda.synchronize()
         assert moe.read_error_flags(ws) == 0
         ref = run_layer(wl, host, dl, inp, T=T)["y"]
-        assert np.array_equal(yh.numpy(), ref), T
+        assert np.array_equal(yh.numpy(), ref), (memory, T)
 
 
 def test_gemm_path_refuses_tiles_wider_than_112():
