@@ -285,6 +285,34 @@ def decode_bench(args, world, rank, local, device, pk):
                      "note": "one weight set replayed (weights L2-resident); not the headline"}
     log(f"decode hot-L2: {res['hot_l2']['us_per_layer']:.2f} us per layer")
 
+    # A few tokens per layer call (verify-batch shapes): up to three run the decode kernel once per
+    # token, four take the grouped GEMM.  CUDA graph over the 40 weight sets; context, not the
+    # headline.
+    small = {}
+    ys = torch.empty((4, wl.d), dtype=torch.float32, device=device)
+    for T in (2, 3, 4):
+        ws_s = moe.alloc_workspace(layers[0].dims(T), device)
+
+        def small_step(s, T=T, ws_s=ws_s):
+            i = (s * T) % (NI - T)
+            for l in range(LAYERS):
+                layers[l].forward(ins[l]["x"][i:i + T], ins[l]["logits"][i:i + T], ys[:T], ws_s)
+
+        with torch.cuda.stream(stream):
+            small_step(0)
+        g_s = capture(lambda: [small_step(s) for s in range(4)], stream)
+        with torch.cuda.stream(stream):
+            g_s.replay()
+        stream.synchronize()
+        reps = max(1, args.steps // 40)
+        ms_s = timed_graph_steps(g_s, 4, g_s, 4 * reps, stream)
+        per_layer = ms_s * 1e3 / (4 * reps * LAYERS)
+        small[f"T{T}"] = {"us_per_layer": per_layer, "tokens_per_s": T * 1e6 / per_layer}
+        if moe.read_error_flags(ws_s) != 0:
+            raise RuntimeError("device error flags set during the small-T runs")
+    res["small_T"] = small
+    log("decode small T: " + ", ".join(f"{k} {v['us_per_layer']:.1f} us/layer" for k, v in small.items()))
+
     # End to end through the C ABI with host buffers: one moe_layer_forward_host call per layer.
     # The buffers are pinned (mapped into the device's address space), so the decode kernel reads
     # x and logits from host memory and writes y there itself; the bytes still cross the CPU-GPU
@@ -593,6 +621,7 @@ def main():
                 "config": config(world), "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": res["e2e"],
                 "gpu_launches": res["gpu_launches"], "clocks": res["clocks"], "error_flags": res["flags"],
                 "decode_hot_l2": res.get("hot_l2"), "decode_e2e_staged": res.get("e2e_staged"),
+                "decode_small_T": res.get("small_T"),
                 "prefill": extras}
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -112,6 +112,7 @@ struct DecodeArgs {
   unsigned long long* sync;   // grid-barrier word (8-byte aligned; count low, generation high)
 };
 bool decode_supported(int d, int E, int k, int F);
+constexpr int kDecodeLoopMaxT = 3;   // layer calls of up to this many tokens run the decode kernel per token
 size_t decode_scratch_floats(int d, int k, int F);   // floats of DecodeArgs::part
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st, bool pdl);
 // One CTA copies a token's x (x_bytes, a multiple of 16) and logits (lg_bytes, a multiple of 4)

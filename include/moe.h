@@ -115,7 +115,7 @@ size_t moe_max_tiles(const moe_dims* dims, int32_t tile_n);
 /* Workspace bytes needed by moe_route, moe_expert_forward and moe_layer_forward for these dims
  * (one size serves all three).  Returns 0 for invalid dims.  The first 4 bytes of the workspace are
  * its error word: kernels only ever set bits in it, so it is sticky across calls.  Bytes 8..15
- * hold the decode path's grid-barrier word (it returns to zero at the end of every T == 1 call).
+ * hold the decode path's grid-barrier word (it returns to zero at the end of every decode launch).
  * Clear both once after allocating the workspace (moe_clear_error_flags); the rest needs no
  * initialisation. */
 size_t moe_workspace_bytes(const moe_dims* dims);
@@ -139,9 +139,10 @@ moe_status moe_expert_forward(const moe_dims* dims, const uint16_t* x, const moe
 /* The whole layer: y[t] = sum_j w[t,j] FFN_{idx[t,j]}(x_t) + sigmoid(x_t . w_sg) FFN_shared(x_t).
  * x bf16 [T, d]; logits fp32 [T, E]; w_shared_gate bf16 [d] (ignored when shared is NULL);
  * y fp32 [T, d].  routing_out may be NULL; when given, its tables are filled as by moe_route.
- * T == 1 runs the fused decode path (fp32 arithmetic on CUDA cores) when d <= 2048, d % 64 == 0,
- * F % 128 == 0, k < 32, E <= 1024 and (k + 1) * F / 32 CTAs fit one per SM; otherwise, and for
- * T > 1, the grouped-GEMM path (fp16 tensor-core operands, fp32 accumulation; needs
+ * T <= 3 runs the fused decode path (fp32 arithmetic on CUDA cores; one launch per token, each
+ * streaming that token's experts) when d <= 2048, d % 64 == 0, F % 128 == 0, k < 32, E <= 1024
+ * and (k + 1) * F / 32 CTAs fit one per SM; otherwise, and for T > 3, the grouped-GEMM path
+ * (fp16 tensor-core operands, fp32 accumulation; needs
  * d % 256 == 0, and routing_out->tile_n <= 112 when routing_out is given; MOE_ERR_UNSUPPORTED
  * otherwise).  Its own block map uses tiles of 112 rows. */
 moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const float* logits,
@@ -157,7 +158,7 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
  * asynchronous; pageable buffers work but the runtime may stage them synchronously.  The
  * workspace must hold moe_workspace_bytes_host(dims) bytes (the first moe_workspace_bytes(dims)
  * of it serve as the layer's workspace, error word included).  No routing tables are returned.
- * With T == 1 on the fused decode kernel and all three buffers page-locked, mapped into the
+ * With T <= 3 on the fused decode kernel and all three buffers page-locked, mapped into the
  * device's address space (cudaHostAlloc memory under unified addressing) and 16-byte aligned, no
  * copies are queued: a one-CTA kernel reads x and logits from host memory into the workspace and
  * the decode kernel writes y into host memory itself. */

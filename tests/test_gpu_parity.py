@@ -198,7 +198,7 @@ def test_layer_tiny_small_T_and_ragged():
     for T in (1, 2, 3, 15):
         got = run_layer(wl, host, dl, inp, T=T)["y"]
         ref = O.moe_layer(inp["x"][:T], inp["logits"][:T], host, wl.k)["y"]
-        tol = DECODE_TOL if T == 1 else EXACT_TOL
+        tol = DECODE_TOL if T <= 3 else EXACT_TOL   # up to three tokens run the fp32 decode kernel
         assert rowwise_err(got, ref) <= tol, T
 
 
@@ -219,6 +219,22 @@ def test_decode_full_size():
         got = run_layer(wl, host, dl, inp)["y"]
         ref, _, _ = O.moe_token(inp["x"][0], inp["logits"][0], host, wl.k)
         assert rowwise_err(got, ref[None, :]) <= DECODE_TOL, seed
+
+
+@pytest.mark.parametrize("T", [2, 3, 4])
+def test_small_T_full_size(T):
+    """Two and three tokens at the decode shape run the fp32 decode kernel once per token (each
+    token within the decode bar, routing tables filled by the routing kernels); four tokens take
+    the grouped-GEMM path."""
+    wl = synth.DECODE
+    host, dl = layer_for(wl)
+    inp = synth.make_inputs(wl, seed=40 + T, T=T)
+    out = run_layer(wl, host, dl, inp, tile_n=112, T=T)
+    assert_routing_equal(out["routing"], inp["logits"][:T], wl.E, wl.k, 112)
+    tol = DECODE_TOL if T <= 3 else EXACT_TOL
+    for t in range(T):
+        ref, _, _ = O.moe_token(inp["x"][t], inp["logits"][t], host, wl.k)
+        assert rowwise_err(out["y"][t:t + 1], ref[None, :]) <= tol, t
 
 
 @pytest.mark.parametrize("d,F,tol", [(256, 384, DECODE_TOL),    # decode path, 3 column blocks of 128
@@ -278,7 +294,7 @@ def test_layer_host_entry_matches_device_entry(memory):
         v.copy_(a)
         return v
 
-    for T in (1, 37):
+    for T in (1, 3, 37):
         inp = synth.make_inputs(wl, seed=30 + T, T=T)
         dm = layer.dims(T)
         ws = moe.alloc_workspace_host(dm)
