@@ -13,8 +13,8 @@ engine; quoted by site, page title and section):
   (mechatronicstore.cl), section "Prefill: pesos comprimidos y enrutamiento en la GPU":
   4-bit affine quantisation by groups, every group of 64 weights shares one bf16 scale and
   one bf16 bias, so w = q * scale + bias.  The packing (eight codes per uint32, lowest
-  nibble = lowest column, groups along the input dimension) is this build's reading; the
-  pages do not state it.
+  nibble = lowest column, groups along the input dimension) is a reading; the pages do not
+  state it.
 * Router -- "Perplexity ouvre le code de Lily..." (lefilia.fr), article body, and the
   mechatronicstore.cl page, section "Tres formas de carga en un mismo modelo": a router
   scores 256 experts and keeps eight, plus one shared expert that every token uses.
@@ -24,7 +24,7 @@ engine; quoted by site, page title and section):
   prefix scan, a scatter and a block map are built on the GPU.  Their exact contents
   (counts, exclusive offsets, permutation sorted by (expert, token), tiles of at most
   tile_n rows per expert in (expert, tile) order, then the shared expert as group E) are
-  this build's definitions.
+  readings; the pages name the tables, not their layout.
 * Expert FFN -- the pages do not name the activation; SwiGLU h = silu(x Wg^T) * (x Wu^T),
   y = h Wd^T is the reading.  The pages state FP32 accumulation for the GPU GEMM; the oracle
   accumulates in fp64 (the exact reference), with an optional mode that rounds the GEMM
