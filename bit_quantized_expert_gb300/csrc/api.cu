@@ -436,6 +436,18 @@ static void* mapped_host(const void* p) {
   return attr.devicePointer;
 }
 
+// True for memory from cudaHostAlloc / cudaMallocHost, which the device may always write.  Memory
+// registered with cudaHostRegister can be read-only for the device (cudaHostRegisterReadOnly) and
+// its flags cannot be queried here, so an output buffer of that kind takes the copy instead.
+static bool host_alloc_writable(const void* p) {
+  unsigned int flags = 0;
+  if (cudaHostGetFlags(&flags, const_cast<void*>(p)) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return true;
+}
+
 static size_t host_staging_at(const moe_dims& d, size_t* x_off, size_t* lg_off, size_t* y_off) {
   const size_t base = (layout_of(d).total + 255) & ~(size_t)255;
   const size_t xb = ((size_t)d.T * d.d * 2 + 255) & ~(size_t)255;
@@ -479,7 +491,7 @@ moe_status moe_layer_forward_host(const moe_dims* dims, const uint16_t* x_host, 
   if (T <= (size_t)kDecodeLoopMaxT && decode_supported(dims->d, dims->E, dims->k, dims->F)) {
     void* xm = mapped_host(x_host);
     void* lm = mapped_host(logits_host);
-    void* ym = mapped_host(y_host);
+    void* ym = host_alloc_writable(y_host) ? mapped_host(y_host) : nullptr;
     if (xm != nullptr && lm != nullptr && ym != nullptr) {
       StageArgs sa{};
       sa.x_src = static_cast<const uint4*>(xm);

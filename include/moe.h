@@ -158,10 +158,11 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
  * asynchronous; pageable buffers work but the runtime may stage them synchronously.  The
  * workspace must hold moe_workspace_bytes_host(dims) bytes (the first moe_workspace_bytes(dims)
  * of it serve as the layer's workspace, error word included).  No routing tables are returned.
- * With T <= 3 on the fused decode kernel and all three buffers page-locked, mapped into the
- * device's address space (cudaHostAlloc memory under unified addressing) and 16-byte aligned, no
- * copies are queued: a one-CTA kernel reads x and logits from host memory into the workspace and
- * the decode kernel writes y into host memory itself. */
+ * With T <= 3 on the fused decode kernel, all three buffers page-locked, mapped into the
+ * device's address space (unified addressing) and 16-byte aligned, and y_host allocated by
+ * cudaHostAlloc / cudaMallocHost (registered memory may be read-only for the device), no copies
+ * are queued: a one-CTA kernel reads x and logits from host memory into the workspace and the
+ * decode kernel writes y into host memory itself. */
 size_t moe_workspace_bytes_host(const moe_dims* dims);
 moe_status moe_layer_forward_host(const moe_dims* dims, const uint16_t* x_host, const float* logits_host,
                                   const moe_experts* routed, const moe_experts* shared,

@@ -275,21 +275,27 @@ def test_decode_in_kernel_routing_ties_and_wide_rows():
             assert rowwise_err(got, ref[None, :]) <= DECODE_TOL, (E, ci)
 
 
-@pytest.mark.parametrize("memory", ["pinned", "pageable", "pinned_unaligned"])
+@pytest.mark.parametrize("memory", ["pinned", "pageable", "pinned_unaligned", "registered"])
 def test_layer_host_entry_matches_device_entry(memory):
-    """moe_layer_forward_host gives the device call's y, bit for bit, on the decode path (T = 1)
-    and the grouped-GEMM path (T = 37): with pinned, mapped, aligned buffers at T = 1 the decode
-    kernel reads and writes host memory itself; pageable or unaligned buffers, and T > 1, take
-    the copies."""
+    """moe_layer_forward_host gives the device call's y, bit for bit, on the decode path (T = 1, 3)
+    and the grouped-GEMM path (T = 37): with page-locked, mapped, aligned buffers at T <= 3 the
+    staging kernel reads host memory and the decode kernel writes y there (y only when it comes
+    from cudaHostAlloc; registered memory takes the copy for y); pageable or unaligned buffers,
+    and T > 3, take the copies."""
     wl = synth.TINY
     host, dl = layer_for(wl)
     layer = moe.Layer(dl["routed"], dl["shared"], dl["w_sg"], wl.d, wl.E, wl.k, wl.F)
-    pin = memory != "pageable"
+    pin = memory in ("pinned", "pinned_unaligned")
     off = 1 if memory == "pinned_unaligned" else 0   # one element past a 16-byte boundary
+    registered = []
 
     def host_buf(a):
         b = torch.zeros((a.shape[0] * a.shape[1] + off,), dtype=a.dtype)
         b = b.pin_memory() if pin else b
+        if memory == "registered":   # page-locked by cudaHostRegister (read-write), not cudaHostAlloc
+            rt = torch.cuda.cudart()
+            assert rt.cudaHostRegister(b.data_ptr(), b.numel() * b.element_size(), 0) == rt.cudaError.success
+            registered.append(b)
         v = b[off:].view(a.shape)
         v.copy_(a)
         return v
@@ -306,6 +312,9 @@ def test_layer_host_entry_matches_device_entry(memory):
         assert moe.read_error_flags(ws) == 0
         ref = run_layer(wl, host, dl, inp, T=T)["y"]
         assert np.array_equal(yh.numpy(), ref), (memory, T)
+    for b in registered:
+        rt = torch.cuda.cudart()
+        assert rt.cudaHostUnregister(b.data_ptr()) == rt.cudaError.success
 
 
 def test_gemm_path_refuses_tiles_wider_than_112():
