@@ -285,9 +285,8 @@ def decode_bench(args, world, rank, local, device, pk):
                      "note": "one weight set replayed (weights L2-resident); not the headline"}
     log(f"decode hot-L2: {res['hot_l2']['us_per_layer']:.2f} us per layer")
 
-    # A few tokens per layer call (verify-batch shapes): up to three run the decode kernel once per
-    # token, four take the grouped GEMM.  CUDA graph over the 40 weight sets; context, not the
-    # headline.
+    # A few tokens per layer call (verify-batch shapes): up to eight run the decode kernel in one
+    # launch.  CUDA graph over the 40 weight sets; context, not the headline.
     small = {}
     ys = torch.empty((4, wl.d), dtype=torch.float32, device=device)
     for T in (2, 3, 4):

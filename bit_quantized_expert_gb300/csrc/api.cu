@@ -53,7 +53,7 @@ Layout layout_of(const moe_dims& d) {
   L.chunk = take(tables_scratch_bytes((int)T, (int)E));   // routing-table scratch
   L.h = take(slots * F * 2);
   L.yperm = take(slots * D * 2);   // fp16 expert outputs of the layer path
-  L.hdec = take(T >= 1 && T <= (size_t)kDecodeLoopMaxT ? decode_scratch_floats((int)D, (int)k, (int)F) * 4 : 0);   // decode partials
+  L.hdec = take(T >= 1 && T <= (size_t)kDecodeLayerMaxT ? T * decode_scratch_floats((int)D, (int)k, (int)F) * 4 : 0);   // decode partials
   L.total = o;
   return L;
 }
@@ -370,11 +370,9 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
   const bool sh = shared != nullptr;
   const moe_dims& d = *dims;
 
-  // One to kDecodeLoopMaxT tokens: the fused decode kernel, one launch per token, chained with
-  // programmatic dependent launches.  Each launch streams the token's k + 1 experts once; at the
-  // decode shape (d 2048, E 256, k 8, F 512) this beats the grouped GEMM up to three tokens
-  // (34 / 51 us against 57 / 61 us for two / three tokens), from four on the GEMM wins.
-  if (d.T <= kDecodeLoopMaxT && decode_supported(d.d, d.E, d.k, d.F)) {
+  // One to kDecodeLayerMaxT tokens: the fused decode kernel, one launch for all of them (each CTA
+  // takes its expert slot of every token in turn, one grid barrier and reduction for all).
+  if (d.T <= kDecodeLayerMaxT && decode_supported(d.d, d.E, d.k, d.F)) {
     DecodeArgs da{};
     da.x = x;
     da.logits = logits;
@@ -396,12 +394,8 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
     da.y = y;
     da.err = err;
     da.sync = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + L.err + kSyncOffset);
-    for (int t = 0; t < d.T; ++t) {
-      da.x = x + (size_t)t * d.d;
-      da.logits = logits + (size_t)t * d.E;
-      da.y = y + (size_t)t * d.d;
-      if (launch_decode(da, st, true) != cudaSuccess) return MOE_ERR_CUDA;
-    }
+    da.T = d.T;
+    if (launch_decode(da, st, true) != cudaSuccess) return MOE_ERR_CUDA;
     if (routing_out != nullptr)
       return cuda_status(run_routing(d, logits, caller_routing(routing_out), nullptr, nullptr, nullptr,
                                      at<int32_t>(workspace, L.chunk), err, st));
@@ -482,13 +476,13 @@ moe_status moe_layer_forward_host(const moe_dims* dims, const uint16_t* x_host, 
   float* logits = reinterpret_cast<float*>(ws + lo);
   float* y = reinterpret_cast<float*>(ws + yo);
   const size_t T = (size_t)dims->T;
-  // Tokens on the fused decode kernel (T <= kDecodeLoopMaxT): when all three buffers are
+  // Tokens on the fused decode kernel (T <= kDecodeLayerMaxT): when all three buffers are
   // page-locked host memory mapped into the device's address space, one small kernel reads x and
   // logits across the CPU-GPU link into the workspace (once, instead of once per CTA of the
   // decode kernel), and the decode kernel writes y into host memory itself -- no copy-engine
   // transfers on the stream.  Anything else (pageable memory, unaligned pointers, more tokens)
   // takes the copies.
-  if (T <= (size_t)kDecodeLoopMaxT && decode_supported(dims->d, dims->E, dims->k, dims->F)) {
+  if (T <= (size_t)kDecodeLayerMaxT && decode_supported(dims->d, dims->E, dims->k, dims->F)) {
     void* xm = mapped_host(x_host);
     void* lm = mapped_host(logits_host);
     void* ym = host_alloc_writable(y_host) ? mapped_host(y_host) : nullptr;

@@ -1,4 +1,4 @@
-// Decode (T = 1) MoE layer as one bandwidth-bound dequant-GEMV kernel.
+// Decode MoE layer (one token, or a few: T <= 8) as one bandwidth-bound dequant-GEMV kernel.
 //
 // At batch 1 there is almost no weight reuse, so weight bandwidth sets the ceiling ("Perplexity
 // libera Lily: inferencia en Rust y Metal para Mac", section "Decode: mover menos bytes por
@@ -25,6 +25,12 @@
 //     half, a generation count in the high half; the last arrival resets the count and bumps the
 //     generation), then sums a slice of rows over all CTAs in a fixed order:
 //     y[r] = sum_c part_c[r] -- deterministic, no atomics on data.
+//
+// A few tokens (T > 1, the kernel<true> instantiation): warp t routes token t; every CTA then
+// takes its expert slot of token 0, 1, ... in turn, fetching the slot's weights again only when
+// its expert changes (the shared expert's stay), and writes part_c per token; one grid barrier
+// and one fixed-order reduction serve all tokens, so each token's y is what a one-token launch
+// gives, bit for bit.  The one-token launch is the kernel<false> instantiation (T fixed at 1).
 //
 // Arithmetic: codes become exact fp32 values q * 16^e via the 2^23 exponent trick (the nibble
 // stays where it is in the word; the activation carries the matching 16^-e), partial dot
@@ -112,6 +118,8 @@ __device__ __forceinline__ unsigned long long ld_acquire(const unsigned long lon
   return v;
 }
 
+// kMulti = false: one token (T fixed at 1, so the token loop and the per-token arrays fold away).
+template <bool kMulti>
 __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t sm[];
   const int d = a.d, F = a.F, k = a.k;
@@ -133,9 +141,10 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
   uint16_t* dsb16 = reinterpret_cast<uint16_t*>(sm + P.dn_sb);       // [s | b][d][GF] (whole)
   float* hbuf = reinterpret_cast<float*>(sm + P.hbuf);               // [RF]
   __shared__ __align__(8) uint64_t bars[kQuarters + 1];   // gate/up quarters, then the down scales
-  __shared__ int e_s;
-  __shared__ float wgt_s;    // w_j (routed) or the shared-expert gate
+  __shared__ int e_s[kDecodeMaxTokens];
+  __shared__ float wgt_s[kDecodeMaxTokens];    // w_j (routed) or the shared-expert gate, per token
   __shared__ int abort_s;
+  const int T = kMulti ? (a.T > 0 ? a.T : 1) : 1;
 
   if (tid == 0) {
     for (int i = 0; i <= kQuarters; ++i) mbar_init(smem_u32(&bars[i]), 1);
@@ -199,149 +208,175 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
   }
   pdl_wait();   // x and logits from upstream kernels are complete and visible past this point
 
-  if (warp == 0 && !shared_cta) {
+  if (warp < T && !shared_cta) {
+    // warp t routes token t; token 0's weights are requested as soon as its expert is known
     int e;
     float w;
-    reg_topk(a.logits, a.E, k, &e, &w);
+    reg_topk(a.logits + (size_t)warp * a.E, a.E, k, &e, &w);
     const int ej = __shfl_sync(0xFFFFFFFFu, e, j);
     const float wj = __shfl_sync(0xFFFFFFFFu, w, j);
     if (lane == 0) {
-      e_s = ej;
-      wgt_s = wj;
-      issue_gu(ej);
+      e_s[warp] = ej;
+      wgt_s[warp] = wj;
+      if (warp == 0) issue_gu(ej);
     }
-  } else if (warp == 1 && shared_cta) {
-    float dot = 0.0f;
-    const uint4* xv = reinterpret_cast<const uint4*>(a.x);
-    const uint4* gv = reinterpret_cast<const uint4*>(a.w_sg);
-    for (int c = lane; c < d / 8; c += 32) {
-      const uint4 xq = __ldg(xv + c), gq = __ldg(gv + c);
-      const uint32_t xw[4] = {xq.x, xq.y, xq.z, xq.w}, gw[4] = {gq.x, gq.y, gq.z, gq.w};
+  } else if (shared_cta) {
+    // warp w: the shared-expert gates of tokens w, w + 8, ...
+    for (int t = warp; t < T; t += kThreadsDec / 32) {
+      float dot = 0.0f;
+      const uint4* xv = reinterpret_cast<const uint4*>(a.x + (size_t)t * d);
+      const uint4* gv = reinterpret_cast<const uint4*>(a.w_sg);
+      for (int c = lane; c < d / 8; c += 32) {
+        const uint4 xq = __ldg(xv + c), gq = __ldg(gv + c);
+        const uint32_t xw[4] = {xq.x, xq.y, xq.z, xq.w}, gw[4] = {gq.x, gq.y, gq.z, gq.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        dot = fmaf(bf16_bits_to_f32(xw[i] & 0xFFFFu), bf16_bits_to_f32(gw[i] & 0xFFFFu), dot);
-        dot = fmaf(bf16_bits_to_f32(xw[i] >> 16), bf16_bits_to_f32(gw[i] >> 16), dot);
+        for (int i = 0; i < 4; ++i) {
+          dot = fmaf(bf16_bits_to_f32(xw[i] & 0xFFFFu), bf16_bits_to_f32(gw[i] & 0xFFFFu), dot);
+          dot = fmaf(bf16_bits_to_f32(xw[i] >> 16), bf16_bits_to_f32(gw[i] >> 16), dot);
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, off);
+      if (lane == 0) {
+        e_s[t] = 0;
+        wgt_s[t] = 1.0f / (1.0f + expf(-dot));
       }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, off);
-    if (lane == 0) wgt_s = 1.0f / (1.0f + expf(-dot));
   }
   pdl_launch_dependents();
   __syncthreads();   // e_s and wgt_s
-  // x: lane l owns quantisation group l (64 inputs).  The loads go out after routing, so the
-  // logits are the first reads behind the dependency wait, and before the down copies; the
-  // gate/up products wait for the weights, which arrive later.
+  // Tokens one after another.  The slot's weights stay in shared memory while the slot's expert
+  // stays the same (always for the shared expert), and are fetched again when it changes; every
+  // fetch is one phase of the copy barriers, so waits use the parity of the fetch count.
   const bool active = lane < G;
-  uint4 xr[8];
-#pragma unroll
-  for (int c8 = 0; c8 < 8; ++c8)
-    xr[c8] = active ? __ldg(reinterpret_cast<const uint4*>(a.x) + lane * 8 + c8) : make_uint4(0u, 0u, 0u, 0u);
-  if (!shared_cta) copy_dn(e_s);
-
-  // ---- gate/up: warp w computes gate and up of rows q*8 + w (q = 0..3) as slots s = 2q + mat;
-  // a reduce-scatter leaves slot s fully summed in lane 4s.
-  float2 xs[32];
-  float xsum = 0.0f;
-#pragma unroll
-  for (int c8 = 0; c8 < 8; ++c8) {
-    const uint32_t wv[4] = {xr[c8].x, xr[c8].y, xr[c8].z, xr[c8].w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float lo = bf16_bits_to_f32(wv[i] & 0xFFFFu), hi = bf16_bits_to_f32(wv[i] >> 16);
-      xsum += lo + hi;
-      xs[c8 * 4 + i] = make_float2(lo * act_prescale(2 * i), hi * act_prescale(2 * i + 1));
-    }
-  }
-  float v8[8];
-#pragma unroll
-  for (int sl = 0; sl < 8; ++sl) v8[sl] = 0.0f;
-  bool ok_all = true;
+  int loads = 1;   // weight fetches so far (token 0's is in flight)
 #pragma unroll 1
-  for (int q = 0; q < kQuarters; ++q) {
-    const bool ok = mbar_wait_warp(smem_u32(&bars[q]), 0, &abort_s, a.err);
-    ok_all = ok_all && ok;
-#pragma unroll
-    for (int mat = 0; mat < 2; ++mat) {
-      const int row = q * kRQ + warp;
-      float v = 0.0f;
-      if (active && ok) {
-        const uint32_t* cw = gcodes + (mat * RF + row) * (d / 8) + lane * 8;
-        const uint4 c0 = *reinterpret_cast<const uint4*>(cw);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(cw + 4);
-        float2 p0 = make_float2(0.0f, 0.0f), p1 = make_float2(0.0f, 0.0f);
-        p0 = word_dot2(c0.x, xs + 0, p0);
-        p1 = word_dot2(c0.y, xs + 4, p1);
-        p0 = word_dot2(c0.z, xs + 8, p0);
-        p1 = word_dot2(c0.w, xs + 12, p1);
-        p0 = word_dot2(c1.x, xs + 16, p0);
-        p1 = word_dot2(c1.y, xs + 20, p1);
-        p0 = word_dot2(c1.z, xs + 24, p0);
-        p1 = word_dot2(c1.w, xs + 28, p1);
-        const float p = (p0.x + p0.y) + (p1.x + p1.y);
-        const float s = bf16_bits_to_f32(gsb[((2 * mat) * RF + row) * G + lane]);
-        const float b = bf16_bits_to_f32(gsb[((2 * mat + 1) * RF + row) * G + lane]);
-        v = fmaf(s, p, b * xsum);
+  for (int t = 0; t < T; ++t) {
+    if (t > 0 && abort_s) break;   // uniform: abort_s is only written inside waits, before the barrier below
+    const int e_t = e_s[t];
+    if (t > 0 && e_t != e_s[t - 1]) {
+      if (tid == 0) {
+        fence_proxy_async_smem();   // the previous token's reads of these buffers are complete
+        issue_gu(e_t);
       }
-      const int sl = 2 * q + mat;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) v8[t] = (t == sl) ? v : v8[t];
+      ++loads;
     }
-  }
-  {
-    float t4[4], t2[2];
-    const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0, b2 = (lane & 4) != 0;
+    const uint32_t ph = (uint32_t)(loads - 1) & 1u;
+    // x: lane l owns quantisation group l (64 inputs).  For token 0 the loads go out after
+    // routing, so the logits are the first reads behind the dependency wait, and before the down
+    // copies; the gate/up products wait for the weights, which arrive later.
+    uint4 xr[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      t4[i] = (b4 ? v8[i + 4] : v8[i]) + __shfl_xor_sync(0xFFFFFFFFu, b4 ? v8[i] : v8[i + 4], 16);
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-      t2[i] = (b3 ? t4[i + 2] : t4[i]) + __shfl_xor_sync(0xFFFFFFFFu, b3 ? t4[i] : t4[i + 2], 8);
-    float t1 = (b2 ? t2[1] : t2[0]) + __shfl_xor_sync(0xFFFFFFFFu, b2 ? t2[0] : t2[1], 4);
-    t1 += __shfl_xor_sync(0xFFFFFFFFu, t1, 2);
-    t1 += __shfl_xor_sync(0xFFFFFFFFu, t1, 1);
-    const float upv = __shfl_down_sync(0xFFFFFFFFu, t1, 4);   // slot 2q+1 (lane 8q+4) -> lane 8q
-    if ((lane & 7) == 0) {
-      const float gv = t1;
-      hbuf[(lane >> 3) * kRQ + warp] = gv / (1.0f + expf(-gv)) * upv;
-    }
-  }
-  cp_async_wait<0>();
-  const bool ok_dn = !P.bulk_sb || mbar_wait_warp(smem_u32(&bars[kQuarters]), 0, &abort_s, a.err);
-  __syncthreads();   // h and this thread's down copies -> visible to the whole CTA
+    for (int c8 = 0; c8 < 8; ++c8)
+      xr[c8] = active ? __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * d) + lane * 8 + c8)
+                      : make_uint4(0u, 0u, 0u, 0u);
+    if ((t == 0 && !shared_cta) || (t > 0 && e_t != e_s[t - 1])) copy_dn(e_t);
 
-  // ---- down share: part_c[r] = wgt * (s * sum_f q h_f + b * sum_f h_f) over f0 .. f0+31.
-  {
-    float2 hv[16];
-    float hsum = 0.0f;
+    // ---- gate/up: warp w computes gate and up of rows q*8 + w (q = 0..3) as slots s = 2q + mat;
+    // a reduce-scatter leaves slot s fully summed in lane 4s.
+    float2 xs[32];
+    float xsum = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float hx = hbuf[2 * i], hy = hbuf[2 * i + 1];
-      hsum += hx + hy;
-      hv[i] = make_float2(hx * act_prescale(2 * i), hy * act_prescale(2 * i + 1));
-    }
-    const float wgt = wgt_s;
-    const bool hi_half = ((f0 / 64) & 1) != 0;   // group f0/64 is the upper bf16 of its pair
-    const int g = f0 / 64;
-    for (int r = tid; r < d && ok_dn; r += kThreadsDec) {
-      const uint4 c = *reinterpret_cast<const uint4*>(dcodes + 4 * r);
-      float2 p0 = make_float2(0.0f, 0.0f), p1 = make_float2(0.0f, 0.0f);
-      p0 = word_dot2(c.x, hv + 0, p0);
-      p1 = word_dot2(c.y, hv + 4, p1);
-      p0 = word_dot2(c.z, hv + 8, p0);
-      p1 = word_dot2(c.w, hv + 12, p1);
-      const float p = (p0.x + p0.y) + (p1.x + p1.y);
-      float s, b;
-      if (P.bulk_sb) {
-        s = bf16_bits_to_f32(dsb16[r * GF + g]);
-        b = bf16_bits_to_f32(dsb16[(d + r) * GF + g]);
-      } else {
-        const uint32_t sp = dsb[r], bp = dsb[d + r];
-        s = bf16_bits_to_f32(hi_half ? (sp >> 16) : (sp & 0xFFFFu));
-        b = bf16_bits_to_f32(hi_half ? (bp >> 16) : (bp & 0xFFFFu));
+    for (int c8 = 0; c8 < 8; ++c8) {
+      const uint32_t wv[4] = {xr[c8].x, xr[c8].y, xr[c8].z, xr[c8].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float lo = bf16_bits_to_f32(wv[i] & 0xFFFFu), hi = bf16_bits_to_f32(wv[i] >> 16);
+        xsum += lo + hi;
+        xs[c8 * 4 + i] = make_float2(lo * act_prescale(2 * i), hi * act_prescale(2 * i + 1));
       }
-      a.part[(size_t)cta * d + r] = wgt * fmaf(s, p, b * hsum);
     }
+    float v8[8];
+#pragma unroll
+    for (int sl = 0; sl < 8; ++sl) v8[sl] = 0.0f;
+    bool ok_all = true;
+#pragma unroll 1
+    for (int q = 0; q < kQuarters; ++q) {
+      const bool ok = mbar_wait_warp(smem_u32(&bars[q]), ph, &abort_s, a.err);
+      ok_all = ok_all && ok;
+#pragma unroll
+      for (int mat = 0; mat < 2; ++mat) {
+        const int row = q * kRQ + warp;
+        float v = 0.0f;
+        if (active && ok) {
+          const uint32_t* cw = gcodes + (mat * RF + row) * (d / 8) + lane * 8;
+          const uint4 c0 = *reinterpret_cast<const uint4*>(cw);
+          const uint4 c1 = *reinterpret_cast<const uint4*>(cw + 4);
+          float2 p0 = make_float2(0.0f, 0.0f), p1 = make_float2(0.0f, 0.0f);
+          p0 = word_dot2(c0.x, xs + 0, p0);
+          p1 = word_dot2(c0.y, xs + 4, p1);
+          p0 = word_dot2(c0.z, xs + 8, p0);
+          p1 = word_dot2(c0.w, xs + 12, p1);
+          p0 = word_dot2(c1.x, xs + 16, p0);
+          p1 = word_dot2(c1.y, xs + 20, p1);
+          p0 = word_dot2(c1.z, xs + 24, p0);
+          p1 = word_dot2(c1.w, xs + 28, p1);
+          const float p = (p0.x + p0.y) + (p1.x + p1.y);
+          const float s = bf16_bits_to_f32(gsb[((2 * mat) * RF + row) * G + lane]);
+          const float b = bf16_bits_to_f32(gsb[((2 * mat + 1) * RF + row) * G + lane]);
+          v = fmaf(s, p, b * xsum);
+        }
+        const int sl = 2 * q + mat;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) v8[t] = (t == sl) ? v : v8[t];
+      }
+    }
+    {
+      float t4[4], t2[2];
+      const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0, b2 = (lane & 4) != 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        t4[i] = (b4 ? v8[i + 4] : v8[i]) + __shfl_xor_sync(0xFFFFFFFFu, b4 ? v8[i] : v8[i + 4], 16);
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        t2[i] = (b3 ? t4[i + 2] : t4[i]) + __shfl_xor_sync(0xFFFFFFFFu, b3 ? t4[i] : t4[i + 2], 8);
+      float t1 = (b2 ? t2[1] : t2[0]) + __shfl_xor_sync(0xFFFFFFFFu, b2 ? t2[0] : t2[1], 4);
+      t1 += __shfl_xor_sync(0xFFFFFFFFu, t1, 2);
+      t1 += __shfl_xor_sync(0xFFFFFFFFu, t1, 1);
+      const float upv = __shfl_down_sync(0xFFFFFFFFu, t1, 4);   // slot 2q+1 (lane 8q+4) -> lane 8q
+      if ((lane & 7) == 0) {
+        const float gv = t1;
+        hbuf[(lane >> 3) * kRQ + warp] = gv / (1.0f + expf(-gv)) * upv;
+      }
+    }
+    cp_async_wait<0>();
+    const bool ok_dn = !P.bulk_sb || mbar_wait_warp(smem_u32(&bars[kQuarters]), ph, &abort_s, a.err);
+    __syncthreads();   // h and this thread's down copies -> visible to the whole CTA
+
+    // ---- down share: part_c[r] = wgt * (s * sum_f q h_f + b * sum_f h_f) over f0 .. f0+31.
+    {
+      float2 hv[16];
+      float hsum = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float hx = hbuf[2 * i], hy = hbuf[2 * i + 1];
+        hsum += hx + hy;
+        hv[i] = make_float2(hx * act_prescale(2 * i), hy * act_prescale(2 * i + 1));
+      }
+      const float wgt = wgt_s[t];
+      const bool hi_half = ((f0 / 64) & 1) != 0;   // group f0/64 is the upper bf16 of its pair
+      const int g = f0 / 64;
+      for (int r = tid; r < d && ok_dn; r += kThreadsDec) {
+        const uint4 c = *reinterpret_cast<const uint4*>(dcodes + 4 * r);
+        float2 p0 = make_float2(0.0f, 0.0f), p1 = make_float2(0.0f, 0.0f);
+        p0 = word_dot2(c.x, hv + 0, p0);
+        p1 = word_dot2(c.y, hv + 4, p1);
+        p0 = word_dot2(c.z, hv + 8, p0);
+        p1 = word_dot2(c.w, hv + 12, p1);
+        const float p = (p0.x + p0.y) + (p1.x + p1.y);
+        float s, b;
+        if (P.bulk_sb) {
+          s = bf16_bits_to_f32(dsb16[r * GF + g]);
+          b = bf16_bits_to_f32(dsb16[(d + r) * GF + g]);
+        } else {
+          const uint32_t sp = dsb[r], bp = dsb[d + r];
+          s = bf16_bits_to_f32(hi_half ? (sp >> 16) : (sp & 0xFFFFu));
+          b = bf16_bits_to_f32(hi_half ? (bp >> 16) : (bp & 0xFFFFu));
+        }
+        a.part[((size_t)t * gridDim.x + cta) * d + r] = wgt * fmaf(s, p, b * hsum);
+      }
+    }
+    __syncthreads();   // this token's reads of the weight buffers and of h are complete
   }
 
   // ---- grid barrier: every CTA arrives once; the last arrival resets the count and bumps the
@@ -374,7 +409,10 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
     const int rpc = (d + n - 1) / n;
     const int r_lo = cta * rpc, r_hi = min(d, r_lo + rpc);
     const int sub = tid & 15;
+#pragma unroll 1
+    for (int t = 0; t < T; ++t)
     for (int rb = r_lo; rb < r_hi; rb += kThreadsDec / 16) {
+      const float* part = a.part + (size_t)t * n * d;
       const int r = rb + (tid >> 4);
       float acc = 0.0f;
       if (r < r_hi) {
@@ -382,25 +420,26 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
 #pragma unroll
         for (int i = 0; i < 10; ++i) {
           const int c = sub + 16 * i;
-          v[i] = c < n ? __ldcg(a.part + (size_t)c * d + r) : 0.0f;
+          v[i] = c < n ? __ldcg(part + (size_t)c * d + r) : 0.0f;
         }
 #pragma unroll
         for (int i = 0; i < 10; ++i) acc += v[i];
-        for (int c = sub + 160; c < n; c += 16) acc += __ldcg(a.part + (size_t)c * d + r);
+        for (int c = sub + 160; c < n; c += 16) acc += __ldcg(part + (size_t)c * d + r);
       }
       acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 8);
       acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 4);
       acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 2);
       acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
-      if (sub == 0 && r < r_hi) a.y[r] = acc;
+      if (sub == 0 && r < r_hi) a.y[(size_t)t * d + r] = acc;
     }
   }
 
   // ---- wind down: after a timeout, copies still in flight must land before the CTA exits.
   if (tid == 0 && abort_s) {
+    const uint32_t last = (uint32_t)(loads - 1) & 1u;   // parity of the last fetch issued
     for (int i = 0; i <= kQuarters; ++i) {
       const long long t0 = clock64();
-      while (!mbar_try_wait(smem_u32(&bars[i]), 0) && clock64() - t0 < 4000000ll) {
+      while (!mbar_try_wait(smem_u32(&bars[i]), last) && clock64() - t0 < 4000000ll) {
       }
     }
   }
@@ -424,9 +463,13 @@ cudaError_t dev_info(DevInfo** out) {
   DevInfo& di = g_dev[dev];
   if (!di.ready) {
     if ((e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecSmemMax);
+    e = cudaFuncSetAttribute(decode_layer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecSmemMax);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      e = cudaFuncSetAttribute(decode_layer_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_layer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecSmemMax);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_layer_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     di.ready = true;
   }
@@ -502,7 +545,11 @@ cudaError_t launch_stage_in(const StageArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+static_assert(kDecodeMaxTokens <= kThreadsDec / 32, "one routing warp per token");
+static_assert(kDecodeLayerMaxT <= kDecodeMaxTokens, "the layer path's decode calls fit one launch");
+
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st, bool pdl) {
+  if (a.T > kDecodeMaxTokens) return cudaErrorInvalidValue;
   const int k1 = a.k + (a.has_shared ? 1 : 0);
   DevInfo* di = nullptr;
   cudaError_t e = dev_info(&di);
@@ -521,7 +568,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st, bool pdl) {
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  e = cudaLaunchKernelEx(&cfg, decode_layer_kernel, a);
+  e = a.T > 1 ? cudaLaunchKernelEx(&cfg, decode_layer_kernel<true>, a) : cudaLaunchKernelEx(&cfg, decode_layer_kernel<false>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -101,19 +101,21 @@ cudaError_t launch_permute_x(const PermuteArgs& a, cudaStream_t st);
 
 // ---------------------------------------------------------------- decode T = 1 (decode.cu)
 struct DecodeArgs {
-  const uint16_t* x;       // bf16 [d]
-  const float* logits;     // [E]
+  const uint16_t* x;       // bf16 [T][d]
+  const float* logits;     // [T][E]
   QPtr gate[2], up[2], down[2];   // [0] routed (stacked over E), [1] shared (may be null)
   const uint16_t* w_sg;    // bf16 [d] or null
   int d, E, k, F, has_shared;
-  float* part;             // scratch: fp32 [(k+1) F / 32][d] per-CTA partial outputs
-  float* y;                // fp32 [d]
+  int T;                   // tokens, 1 .. kDecodeMaxTokens (0 reads as 1)
+  float* part;             // scratch: fp32 [T][(k+1) F / 32][d] per-CTA partial outputs
+  float* y;                // fp32 [T][d]
   uint32_t* err;
   unsigned long long* sync;   // grid-barrier word (8-byte aligned; count low, generation high)
 };
 bool decode_supported(int d, int E, int k, int F);
-constexpr int kDecodeLoopMaxT = 3;   // layer calls of up to this many tokens run the decode kernel per token
-size_t decode_scratch_floats(int d, int k, int F);   // floats of DecodeArgs::part
+constexpr int kDecodeMaxTokens = 8;   // tokens one decode launch can take (one routing warp each)
+constexpr int kDecodeLayerMaxT = 8;    // layer calls of up to this many tokens take the decode kernel
+size_t decode_scratch_floats(int d, int k, int F);   // floats of DecodeArgs::part per token
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st, bool pdl);
 // One CTA copies a token's x (x_bytes, a multiple of 16) and logits (lg_bytes, a multiple of 4)
 // from page-locked, mapped host memory (16-byte aligned) into device buffers, once, so that the

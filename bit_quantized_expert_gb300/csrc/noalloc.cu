@@ -113,6 +113,7 @@ extern "C" moe_status moe_layer_forward_decode_noalloc(const moe_dims* dims, con
   da.k = dims->k;
   da.F = dims->F;
   da.has_shared = sh ? 1 : 0;
+  da.T = 1;
   da.part = scratch + kNoAllocHeadFloats;
   da.y = y;
   da.err = err;

@@ -139,9 +139,10 @@ moe_status moe_expert_forward(const moe_dims* dims, const uint16_t* x, const moe
 /* The whole layer: y[t] = sum_j w[t,j] FFN_{idx[t,j]}(x_t) + sigmoid(x_t . w_sg) FFN_shared(x_t).
  * x bf16 [T, d]; logits fp32 [T, E]; w_shared_gate bf16 [d] (ignored when shared is NULL);
  * y fp32 [T, d].  routing_out may be NULL; when given, its tables are filled as by moe_route.
- * T <= 3 runs the fused decode path (fp32 arithmetic on CUDA cores; one launch per token, each
- * streaming that token's experts) when d <= 2048, d % 64 == 0, F % 128 == 0, k < 32, E <= 1024
- * and (k + 1) * F / 32 CTAs fit one per SM; otherwise, and for T > 3, the grouped-GEMM path
+ * T <= 8 runs the fused decode path (fp32 arithmetic on CUDA cores; one launch for all tokens,
+ * each expert slot taking the tokens in turn) when d <= 2048, d % 64 == 0, F % 128 == 0, k < 32,
+ * E <= 1024 and (k + 1) * F / 32 CTAs fit one per SM; otherwise, and for T > 8, the grouped-GEMM
+ * path
  * (fp16 tensor-core operands, fp32 accumulation; needs
  * d % 256 == 0, and routing_out->tile_n <= 112 when routing_out is given; MOE_ERR_UNSUPPORTED
  * otherwise).  Its own block map uses tiles of 112 rows. */
@@ -158,7 +159,7 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
  * asynchronous; pageable buffers work but the runtime may stage them synchronously.  The
  * workspace must hold moe_workspace_bytes_host(dims) bytes (the first moe_workspace_bytes(dims)
  * of it serve as the layer's workspace, error word included).  No routing tables are returned.
- * With T <= 3 on the fused decode kernel, all three buffers page-locked, mapped into the
+ * With T <= 8 on the fused decode kernel, all three buffers page-locked, mapped into the
  * device's address space (unified addressing) and 16-byte aligned, and y_host allocated by
  * cudaHostAlloc / cudaMallocHost (registered memory may be read-only for the device), no copies
  * are queued: a one-CTA kernel reads x and logits from host memory into the workspace and the

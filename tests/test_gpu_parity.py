@@ -23,6 +23,7 @@ pytestmark = pytest.mark.gpu
 EXACT_TOL = 2e-3
 EMUL_TOL = 5e-4
 DECODE_TOL = 2e-5
+DECODE_MAX_T = 8   # layer calls of up to this many tokens take the fp32 decode kernel
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -198,7 +199,7 @@ def test_layer_tiny_small_T_and_ragged():
     for T in (1, 2, 3, 15):
         got = run_layer(wl, host, dl, inp, T=T)["y"]
         ref = O.moe_layer(inp["x"][:T], inp["logits"][:T], host, wl.k)["y"]
-        tol = DECODE_TOL if T <= 3 else EXACT_TOL   # up to three tokens run the fp32 decode kernel
+        tol = DECODE_TOL if T <= DECODE_MAX_T else EXACT_TOL   # a few tokens run the fp32 decode kernel
         assert rowwise_err(got, ref) <= tol, T
 
 
@@ -221,20 +222,42 @@ def test_decode_full_size():
         assert rowwise_err(got, ref[None, :]) <= DECODE_TOL, seed
 
 
-@pytest.mark.parametrize("T", [2, 3, 4])
+@pytest.mark.parametrize("T", [2, 3, 4, 6, 8, 9])
 def test_small_T_full_size(T):
-    """Two and three tokens at the decode shape run the fp32 decode kernel once per token (each
-    token within the decode bar, routing tables filled by the routing kernels); four tokens take
-    the grouped-GEMM path."""
+    """A few tokens at the decode shape: up to DECODE_MAX_T run the fp32 decode kernel in one
+    launch (each token within the decode bar, routing tables filled by the routing kernels), more
+    take the grouped-GEMM path."""
     wl = synth.DECODE
     host, dl = layer_for(wl)
     inp = synth.make_inputs(wl, seed=40 + T, T=T)
     out = run_layer(wl, host, dl, inp, tile_n=112, T=T)
     assert_routing_equal(out["routing"], inp["logits"][:T], wl.E, wl.k, 112)
-    tol = DECODE_TOL if T <= 3 else EXACT_TOL
+    tol = DECODE_TOL if T <= DECODE_MAX_T else EXACT_TOL
     for t in range(T):
         ref, _, _ = O.moe_token(inp["x"][t], inp["logits"][t], host, wl.k)
         assert rowwise_err(out["y"][t:t + 1], ref[None, :]) <= tol, t
+
+
+def test_decode_tokens_sharing_experts():
+    """Tokens of one decode launch that pick the same experts: with equal logits every expert slot
+    keeps its expert from token to token (the weights stay in shared memory); a token repeated
+    exactly gives the same y bit for bit; every token within the decode bar."""
+    wl = synth.DECODE
+    host, dl = layer_for(wl)
+    T = 5
+    inp = synth.make_inputs(wl, seed=77, T=T)
+    x = inp["x"].copy()
+    lg = inp["logits"].copy()
+    lg[1:4] = lg[0]          # tokens 0..3: same experts, different activations
+    x[4] = x[2]
+    lg[4] = lg[2]            # token 4 repeats token 2
+    inp = {"x": x, "logits": lg}
+    out = run_layer(wl, host, dl, inp, tile_n=112, T=T)
+    assert_routing_equal(out["routing"], lg, wl.E, wl.k, 112)
+    assert np.array_equal(out["y"][4], out["y"][2])
+    for t in range(T):
+        ref, _, _ = O.moe_token(x[t], lg[t], host, wl.k)
+        assert rowwise_err(out["y"][t:t + 1], ref[None, :]) <= DECODE_TOL, t
 
 
 @pytest.mark.parametrize("d,F,tol", [(256, 384, DECODE_TOL),    # decode path, 3 column blocks of 128
@@ -334,8 +357,10 @@ def test_gemm_path_refuses_tiles_wider_than_112():
 
 
 def test_gemm_path_needs_d_multiple_of_256():
-    """The grouped-GEMM path pairs 128-row blocks of d: d = 384 at T > 1 is refused up front."""
-    wl = synth.Workload("d384", T=8, d=384, E=16, k=2, F=128, F_shared=128)
+    """The grouped-GEMM path pairs 128-row blocks of d: d = 384 beyond DECODE_MAX_T tokens is
+    refused up front, while DECODE_MAX_T tokens run the decode kernel, which takes it."""
+    T = DECODE_MAX_T + 1
+    wl = synth.Workload("d384", T=T, d=384, E=16, k=2, F=128, F_shared=128)
     host = synth.make_layer(wl)
     dl = moe.to_device_layer(host)
     inp = synth.make_inputs(wl, seed=9)
@@ -346,6 +371,9 @@ def test_gemm_path_needs_d_multiple_of_256():
     with pytest.raises(moe.MoeError) as ei:
         moe.layer_forward(dm, x, lg, dl["routed"], dl["shared"], dl["w_sg"], y, ws)
     assert ei.value.status == 2   # MOE_ERR_UNSUPPORTED
+    got = run_layer(wl, host, dl, inp, T=DECODE_MAX_T)["y"]
+    ref = O.moe_layer(inp["x"][:DECODE_MAX_T], inp["logits"][:DECODE_MAX_T], host, wl.k)["y"]
+    assert rowwise_err(got, ref) <= DECODE_TOL
 
 
 def test_decode_routing_out_matches_oracle():
