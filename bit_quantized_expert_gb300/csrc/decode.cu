@@ -254,13 +254,7 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
   for (int t = 0; t < T; ++t) {
     if (t > 0 && abort_s) break;   // uniform: abort_s is only written inside waits, before the barrier below
     const int e_t = e_s[t];
-    if (t > 0 && e_t != e_s[t - 1]) {
-      if (tid == 0) {
-        fence_proxy_async_smem();   // the previous token's reads of these buffers are complete
-        issue_gu(e_t);
-      }
-      ++loads;
-    }
+    if (t > 0 && e_t != e_s[t - 1]) ++loads;   // gate/up rows requested during the last down phase
     const uint32_t ph = (uint32_t)(loads - 1) & 1u;
     // x: lane l owns quantisation group l (64 inputs).  For token 0 the loads go out after
     // routing, so the logits are the first reads behind the dependency wait, and before the down
@@ -342,6 +336,13 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
     cp_async_wait<0>();
     const bool ok_dn = !P.bulk_sb || mbar_wait_warp(smem_u32(&bars[kQuarters]), ph, &abort_s, a.err);
     __syncthreads();   // h and this thread's down copies -> visible to the whole CTA
+    // The gate/up buffers are free from here on (the down share reads h and the down buffers):
+    // request the next token's gate/up rows now, so they arrive during this token's down share.
+    // abort_s cannot change after the barrier above (no waits follow in this token).
+    if (kMulti && tid == 0 && t + 1 < T && e_s[t + 1] != e_t && !abort_s) {
+      fence_proxy_async_smem();   // this token's reads of the gate/up buffers are complete
+      issue_gu(e_s[t + 1]);
+    }
 
     // ---- down share: part_c[r] = wgt * (s * sum_f q h_f + b * sum_f h_f) over f0 .. f0+31.
     {
