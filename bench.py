@@ -44,7 +44,7 @@ NI = 64   # distinct input rows per layer for decode
 # dram__bytes_read.sum + dram__bytes_write.sum of one decode_layer_kernel launch at the decode
 # shape (ncu capture summarised in profiles/decode_layer_kernel_decode_T1.md); reset to None
 # whenever that kernel changes until it is captured again.
-DECODE_NCU_TRAFFIC = 16000640
+DECODE_NCU_TRAFFIC = 16001280
 
 
 def parse():
