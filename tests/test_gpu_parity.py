@@ -258,6 +258,8 @@ def test_decode_tokens_sharing_experts():
     for t in range(T):
         ref, _, _ = O.moe_token(x[t], lg[t], host, wl.k)
         assert rowwise_err(out["y"][t:t + 1], ref[None, :]) <= DECODE_TOL, t
+        one = run_layer(wl, host, dl, {"x": x[t:t + 1], "logits": lg[t:t + 1]}, T=1)["y"]
+        assert np.array_equal(out["y"][t], one[0]), t   # same as the token's one-token launch
 
 
 @pytest.mark.parametrize("d,F,tol", [(256, 384, DECODE_TOL),    # decode path, 3 column blocks of 128
