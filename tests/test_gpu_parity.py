@@ -300,7 +300,7 @@ def test_decode_in_kernel_routing_ties_and_wide_rows():
             assert rowwise_err(got, ref[None, :]) <= DECODE_TOL, (E, ci)
 
 
-@pytest.mark.parametrize("memory", ["pinned", "pageable", "pinned_unaligned", "registered"])
+@pytest.mark.parametrize("memory", ["pinned", "pinned_rows", "pageable", "pinned_unaligned", "registered"])
 def test_layer_host_entry_matches_device_entry(memory):
     """moe_layer_forward_host gives the device call's y, bit for bit, on the decode path (T = 1, 3)
     and the grouped-GEMM path (T = 37): with page-locked, mapped, aligned buffers at T <= 3 the
@@ -310,11 +310,13 @@ def test_layer_host_entry_matches_device_entry(memory):
     wl = synth.TINY
     host, dl = layer_for(wl)
     layer = moe.Layer(dl["routed"], dl["shared"], dl["w_sg"], wl.d, wl.E, wl.k, wl.F)
-    pin = memory in ("pinned", "pinned_unaligned")
-    off = 1 if memory == "pinned_unaligned" else 0   # one element past a 16-byte boundary
+    pin = memory in ("pinned", "pinned_rows", "pinned_unaligned")
     registered = []
 
     def host_buf(a):
+        # pinned_unaligned: one element past a 16-byte boundary; pinned_rows: two rows into the
+        # allocation (an interior, aligned pointer)
+        off = {"pinned_unaligned": 1, "pinned_rows": 2 * a.shape[1]}.get(memory, 0)
         b = torch.zeros((a.shape[0] * a.shape[1] + off,), dtype=a.dtype)
         b = b.pin_memory() if pin else b
         if memory == "registered":   # page-locked by cudaHostRegister (read-write), not cudaHostAlloc
