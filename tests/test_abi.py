@@ -49,6 +49,20 @@ def test_workspace_and_tile_bounds(lib):
     assert moe.max_tiles(dm, 17) == 0 and moe.max_tiles(dm, 256) == 0
 
 
+def test_workspace_holds_decode_partials_per_token(lib):
+    """Up to eight tokens run one decode launch that keeps (k+1) F/32 partial rows of d floats per
+    token: the workspace grows by at least that much per token up to eight, and the host-buffer
+    entry point's workspace adds room for x, logits and y behind it."""
+    d, E, k, F = 2048, 256, 8, 512
+    part = (k + 1) * (F // 32) * d * 4
+    sizes = [moe.workspace_bytes(moe.dims(T, d, E, k, F, F)) for T in range(1, 10)]
+    for T in range(1, 9):
+        assert sizes[T - 1] >= T * part, T
+    for T in (1, 3, 8, 9, 64):
+        dm = moe.dims(T, d, E, k, F, F)
+        assert lib.moe_workspace_bytes_host(ctypes.byref(dm)) >= moe.workspace_bytes(dm) + T * (d * 2 + E * 4 + d * 4)
+
+
 @pytest.mark.parametrize("bad", [
     dict(T=-1), dict(k=0), dict(k=17, E=16), dict(d=200), dict(F=192), dict(F_shared=256),
     dict(E=2000), dict(k=40, E=64)])
