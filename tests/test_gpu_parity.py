@@ -238,6 +238,21 @@ def test_small_T_full_size(T):
         assert rowwise_err(out["y"][t:t + 1], ref[None, :]) <= tol, t
 
 
+@pytest.mark.parametrize("T", [1, 3, 37])
+def test_layer_without_shared_expert(T):
+    """No shared expert (shared = NULL, F_shared = 0): the one-token and multi-token decode
+    launches (k CTAs per slice column, no gate) and the grouped-GEMM path (no group E, T*k slots)."""
+    wl = synth.Workload("noshared", T=T, d=256, E=16, k=2, F=128, F_shared=0)
+    host = synth.make_layer(wl, seed=5)
+    assert host["shared"] is None
+    dl = moe.to_device_layer(host)
+    inp = synth.make_inputs(wl, seed=6)
+    out = run_layer(wl, host, dl, inp, tile_n=112)
+    assert_routing_equal(out["routing"], inp["logits"], wl.E, wl.k, 112, with_shared=False)
+    ref = O.moe_layer(inp["x"], inp["logits"], host, wl.k)["y"]
+    assert rowwise_err(out["y"], ref) <= (DECODE_TOL if T <= DECODE_MAX_T else EXACT_TOL)
+
+
 def test_decode_tokens_sharing_experts():
     """Tokens of one decode launch that pick the same experts: with equal logits every expert slot
     keeps its expert from token to token (the weights stay in shared memory); a token repeated
