@@ -142,10 +142,10 @@ moe_status moe_expert_forward(const moe_dims* dims, const uint16_t* x, const moe
  * T <= 8 runs the fused decode path (fp32 arithmetic on CUDA cores; one launch for all tokens,
  * each expert slot taking the tokens in turn) when d <= 2048, d % 64 == 0, F % 128 == 0, k < 32,
  * E <= 1024 and (k + 1) * F / 32 CTAs fit one per SM; otherwise, and for T > 8, the grouped-GEMM
- * path
- * (fp16 tensor-core operands, fp32 accumulation; needs
- * d % 256 == 0, and routing_out->tile_n <= 112 when routing_out is given; MOE_ERR_UNSUPPORTED
- * otherwise).  Its own block map uses tiles of 112 rows. */
+ * path (fp16 tensor-core operands, fp32 accumulation; needs d % 256 == 0, and
+ * routing_out->tile_n <= 112 when routing_out is given; MOE_ERR_UNSUPPORTED otherwise).  Its own
+ * block map uses tiles of 112 rows.  The decode path's workspace holds (k + 1) * F / 32 * d
+ * floats of partial outputs per token. */
 moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const float* logits,
                              const moe_experts* routed, const moe_experts* shared, const uint16_t* w_shared_gate,
                              float* y, const moe_routing* routing_out, void* workspace, size_t workspace_bytes,
