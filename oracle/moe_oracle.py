@@ -89,7 +89,10 @@ def round_fp32(v):
 # ------------------------------------------------------------------------------------------
 
 def unpack_codes(codes) -> np.ndarray:
-    """uint32 words [..., C/8] -> 4-bit codes [..., C]; column c = 8*w + i sits in bits 4i..4i+3."""
+    """uint32 words [..., C/8] -> 4-bit codes [..., C]; column c = 8*w + i sits in bits 4i..4i+3.
+    4-bit codes: "Perplexity libera Lily..." (mechatronicstore.cl),
+    section "Prefill: pesos comprimidos y enrutamiento en la GPU"; the packing order is a
+    reading (the pages do not give it)."""
     codes = np.asarray(codes, dtype=np.uint32)
     shifts = (4 * np.arange(8, dtype=np.uint32))
     q = (codes[..., None] >> shifts) & np.uint32(0xF)
@@ -97,7 +100,9 @@ def unpack_codes(codes) -> np.ndarray:
 
 
 def dequant(codes, scales, biases) -> np.ndarray:
-    """w[r, c] = q[r, c] * scale[r, c // 64] + bias[r, c // 64], exact in float64."""
+    """w[r, c] = q[r, c] * scale[r, c // 64] + bias[r, c // 64], exact in float64.
+    Affine groups of 64 with one bf16 scale and one bf16 bias: "Perplexity libera Lily..."
+    (mechatronicstore.cl), section "Prefill: pesos comprimidos y enrutamiento en la GPU"."""
     q = unpack_codes(codes).astype(np.float64)
     s = np.repeat(bf16_to_f64(scales), GROUP, axis=-1)
     b = np.repeat(bf16_to_f64(biases), GROUP, axis=-1)
@@ -122,6 +127,9 @@ def route_topk(logits, k: int):
     """Per token, the k largest fp32 logits in descending order; equal logits go to the lower
     expert index (-0.0 equals +0.0); NaN ranks below every number.  Weights are the softmax
     of the selected logits (renormalised over the k), computed in float64.
+    A router keeps 8 of 256 experts: "Perplexity ouvre le code de Lily..." (lefilia.fr),
+    article body, and "Perplexity libera Lily..." (mechatronicstore.cl), section "Tres formas
+    de carga en un mismo modelo"; the order, the tie rule and the weight function are readings.
 
     Returns idx int32 [T,k] and w float64 [T,k].
     """
@@ -138,6 +146,8 @@ def route_topk(logits, k: int):
 
 def routing_tables(idx, E: int, tile_n: int, with_shared: bool = True) -> dict:
     """Histogram, exclusive scan, permutation and block map of the top-k assignments.
+    The pages name these four steps ("Perplexity libera Lily..." (mechatronicstore.cl), section
+    "Prefill: pesos comprimidos y enrutamiento en la GPU"); their layout below is a reading.
 
     Assignment a = t*k + j routes token t to expert idx[t, j].
       counts[e]   number of assignments to expert e                       int32 [E]
@@ -216,14 +226,18 @@ def expert_ffn(xe, Wg, Wu, Wd, operands=None, out16=False):
 
 
 def shared_gate(x, w_sg_bits):
-    """sigmoid(x . w_sg) per token (float64)."""
+    """sigmoid(x . w_sg) per token (float64).  The always-on shared expert: "Perplexity libera
+    Lily..." (mechatronicstore.cl), section "Tres formas de carga en un mismo modelo"; its
+    sigmoid gate is a reading."""
     return sigmoid(np.asarray(x, dtype=np.float64) @ bf16_to_f64(w_sg_bits))
 
 
 def moe_layer(x_bits, logits, layer: dict, k: int, tile_n: int = 128, operands=None, out16=False) -> dict:
     """One MoE layer: route, run every expert on its tokens (grouped by the permutation),
     run the shared expert on all tokens, and combine.  Returns y (float64 [T,d]) and the
-    routing tables."""
+    routing tables.  Composition of the steps above: "Perplexity libera Lily..." (mechatronicstore.cl),
+    sections "Tres formas de carga en un mismo modelo" and "Prefill: pesos comprimidos y
+    enrutamiento en la GPU"."""
     x = bf16_to_f64(x_bits)
     T, d = x.shape
     routed = layer["routed"]
@@ -254,7 +268,7 @@ def moe_layer(x_bits, logits, layer: dict, k: int, tile_n: int = 128, operands=N
 
 def moe_token(x_bits_row, logits_row, layer: dict, k: int, operands=None, out16=False):
     """The layer for one token (float64 [d]); the same definition, without routing tables.
-    Used to check sampled tokens of large workloads one by one."""
+    Used to check sampled tokens of large workloads one by one (same sources as moe_layer)."""
     x = bf16_to_f64(np.asarray(x_bits_row)[None, :])
     idx, w = route_topk(np.asarray(logits_row, dtype=np.float32)[None, :], k)
     y = np.zeros(x.shape[1], dtype=np.float64)
@@ -273,7 +287,8 @@ def moe_token(x_bits_row, logits_row, layer: dict, k: int, operands=None, out16=
 
 def rmsnorm_bf16(x_resid, gamma_bits, eps: float):
     """h = x / sqrt(mean(x^2) + eps) * gamma, rounded to bf16 (the layer's input type).
-    Returns (h float64 values, h bf16 bits)."""
+    Returns (h float64 values, h bf16 bits).  The pre-norm block of the layer stack is a
+    reading (the pages describe the MoE layer, not the blocks around it)."""
     x = np.asarray(x_resid, dtype=np.float64)
     r = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
     h = round_bf16(x * r * bf16_to_f64(gamma_bits))
@@ -282,7 +297,9 @@ def rmsnorm_bf16(x_resid, gamma_bits, eps: float):
 
 
 def router_logits(h, w_router_bits):
-    """logits = h W_r^T, accumulated in float64 and rounded to fp32 (the routing input type)."""
+    """logits = h W_r^T, accumulated in float64 and rounded to fp32 (the routing input type).
+    The router that scores the 256 experts: "Perplexity libera Lily..." (mechatronicstore.cl), section
+    "Tres formas de carga en un mismo modelo"; a linear router is a reading."""
     return round_fp32(np.asarray(h, dtype=np.float64) @ bf16_to_f64(w_router_bits).T).astype(np.float32)
 
 
