@@ -384,3 +384,127 @@ def test_rmsnorm_constant_row_closed_form():
         want = O.round_bf16(np.array([c / math.sqrt(c * c + 1e-6)]))[0]
         assert np.all(h == want)
         assert np.array_equal(O.bf16_to_f64(bits), h)
+
+
+# ------------------------------------------------------------------------------ pre-norm block and stack
+
+def test_rmsnorm_closed_form_with_gamma_per_column():
+    """x = (3, 4, 0, ..., 0): mean(x^2) = 25/d, so h_c = x_c * gamma_c / sqrt(25/d + eps); a gamma
+    that differs per column shows a norm that drops gamma or applies it along the wrong axis."""
+    d, eps = 64, 1e-6
+    x = np.zeros((2, d))
+    x[0, 0], x[0, 1] = 3.0, 4.0
+    x[1, 5] = -2.0
+    g = np.ones(d, np.float32)
+    g[1], g[5] = 2.0, 0.5
+    gbits = synth.f32_to_bf16_bits(g)
+    h, bits = O.rmsnorm_bf16(x, gbits, eps)
+    r0 = 1.0 / math.sqrt(25.0 / d + eps)
+    r1 = 1.0 / math.sqrt(4.0 / d + eps)
+    want = np.zeros((2, d))
+    want[0, 0] = 3.0 * r0
+    want[0, 1] = 4.0 * r0 * 2.0
+    want[1, 5] = -2.0 * r1 * 0.5
+    assert np.array_equal(h, O.round_bf16(want))
+    assert np.array_equal(O.bf16_to_f64(bits), h)
+
+
+def test_router_logits_one_hot_selects_a_column():
+    """A one-hot h at column c returns column c of W_r (logit e = W_r[e, c], exact in fp32): a
+    transposed product, a wrong axis or a stray scale shows."""
+    rng = np.random.default_rng(13)
+    E, d = 12, 128
+    wr = synth.f32_to_bf16_bits((rng.standard_normal((E, d)) / math.sqrt(d)).astype(np.float32))
+    W = O.bf16_to_f64(wr)
+    for c in (0, 37, d - 1):
+        h = np.zeros((1, d))
+        h[0, c] = 1.0
+        lg = O.router_logits(h, wr)
+        assert lg.dtype == np.float32 and lg.shape == (1, E)
+        assert np.array_equal(lg[0].astype(np.float64), W[:, c])
+        h[0, c] = -2.0
+        assert np.array_equal(O.router_logits(h, wr)[0].astype(np.float64), -2.0 * W[:, c])
+
+
+def test_router_logits_round_once_to_fp32():
+    """The sum is formed exactly and rounded once to fp32 (the library cast of the exact value):
+    1 + 2^-24 + 2^-24 = 1 + 2^-23 is an fp32 number, while fp32 accumulation would give 1."""
+    d = 64
+    h = np.zeros((1, d))
+    h[0, :3] = (1.0, 2.0 ** -24, 2.0 ** -24)
+    wr = synth.f32_to_bf16_bits(np.ones((2, d), np.float32))
+    lg = O.router_logits(h, wr)
+    assert lg[0, 0] == np.float32(1.0 + 2.0 ** -23) and lg[0, 0] != np.float32(1.0)
+    h[0, :3] = (1.0, 2.0 ** -25, 0.0)
+    assert O.router_logits(h, wr)[0, 1] == np.float32(1.0 + 2.0 ** -25) == np.float32(1.0)
+
+
+def _zero_layer(E, d, F):
+    z = lambda n, R, C: _qmat_from(np.full((n, R, C), 8), np.ones((n, R, C // 64)), np.full((n, R, C // 64), -8.0))
+    return {"routed": {"gate": z(E, F, d), "up": z(E, F, d), "down": z(E, d, F)},
+            "shared": {"gate": z(1, F, d), "up": z(1, F, d), "down": z(1, d, F)},
+            "w_sg": synth.f32_to_bf16_bits(np.zeros(d, np.float32))}
+
+
+def _plain_router(E, d, seed):
+    rng = np.random.default_rng(seed)
+    return {"gamma": synth.f32_to_bf16_bits(np.ones(d, np.float32)),
+            "w_router": synth.f32_to_bf16_bits((rng.standard_normal((E, d)) / math.sqrt(d)).astype(np.float32))}
+
+
+def test_stack_of_zero_layers_leaves_the_residual_unchanged():
+    E, d, F, k = 4, 64, 64, 2
+    layers = [_zero_layer(E, d, F) for _ in range(3)]
+    routers = [_plain_router(E, d, s) for s in range(3)]
+    x0 = np.random.default_rng(1).standard_normal((3, d))
+    x, picks = O.stack_tokens(x0, layers, routers, k)
+    assert np.array_equal(x, x0)
+    assert len(picks) == 3 and all(p.shape == (3, k) for p in picks)
+
+
+def test_stack_identity_experts_two_layers_closed_form():
+    """Identical identity experts (so the weights of the k picks sum to 1 whatever the router
+    picks) and a zero shared expert: each layer adds f(h)_c = silu(h_c) h_c for c < F (0 beyond)
+    with h = bf16(RMSNorm(x)).  The update must use the normed h, and be added to the residual
+    x rather than to h: computed here in plain Python, element by element."""
+    E, d, F, k, eps = 3, 128, 64, 2, 1e-6
+    lay = _identity_layer(E, d, F)
+    lay["shared"] = _zero_layer(E, d, F)["shared"]
+    layers = [lay, lay]
+    routers = [_plain_router(E, d, s) for s in (3, 4)]
+    x0 = np.random.default_rng(8).standard_normal((2, d))
+    got, _ = O.stack_tokens(x0, layers, routers, k, eps=eps)
+    for t in range(2):
+        x = [float(v) for v in x0[t]]
+        for _ in range(2):
+            ms = sum(v * v for v in x) / d
+            r = 1.0 / math.sqrt(ms + eps)
+            h = [float(O.round_bf16(np.array([v * r]))[0]) for v in x]
+            x = [x[c] + (h[c] * h[c] / (1.0 + math.exp(-h[c])) if c < F else 0.0) for c in range(d)]
+        assert np.allclose(got[t], x, rtol=1e-13, atol=1e-15)
+
+
+def test_stack_one_layer_matches_dense_bruteforce_and_forced_logits_drive_picks():
+    """One layer of the stack equals the plain-Python dense evaluation of the layer applied to a
+    hand-normed input, plus the residual; forced logits replace the router's choice."""
+    wl = synth.Workload("micro_stack", T=2, d=64, E=4, k=2, F=64, F_shared=64)
+    layer = synth.make_layer(wl, seed=3)
+    rt = _plain_router(wl.E, wl.d, 5)
+    x0 = np.random.default_rng(2).standard_normal((wl.T, wl.d)) * 2.0
+    got, picks = O.stack_tokens(x0, [layer], [rt], wl.k)
+    hbits = np.zeros((wl.T, wl.d), np.uint16)
+    lg = np.zeros((wl.T, wl.E), np.float32)
+    Wr = O.bf16_to_f64(rt["w_router"])
+    for t in range(wl.T):
+        r = 1.0 / math.sqrt(sum(float(v) ** 2 for v in x0[t]) / wl.d + 1e-6)
+        hbits[t] = synth.f32_to_bf16_bits(np.array([float(v) * r for v in x0[t]], np.float32))
+        hv = O.bf16_to_f64(hbits[t])
+        lg[t] = [np.float32(sum(hv[c] * Wr[e, c] for c in range(wl.d))) for e in range(wl.E)]
+    want = x0 + _python_dense_layer(hbits, lg, layer, wl.k)
+    assert np.allclose(got, want, rtol=1e-9, atol=1e-11)
+    assert picks[0].tolist() == [_python_topk(lg[t].tolist(), wl.k) for t in range(wl.T)]
+    forced = [np.tile(np.array([[0.0, 1.0, 3.0, 2.0]], np.float32), (wl.T, 1))]
+    got_f, picks_f = O.stack_tokens(x0, [layer], [rt], wl.k, forced_logits=forced)
+    assert picks_f[0].tolist() == [[2, 3]] * wl.T
+    want_f = x0 + _python_dense_layer(hbits, forced[0], layer, wl.k)
+    assert np.allclose(got_f, want_f, rtol=1e-9, atol=1e-11)
