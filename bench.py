@@ -42,9 +42,9 @@ METRIC = "MoE-layer tokens/s (decode T=1, prefill T=512/4096); % of HBM/tensor r
 LAYERS = 40
 NI = 64   # distinct input rows per layer for decode
 # dram__bytes_read.sum + dram__bytes_write.sum of one decode_layer_kernel launch at the decode
-# shape (ncu capture summarised in profiles/decode_layer_kernel_decode_T1.md); reset to None
-# whenever that kernel changes until it is captured again.
-DECODE_NCU_TRAFFIC = 16001280
+# shape, from one ncu capture of `bench.py --profile decode`; None whenever that kernel has
+# changed since the capture.
+DECODE_NCU_TRAFFIC = None
 
 
 def parse():
@@ -258,10 +258,10 @@ def decode_bench(args, world, rank, local, device, pk):
     tokens = LAYERS * args.steps * world
     res = {
         "value": tokens / (ms_max / 1e3), "ms_per_step": ms_max / args.steps, "clocks": ck, "flags": flags,
-        "roofline": {"kernel": "decode_layer_kernel (one cooperative launch per layer call)",
+        "roofline": {"kernel": "decode_layer_kernel (one clustered launch per layer call)",
                      "bound": "hbm", "achieved": per_step_bytes / step_s / 1e9, "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": per_step_bytes / step_s / 1e9 / pk["hbm_gbs"],
-                     "traffic": DECODE_NCU_TRAFFIC, "traffic_source": "profiles/decode_layer_kernel_decode_T1.md",
+                     "traffic": DECODE_NCU_TRAFFIC,
                      "algorithmic_bytes_per_launch": per_call, "peak_source": pk["source"]},
         "gpu_launches": LAYERS * args.steps,   # one decode_layer_kernel per layer call
     }

@@ -154,7 +154,7 @@ def alloc_workspace(dm: Dims, device="cuda"):
     """Workspace for these dims with its error word cleared."""
     import torch
     ws = torch.empty(workspace_bytes(dm), dtype=torch.uint8, device=device)
-    ws[:256].zero_()
+    ws[:2048].zero_()
     return ws
 
 
@@ -169,7 +169,7 @@ def alloc_workspace_host(dm: Dims, device="cuda"):
     """Workspace (with the host-call staging area) for these dims, its error word cleared."""
     import torch
     ws = torch.empty(workspace_bytes_host(dm), dtype=torch.uint8, device=device)
-    ws[:256].zero_()
+    ws[:2048].zero_()
     return ws
 
 

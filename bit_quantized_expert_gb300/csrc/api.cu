@@ -19,9 +19,8 @@ struct Layout {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// The first 256 bytes of a workspace: the error word at 0, the decode path's grid-barrier word
-// (64-bit, arrivals in the low half and a generation count in the high half) at kSyncOffset.
-constexpr size_t kSyncOffset = 8;
+// The first kWsHeadBytes of a workspace: the error word at 0 and the decode path's arrival
+// counters at kCountersOffset (kernels.h); both must be zero before the first call.
 
 size_t max_tiles_of(long long T, long long k, long long E, long long tile_n, bool shared) {
   return (size_t)(T * k / tile_n + std::min(E, T * k) + (shared ? (T + tile_n - 1) / tile_n : 0));
@@ -38,7 +37,7 @@ Layout layout_of(const moe_dims& d) {
   const size_t T = d.T, k = d.k, E = d.E, D = d.d, F = d.F;
   const bool sh = d.F_shared > 0;
   const size_t slots = T * k + (sh ? T : 0);
-  L.err = take(256);
+  L.err = take(kWsHeadBytes);
   L.xperm = take(slots * D * 2);
   L.gs = take(T * 4);
   L.idx = take(T * k * 4);
@@ -60,16 +59,23 @@ Layout layout_of(const moe_dims& d) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
+int check_layer_dims(int T, int d, int E, int k, int F, int F_shared) {
+  if (T < 0 || k < 1 || E < 1 || k > E || d < 1 || F < 1 || F_shared < 0) return MOE_ERR_INVALID_ARG;
+  if (k > 32 || E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (d % 128 != 0 || F % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (F_shared != 0 && F_shared != F) return MOE_ERR_UNSUPPORTED;
+  if ((long long)T * (k + 1) >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  if ((long long)d * F >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+namespace {
+
 moe_status check_dims(const moe_dims* d) {
   if (d == nullptr) return MOE_ERR_INVALID_ARG;
-  if (d->T < 0 || d->k < 1 || d->E < 1 || d->k > d->E || d->d < 1 || d->F < 1 || d->F_shared < 0)
-    return MOE_ERR_INVALID_ARG;
-  if (d->k > 32 || d->E > 1024) return MOE_ERR_UNSUPPORTED;
-  if (d->d % 128 != 0 || d->F % 128 != 0) return MOE_ERR_UNSUPPORTED;
-  if (d->F_shared != 0 && d->F_shared != d->F) return MOE_ERR_UNSUPPORTED;
-  if ((long long)d->T * (d->k + 1) >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
-  if ((long long)d->d * d->F >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
-  return MOE_OK;
+  return static_cast<moe_status>(check_layer_dims(d->T, d->d, d->E, d->k, d->F, d->F_shared));
 }
 
 moe_status check_qmat(const moe_qmat& q) {
@@ -151,6 +157,24 @@ bool encode_f16_rows(CUtensorMap* m, const uint16_t* p, long long rows, int cols
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+}  // namespace
+
+// Down-projection codes of n stacked [d, F] matrices as a 2-D uint32 tensor {F/8, n*d}, box of 16
+// words (the 128 columns of one decode cluster) by decode_box_rows rows, no swizzle.
+bool encode_decode_down(CUtensorMap* m, const uint32_t* codes, int n, int d, int F) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)(F / 8), (cuuint64_t)n * (cuuint64_t)d};
+  const cuuint64_t strides[1] = {(cuuint64_t)(F / 8) * 4};
+  const cuuint32_t box[2] = {16, (cuuint32_t)decode_box_rows(d, F)};
+  const cuuint32_t es[2] = {1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(codes), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
 
 // Row-major bf16 matrix [rows, cols] with a 64 x 128 box in the 128-byte swizzle.
 bool encode_bf16_rows(CUtensorMap* m, const uint16_t* p, long long rows, int cols) {
@@ -371,7 +395,7 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
   const moe_dims& d = *dims;
 
   // One to kDecodeLayerMaxT tokens: the fused decode kernel, one launch for all of them (each CTA
-  // takes its expert slot of every token in turn, one grid barrier and reduction for all).
+  // takes its expert slot of every token in turn; per-token arrival counters for the combine).
   if (d.T <= kDecodeLayerMaxT && decode_supported(d.d, d.E, d.k, d.F)) {
     DecodeArgs da{};
     da.x = x;
@@ -393,9 +417,13 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
     da.part = at<float>(workspace, L.hdec);
     da.y = y;
     da.err = err;
-    da.sync = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + L.err + kSyncOffset);
+    da.cnt = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + L.err + kCountersOffset);
     da.T = d.T;
-    if (launch_decode(da, st, true) != cudaSuccess) return MOE_ERR_CUDA;
+    DecodeMaps dmaps{};
+    if (!encode_decode_down(&dmaps.down[0], routed->down.codes, d.E, d.d, d.F) ||
+        !encode_decode_down(&dmaps.down[1], sh ? shared->down.codes : routed->down.codes, sh ? 1 : d.E, d.d, d.F))
+      return MOE_ERR_CUDA;
+    if (launch_decode(dmaps, da, st, true) != cudaSuccess) return MOE_ERR_CUDA;
     if (routing_out != nullptr)
       return cuda_status(run_routing(d, logits, caller_routing(routing_out), nullptr, nullptr, nullptr,
                                      at<int32_t>(workspace, L.chunk), err, st));
@@ -535,8 +563,8 @@ moe_status moe_rmsnorm_router(const moe_dims* dims, float* x_resid, const float*
 moe_status moe_clear_error_flags(void* workspace, size_t workspace_bytes, void* stream) {
   if (workspace == nullptr) return MOE_ERR_INVALID_ARG;
   if (workspace_bytes < 4) return MOE_ERR_WORKSPACE;
-  // The error word, and (in workspaces large enough for a layer) the decode grid-barrier word.
-  const size_t n = workspace_bytes >= kSyncOffset + 8 ? kSyncOffset + 8 : 4;
+  // The error word, and (in workspaces large enough for a layer) the decode arrival counters.
+  const size_t n = std::min(workspace_bytes, kWsHeadBytes) & ~(size_t)3;
   return cuda_status(cudaMemsetAsync(workspace, 0, n, static_cast<cudaStream_t>(stream)));
 }
 
@@ -546,9 +574,8 @@ moe_status moe_read_error_flags(void* workspace, size_t workspace_bytes, uint32_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemcpy(flags, workspace, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
-  // After a timed-out wait the grid-barrier word may hold a partial count: reset it too (the
-  // stream is idle here).
-  const size_t n = ((*flags & 1u) != 0 && workspace_bytes >= kSyncOffset + 8) ? kSyncOffset + 8 : 4;
+  // After a timed-out wait the decode arrival counters are reset too (the stream is idle here).
+  const size_t n = (*flags & 1u) != 0 ? std::min(workspace_bytes, kWsHeadBytes) & ~(size_t)3 : 4;
   if (cudaMemset(workspace, 0, n) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }

@@ -6,36 +6,38 @@
 // 0.2% and that matrix ops reached 97.9% of bandwidth ("Perplexity открыла код Lily...",
 // section "Спекулятивное декодирование не взлетело").  On a GB300 one layer's routed weights
 // (~16 MB) stream in ~2.3 us, so the layer is as much a latency chain as a bandwidth problem:
-// the design keeps that chain short.
+// the design keeps that chain short and free of grid-wide waits.
 //
-// One cooperative launch per layer; CTA c (grid = (k+1) F / 32, one per SM, all co-resident)
-// owns rows f0 = 32 (c mod F/32) .. f0+31 of expert slot j = c / (F/32) (k = the shared expert):
-//   * before the programmatic-launch wait, shared-expert CTAs start their weight copies (weights
-//     are never written upstream, so they may be read early);
-//   * after it, warp 0 routes the token in registers (top-k of the 1 KB of logits; cheaper than a
-//     routing kernel and its launch) and starts the bulk copies of the 32 gate rows and 32 up rows
-//     (four quarters, one mbarrier each, so compute starts on the first quarter), while every
-//     thread copies the matching 32-column block of the down matrix (all d rows, 16 B each) with
-//     cp.async, and one thread bulk-copies the expert's down scales and biases whole (contiguous,
-//     so two large requests replace two small ones per row);
-//   * the CTA computes its 32 SwiGLU outputs h, then its share of the down projection,
-//     part_c[r] = w_j * sum_{f in f0..f0+31} W_down[e_j][r][f] h[f] for every output row r
-//     (a split over F: no CTA needs another CTA's h);
-//   * every CTA writes part_c and arrives at a grid barrier (one 64-bit word: arrivals in the low
-//     half, a generation count in the high half; the last arrival resets the count and bumps the
-//     generation), then sums a slice of rows over all CTAs in a fixed order:
-//     y[r] = sum_c part_c[r] -- deterministic, no atomics on data.
-//
-// A few tokens (T > 1, the kernel<true> instantiation): warp t routes token t; every CTA then
-// takes its expert slot of token 0, 1, ... in turn, fetching the slot's weights again only when
-// its expert changes (the shared expert's stay), and writes part_c per token; one grid barrier
-// and one fixed-order reduction serve all tokens, so each token's y is what a one-token launch
-// gives, bit for bit.  The one-token launch is the kernel<false> instantiation (T fixed at 1).
+// Work split.  Expert slot j (0..k-1 routed, k = the shared expert) gets S = F / 32 CTAs; CTA s of
+// the slot owns gate/up rows f0 = 32 s .. f0+31.  The S CTAs of a slot form S / 4 thread-block
+// clusters of C = 4 CTAs; cluster q covers the F columns KC0 = 128 q .. KC0 + 127 of the down
+// projection, and its CTA of rank c owns down rows r0 = c d / 4 .. r0 + d / 4 - 1 over those
+// columns.  Clusters of four are what the GPU can co-schedule one CTA per SM across all SMs (larger
+// clusters are placed two CTAs to an SM, or wait for a second wave).  Per token:
+//   * routing: after the programmatic-launch wait every CTA ranks the 1 KB of logits itself (all
+//     eight warps: per-warp candidate ranks by shuffles, then the 8 k survivors ranked in shared
+//     memory) -- no routing kernel on the critical path -- and immediately bulk-copies its gate/up
+//     rows (four quarters, one mbarrier each, so compute starts on the first quarter) and its down
+//     rows (the cluster's 64-byte column block of each row, as one or two 2-D tensor copies) with
+//     their scales and biases.  Shared-expert CTAs start their copies before the wait: weights are
+//     never written upstream;
+//   * each CTA computes its 32 SwiGLU outputs h and writes them into the shared memory of every
+//     CTA of its cluster (distributed shared memory), then the cluster barrier;
+//   * each CTA computes its d / C down rows over the cluster's 32 C columns of h, scaled by the
+//     slot's routing weight (or the shared expert's gate), and stores them as one partial of each
+//     of its row slices (128 rows);
+//   * combine: per row slice an arrival counter; the CTA that arrives last sums the slice's
+//     (k+1) S / C partials in a fixed slot order, writes y and resets the counter.  Nobody waits
+//     on another cluster; the order of the sum never depends on arrival order.
+// Several tokens (the kMulti instantiation): warp t routes token t; every CTA then takes its
+// slot of token 0, 1, ... in turn, fetching the slot's weights again only when its expert changes
+// (the shared expert's stay), with double-buffered h exchange slots and per-token counters, so
+// each token's y is what a one-token launch gives, bit for bit.
 //
 // Arithmetic: codes become exact fp32 values q * 16^e via the 2^23 exponent trick (the nibble
 // stays where it is in the word; the activation carries the matching 16^-e), partial dot
 // products sum_c q_c x_c accumulate in fp32 with packed two-lane FMAs, and w = q*s + b enters as
-// s * sum(q x) + b * sum(x) per quantisation group (per half group for the down rows).
+// s * sum(q x) + b * sum(x) per quantisation group.
 #include <algorithm>
 #include <mutex>
 
@@ -46,12 +48,14 @@
 namespace moe {
 namespace {
 
-constexpr int RF = 32;   // gate/up rows (and down columns) per CTA
+constexpr int RF = 32;   // gate/up rows per CTA
 constexpr int kQuarters = 4;
 constexpr int kRQ = RF / kQuarters;   // gate/up rows per quarter
 constexpr int kMaxE = 1024;
 constexpr float kMagic = 8388608.0f;   // 2^23
 constexpr int kThreadsDec = 256;
+constexpr int kWarpsDec = kThreadsDec / 32;
+constexpr int kSliceRows = 128;        // rows of y per combine slice
 
 // Activation pre-scale matching the position of code n (0..7) of a word after extraction.
 __host__ __device__ constexpr float act_prescale(int n) {
@@ -77,72 +81,160 @@ __device__ __forceinline__ float2 word_dot2(uint32_t w, const float2* xs, float2
   return acc;
 }
 
-// Shared-memory plan of one CTA (byte offsets, 16-byte aligned regions).
+// CTAs per thread-block cluster (S = F / 32 is a multiple of 4).
+constexpr int kC = 4;
+
+// Geometry and shared-memory plan of one launch (byte offsets, 16-byte aligned regions).
 struct DecPlan {
-  int d, F, k1, G, GF, grid;
-  bool bulk_sb;   // the down scales and biases of the expert copied whole (two bulk copies)
-  uint32_t gu_codes, gu_sb, dn_codes, dn_sb, hbuf, bytes;
-  __host__ __device__ DecPlan(int d_, int F_, int k1_) : d(d_), F(F_), k1(k1_) {
+  int d, F, k1, G, GF, S, C, NQ, DR, KC, GP, NSC, nslices, NP, grid, box_rows;
+  uint32_t gu_codes, gu_sb, dn_codes, dn_sb, hclu, bytes;
+  // multi: several tokens per launch (two h exchange slots, alternating by token)
+  __host__ __device__ DecPlan(int d_, int F_, int k1_, bool multi) : d(d_), F(F_), k1(k1_) {
     G = d / 64;
     GF = F / 64;
-    grid = k1 * (F / RF);
-    bulk_sb = 4u * (uint32_t)d * (uint32_t)GF <= 64u * 1024u;
+    S = F / RF;
+    C = kC;
+    NQ = S / C;                 // clusters per slot
+    DR = d / C;                 // down rows per CTA
+    KC = RF * C;                // down columns (F) per cluster
+    GP = KC / 64;               // quantisation groups per down row and cluster
+    NSC = (DR + kSliceRows - 1) / kSliceRows;   // combine slices per CTA
+    nslices = C * NSC;
+    NP = k1 * NQ;               // partials per row of y
+    grid = k1 * S;
+    box_rows = DR <= 256 ? DR : DR / ((DR + 255) / 256);   // rows per 2-D copy of the down codes
     uint32_t o = 0;
-    gu_codes = o;  o += 2u * RF * (d / 2);   // [gate|up][RF][d/8] u32
-    gu_sb = o;     o += 4u * RF * G * 2;     // [g.s|g.b|u.s|u.b][RF][G] bf16
+    gu_codes = o;  o += 2u * RF * (d / 2);        // [gate|up][RF][d/8] u32
+    gu_sb = o;     o += 4u * RF * G * 2;          // [g.s|g.b|u.s|u.b][RF][G] bf16
+    o = (o + 127u) & ~127u;
+    dn_codes = o;  o += (uint32_t)DR * (KC / 2);  // [DR][KC/8] u32
+    dn_sb = o;     o += 4u * DR * GF;             // [s|b][DR][GF] bf16: whole scale and bias rows
     o = (o + 15u) & ~15u;
-    dn_codes = o;  o += 16u * d;             // [d][4] u32: code words f0/8 .. f0/8+3 of every row
-    dn_sb = o;                               // [s|b][d][GF] bf16 (whole matrices), or
-    o += bulk_sb ? 4u * d * GF : 8u * d;     // [s|b][d] u32: the bf16 pair holding group f0/64
-    hbuf = o;      o += 4u * RF;             // h of rows f0 .. f0+31, fp32
+    hclu = o;      o += (multi ? 2u : 1u) * 4u * KC;   // h of the cluster's columns, fp32, per exchange slot
     bytes = (o + 15u) & ~15u;
   }
 };
 
-// Warp-wide top-k of logits[0..E) and the softmax of the selected logits, with the candidates
-// held in registers (8 per lane up to E = 256, else 32); lane j < k returns expert j and its
-// weight.
-__device__ __forceinline__ void reg_topk(const float* __restrict__ logits, int E, int k, int* e_out, float* w_out) {
-  if (E <= 256) warp_topk_softmax<8>(logits, E, k, e_out, w_out);
-  else warp_topk_softmax<32>(logits, E, k, e_out, w_out);
+// ---------------------------------------------------------------- cluster helpers (PTX ISA)
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address in the shared memory of cluster CTA `rank` matching this CTA's shared address `a`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t a, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
 }
 
-__device__ __forceinline__ unsigned long long atom_add_release(unsigned long long* p, unsigned long long v) {
-  unsigned long long old;
-  asm volatile("atom.add.release.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
-  return old;
-}
-__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
+// ---------------------------------------------------------------- routing of one token
+// Softmax of the k selected logits, shared by the one-token and the several-token paths so that
+// both give the same weights bit for bit: lane j < k holds the j-th selected logit my_v, vmax is
+// the largest; returns lane j's weight.
+__device__ __forceinline__ float softmax_tail(float my_v, float vmax, int k, int lane) {
+  const float my_ex = lane < k ? expf(my_v - vmax) : 0.0f;
+  float s = my_ex;   // lanes >= k hold 0
+  if (k > 8) {
+    s += __shfl_xor_sync(0xFFFFFFFFu, s, 16);
+    s += __shfl_xor_sync(0xFFFFFFFFu, s, 8);
+  }
+  s += __shfl_xor_sync(0xFFFFFFFFu, s, 4);
+  s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
+  s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
+  return my_ex / s;
 }
 
-// kMulti = false: one token (T fixed at 1, so the token loop and the per-token arrays fold away).
+// 64-bit candidate key: the logit's order-preserving key above, the complement of the expert
+// index below, so that a larger key is a larger logit or, for equal logits, a lower index; every
+// candidate is distinct and 0 marks padding.
+__device__ __forceinline__ uint64_t cand_key(float v, int e) {
+  return ((uint64_t)logit_key(v) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)e);
+}
+__device__ __forceinline__ int cand_expert(uint64_t c) { return (int)(0xFFFFFFFFu - (uint32_t)c); }
+
+// The k best candidates of a row of E <= 256 * NE logits, by the whole CTA (every thread calls
+// it): thread t holds experts t + 256 i; each warp ranks its candidates against the warp's
+// (broadcast reads of the warp's keys from shared memory) and keeps its k best in `cand`
+// [kWarpsDec][k]; then the first 8 k threads rank those against each other and the k best land in
+// sel[0..k-1] in descending order.  `keys` holds kThreadsDec * NE entries.  Two block barriers.
+template <int NE>
+__device__ __forceinline__ void block_topk(const float* __restrict__ row, int E, int k, uint64_t* keys,
+                                           uint64_t* cand, uint64_t* sel) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint64_t key[NE];
+  int rank[NE];
+#pragma unroll
+  for (int i = 0; i < NE; ++i) {
+    const int e = tid + kThreadsDec * i;
+    key[i] = e < E ? cand_key(__ldg(row + e), e) : 0ull;
+    rank[i] = 0;
+    keys[(warp * NE + i) * 32 + lane] = key[i];
+  }
+  for (int i = lane; i < k; i += 32) cand[warp * k + i] = 0ull;
+  __syncwarp();
+  const uint64_t* wk = keys + warp * NE * 32;
+#pragma unroll 8
+  for (int c = 0; c < 32 * NE; ++c) {
+    const uint64_t o = wk[c];
+#pragma unroll
+    for (int m = 0; m < NE; ++m) rank[m] += o > key[m] ? 1 : 0;
+  }
+#pragma unroll
+  for (int m = 0; m < NE; ++m)
+    if (key[m] != 0ull && rank[m] < k) cand[warp * k + rank[m]] = key[m];
+  __syncthreads();
+  const int nc = kWarpsDec * k;
+  if (tid < nc) {
+    const uint64_t mine = cand[tid];
+    int r = 0;
+#pragma unroll 8
+    for (int c = 0; c < nc; ++c) r += cand[c] > mine ? 1 : 0;
+    if (mine != 0ull && r < k) sel[r] = mine;
+  }
+  __syncthreads();
+}
+
 template <bool kMulti>
-__global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreadsDec, kMulti ? 1 : 2)
+    decode_layer_kernel(const __grid_constant__ DecodeMaps maps, const DecodeArgs a) {
+  constexpr int C = kC;
   extern __shared__ __align__(128) uint8_t sm[];
   const int d = a.d, F = a.F, k = a.k;
   const int k1 = k + (a.has_shared ? 1 : 0);
-  const DecPlan P(d, F, k1);
+  const DecPlan P(d, F, k1, kMulti);
   const int G = P.G, GF = P.GF;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x;
-  const int jobs = F / RF;
-  const int j = cta / jobs;            // expert slot: 0..k-1 routed, k shared
-  const int f0 = (cta % jobs) * RF;    // first gate/up row = first down column
+  const int j = cta / P.S;              // expert slot: 0..k-1 routed, k shared
+  const int sidx = cta % P.S;
+  const int qc = sidx / C;              // cluster of the slot: down columns KC0 .. KC0 + KC - 1
+  const int crank = sidx % C;           // rank in the cluster: down rows r0 .. r0 + DR - 1
+  const int f0 = sidx * RF;             // first gate/up row
+  const int kc0 = qc * P.KC;
+  const int r0 = crank * P.DR;
   const bool shared_cta = (j == k);
   const int wset = shared_cta ? 1 : 0;
 
   uint32_t* gcodes = reinterpret_cast<uint32_t*>(sm + P.gu_codes);   // gate [RF][d/8], then up
   uint16_t* gsb = reinterpret_cast<uint16_t*>(sm + P.gu_sb);         // [g.s | g.b | u.s | u.b][RF][G]
-  uint32_t* dcodes = reinterpret_cast<uint32_t*>(sm + P.dn_codes);   // [d][4]
-  uint32_t* dsb = reinterpret_cast<uint32_t*>(sm + P.dn_sb);         // [s | b][d] (pairs), or
-  uint16_t* dsb16 = reinterpret_cast<uint16_t*>(sm + P.dn_sb);       // [s | b][d][GF] (whole)
-  float* hbuf = reinterpret_cast<float*>(sm + P.hbuf);               // [RF]
-  __shared__ __align__(8) uint64_t bars[kQuarters + 1];   // gate/up quarters, then the down scales
+  uint32_t* dcodes = reinterpret_cast<uint32_t*>(sm + P.dn_codes);   // [DR][KC/8]
+  uint16_t* dsb = reinterpret_cast<uint16_t*>(sm + P.dn_sb);         // [s | b][DR][GF]
+  float* hclu = reinterpret_cast<float*>(sm + P.hclu);               // [2][KC]
+  __shared__ __align__(8) uint64_t bars[kQuarters + 1];   // gate/up quarters, then the down rows
+  __shared__ __align__(16) uint64_t cand[kWarpsDec * 32];
+  __shared__ __align__(16) uint64_t keys_s[kMulti ? 1 : kMaxE];
+  __shared__ uint64_t sel[32];
   __shared__ int e_s[kDecodeMaxTokens];
   __shared__ float wgt_s[kDecodeMaxTokens];    // w_j (routed) or the shared-expert gate, per token
+  __shared__ int last_s[8];
   __shared__ int abort_s;
   const int T = kMulti ? (a.T > 0 ? a.T : 1) : 1;
 
@@ -152,77 +244,81 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
     mbar_fence_init();
   }
   __syncthreads();
+  cluster_arrive_relaxed();   // this CTA runs: its shared memory may now receive the cluster's h
 
   // Gate and up rows f0 .. f0+31 of expert e (code words by quarter; scales and biases with the
-  // first quarter).
-  auto issue_gu = [&](int e) {
+  // first quarter).  Lanes 0..3 of one warp, lane q issuing quarter q (lane 0 also the scales and
+  // biases), so the copies leave together.
+  auto issue_gu = [&](int e, int q) {
     const QPtr& g = a.gate[wset];
     const QPtr& u = a.up[wset];
     const uint32_t cb = kRQ * (d / 2), sb = RF * G * 2;
     const size_t rowb = (size_t)e * F + f0;
-    for (int q = 0; q < kQuarters; ++q) {
-      const uint32_t bar = smem_u32(&bars[q]);
-      const size_t row0 = rowb + q * kRQ;
-      mbar_arrive_expect_tx(bar, 2 * cb + (q == 0 ? 4 * sb : 0));
-      if (q == 0) {
-        bulk_g2s(smem_u32(gsb + 0 * RF * G), g.scales + rowb * G, sb, bar);
-        bulk_g2s(smem_u32(gsb + 1 * RF * G), g.biases + rowb * G, sb, bar);
-        bulk_g2s(smem_u32(gsb + 2 * RF * G), u.scales + rowb * G, sb, bar);
-        bulk_g2s(smem_u32(gsb + 3 * RF * G), u.biases + rowb * G, sb, bar);
-      }
-      bulk_g2s(smem_u32(gcodes + (q * kRQ) * (d / 8)), g.codes + row0 * (d / 8), cb, bar);
-      bulk_g2s(smem_u32(gcodes + (RF + q * kRQ) * (d / 8)), u.codes + row0 * (d / 8), cb, bar);
+    const uint32_t bar = smem_u32(&bars[q]);
+    const size_t row0 = rowb + q * kRQ;
+    mbar_arrive_expect_tx(bar, 2 * cb + (q == 0 ? 4 * sb : 0));
+    bulk_g2s(smem_u32(gcodes + (q * kRQ) * (d / 8)), g.codes + row0 * (d / 8), cb, bar);
+    bulk_g2s(smem_u32(gcodes + (RF + q * kRQ) * (d / 8)), u.codes + row0 * (d / 8), cb, bar);
+    if (q == 0) {
+      bulk_g2s(smem_u32(gsb + 0 * RF * G), g.scales + rowb * G, sb, bar);
+      bulk_g2s(smem_u32(gsb + 1 * RF * G), g.biases + rowb * G, sb, bar);
+      bulk_g2s(smem_u32(gsb + 2 * RF * G), u.scales + rowb * G, sb, bar);
+      bulk_g2s(smem_u32(gsb + 3 * RF * G), u.biases + rowb * G, sb, bar);
     }
   };
-  // Columns f0 .. f0+31 of every row of the down matrix of expert e: 16 code bytes per row, and
-  // the row's scale and bias of group f0/64 -- where they fit, as the expert's whole scale and
-  // bias matrices (two contiguous bulk copies instead of two small requests per row), else as the
-  // 4-byte aligned bf16 pairs holding the group.
-  auto copy_dn = [&](int e) {
+  // Down rows r0 .. r0+DR-1 of expert e over the cluster's columns (the 64-byte column block of
+  // each row: 2-D tensor copies of box_rows rows) and their whole scale and bias rows
+  // (contiguous).  One thread.
+  auto issue_dn = [&](int e) {
     const QPtr& q = a.down[wset];
-    if (P.bulk_sb) {
-      if (tid == 0) {
-        const uint32_t bar = smem_u32(&bars[kQuarters]);
-        const uint32_t nb = 2u * d * GF;
-        mbar_arrive_expect_tx(bar, 2u * nb);
-        bulk_g2s(smem_u32(dsb16), q.scales + (size_t)e * d * GF, nb, bar);
-        bulk_g2s(smem_u32(dsb16 + d * GF), q.biases + (size_t)e * d * GF, nb, bar);
-      }
-    }
-    const int g2 = (f0 / 64) & ~1;
-    for (int r = tid; r < d; r += kThreadsDec) {
-      const size_t row = (size_t)e * d + r;
-      cp_async_16(smem_u32(dcodes + 4 * r), q.codes + row * (F / 8) + f0 / 8);
-      if (!P.bulk_sb) {
-        cp_async_4(smem_u32(dsb + r), q.scales + row * GF + g2);
-        cp_async_4(smem_u32(dsb + d + r), q.biases + row * GF + g2);
-      }
-    }
-    cp_async_commit();
+    const uint32_t bar = smem_u32(&bars[kQuarters]);
+    const uint32_t rb = P.KC / 2;                 // code bytes per row and cluster
+    const uint32_t sbb = (uint32_t)P.DR * GF * 2;
+    const size_t row0 = (size_t)e * d + r0;
+    mbar_arrive_expect_tx(bar, (uint32_t)P.DR * rb + 2u * sbb);
+    for (int r = 0; r < P.DR; r += P.box_rows)
+      tma_load_2d(smem_u32(dcodes) + r * rb, &maps.down[wset], bar, kc0 / 8, (int)(row0 + r));
+    bulk_g2s(smem_u32(dsb), q.scales + row0 * GF, sbb, bar);
+    bulk_g2s(smem_u32(dsb + P.DR * GF), q.biases + row0 * GF, sbb, bar);
   };
 
   // Weights are never written upstream: the shared expert's copies start before the wait.
-  if (shared_cta) {
-    if (tid == 0) issue_gu(0);
-    copy_dn(0);
-  }
+  if (shared_cta && tid < kQuarters) issue_gu(0, tid);
+  if (shared_cta && tid == 32) issue_dn(0);
+  if (tid == 32) prefetch_tmap(&maps.down[wset]);
   pdl_wait();   // x and logits from upstream kernels are complete and visible past this point
 
-  if (warp < T && !shared_cta) {
-    // warp t routes token t; token 0's weights are requested as soon as its expert is known
+  if (!kMulti) {
+    if (!shared_cta) {
+      if (a.E <= kThreadsDec) block_topk<1>(a.logits, a.E, k, keys_s, cand, sel);
+      else block_topk<kMaxE / kThreadsDec>(a.logits, a.E, k, keys_s, cand, sel);
+      const int ej = cand_expert(sel[j]);
+      if (tid < kQuarters) issue_gu(ej, tid);
+      if (tid == 0) e_s[0] = ej;
+      if (tid == 32) issue_dn(ej);
+      if (warp == 2) {
+        const float v = lane < k ? key_logit((uint32_t)(sel[lane] >> 32)) : 0.0f;
+        const float w = softmax_tail(v, key_logit((uint32_t)(sel[0] >> 32)), k, lane);
+        if (lane == j) wgt_s[0] = w;
+      }
+    }
+  } else if (warp < T && !shared_cta) {
+    // warp t routes token t; token 0's gate/up rows are requested as soon as its expert is known
     int e;
     float w;
-    reg_topk(a.logits + (size_t)warp * a.E, a.E, k, &e, &w);
+    if (a.E <= 256) warp_topk_softmax<8>(a.logits + (size_t)warp * a.E, a.E, k, &e, &w);
+    else warp_topk_softmax<32>(a.logits + (size_t)warp * a.E, a.E, k, &e, &w);
     const int ej = __shfl_sync(0xFFFFFFFFu, e, j);
     const float wj = __shfl_sync(0xFFFFFFFFu, w, j);
     if (lane == 0) {
       e_s[warp] = ej;
       wgt_s[warp] = wj;
-      if (warp == 0) issue_gu(ej);
     }
-  } else if (shared_cta) {
+    if (warp == 0 && lane < kQuarters) issue_gu(ej, lane);
+  }
+  if (shared_cta) {
     // warp w: the shared-expert gates of tokens w, w + 8, ...
-    for (int t = warp; t < T; t += kThreadsDec / 32) {
+    for (int t = warp; t < T; t += kWarpsDec) {
       float dot = 0.0f;
       const uint4* xv = reinterpret_cast<const uint4*>(a.x + (size_t)t * d);
       const uint4* gv = reinterpret_cast<const uint4*>(a.w_sg);
@@ -245,26 +341,27 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
   }
   pdl_launch_dependents();
   __syncthreads();   // e_s and wgt_s
+  if (kMulti && !shared_cta && tid == 32) issue_dn(e_s[0]);
+  cluster_wait_acquire();   // every CTA of the cluster runs (pairs with the arrive above)
+
   // Tokens one after another.  The slot's weights stay in shared memory while the slot's expert
   // stays the same (always for the shared expert), and are fetched again when it changes; every
   // fetch is one phase of the copy barriers, so waits use the parity of the fetch count.
   const bool active = lane < G;
-  int loads = 1;   // weight fetches so far (token 0's is in flight)
+  int loads = 1;   // weight fetches so far (token 0's are in flight)
 #pragma unroll 1
   for (int t = 0; t < T; ++t) {
-    if (t > 0 && abort_s) break;   // uniform: abort_s is only written inside waits, before the barrier below
     const int e_t = e_s[t];
-    if (t > 0 && e_t != e_s[t - 1]) ++loads;   // gate/up rows requested during the last down phase
+    const bool refetch = t > 0 && e_t != e_s[t - 1];
+    if (refetch) ++loads;   // requested during the previous token
     const uint32_t ph = (uint32_t)(loads - 1) & 1u;
-    // x: lane l owns quantisation group l (64 inputs).  For token 0 the loads go out after
-    // routing, so the logits are the first reads behind the dependency wait, and before the down
-    // copies; the gate/up products wait for the weights, which arrive later.
+    float* hx = hclu + (t & 1) * P.KC;   // this token's exchange slot
+    // x: lane l owns quantisation group l (64 inputs)
     uint4 xr[8];
 #pragma unroll
     for (int c8 = 0; c8 < 8; ++c8)
       xr[c8] = active ? __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * d) + lane * 8 + c8)
                       : make_uint4(0u, 0u, 0u, 0u);
-    if ((t == 0 && !shared_cta) || (t > 0 && e_t != e_s[t - 1])) copy_dn(e_t);
 
     // ---- gate/up: warp w computes gate and up of rows q*8 + w (q = 0..3) as slots s = 2q + mat;
     // a reduce-scatter leaves slot s fully summed in lane 4s.
@@ -283,11 +380,9 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
     float v8[8];
 #pragma unroll
     for (int sl = 0; sl < 8; ++sl) v8[sl] = 0.0f;
-    bool ok_all = true;
 #pragma unroll 1
     for (int q = 0; q < kQuarters; ++q) {
       const bool ok = mbar_wait_warp(smem_u32(&bars[q]), ph, &abort_s, a.err);
-      ok_all = ok_all && ok;
 #pragma unroll
       for (int mat = 0; mat < 2; ++mat) {
         const int row = q * kRQ + warp;
@@ -312,7 +407,7 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
         }
         const int sl = 2 * q + mat;
 #pragma unroll
-        for (int t = 0; t < 8; ++t) v8[t] = (t == sl) ? v : v8[t];
+        for (int i = 0; i < 8; ++i) v8[i] = (i == sl) ? v : v8[i];
       }
     }
     {
@@ -329,109 +424,143 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
       t1 += __shfl_xor_sync(0xFFFFFFFFu, t1, 1);
       const float upv = __shfl_down_sync(0xFFFFFFFFu, t1, 4);   // slot 2q+1 (lane 8q+4) -> lane 8q
       if ((lane & 7) == 0) {
+        // h of row (lane / 8) * 8 + warp, written into every cluster CTA's exchange slot
         const float gv = t1;
-        hbuf[(lane >> 3) * kRQ + warp] = gv / (1.0f + expf(-gv)) * upv;
+        const float hv = gv / (1.0f + expf(-gv)) * upv;
+        const uint32_t loc = smem_u32(hx + sidx % C * RF + (lane >> 3) * kRQ + warp);
+#pragma unroll 1
+        for (int r = 0; r < C; ++r) st_cluster_f32(cluster_map(loc, (uint32_t)r), hv);
       }
     }
-    cp_async_wait<0>();
-    const bool ok_dn = !P.bulk_sb || mbar_wait_warp(smem_u32(&bars[kQuarters]), ph, &abort_s, a.err);
-    __syncthreads();   // h and this thread's down copies -> visible to the whole CTA
-    // The gate/up buffers are free from here on (the down share reads h and the down buffers):
-    // request the next token's gate/up rows now, so they arrive during this token's down share.
-    // abort_s cannot change after the barrier above (no waits follow in this token).
-    if (kMulti && tid == 0 && t + 1 < T && e_s[t + 1] != e_t && !abort_s) {
-      fence_proxy_async_smem();   // this token's reads of the gate/up buffers are complete
-      issue_gu(e_s[t + 1]);
+    cluster_arrive_release();   // this CTA's h is in every cluster CTA's slot; its gate/up reads are done
+    // The gate/up buffers are free once the whole CTA is past the gate/up reads: the next token's
+    // gate/up rows are requested while this token's down share runs.  abort_s is only written
+    // inside waits, so every thread of the CTA reads the same value here after the wait below.
+    cluster_wait_acquire();     // every CTA's h has arrived
+    if (kMulti && tid < kQuarters && t + 1 < T && e_s[t + 1] != e_t && !abort_s) {
+      fence_proxy_async_smem();   // this token's generic reads of the gate/up buffers come first
+      issue_gu(e_s[t + 1], tid);
     }
 
-    // ---- down share: part_c[r] = wgt * (s * sum_f q h_f + b * sum_f h_f) over f0 .. f0+31.
+    // ---- down share: rows r0 .. r0+DR-1 over the cluster's columns kc0 .. kc0+KC-1.  GP lanes per
+    // row, lane g taking quantisation group g of the columns; GP-lane butterfly; the group-0 lane
+    // stores wgt * (sum_g s_g sum q h + b_g sum h) as this CTA's partial of the row.  Two rows per
+    // lane and iteration, their shared-memory loads issued together.
+    const bool ok_dn = mbar_wait_warp(smem_u32(&bars[kQuarters]), ph, &abort_s, a.err);
     {
-      float2 hv[16];
+      constexpr int GP = kC * RF / 64;
+      constexpr int rpp = 32 / GP;   // rows per warp pass
+      const int g = lane % GP;
+      float2 hv[32];
       float hsum = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float hx = hbuf[2 * i], hy = hbuf[2 * i + 1];
-        hsum += hx + hy;
-        hv[i] = make_float2(hx * act_prescale(2 * i), hy * act_prescale(2 * i + 1));
+      for (int i = 0; i < 32; ++i) {
+        const float2 h2 = *reinterpret_cast<const float2*>(hx + g * 64 + 2 * i);
+        hsum += h2.x + h2.y;
+        hv[i] = make_float2(h2.x * act_prescale((2 * i) & 7), h2.y * act_prescale((2 * i + 1) & 7));
       }
       const float wgt = wgt_s[t];
-      const bool hi_half = ((f0 / 64) & 1) != 0;   // group f0/64 is the upper bf16 of its pair
-      const int g = f0 / 64;
-      for (int r = tid; r < d && ok_dn; r += kThreadsDec) {
-        const uint4 c = *reinterpret_cast<const uint4*>(dcodes + 4 * r);
-        float2 p0 = make_float2(0.0f, 0.0f), p1 = make_float2(0.0f, 0.0f);
-        p0 = word_dot2(c.x, hv + 0, p0);
-        p1 = word_dot2(c.y, hv + 4, p1);
-        p0 = word_dot2(c.z, hv + 8, p0);
-        p1 = word_dot2(c.w, hv + 12, p1);
-        const float p = (p0.x + p0.y) + (p1.x + p1.y);
-        float s, b;
-        if (P.bulk_sb) {
-          s = bf16_bits_to_f32(dsb16[r * GF + g]);
-          b = bf16_bits_to_f32(dsb16[(d + r) * GF + g]);
-        } else {
-          const uint32_t sp = dsb[r], bp = dsb[d + r];
-          s = bf16_bits_to_f32(hi_half ? (sp >> 16) : (sp & 0xFFFFu));
-          b = bf16_bits_to_f32(hi_half ? (bp >> 16) : (bp & 0xFFFFu));
-        }
-        a.part[((size_t)t * gridDim.x + cta) * d + r] = wgt * fmaf(s, p, b * hsum);
-      }
-    }
-    __syncthreads();   // this token's reads of the weight buffers and of h are complete
-  }
-
-  // ---- grid barrier: every CTA arrives once; the last arrival resets the count and bumps the
-  // generation in one atomic.  The partial stores are ordered before the arrival by the block
-  // barrier and the fence; the acquire load and fence order the reads below after it.
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const unsigned long long n = gridDim.x;
-    const unsigned long long old = atom_add_release(a.sync, 1ull);
-    if ((old & 0xFFFFFFFFull) == n - 1ull) atom_add_release(a.sync, (1ull << 32) - n);
-    const unsigned long long g0 = old >> 32;
-    const long long t0 = clock64();
-    while ((ld_acquire(a.sync) >> 32) == g0) {
-      if (clock64() - t0 > kWaitTimeoutCycles) {
-        abort_s = 1;
-        raise_flag(a.err, kErrWaitTimeout);
-        break;
-      }
-    }
-    __threadfence();
-  }
-  __syncthreads();
-
-  // ---- y rows of this CTA: sum of all CTAs' partials in a fixed order (16 lanes per row, each
-  // summing every 16th CTA in increasing order, then a fixed butterfly).  The first ten loads of
-  // a lane go out together (one L2 round trip for grids up to 160 CTAs).
-  if (!abort_s) {
-    const int n = gridDim.x;
-    const int rpc = (d + n - 1) / n;
-    const int r_lo = cta * rpc, r_hi = min(d, r_lo + rpc);
-    const int sub = tid & 15;
+      const int gcol = kc0 / 64 + g;
+      float* part_t = a.part + (size_t)t * P.nslices * P.NP * kSliceRows;
+      const int p = j * P.NQ + qc;
 #pragma unroll 1
-    for (int t = 0; t < T; ++t)
-    for (int rb = r_lo; rb < r_hi; rb += kThreadsDec / 16) {
-      const float* part = a.part + (size_t)t * n * d;
-      const int r = rb + (tid >> 4);
-      float acc = 0.0f;
-      if (r < r_hi) {
-        float v[10];
+      for (int pass = warp; pass * rpp < P.DR; pass += 2 * kWarpsDec) {
+        int r[2];
+        uint4 c[2][2];
+        float sc[2], bi[2];
 #pragma unroll
-        for (int i = 0; i < 10; ++i) {
-          const int c = sub + 16 * i;
-          v[i] = c < n ? __ldcg(part + (size_t)c * d + r) : 0.0f;
+        for (int u = 0; u < 2; ++u) {
+          r[u] = (pass + u * kWarpsDec) * rpp + lane / GP;
+          const bool in = r[u] < P.DR && ok_dn;
+          const uint32_t* cw = dcodes + (in ? r[u] : 0) * (P.KC / 8) + g * 8;
+          c[u][0] = *reinterpret_cast<const uint4*>(cw);
+          c[u][1] = *reinterpret_cast<const uint4*>(cw + 4);
+          sc[u] = bf16_bits_to_f32(dsb[(in ? r[u] : 0) * GF + gcol]);
+          bi[u] = bf16_bits_to_f32(dsb[(P.DR + (in ? r[u] : 0)) * GF + gcol]);
         }
 #pragma unroll
-        for (int i = 0; i < 10; ++i) acc += v[i];
-        for (int c = sub + 160; c < n; c += 16) acc += __ldcg(part + (size_t)c * d + r);
+        for (int u = 0; u < 2; ++u) {
+          float2 p0 = make_float2(0.0f, 0.0f), p1 = make_float2(0.0f, 0.0f);
+          p0 = word_dot2(c[u][0].x, hv + 0, p0);
+          p1 = word_dot2(c[u][0].y, hv + 4, p1);
+          p0 = word_dot2(c[u][0].z, hv + 8, p0);
+          p1 = word_dot2(c[u][0].w, hv + 12, p1);
+          p0 = word_dot2(c[u][1].x, hv + 16, p0);
+          p1 = word_dot2(c[u][1].y, hv + 20, p1);
+          p0 = word_dot2(c[u][1].z, hv + 24, p0);
+          p1 = word_dot2(c[u][1].w, hv + 28, p1);
+          const float pq = (p0.x + p0.y) + (p1.x + p1.y);
+          float v = fmaf(sc[u], pq, bi[u] * hsum);
+#pragma unroll
+          for (int off = GP >> 1; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+          if (g == 0 && r[u] < P.DR) {
+            const int sl = crank * P.NSC + r[u] / kSliceRows;
+            part_t[((size_t)sl * P.NP + p) * kSliceRows + r[u] % kSliceRows] = wgt * v;
+          }
+        }
       }
-      acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 8);
-      acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 4);
-      acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 2);
-      acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
-      if (sub == 0 && r < r_hi) a.y[(size_t)t * d + r] = acc;
+    }
+    __syncthreads();   // this token's partials are stored; the down buffers are free
+    if (kMulti && tid == 32 && t + 1 < T && e_s[t + 1] != e_t && !abort_s) {
+      fence_proxy_async_smem();   // this token's generic reads of the down buffers come first
+      issue_dn(e_s[t + 1]);
+    }
+
+    // ---- combine: one arrival per row slice of this CTA; the last of the NP arrivals sums the
+    // slice's partials in slot order.  Arrivals happen even after a timed-out wait, so counters
+    // always return to zero.
+    uint32_t* cnt_t = a.cnt + (size_t)t * P.nslices;
+    if (tid < P.NSC) {
+      const int sl = crank * P.NSC + tid;
+      __threadfence();
+      const uint32_t old = atomicAdd(cnt_t + sl, 1u);
+      last_s[tid] = (old == (uint32_t)(P.NP - 1)) ? 1 : 0;
+      if (old == (uint32_t)(P.NP - 1)) cnt_t[sl] = 0u;
+      __threadfence();
+    }
+    __syncthreads();
+    // Rows of the slices this CTA completed.  Each partial is 128 contiguous floats written whole by
+    // one CTA; 64 threads per slice, a lane pair per four rows, lane 2i+h summing partials
+    // h*NH .. min(NP, (h+1)*NH) - 1 in order as float4s (loads all in flight together), then the
+    // pair adds its two halves, first half first.
+    {
+      const int NH = (P.NP + 1) / 2;
+      const int half = tid & 1;
+      const int row4 = (tid & 63) >> 1;
+      for (int i = tid >> 6; i < P.NSC; i += kThreadsDec / 64) {
+        const int sl = crank * P.NSC + i;
+        const int rows = min(kSliceRows, P.DR - i * kSliceRows);
+        if (!last_s[i]) continue;   // uniform over the lane pair and the warp
+        const float4* pr = reinterpret_cast<const float4*>(a.part + ((size_t)t * P.nslices + sl) * P.NP * kSliceRows) +
+                           row4;
+        const int p_lo = half * NH, p_hi = min(P.NP, p_lo + NH);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        constexpr int kBatch = 18;   // float4 loads in flight per thread
+        for (int c0 = p_lo; c0 < p_hi; c0 += kBatch) {
+          float4 v[kBatch];
+#pragma unroll
+          for (int c = 0; c < kBatch; ++c)
+            v[c] = c0 + c < p_hi ? __ldcg(pr + (size_t)(c0 + c) * (kSliceRows / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < kBatch; ++c) {
+            if (c0 + c < p_hi) {
+              acc.x += v[c].x;
+              acc.y += v[c].y;
+              acc.z += v[c].z;
+              acc.w += v[c].w;
+            }
+          }
+        }
+        float4 o;
+        o.x = __shfl_xor_sync(0xFFFFFFFFu, acc.x, 1);
+        o.y = __shfl_xor_sync(0xFFFFFFFFu, acc.y, 1);
+        o.z = __shfl_xor_sync(0xFFFFFFFFu, acc.z, 1);
+        o.w = __shfl_xor_sync(0xFFFFFFFFu, acc.w, 1);
+        if (half == 0 && 4 * row4 < rows) {
+          const float4 sum = make_float4(acc.x + o.x, acc.y + o.y, acc.z + o.z, acc.w + o.w);
+          *reinterpret_cast<float4*>(a.y + (size_t)t * d + r0 + i * kSliceRows + 4 * row4) = sum;
+        }
+      }
     }
   }
 
@@ -446,54 +575,48 @@ __global__ void __launch_bounds__(kThreadsDec, 1) decode_layer_kernel(const Deco
   }
 }
 
-struct DevInfo {
-  int sms = 0;
-  bool ready = false;
-};
 constexpr int kMaxDev = 64;
-DevInfo g_dev[kMaxDev];
+bool g_ready[kMaxDev];
 std::mutex g_dev_mu;
 constexpr size_t kDecSmemMax = 200 * 1024;
 
-cudaError_t dev_info(DevInfo** out) {
+cudaError_t ensure_attrs() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_dev_mu);
-  DevInfo& di = g_dev[dev];
-  if (!di.ready) {
-    if ((e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_layer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecSmemMax);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_layer_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_layer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecSmemMax);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_layer_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e != cudaSuccess) return e;
-    di.ready = true;
+  if (!g_ready[dev]) {
+    for (auto f : {decode_layer_kernel<false>, decode_layer_kernel<true>}) {
+      if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecSmemMax)) != cudaSuccess)
+        return e;
+      if ((e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100)) != cudaSuccess) return e;
+    }
+    g_ready[dev] = true;
   }
-  *out = &di;
   return cudaSuccess;
 }
 
 }  // namespace
 
-size_t decode_scratch_floats(int d, int k, int F) { return (size_t)(k + 1) * (F / RF) * d; }
+size_t decode_scratch_floats(int d, int k, int F) {
+  const DecPlan P(d, F, k + 1, false);
+  return (size_t)P.nslices * P.NP * kSliceRows;
+}
+
+int decode_counters(int d, int F) {
+  const DecPlan P(d, F, 1, false);
+  return P.nslices;
+}
 
 bool decode_supported(int d, int E, int k, int F) {
   const int k1 = k + 1;
   // One quantisation group per lane in the gate/up rows: d <= 2048 (and d a multiple of 64).
-  // F a multiple of 128: the down columns f0 .. f0+31 of a CTA lie in one bf16 pair of
-  // scale (bias) values that starts on a 4-byte boundary (F / 64 even).
+  // F a multiple of 128: 32 gate/up rows per CTA and whole quantisation groups per cluster.
   if (k1 > 32 || E > kMaxE || d > 2048 || d % 64 != 0 || F % 128 != 0) return false;
-  const DecPlan P(d, F, k1);
-  if (P.bytes > kDecSmemMax) return false;
-  // Every CTA must be resident at once (one per SM): the grid barrier waits on all of them.
-  DevInfo* di = nullptr;
-  if (dev_info(&di) != cudaSuccess) return false;
-  return P.grid <= di->sms;
+  const DecPlan P(d, F, k1, true);
+  if (P.bytes > kDecSmemMax || P.nslices > kDecodeMaxSlices || P.NSC > 8) return false;
+  return true;
 }
 
 constexpr int kStageThreads = 256;
@@ -546,20 +669,24 @@ cudaError_t launch_stage_in(const StageArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-static_assert(kDecodeMaxTokens <= kThreadsDec / 32, "one routing warp per token");
+static_assert(kDecodeMaxTokens <= kWarpsDec, "one routing warp per token");
+static_assert(kC * RF % 64 == 0 && 32 % (kC * RF / 64) == 0, "whole quantisation groups per cluster");
 static_assert(kDecodeLayerMaxT <= kDecodeMaxTokens, "the layer path's decode calls fit one launch");
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st, bool pdl) {
+int decode_box_rows(int d, int F) { return DecPlan(d, F, 1, false).box_rows; }
+
+cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& a, cudaStream_t st, bool pdl) {
   if (a.T > kDecodeMaxTokens) return cudaErrorInvalidValue;
   const int k1 = a.k + (a.has_shared ? 1 : 0);
-  DevInfo* di = nullptr;
-  cudaError_t e = dev_info(&di);
+  if (!decode_supported(a.d, a.E, a.k, a.F)) return cudaErrorInvalidConfiguration;
+  cudaError_t e = ensure_attrs();
   if (e != cudaSuccess) return e;
-  const DecPlan P(a.d, a.F, k1);
-  if (P.grid > di->sms || P.bytes > kDecSmemMax) return cudaErrorInvalidConfiguration;
+  const DecPlan P(a.d, a.F, k1, a.T > 1);
   cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kC;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
@@ -569,7 +696,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st, bool pdl) {
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  e = a.T > 1 ? cudaLaunchKernelEx(&cfg, decode_layer_kernel<true>, a) : cudaLaunchKernelEx(&cfg, decode_layer_kernel<false>, a);
+  e = a.T > 1 ? cudaLaunchKernelEx(&cfg, decode_layer_kernel<true>, maps, a)
+              : cudaLaunchKernelEx(&cfg, decode_layer_kernel<false>, maps, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -99,7 +99,7 @@ struct PermuteArgs {
 };
 cudaError_t launch_permute_x(const PermuteArgs& a, cudaStream_t st);
 
-// ---------------------------------------------------------------- decode T = 1 (decode.cu)
+// ---------------------------------------------------------------- decode T <= 8 (decode.cu)
 struct DecodeArgs {
   const uint16_t* x;       // bf16 [T][d]
   const float* logits;     // [T][E]
@@ -107,16 +107,37 @@ struct DecodeArgs {
   const uint16_t* w_sg;    // bf16 [d] or null
   int d, E, k, F, has_shared;
   int T;                   // tokens, 1 .. kDecodeMaxTokens (0 reads as 1)
-  float* part;             // scratch: fp32 [T][(k+1) F / 32][d] per-CTA partial outputs
+  float* part;             // scratch: fp32 [T][decode_scratch_floats] partial outputs per row slice
+  uint32_t* cnt;           // arrival counters [T][decode_counters]: zero before the first launch;
+                           // every launch leaves them zero
   float* y;                // fp32 [T][d]
   uint32_t* err;
-  unsigned long long* sync;   // grid-barrier word (8-byte aligned; count low, generation high)
 };
+// Tensor maps of a decode launch: the down-projection codes of the routed [0] and shared [1]
+// expert sets as 2-D uint32 tensors {F/8 words, n*d rows}, box 16 words x decode_box_rows rows.
+struct DecodeMaps {
+  CUtensorMap down[2];
+};
+int decode_box_rows(int d, int F);
 bool decode_supported(int d, int E, int k, int F);
 constexpr int kDecodeMaxTokens = 8;   // tokens one decode launch can take (one routing warp each)
 constexpr int kDecodeLayerMaxT = 8;    // layer calls of up to this many tokens take the decode kernel
+constexpr int kDecodeMaxSlices = 32;   // combine slices (arrival counters) per token, at most
 size_t decode_scratch_floats(int d, int k, int F);   // floats of DecodeArgs::part per token
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st, bool pdl);
+int decode_counters(int d, int F);                    // counters of DecodeArgs::cnt per token
+cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& a, cudaStream_t st, bool pdl);
+// Encodes DecodeMaps::down[i] for n stacked [d, F] down matrices (api.cu); false on failure.
+bool encode_decode_down(CUtensorMap* m, const uint32_t* codes, int n, int d, int F);
+
+// Workspace head shared by the C ABI and the allocation-free entry point: the error word at 0,
+// the decode arrival counters from kCountersOffset (kDecodeMaxTokens * kDecodeMaxSlices words).
+constexpr size_t kWsHeadBytes = 2048;
+constexpr size_t kCountersOffset = 1024;
+static_assert(kCountersOffset + 4 * kDecodeMaxTokens * kDecodeMaxSlices <= kWsHeadBytes, "head holds the counters");
+
+// Host-side dims rules of every layer call (api.cu); MOE_OK = 0.
+int check_layer_dims(int T, int d, int E, int k, int F, int F_shared);
+
 // One CTA copies a token's x (x_bytes, a multiple of 16) and logits (lg_bytes, a multiple of 4)
 // from page-locked, mapped host memory (16-byte aligned) into device buffers, once, so that the
 // decode kernel's many readers hit device memory; launched with programmatic serialisation, it

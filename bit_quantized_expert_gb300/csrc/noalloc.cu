@@ -6,9 +6,9 @@
 // latency-critical decode loop that must never enter cudaMalloc or cudaFree, which may
 // synchronise the whole device; or a host program that only holds pointers to weights, inputs
 // and outputs and has no allocator of its own.  moe_layer_forward_decode_noalloc serves them: the
-// only scratch it needs (an error word, a grid-barrier word and the decode kernel's per-CTA
-// partial outputs) lives in the file-scope device array below, which every GPU that loads this library
-// holds until the process exits.
+// only scratch it needs (an error word, the decode kernel's arrival counters and its partial
+// outputs per row slice) lives in the file-scope device array below, which every GPU that loads
+// this library holds until the process exits.
 #include <mutex>
 
 #include "../../include/moe.h"
@@ -17,10 +17,10 @@
 namespace moe {
 namespace {
 
-// The first 64 floats (256 bytes) hold the error word and the grid-barrier word; then the
-// decode kernel's per-CTA partial outputs, (k + 1) F / 32 rows of d fp32 values.
-constexpr int kNoAllocHeadFloats = 64;
-constexpr size_t kNoAllocMaxPart = 327680;   // upper bound on (k + 1) (F / 32) d: 1.25 MB
+// The first kWsHeadBytes hold the error word and the decode arrival counters, laid out as in a
+// workspace; then the decode kernel's partial outputs of one token (decode_scratch_floats).
+constexpr int kNoAllocHeadFloats = (int)(kWsHeadBytes / 4);
+constexpr size_t kNoAllocMaxPart = 131072;   // upper bound on the partial outputs: 512 KB
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocHeadFloats + kNoAllocMaxPart];
 
 constexpr int kMaxDevices = 64;
@@ -71,7 +71,9 @@ extern "C" moe_status moe_layer_forward_decode_noalloc(const moe_dims* dims, con
                                                        const moe_experts* routed, const moe_experts* shared,
                                                        const uint16_t* w_shared_gate, float* y, void* stream) {
   if (dims == nullptr || routed == nullptr) return MOE_ERR_INVALID_ARG;
-  if (moe_workspace_bytes(dims) == 0) return MOE_ERR_INVALID_ARG;   // the dims rules of moe_layer_forward
+  // the dims rules of moe_layer_forward, with its status codes
+  const int ds = check_layer_dims(dims->T, dims->d, dims->E, dims->k, dims->F, dims->F_shared);
+  if (ds != MOE_OK) return static_cast<moe_status>(ds);
   if (dims->T == 0) return MOE_OK;
   if (dims->T != 1) return MOE_ERR_UNSUPPORTED;                      // one token per call
   const bool sh = shared != nullptr;
@@ -91,10 +93,10 @@ extern "C" moe_status moe_layer_forward_decode_noalloc(const moe_dims* dims, con
   if (scratch_for_current_device(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* err = reinterpret_cast<uint32_t*>(scratch);
-  // The array keeps the previous call's contents: the error word and the grid-barrier word
-  // (bytes 8..15) start every call at zero.  Every partial is written before the grid barrier
-  // and read after it.
-  if (cudaMemsetAsync(err, 0, 16, st) != cudaSuccess) return MOE_ERR_CUDA;
+  // The array keeps the previous call's contents: the error word and the arrival counters start
+  // every call at zero.  Every partial is written before its counter arrival and read only by the
+  // last arrival of its slice.
+  if (cudaMemsetAsync(err, 0, kWsHeadBytes, st) != cudaSuccess) return MOE_ERR_CUDA;
 
   DecodeArgs da{};
   da.x = x;
@@ -117,6 +119,11 @@ extern "C" moe_status moe_layer_forward_decode_noalloc(const moe_dims* dims, con
   da.part = scratch + kNoAllocHeadFloats;
   da.y = y;
   da.err = err;
-  da.sync = reinterpret_cast<unsigned long long*>(scratch + 2);
-  return launch_decode(da, st, true) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  da.cnt = reinterpret_cast<uint32_t*>(scratch) + kCountersOffset / 4;
+  DecodeMaps dmaps{};
+  if (!encode_decode_down(&dmaps.down[0], routed->down.codes, dims->E, dims->d, dims->F) ||
+      !encode_decode_down(&dmaps.down[1], sh ? shared->down.codes : routed->down.codes, sh ? 1 : dims->E, dims->d,
+                          dims->F))
+    return MOE_ERR_CUDA;
+  return launch_decode(dmaps, da, st, true) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

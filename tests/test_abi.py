@@ -50,11 +50,12 @@ def test_workspace_and_tile_bounds(lib):
 
 
 def test_workspace_holds_decode_partials_per_token(lib):
-    """Up to eight tokens run one decode launch that keeps (k+1) F/32 partial rows of d floats per
-    token: the workspace grows by at least that much per token up to eight, and the host-buffer
-    entry point's workspace adds room for x, logits and y behind it."""
+    """Up to eight tokens run one decode launch that keeps, per token, one partial of every row of y
+    per expert slot and cluster ((k+1) slots x F/512 clusters of 16 CTAs at F = 512, rows in
+    128-row slices): the workspace grows by at least that much per token up to eight, and the
+    host-buffer entry point's workspace adds room for x, logits and y behind it."""
     d, E, k, F = 2048, 256, 8, 512
-    part = (k + 1) * (F // 32) * d * 4
+    part = (k + 1) * (F // 512) * d * 4
     sizes = [moe.workspace_bytes(moe.dims(T, d, E, k, F, F)) for T in range(1, 10)]
     for T in range(1, 9):
         assert sizes[T - 1] >= T * part, T
