@@ -285,6 +285,42 @@ def decode_bench(args, world, rank, local, device, pk):
                      "note": "one weight set replayed (weights L2-resident); not the headline"}
     log(f"decode hot-L2: {res['hot_l2']['us_per_layer']:.2f} us per layer")
 
+    # Bandwidth ceiling of the decode access pattern: the loads-only replica of the decode launch
+    # (same grid, clusters, copies and programmatic launch; experts given, no arithmetic) over the
+    # same 40 weight sets and the same routing as the timed steps.
+    idx = []
+    for l in range(LAYERS):
+        r = moe.alloc_routing(layers[l].dims(NI), 112, device)
+        ws_r = moe.alloc_workspace(layers[l].dims(NI), device)
+        moe.route(layers[l].dims(NI), ins[l]["logits"], r, ws_r)
+        idx.append(r["idx"].clone())
+        del r, ws_r
+    torch.cuda.synchronize()
+
+    def probe_step(s):
+        i = s % NI
+        for l in range(LAYERS):
+            moe.decode_stream_probe(dm, idx[l][i], layers[l].routed, layers[l].shared, ws)
+
+    with torch.cuda.stream(stream):
+        for s in range(3):
+            probe_step(s)
+    g_probe = capture(lambda: [probe_step(s) for s in range(G)], stream)
+    with torch.cuda.stream(stream):
+        g_probe.replay()
+    stream.synchronize()
+    p_steps = max(G, args.steps // 2 // G * G)
+    p_ms = timed_graph_steps(g_probe, G, g_probe, p_steps, stream)
+    p_us = p_ms * 1e3 / (p_steps * LAYERS)
+    res["loads_only"] = {"us_per_layer": p_us, "GB_s": per_call / (p_us * 1e-6) / 1e9,
+                         "frac": per_call / (p_us * 1e-6) / 1e9 / pk["hbm_gbs"],
+                         "note": "loads-only replica of the decode launch (moe_decode_stream_probe): same grid, "
+                                 "clusters, shared memory, weight copies and programmatic launch, experts given, "
+                                 "no arithmetic; the bandwidth ceiling of this access pattern"}
+    if moe.read_error_flags(ws) != 0:
+        raise RuntimeError("device error flags set during the loads-only runs")
+    log(f"decode loads-only: {p_us:.2f} us per layer ({res['loads_only']['GB_s']:.0f} GB/s)")
+
     # A few tokens per layer call (verify-batch shapes): up to eight run the decode kernel in one
     # launch.  CUDA graph over the 40 weight sets; context, not the headline.
     small = {}
@@ -620,7 +656,7 @@ def main():
                 "config": config(world), "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": res["e2e"],
                 "gpu_launches": res["gpu_launches"], "clocks": res["clocks"], "error_flags": res["flags"],
                 "decode_hot_l2": res.get("hot_l2"), "decode_e2e_staged": res.get("e2e_staged"),
-                "decode_small_T": res.get("small_T"),
+                "decode_small_T": res.get("small_T"), "decode_loads_only": res.get("loads_only"),
                 "prefill": extras}
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -15,11 +15,11 @@ import os
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG_DIR, "libmoe_gb300.so")
 
-# Symbols declared in include/moe.h.
+# Symbols declared in include/moe.h and include/moe_probe.h.
 EXPORTED = ("moe_status_string", "moe_max_tiles", "moe_workspace_bytes", "moe_route",
             "moe_expert_forward", "moe_layer_forward", "moe_rmsnorm_router", "moe_clear_error_flags",
             "moe_read_error_flags", "moe_layer_forward_decode_noalloc", "moe_workspace_bytes_host",
-            "moe_layer_forward_host")
+            "moe_layer_forward_host", "moe_decode_stream_probe")
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_MISALIGNED",
           4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA"}
@@ -87,6 +87,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_layer_forward_host.argtypes = [P(Dims), VP, VP, P(ExpertsC), P(ExpertsC), VP, VP, VP, S, VP]
     lib.moe_layer_forward_decode_noalloc.restype = ctypes.c_int
     lib.moe_layer_forward_decode_noalloc.argtypes = [P(Dims), VP, VP, P(ExpertsC), P(ExpertsC), VP, VP, VP]
+    lib.moe_decode_stream_probe.restype = ctypes.c_int
+    lib.moe_decode_stream_probe.argtypes = [P(Dims), VP, P(ExpertsC), P(ExpertsC), VP, S, VP]
     lib.moe_clear_error_flags.restype = ctypes.c_int
     lib.moe_clear_error_flags.argtypes = [VP, S, VP]
     lib.moe_read_error_flags.restype = ctypes.c_int
@@ -154,7 +156,7 @@ def alloc_workspace(dm: Dims, device="cuda"):
     """Workspace for these dims with its error word cleared."""
     import torch
     ws = torch.empty(workspace_bytes(dm), dtype=torch.uint8, device=device)
-    ws[:2048].zero_()
+    ws[:256].zero_()
     return ws
 
 
@@ -169,7 +171,7 @@ def alloc_workspace_host(dm: Dims, device="cuda"):
     """Workspace (with the host-call staging area) for these dims, its error word cleared."""
     import torch
     ws = torch.empty(workspace_bytes_host(dm), dtype=torch.uint8, device=device)
-    ws[:2048].zero_()
+    ws[:256].zero_()
     return ws
 
 
@@ -237,6 +239,15 @@ def layer_forward_decode_noalloc(dm: Dims, x, logits, routed: dict, shared: dict
     _check(load_library().moe_layer_forward_decode_noalloc(
         ctypes.byref(dm), _ptr(x), _ptr(logits), ctypes.byref(re), ctypes.byref(se) if se is not None else None,
         _ptr(w_sg), _ptr(y), _stream(stream)), "moe_layer_forward_decode_noalloc")
+
+
+def decode_stream_probe(dm: Dims, idx, routed: dict, shared: dict | None, workspace, stream=None):
+    """Loads-only replica of the one-token decode launch (include/moe_probe.h): moves the weight
+    bytes of the experts in idx (int32 [k]) and nothing else."""
+    re, se = experts_struct(routed), experts_struct(shared)
+    _check(load_library().moe_decode_stream_probe(ctypes.byref(dm), _ptr(idx), ctypes.byref(re),
+                                                  ctypes.byref(se) if se is not None else None, _ptr(workspace),
+                                                  workspace.numel(), _stream(stream)), "moe_decode_stream_probe")
 
 
 def read_error_flags(workspace, stream=None) -> int:

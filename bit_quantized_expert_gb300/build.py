@@ -30,7 +30,8 @@ def _nvcc() -> str:
 
 def _deps() -> list[str]:
     hdrs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
-    hdrs.append(os.path.join(os.path.dirname(PKG), "include", "moe.h"))
+    inc = os.path.join(os.path.dirname(PKG), "include")
+    hdrs += [os.path.join(inc, f) for f in os.listdir(inc) if f.endswith(".h")]
     return hdrs
 
 

@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "../../include/moe.h"
+#include "../../include/moe_probe.h"
 #include "kernels.h"
 
 namespace moe {
@@ -19,8 +20,7 @@ struct Layout {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// The first kWsHeadBytes of a workspace: the error word at 0 and the decode path's arrival
-// counters at kCountersOffset (kernels.h); both must be zero before the first call.
+// The first kWsHeadBytes of a workspace: the error word at 0 (zero before the first call).
 
 size_t max_tiles_of(long long T, long long k, long long E, long long tile_n, bool shared) {
   return (size_t)(T * k / tile_n + std::min(E, T * k) + (shared ? (T + tile_n - 1) / tile_n : 0));
@@ -417,7 +417,6 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
     da.part = at<float>(workspace, L.hdec);
     da.y = y;
     da.err = err;
-    da.cnt = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + L.err + kCountersOffset);
     da.T = d.T;
     DecodeMaps dmaps{};
     if (!encode_decode_down(&dmaps.down[0], routed->down.codes, d.E, d.d, d.F) ||
@@ -560,11 +559,47 @@ moe_status moe_rmsnorm_router(const moe_dims* dims, float* x_resid, const float*
   return cuda_status(launch_router(maps, ra, st));
 }
 
+moe_status moe_decode_stream_probe(const moe_dims* dims, const int32_t* idx, const moe_experts* routed,
+                                   const moe_experts* shared, void* workspace, size_t workspace_bytes, void* stream) {
+  moe_status s = check_dims(dims);
+  if (s != MOE_OK) return s;
+  if ((s = check_experts(routed)) != MOE_OK) return s;
+  if (shared != nullptr && (s = check_experts(shared)) != MOE_OK) return s;
+  if ((shared != nullptr) != (dims->F_shared > 0)) return MOE_ERR_INVALID_ARG;
+  if (dims->T == 0) return MOE_OK;
+  if (dims->T != 1 || !decode_supported(dims->d, dims->E, dims->k, dims->F)) return MOE_ERR_UNSUPPORTED;
+  if ((s = check_ptr(idx)) != MOE_OK) return s;
+  if ((s = check_ptr(workspace)) != MOE_OK) return s == MOE_ERR_INVALID_ARG ? MOE_ERR_WORKSPACE : s;
+  if (workspace_bytes < 4) return MOE_ERR_WORKSPACE;
+  const moe_dims& d = *dims;
+  const bool sh = shared != nullptr;
+  StreamArgs a{};
+  a.gate[0] = qptr(routed->gate);
+  a.up[0] = qptr(routed->up);
+  a.down[0] = qptr(routed->down);
+  if (sh) {
+    a.gate[1] = qptr(shared->gate);
+    a.up[1] = qptr(shared->up);
+    a.down[1] = qptr(shared->down);
+  }
+  a.idx = idx;
+  a.d = d.d;
+  a.E = d.E;
+  a.k = d.k;
+  a.F = d.F;
+  a.has_shared = sh ? 1 : 0;
+  a.err = at<uint32_t>(workspace, 0);
+  DecodeMaps maps{};
+  if (!encode_decode_down(&maps.down[0], routed->down.codes, d.E, d.d, d.F) ||
+      !encode_decode_down(&maps.down[1], sh ? shared->down.codes : routed->down.codes, sh ? 1 : d.E, d.d, d.F))
+    return MOE_ERR_CUDA;
+  return cuda_status(launch_decode_stream(maps, a, static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_clear_error_flags(void* workspace, size_t workspace_bytes, void* stream) {
   if (workspace == nullptr) return MOE_ERR_INVALID_ARG;
   if (workspace_bytes < 4) return MOE_ERR_WORKSPACE;
-  // The error word, and (in workspaces large enough for a layer) the decode arrival counters.
-  const size_t n = std::min(workspace_bytes, kWsHeadBytes) & ~(size_t)3;
+  const size_t n = 4;   // the error word
   return cuda_status(cudaMemsetAsync(workspace, 0, n, static_cast<cudaStream_t>(stream)));
 }
 
@@ -574,9 +609,7 @@ moe_status moe_read_error_flags(void* workspace, size_t workspace_bytes, uint32_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemcpy(flags, workspace, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
-  // After a timed-out wait the decode arrival counters are reset too (the stream is idle here).
-  const size_t n = (*flags & 1u) != 0 ? std::min(workspace_bytes, kWsHeadBytes) & ~(size_t)3 : 4;
-  if (cudaMemset(workspace, 0, n) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(workspace, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 

@@ -16,6 +16,7 @@ namespace moe {
 constexpr uint32_t kErrWaitTimeout = 1u;   // a bounded wait gave up; outputs are invalid
 constexpr uint32_t kErrFp16Range = 2u;     // a value did not fit the fp16 operand type
 constexpr uint32_t kErrBadRouting = 4u;    // routing tables inconsistent with the dims
+constexpr uint32_t kErrNonFinite = 8u;     // an activation of the decode path is not finite
 
 // About two seconds at the maximum SM clock: no correct launch waits this long.
 constexpr long long kWaitTimeoutCycles = 4000000000ll;

@@ -21,23 +21,26 @@
 //     rows (the cluster's 64-byte column block of each row, as one or two 2-D tensor copies) with
 //     their scales and biases.  Shared-expert CTAs start their copies before the wait: weights are
 //     never written upstream;
-//   * each CTA computes its 32 SwiGLU outputs h and writes them into the shared memory of every
-//     CTA of its cluster (distributed shared memory), then the cluster barrier;
+//   * each CTA computes its 32 SwiGLU outputs h, turns them into fixed-point byte planes (see
+//     Planes) and writes those into the shared memory of every CTA of its cluster (distributed
+//     shared memory), then the cluster barrier;
 //   * each CTA computes its d / C down rows over the cluster's 32 C columns of h, scaled by the
 //     slot's routing weight (or the shared expert's gate), and stores them as one partial of each
 //     of its row slices (128 rows);
-//   * combine: per row slice an arrival counter; the CTA that arrives last sums the slice's
-//     (k+1) S / C partials in a fixed slot order, writes y and resets the counter.  Nobody waits
-//     on another cluster; the order of the sum never depends on arrival order.
+//   * combine: a second, small kernel (launched with programmatic dependent launch, so its CTAs
+//     are resident and waiting when the decode launch ends) sums each row's (k+1) S / C partials
+//     in a fixed order and writes y.  Nobody waits on another cluster inside the decode launch;
+//     the order of the sum never depends on the order in which CTAs finish.
 // Several tokens (the kMulti instantiation): warp t routes token t; every CTA then takes its
 // slot of token 0, 1, ... in turn, fetching the slot's weights again only when its expert changes
-// (the shared expert's stay), with double-buffered h exchange slots and per-token counters, so
+// (the shared expert's stay), with double-buffered h exchange slots and partials per token, so
 // each token's y is what a one-token launch gives, bit for bit.
 //
-// Arithmetic: codes become exact fp32 values q * 16^e via the 2^23 exponent trick (the nibble
-// stays where it is in the word; the activation carries the matching 16^-e), partial dot
-// products sum_c q_c x_c accumulate in fp32 with packed two-lane FMAs, and w = q*s + b enters as
-// s * sum(q x) + b * sum(x) per quantisation group.
+// Arithmetic: w = q*s + b enters as s * sum(q x) + b * sum(x) per quantisation group; sum(q x) is
+// an exact integer dot product (dp4a) of the 4-bit codes with the group's activations held as
+// 23-bit fixed point relative to the group's largest (Planes below), and everything after it is
+// fp32.  Per code word that is two masks and six dp4a, against about twice the issue slots for
+// an fp32 dequantise-and-multiply.
 #include <algorithm>
 #include <mutex>
 
@@ -52,34 +55,109 @@ constexpr int RF = 32;   // gate/up rows per CTA
 constexpr int kQuarters = 4;
 constexpr int kRQ = RF / kQuarters;   // gate/up rows per quarter
 constexpr int kMaxE = 1024;
-constexpr float kMagic = 8388608.0f;   // 2^23
 constexpr int kThreadsDec = 256;
 constexpr int kWarpsDec = kThreadsDec / 32;
 constexpr int kSliceRows = 128;        // rows of y per combine slice
 
-// Activation pre-scale matching the position of code n (0..7) of a word after extraction.
-__host__ __device__ constexpr float act_prescale(int n) {
-  return n % 8 == 0 ? 1.0f : n % 8 == 1 ? 0.0625f : n % 8 == 2 ? 0.00390625f : n % 8 == 3 ? 0.000244140625f
-       : n % 8 == 4 ? 1.52587890625e-05f : n % 8 == 5 ? 0.00390625f : n % 8 == 6 ? 0.000244140625f
-       : 1.52587890625e-05f;
+// ---------------------------------------------------------------- exact integer dot products
+// Activations v_c become 23-bit two's-complement fixed point V_c = round(v_c 2^(22-e)), with e the
+// smallest exponent such that every |v| of the block is below 2^e, held as three byte planes
+// V = hi 2^16 + mid 2^8 + lo (hi signed, mid and lo unsigned: bytes 2, 1, 0 of V).  Byte j of
+// plane word [2w + o] is V of column 8w + 2j + o: the byte order in which a 32-bit code word splits
+// into its even nibbles (w & 0x0F0F0F0F) and odd nibbles ((w >> 4) & 0x0F0F0F0F).  sum_c q_c v_c
+// over a quantisation group (eight code words) is then six dp4a per word, exact in 32-bit integers,
+// recombined once in fp32.  The gate/up activations use one exponent per group; h uses one per 32
+// columns (the block one CTA produces), so a group has an exponent per half.  Elements more than
+// 2^23 below their block's largest are rounded, which keeps a sum within fp32 accumulation error.
+struct Planes {
+  uint32_t p[3][16];   // [hi | mid | lo][2 w + o], words 0..7 of the group
+  float scale[2];      // 2^(e - 22) of code words 0..3 and 4..7
+  float sum;           // sum of the group's values (fp32), for the bias term
+};
+
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
 }
 
-__device__ __forceinline__ float2 magic_pair(uint32_t a, uint32_t b) {
-  return make_float2(__uint_as_float(a | 0x4B000000u), __uint_as_float(b | 0x4B000000u));
+// e with |v| < 2^e for every v whose magnitude bits are at most mbits (the largest |v| as uint32;
+// bit patterns of non-negative floats order like the values), clamped below at -104 so that
+// 2^(22 - e) is a normal float; values under 2^-104 then round towards 0.
+__device__ __forceinline__ int block_exponent(uint32_t mbits) { return max((int)((mbits >> 23) & 0xFFu) - 126, -104); }
+__device__ __forceinline__ float pow2i(int k) { return __int_as_float((127 + k) << 23); }   // -126 <= k <= 127
+// round(v * scale) for |v * scale| < 2^22: adding 1.5 * 2^23 leaves the rounded integer in the low bits.
+__device__ __forceinline__ int fixed23(float v, float scale) {
+  return __float_as_int(fmaf(v, scale, 12582912.0f)) - 0x4B400000;
+}
+// Planes words of four fixed-point values (columns 8w + o, + 2, + 4, + 6).
+__device__ __forceinline__ void pack4(int v0, int v1, int v2, int v3, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
+  const uint32_t a = __byte_perm(v0, v1, 0x5140), b = __byte_perm(v2, v3, 0x5140);
+  lo = __byte_perm(a, b, 0x5410);
+  mid = __byte_perm(a, b, 0x7632);
+  hi = __byte_perm(__byte_perm(v0, v1, 0x0062), __byte_perm(v2, v3, 0x0062), 0x5410);
 }
 
-// acc += sum over the 8 codes of word w of q_c * xs[c] (xs pre-scaled by act_prescale), as four
-// packed pairs (codes 0,1 / 2,3 / 4,5 / 6,7).  Codes 5..7 are taken from w >> 12 so that every
-// extracted value stays below 2^20 and is exact.
-__device__ __forceinline__ float2 word_dot2(uint32_t w, const float2* xs, float2 acc) {
-  const uint32_t w12 = w >> 12;
-  const float2 m = make_float2(-kMagic, -kMagic);
-  acc = __ffma2_rn(__fadd2_rn(magic_pair(w & 0xFu, w & 0xF0u), m), xs[0], acc);
-  acc = __ffma2_rn(__fadd2_rn(magic_pair(w & 0xF00u, w & 0xF000u), m), xs[1], acc);
-  acc = __ffma2_rn(__fadd2_rn(magic_pair(w & 0xF0000u, w12 & 0xF00u), m), xs[2], acc);
-  acc = __ffma2_rn(__fadd2_rn(magic_pair(w12 & 0xF000u, w12 & 0xF0000u), m), xs[3], acc);
-  return acc;
+// The 64 bf16 activations of one quantisation group (eight uint4 = columns 0..63) -> planes with
+// one exponent.  Returns false when a value is not finite.
+__device__ __forceinline__ bool planes_of_bf16(const uint4 (&xr)[8], Planes& P) {
+  uint32_t mb = 0;
+  float sum = 0.0f;
+#pragma unroll
+  for (int c8 = 0; c8 < 8; ++c8) {
+    const uint32_t wv[4] = {xr[c8].x, xr[c8].y, xr[c8].z, xr[c8].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      mb = max(mb, (wv[i] << 16) & 0x7FFF0000u);
+      mb = max(mb, wv[i] & 0x7FFF0000u);
+      sum += bf16_bits_to_f32(wv[i] & 0xFFFFu) + bf16_bits_to_f32(wv[i] >> 16);
+    }
+  }
+  const int e = block_exponent(mb);
+  const float sc = pow2i(22 - e);
+  P.scale[0] = P.scale[1] = pow2i(e - 22);
+  P.sum = sum;
+#pragma unroll
+  for (int c8 = 0; c8 < 8; ++c8) {
+    const uint32_t wv[4] = {xr[c8].x, xr[c8].y, xr[c8].z, xr[c8].w};
+#pragma unroll
+    for (int o = 0; o < 2; ++o) {
+      int v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = fixed23(bf16_bits_to_f32(o ? (wv[i] >> 16) : (wv[i] & 0xFFFFu)), sc);
+      pack4(v[0], v[1], v[2], v[3], P.p[0][2 * c8 + o], P.p[1][2 * c8 + o], P.p[2][2 * c8 + o]);
+    }
+  }
+  return ((mb >> 23) & 0xFFu) != 0xFFu;
 }
+
+// sum_c q_c v_c over the 64 columns of eight code words c0, c1 (one quantisation group).
+__device__ __forceinline__ float group_dot(const uint4& c0, const uint4& c1, const Planes& P) {
+  const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  int s[2][3] = {{0, 0, 0}, {0, 0, 0}};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t ev = w[j] & 0x0F0F0F0Fu, od = (w[j] >> 4) & 0x0F0F0F0Fu;
+    int* a = s[j >> 2];
+    a[0] = dp4a_us(ev, P.p[0][2 * j], a[0]);
+    a[0] = dp4a_us(od, P.p[0][2 * j + 1], a[0]);
+    a[1] = dp4a_uu(ev, P.p[1][2 * j], a[1]);
+    a[1] = dp4a_uu(od, P.p[1][2 * j + 1], a[1]);
+    a[2] = dp4a_uu(ev, P.p[2][2 * j], a[2]);
+    a[2] = dp4a_uu(od, P.p[2][2 * j + 1], a[2]);
+  }
+  const float t0 = (float)s[0][0] * 65536.0f + (float)s[0][1] * 256.0f + (float)s[0][2];
+  const float t1 = (float)s[1][0] * 65536.0f + (float)s[1][1] * 256.0f + (float)s[1][2];
+  return fmaf(t0, P.scale[0], t1 * P.scale[1]);
+}
+
+// Exchange block of one CTA's 32 h values (their planes, exponent and sum), 32 words.
+constexpr int kHBlockWords = 32;
 
 // CTAs per thread-block cluster (S = F / 32 is a multiple of 4).
 constexpr int kC = 4;
@@ -131,8 +209,8 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t a, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_cluster_f32(uint32_t a, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+__device__ __forceinline__ void st_cluster_u32(uint32_t a, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 
 // ---------------------------------------------------------------- routing of one token
@@ -202,8 +280,44 @@ __device__ __forceinline__ void block_topk(const float* __restrict__ row, int E,
   __syncthreads();
 }
 
+// ---------------------------------------------------------------- weight copies of one CTA
+// Shared by the layer kernel and its loads-only replica, so both move exactly the same bytes.
+
+// Quarter q of the gate and up rows f0 .. f0+31 of expert e (scales and biases with quarter 0).
+// One thread per quarter; the four quarters are issued by four threads at once.
+__device__ __forceinline__ void issue_gate_up(const DecPlan& P, const QPtr& g, const QPtr& u, int e, int f0, int q,
+                                              uint32_t gcodes, uint32_t gsb, uint32_t bar) {
+  const int d = P.d, G = P.G;
+  const uint32_t cb = kRQ * (d / 2), sb = RF * G * 2;
+  const size_t rowb = (size_t)e * P.F + f0;
+  const size_t row0 = rowb + q * kRQ;
+  mbar_arrive_expect_tx(bar, 2 * cb + (q == 0 ? 4 * sb : 0));
+  bulk_g2s(gcodes + (uint32_t)(q * kRQ) * (d / 2), g.codes + row0 * (d / 8), cb, bar);
+  bulk_g2s(gcodes + (uint32_t)(RF + q * kRQ) * (d / 2), u.codes + row0 * (d / 8), cb, bar);
+  if (q == 0) {
+    bulk_g2s(gsb + 0 * sb, g.scales + rowb * G, sb, bar);
+    bulk_g2s(gsb + 1 * sb, g.biases + rowb * G, sb, bar);
+    bulk_g2s(gsb + 2 * sb, u.scales + rowb * G, sb, bar);
+    bulk_g2s(gsb + 3 * sb, u.biases + rowb * G, sb, bar);
+  }
+}
+
+// Down rows r0 .. r0+DR-1 of expert e over the cluster's columns kc0 .. kc0+KC-1 (the 64-byte
+// column block of each row, as 2-D tensor copies of box_rows rows) and their whole scale and bias
+// rows (contiguous).  One thread.
+__device__ __forceinline__ void issue_down(const DecPlan& P, const QPtr& qd, const CUtensorMap* map, int e, int r0,
+                                           int kc0, uint32_t dcodes, uint32_t dsb, uint32_t bar) {
+  const uint32_t rb = P.KC / 2;                 // code bytes per row and cluster
+  const uint32_t sbb = (uint32_t)P.DR * P.GF * 2;
+  const size_t row0 = (size_t)e * P.d + r0;
+  mbar_arrive_expect_tx(bar, (uint32_t)P.DR * rb + 2u * sbb);
+  for (int r = 0; r < P.DR; r += P.box_rows) tma_load_2d(dcodes + r * rb, map, bar, kc0 / 8, (int)(row0 + r));
+  bulk_g2s(dsb, qd.scales + row0 * P.GF, sbb, bar);
+  bulk_g2s(dsb + sbb, qd.biases + row0 * P.GF, sbb, bar);
+}
+
 template <bool kMulti>
-__global__ void __launch_bounds__(kThreadsDec, kMulti ? 1 : 2)
+__global__ void __launch_bounds__(kThreadsDec, 1)
     decode_layer_kernel(const __grid_constant__ DecodeMaps maps, const DecodeArgs a) {
   constexpr int C = kC;
   extern __shared__ __align__(128) uint8_t sm[];
@@ -234,7 +348,8 @@ __global__ void __launch_bounds__(kThreadsDec, kMulti ? 1 : 2)
   __shared__ uint64_t sel[32];
   __shared__ int e_s[kDecodeMaxTokens];
   __shared__ float wgt_s[kDecodeMaxTokens];    // w_j (routed) or the shared-expert gate, per token
-  __shared__ int last_s[8];
+  __shared__ float hloc[RF];   // this CTA's h (rows f0 .. f0+31)
+  __shared__ int vloc[RF];     // ... as 23-bit fixed point
   __shared__ int abort_s;
   const int T = kMulti ? (a.T > 0 ? a.T : 1) : 1;
 
@@ -246,40 +361,12 @@ __global__ void __launch_bounds__(kThreadsDec, kMulti ? 1 : 2)
   __syncthreads();
   cluster_arrive_relaxed();   // this CTA runs: its shared memory may now receive the cluster's h
 
-  // Gate and up rows f0 .. f0+31 of expert e (code words by quarter; scales and biases with the
-  // first quarter).  Lanes 0..3 of one warp, lane q issuing quarter q (lane 0 also the scales and
-  // biases), so the copies leave together.
   auto issue_gu = [&](int e, int q) {
-    const QPtr& g = a.gate[wset];
-    const QPtr& u = a.up[wset];
-    const uint32_t cb = kRQ * (d / 2), sb = RF * G * 2;
-    const size_t rowb = (size_t)e * F + f0;
-    const uint32_t bar = smem_u32(&bars[q]);
-    const size_t row0 = rowb + q * kRQ;
-    mbar_arrive_expect_tx(bar, 2 * cb + (q == 0 ? 4 * sb : 0));
-    bulk_g2s(smem_u32(gcodes + (q * kRQ) * (d / 8)), g.codes + row0 * (d / 8), cb, bar);
-    bulk_g2s(smem_u32(gcodes + (RF + q * kRQ) * (d / 8)), u.codes + row0 * (d / 8), cb, bar);
-    if (q == 0) {
-      bulk_g2s(smem_u32(gsb + 0 * RF * G), g.scales + rowb * G, sb, bar);
-      bulk_g2s(smem_u32(gsb + 1 * RF * G), g.biases + rowb * G, sb, bar);
-      bulk_g2s(smem_u32(gsb + 2 * RF * G), u.scales + rowb * G, sb, bar);
-      bulk_g2s(smem_u32(gsb + 3 * RF * G), u.biases + rowb * G, sb, bar);
-    }
+    issue_gate_up(P, a.gate[wset], a.up[wset], e, f0, q, smem_u32(gcodes), smem_u32(gsb), smem_u32(&bars[q]));
   };
-  // Down rows r0 .. r0+DR-1 of expert e over the cluster's columns (the 64-byte column block of
-  // each row: 2-D tensor copies of box_rows rows) and their whole scale and bias rows
-  // (contiguous).  One thread.
   auto issue_dn = [&](int e) {
-    const QPtr& q = a.down[wset];
-    const uint32_t bar = smem_u32(&bars[kQuarters]);
-    const uint32_t rb = P.KC / 2;                 // code bytes per row and cluster
-    const uint32_t sbb = (uint32_t)P.DR * GF * 2;
-    const size_t row0 = (size_t)e * d + r0;
-    mbar_arrive_expect_tx(bar, (uint32_t)P.DR * rb + 2u * sbb);
-    for (int r = 0; r < P.DR; r += P.box_rows)
-      tma_load_2d(smem_u32(dcodes) + r * rb, &maps.down[wset], bar, kc0 / 8, (int)(row0 + r));
-    bulk_g2s(smem_u32(dsb), q.scales + row0 * GF, sbb, bar);
-    bulk_g2s(smem_u32(dsb + P.DR * GF), q.biases + row0 * GF, sbb, bar);
+    issue_down(P, a.down[wset], &maps.down[wset], e, r0, kc0, smem_u32(dcodes), smem_u32(dsb),
+               smem_u32(&bars[kQuarters]));
   };
 
   // Weights are never written upstream: the shared expert's copies start before the wait.
@@ -365,18 +452,9 @@ __global__ void __launch_bounds__(kThreadsDec, kMulti ? 1 : 2)
 
     // ---- gate/up: warp w computes gate and up of rows q*8 + w (q = 0..3) as slots s = 2q + mat;
     // a reduce-scatter leaves slot s fully summed in lane 4s.
-    float2 xs[32];
-    float xsum = 0.0f;
-#pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) {
-      const uint32_t wv[4] = {xr[c8].x, xr[c8].y, xr[c8].z, xr[c8].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float lo = bf16_bits_to_f32(wv[i] & 0xFFFFu), hi = bf16_bits_to_f32(wv[i] >> 16);
-        xsum += lo + hi;
-        xs[c8 * 4 + i] = make_float2(lo * act_prescale(2 * i), hi * act_prescale(2 * i + 1));
-      }
-    }
+    Planes xp;
+    if (!planes_of_bf16(xr, xp) && active) raise_flag(a.err, kErrNonFinite);
+    const float xsum = xp.sum;
     float v8[8];
 #pragma unroll
     for (int sl = 0; sl < 8; ++sl) v8[sl] = 0.0f;
@@ -391,16 +469,7 @@ __global__ void __launch_bounds__(kThreadsDec, kMulti ? 1 : 2)
           const uint32_t* cw = gcodes + (mat * RF + row) * (d / 8) + lane * 8;
           const uint4 c0 = *reinterpret_cast<const uint4*>(cw);
           const uint4 c1 = *reinterpret_cast<const uint4*>(cw + 4);
-          float2 p0 = make_float2(0.0f, 0.0f), p1 = make_float2(0.0f, 0.0f);
-          p0 = word_dot2(c0.x, xs + 0, p0);
-          p1 = word_dot2(c0.y, xs + 4, p1);
-          p0 = word_dot2(c0.z, xs + 8, p0);
-          p1 = word_dot2(c0.w, xs + 12, p1);
-          p0 = word_dot2(c1.x, xs + 16, p0);
-          p1 = word_dot2(c1.y, xs + 20, p1);
-          p0 = word_dot2(c1.z, xs + 24, p0);
-          p1 = word_dot2(c1.w, xs + 28, p1);
-          const float p = (p0.x + p0.y) + (p1.x + p1.y);
+          const float p = group_dot(c0, c1, xp);
           const float s = bf16_bits_to_f32(gsb[((2 * mat) * RF + row) * G + lane]);
           const float b = bf16_bits_to_f32(gsb[((2 * mat + 1) * RF + row) * G + lane]);
           v = fmaf(s, p, b * xsum);
@@ -424,15 +493,42 @@ __global__ void __launch_bounds__(kThreadsDec, kMulti ? 1 : 2)
       t1 += __shfl_xor_sync(0xFFFFFFFFu, t1, 1);
       const float upv = __shfl_down_sync(0xFFFFFFFFu, t1, 4);   // slot 2q+1 (lane 8q+4) -> lane 8q
       if ((lane & 7) == 0) {
-        // h of row (lane / 8) * 8 + warp, written into every cluster CTA's exchange slot
         const float gv = t1;
-        const float hv = gv / (1.0f + expf(-gv)) * upv;
-        const uint32_t loc = smem_u32(hx + sidx % C * RF + (lane >> 3) * kRQ + warp);
-#pragma unroll 1
-        for (int r = 0; r < C; ++r) st_cluster_f32(cluster_map(loc, (uint32_t)r), hv);
+        hloc[(lane >> 3) * kRQ + warp] = gv / (1.0f + expf(-gv)) * upv;   // h of row (lane / 8) * 8 + warp
       }
     }
-    cluster_arrive_release();   // this CTA's h is in every cluster CTA's slot; its gate/up reads are done
+    __syncthreads();   // the CTA's 32 h values are in hloc; its gate/up reads are done
+    if (warp == 0) {
+      // The 32 h values (columns 32 crank .. + 31 of the cluster) as one planes block, written into
+      // every cluster CTA's exchange slot: lane l holds column l; lanes 0..23 build plane word
+      // lane % 8 of plane lane / 8, lane 24 the exponent, lane 25 the sum.
+      const float hv = hloc[lane];
+      if (!(fabsf(hv) <= 3.402823466e38f)) raise_flag(a.err, kErrNonFinite);
+      const uint32_t mb = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(hv) & 0x7FFFFFFFu);
+      float hs = hv;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) hs += __shfl_xor_sync(0xFFFFFFFFu, hs, off);
+      const int e = block_exponent(mb);
+      vloc[lane] = fixed23(hv, pow2i(22 - e));
+      __syncwarp();
+      uint32_t word = 0;
+      if (lane < 24) {
+        const int pl = lane >> 3, wi = lane & 7, w = wi >> 1, o = wi & 1;
+        uint32_t hi, mid, lo;
+        pack4(vloc[8 * w + o], vloc[8 * w + 2 + o], vloc[8 * w + 4 + o], vloc[8 * w + 6 + o], hi, mid, lo);
+        word = pl == 0 ? hi : pl == 1 ? mid : lo;
+      } else if (lane == 24) {
+        word = __float_as_uint(pow2i(e - 22));
+      } else if (lane == 25) {
+        word = __float_as_uint(hs);
+      }
+      if (lane < 26) {
+        const uint32_t loc = smem_u32(hx + crank * kHBlockWords + lane);
+#pragma unroll
+        for (int r = 0; r < C; ++r) st_cluster_u32(cluster_map(loc, (uint32_t)r), word);
+      }
+    }
+    cluster_arrive_release();   // this CTA's h block is in every cluster CTA's slot
     // The gate/up buffers are free once the whole CTA is past the gate/up reads: the next token's
     // gate/up rows are requested while this token's down share runs.  abort_s is only written
     // inside waits, so every thread of the CTA reads the same value here after the wait below.
@@ -451,14 +547,31 @@ __global__ void __launch_bounds__(kThreadsDec, kMulti ? 1 : 2)
       constexpr int GP = kC * RF / 64;
       constexpr int rpp = 32 / GP;   // rows per warp pass
       const int g = lane % GP;
-      float2 hv[32];
-      float hsum = 0.0f;
+      // group g of the cluster's columns: the h blocks of CTAs 2g (code words 0..3) and 2g + 1 (4..7)
+      Planes hp;
+      {
+        const uint32_t* blk = reinterpret_cast<const uint32_t*>(hx) + 2 * g * kHBlockWords;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float2 h2 = *reinterpret_cast<const float2*>(hx + g * 64 + 2 * i);
-        hsum += h2.x + h2.y;
-        hv[i] = make_float2(h2.x * act_prescale((2 * i) & 7), h2.y * act_prescale((2 * i + 1) & 7));
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t* bh = blk + half * kHBlockWords;
+#pragma unroll
+          for (int pl = 0; pl < 3; ++pl) {
+            const uint4 u0 = *reinterpret_cast<const uint4*>(bh + 8 * pl);
+            const uint4 u1 = *reinterpret_cast<const uint4*>(bh + 8 * pl + 4);
+            hp.p[pl][8 * half + 0] = u0.x;
+            hp.p[pl][8 * half + 1] = u0.y;
+            hp.p[pl][8 * half + 2] = u0.z;
+            hp.p[pl][8 * half + 3] = u0.w;
+            hp.p[pl][8 * half + 4] = u1.x;
+            hp.p[pl][8 * half + 5] = u1.y;
+            hp.p[pl][8 * half + 6] = u1.z;
+            hp.p[pl][8 * half + 7] = u1.w;
+          }
+          hp.scale[half] = __uint_as_float(bh[24]);
+        }
+        hp.sum = __uint_as_float(blk[25]) + __uint_as_float(blk[kHBlockWords + 25]);
       }
+      const float hsum = hp.sum;
       const float wgt = wgt_s[t];
       const int gcol = kc0 / 64 + g;
       float* part_t = a.part + (size_t)t * P.nslices * P.NP * kSliceRows;
@@ -480,16 +593,7 @@ __global__ void __launch_bounds__(kThreadsDec, kMulti ? 1 : 2)
         }
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          float2 p0 = make_float2(0.0f, 0.0f), p1 = make_float2(0.0f, 0.0f);
-          p0 = word_dot2(c[u][0].x, hv + 0, p0);
-          p1 = word_dot2(c[u][0].y, hv + 4, p1);
-          p0 = word_dot2(c[u][0].z, hv + 8, p0);
-          p1 = word_dot2(c[u][0].w, hv + 12, p1);
-          p0 = word_dot2(c[u][1].x, hv + 16, p0);
-          p1 = word_dot2(c[u][1].y, hv + 20, p1);
-          p0 = word_dot2(c[u][1].z, hv + 24, p0);
-          p1 = word_dot2(c[u][1].w, hv + 28, p1);
-          const float pq = (p0.x + p0.y) + (p1.x + p1.y);
+          const float pq = group_dot(c[u][0], c[u][1], hp);
           float v = fmaf(sc[u], pq, bi[u] * hsum);
 #pragma unroll
           for (int off = GP >> 1; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
@@ -506,62 +610,6 @@ __global__ void __launch_bounds__(kThreadsDec, kMulti ? 1 : 2)
       issue_dn(e_s[t + 1]);
     }
 
-    // ---- combine: one arrival per row slice of this CTA; the last of the NP arrivals sums the
-    // slice's partials in slot order.  Arrivals happen even after a timed-out wait, so counters
-    // always return to zero.
-    uint32_t* cnt_t = a.cnt + (size_t)t * P.nslices;
-    if (tid < P.NSC) {
-      const int sl = crank * P.NSC + tid;
-      __threadfence();
-      const uint32_t old = atomicAdd(cnt_t + sl, 1u);
-      last_s[tid] = (old == (uint32_t)(P.NP - 1)) ? 1 : 0;
-      if (old == (uint32_t)(P.NP - 1)) cnt_t[sl] = 0u;
-      __threadfence();
-    }
-    __syncthreads();
-    // Rows of the slices this CTA completed.  Each partial is 128 contiguous floats written whole by
-    // one CTA; 64 threads per slice, a lane pair per four rows, lane 2i+h summing partials
-    // h*NH .. min(NP, (h+1)*NH) - 1 in order as float4s (loads all in flight together), then the
-    // pair adds its two halves, first half first.
-    {
-      const int NH = (P.NP + 1) / 2;
-      const int half = tid & 1;
-      const int row4 = (tid & 63) >> 1;
-      for (int i = tid >> 6; i < P.NSC; i += kThreadsDec / 64) {
-        const int sl = crank * P.NSC + i;
-        const int rows = min(kSliceRows, P.DR - i * kSliceRows);
-        if (!last_s[i]) continue;   // uniform over the lane pair and the warp
-        const float4* pr = reinterpret_cast<const float4*>(a.part + ((size_t)t * P.nslices + sl) * P.NP * kSliceRows) +
-                           row4;
-        const int p_lo = half * NH, p_hi = min(P.NP, p_lo + NH);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        constexpr int kBatch = 18;   // float4 loads in flight per thread
-        for (int c0 = p_lo; c0 < p_hi; c0 += kBatch) {
-          float4 v[kBatch];
-#pragma unroll
-          for (int c = 0; c < kBatch; ++c)
-            v[c] = c0 + c < p_hi ? __ldcg(pr + (size_t)(c0 + c) * (kSliceRows / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int c = 0; c < kBatch; ++c) {
-            if (c0 + c < p_hi) {
-              acc.x += v[c].x;
-              acc.y += v[c].y;
-              acc.z += v[c].z;
-              acc.w += v[c].w;
-            }
-          }
-        }
-        float4 o;
-        o.x = __shfl_xor_sync(0xFFFFFFFFu, acc.x, 1);
-        o.y = __shfl_xor_sync(0xFFFFFFFFu, acc.y, 1);
-        o.z = __shfl_xor_sync(0xFFFFFFFFu, acc.z, 1);
-        o.w = __shfl_xor_sync(0xFFFFFFFFu, acc.w, 1);
-        if (half == 0 && 4 * row4 < rows) {
-          const float4 sum = make_float4(acc.x + o.x, acc.y + o.y, acc.z + o.z, acc.w + o.w);
-          *reinterpret_cast<float4*>(a.y + (size_t)t * d + r0 + i * kSliceRows + 4 * row4) = sum;
-        }
-      }
-    }
   }
 
   // ---- wind down: after a timeout, copies still in flight must land before the CTA exits.
@@ -573,6 +621,90 @@ __global__ void __launch_bounds__(kThreadsDec, kMulti ? 1 : 2)
       }
     }
   }
+}
+
+// Loads-only replica of decode_layer_kernel's weight traffic for one token, a measurement aid
+// (the bandwidth ceiling of this access pattern): same grid, clusters, shared-memory plan,
+// programmatic launch and weight copies, with the experts given instead of routed; it waits for
+// every copy to land and does no arithmetic.
+__global__ void __launch_bounds__(kThreadsDec, 2)
+    decode_stream_kernel(const __grid_constant__ DecodeMaps maps, const StreamArgs a) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  const int k1 = a.k + (a.has_shared ? 1 : 0);
+  const DecPlan P(a.d, a.F, k1, false);
+  const int tid = threadIdx.x;
+  const int cta = blockIdx.x;
+  const int j = cta / P.S;
+  const int sidx = cta % P.S;
+  const int kc0 = (sidx / kC) * P.KC;
+  const int r0 = (sidx % kC) * P.DR;
+  const int f0 = sidx * RF;
+  const bool shared_cta = (j == a.k);
+  const int wset = shared_cta ? 1 : 0;
+  __shared__ __align__(8) uint64_t bars[kQuarters + 1];
+  __shared__ int abort_s;
+  if (tid == 0) {
+    for (int i = 0; i <= kQuarters; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    abort_s = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  auto issue = [&](int e) {
+    if (tid < kQuarters)
+      issue_gate_up(P, a.gate[wset], a.up[wset], e, f0, tid, smem_u32(sm + P.gu_codes), smem_u32(sm + P.gu_sb),
+                    smem_u32(&bars[tid]));
+    if (tid == 32)
+      issue_down(P, a.down[wset], &maps.down[wset], e, r0, kc0, smem_u32(sm + P.dn_codes), smem_u32(sm + P.dn_sb),
+                 smem_u32(&bars[kQuarters]));
+  };
+  if (shared_cta) issue(0);
+  pdl_wait();
+  if (!shared_cta) issue(__ldg(a.idx + j));
+  pdl_launch_dependents();
+  for (int i = 0; i <= kQuarters; ++i) mbar_wait_warp(smem_u32(&bars[i]), 0, &abort_s, a.err);
+  __syncthreads();
+  if (tid == 0 && abort_s) {   // copies still in flight land before the CTA exits
+    for (int i = 0; i <= kQuarters; ++i) {
+      const long long t0 = clock64();
+      while (!mbar_try_wait(smem_u32(&bars[i]), 0) && clock64() - t0 < 4000000ll) {
+      }
+    }
+  }
+}
+
+// y[t][r] = the sum of the NP partials of row r, one warp per four rows (float4), lane l summing
+// partials l, l + 32, ... in order, then a 32-lane butterfly: every lane ends with the same bits,
+// whatever the order in which the decode CTAs finished.  Grid (d / 32, T), 256 threads.
+__global__ void __launch_bounds__(256) decode_reduce_kernel(const ReduceArgs a) {
+  // The next launch on the stream may start its prologue now: a decode launch reads nothing written
+  // here or by the decode launch before its own dependency wait.
+  pdl_launch_dependents();
+  pdl_wait();   // every partial of the decode launch is stored
+  const DecPlan P(a.d, a.F, a.k1, false);
+  const int t = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 32 + warp * 4;
+  if (r >= a.d) return;
+  const int crank = r / P.DR, i = (r % P.DR) / kSliceRows, rr = (r % P.DR) % kSliceRows;
+  const int sl = crank * P.NSC + i;
+  const float4* base =
+      reinterpret_cast<const float4*>(a.part + ((size_t)t * P.nslices + sl) * P.NP * kSliceRows + rr);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int p = lane; p < P.NP; p += 32) {
+    const float4 v = __ldcg(base + (size_t)p * (kSliceRows / 4));
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    acc.x += __shfl_xor_sync(0xFFFFFFFFu, acc.x, off);
+    acc.y += __shfl_xor_sync(0xFFFFFFFFu, acc.y, off);
+    acc.z += __shfl_xor_sync(0xFFFFFFFFu, acc.z, off);
+    acc.w += __shfl_xor_sync(0xFFFFFFFFu, acc.w, off);
+  }
+  if (lane == 0) *reinterpret_cast<float4*>(a.y + (size_t)t * a.d + r) = acc;
 }
 
 constexpr int kMaxDev = 64;
@@ -592,6 +724,9 @@ cudaError_t ensure_attrs() {
         return e;
       if ((e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100)) != cudaSuccess) return e;
     }
+    if ((e = cudaFuncSetAttribute(decode_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kDecSmemMax)) != cudaSuccess)
+      return e;
     g_ready[dev] = true;
   }
   return cudaSuccess;
@@ -604,18 +739,13 @@ size_t decode_scratch_floats(int d, int k, int F) {
   return (size_t)P.nslices * P.NP * kSliceRows;
 }
 
-int decode_counters(int d, int F) {
-  const DecPlan P(d, F, 1, false);
-  return P.nslices;
-}
-
 bool decode_supported(int d, int E, int k, int F) {
   const int k1 = k + 1;
   // One quantisation group per lane in the gate/up rows: d <= 2048 (and d a multiple of 64).
   // F a multiple of 128: 32 gate/up rows per CTA and whole quantisation groups per cluster.
   if (k1 > 32 || E > kMaxE || d > 2048 || d % 64 != 0 || F % 128 != 0) return false;
   const DecPlan P(d, F, k1, true);
-  if (P.bytes > kDecSmemMax || P.nslices > kDecodeMaxSlices || P.NSC > 8) return false;
+  if (P.bytes > kDecSmemMax) return false;
   return true;
 }
 
@@ -698,6 +828,40 @@ cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& a, cudaStrea
   cfg.numAttrs = pdl ? 2 : 1;
   e = a.T > 1 ? cudaLaunchKernelEx(&cfg, decode_layer_kernel<true>, maps, a)
               : cudaLaunchKernelEx(&cfg, decode_layer_kernel<false>, maps, a);
+  if (e != cudaSuccess) return e;
+  // The fixed-order sum of the partials, launched to start as soon as the decode launch allows.
+  ReduceArgs ra{a.part, a.y, a.d, a.F, k1};
+  cudaLaunchConfig_t rc = {};
+  rc.gridDim = dim3((unsigned)((a.d + 31) / 32), (unsigned)(a.T > 0 ? a.T : 1));
+  rc.blockDim = dim3(256);
+  rc.stream = st;
+  rc.attrs = &attr[1];
+  rc.numAttrs = 1;
+  e = cudaLaunchKernelEx(&rc, decode_reduce_kernel, ra);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_stream(const DecodeMaps& maps, const StreamArgs& a, cudaStream_t st) {
+  if (!decode_supported(a.d, a.E, a.k, a.F)) return cudaErrorInvalidConfiguration;
+  cudaError_t e = ensure_attrs();
+  if (e != cudaSuccess) return e;
+  const DecPlan P(a.d, a.F, a.k + (a.has_shared ? 1 : 0), false);
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kC;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(P.grid);
+  cfg.blockDim = dim3(kThreadsDec);
+  cfg.dynamicSmemBytes = P.bytes;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, decode_stream_kernel, maps, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

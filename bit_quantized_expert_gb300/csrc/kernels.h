@@ -108,8 +108,6 @@ struct DecodeArgs {
   int d, E, k, F, has_shared;
   int T;                   // tokens, 1 .. kDecodeMaxTokens (0 reads as 1)
   float* part;             // scratch: fp32 [T][decode_scratch_floats] partial outputs per row slice
-  uint32_t* cnt;           // arrival counters [T][decode_counters]: zero before the first launch;
-                           // every launch leaves them zero
   float* y;                // fp32 [T][d]
   uint32_t* err;
 };
@@ -122,18 +120,28 @@ int decode_box_rows(int d, int F);
 bool decode_supported(int d, int E, int k, int F);
 constexpr int kDecodeMaxTokens = 8;   // tokens one decode launch can take (one routing warp each)
 constexpr int kDecodeLayerMaxT = 8;    // layer calls of up to this many tokens take the decode kernel
-constexpr int kDecodeMaxSlices = 32;   // combine slices (arrival counters) per token, at most
 size_t decode_scratch_floats(int d, int k, int F);   // floats of DecodeArgs::part per token
-int decode_counters(int d, int F);                    // counters of DecodeArgs::cnt per token
+// The decode launch's second kernel: y from the partials (DecodeArgs::part, ::y; k1 expert slots).
+struct ReduceArgs {
+  const float* part;
+  float* y;
+  int d, F, k1;
+};
 cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& a, cudaStream_t st, bool pdl);
+// Loads-only replica of the decode kernel's weight copies for one token whose k experts are given
+// (a measurement aid; see decode_stream_kernel).
+struct StreamArgs {
+  QPtr gate[2], up[2], down[2];
+  const int32_t* idx;      // [k] experts of the token, in slot order
+  int d, E, k, F, has_shared;
+  uint32_t* err;
+};
+cudaError_t launch_decode_stream(const DecodeMaps& maps, const StreamArgs& a, cudaStream_t st);
 // Encodes DecodeMaps::down[i] for n stacked [d, F] down matrices (api.cu); false on failure.
 bool encode_decode_down(CUtensorMap* m, const uint32_t* codes, int n, int d, int F);
 
-// Workspace head shared by the C ABI and the allocation-free entry point: the error word at 0,
-// the decode arrival counters from kCountersOffset (kDecodeMaxTokens * kDecodeMaxSlices words).
-constexpr size_t kWsHeadBytes = 2048;
-constexpr size_t kCountersOffset = 1024;
-static_assert(kCountersOffset + 4 * kDecodeMaxTokens * kDecodeMaxSlices <= kWsHeadBytes, "head holds the counters");
+// Workspace head shared by the C ABI and the allocation-free entry point: the error word at 0.
+constexpr size_t kWsHeadBytes = 256;
 
 // Host-side dims rules of every layer call (api.cu); MOE_OK = 0.
 int check_layer_dims(int T, int d, int E, int k, int F, int F_shared);

@@ -6,8 +6,8 @@
 // latency-critical decode loop that must never enter cudaMalloc or cudaFree, which may
 // synchronise the whole device; or a host program that only holds pointers to weights, inputs
 // and outputs and has no allocator of its own.  moe_layer_forward_decode_noalloc serves them: the
-// only scratch it needs (an error word, the decode kernel's arrival counters and its partial
-// outputs per row slice) lives in the file-scope device array below, which every GPU that loads
+// only scratch it needs (an error word and the decode kernel's partial outputs per row slice)
+// lives in the file-scope device array below, which every GPU that loads
 // this library holds until the process exits.
 #include <mutex>
 
@@ -17,8 +17,8 @@
 namespace moe {
 namespace {
 
-// The first kWsHeadBytes hold the error word and the decode arrival counters, laid out as in a
-// workspace; then the decode kernel's partial outputs of one token (decode_scratch_floats).
+// The first kWsHeadBytes hold the error word, as in a workspace; then the decode kernel's partial
+// outputs of one token (decode_scratch_floats).
 constexpr int kNoAllocHeadFloats = (int)(kWsHeadBytes / 4);
 constexpr size_t kNoAllocMaxPart = 131072;   // upper bound on the partial outputs: 512 KB
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocHeadFloats + kNoAllocMaxPart];
@@ -93,10 +93,9 @@ extern "C" moe_status moe_layer_forward_decode_noalloc(const moe_dims* dims, con
   if (scratch_for_current_device(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* err = reinterpret_cast<uint32_t*>(scratch);
-  // The array keeps the previous call's contents: the error word and the arrival counters start
-  // every call at zero.  Every partial is written before its counter arrival and read only by the
-  // last arrival of its slice.
-  if (cudaMemsetAsync(err, 0, kWsHeadBytes, st) != cudaSuccess) return MOE_ERR_CUDA;
+  // The array keeps the previous call's contents: the error word starts every call at zero.  Every
+  // partial is written by the decode kernel before the reduce kernel of the same call reads it.
+  if (cudaMemsetAsync(err, 0, 4, st) != cudaSuccess) return MOE_ERR_CUDA;
 
   DecodeArgs da{};
   da.x = x;
@@ -119,7 +118,6 @@ extern "C" moe_status moe_layer_forward_decode_noalloc(const moe_dims* dims, con
   da.part = scratch + kNoAllocHeadFloats;
   da.y = y;
   da.err = err;
-  da.cnt = reinterpret_cast<uint32_t*>(scratch) + kCountersOffset / 4;
   DecodeMaps dmaps{};
   if (!encode_decode_down(&dmaps.down[0], routed->down.codes, dims->E, dims->d, dims->F) ||
       !encode_decode_down(&dmaps.down[1], sh ? shared->down.codes : routed->down.codes, sh ? 1 : dims->E, dims->d,

@@ -1,4 +1,4 @@
-"""The C-ABI library: it loads, exports every symbol include/moe.h declares, and its host-side
+"""The C-ABI library: it loads, exports every symbol the headers in include/ declare, and its host-side
 argument checks and size queries behave as documented.  No kernel runs here (no GPU needed):
 every call below returns from the host checks before any CUDA work is enqueued."""
 import ctypes
@@ -13,9 +13,13 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _declared():
-    with open(os.path.join(ROOT, "include", "moe.h")) as f:
-        src = f.read()
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\*\s]+?\b(moe_\w+)\s*\(", src, re.M)))
+    names = set()
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            with open(os.path.join(ROOT, "include", h)) as f:
+                src = f.read()
+            names |= set(re.findall(r"^\s*(?:const\s+)?[\w\*\s]+?\b(moe_\w+)\s*\(", src, re.M))
+    return sorted(names)
 
 
 @pytest.fixture(scope="module")

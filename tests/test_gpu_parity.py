@@ -572,3 +572,23 @@ def test_stack_full_size_sampled_tokens():
     for l in range(depth):
         assert np.array_equal(np.sort(picks[l][rows], axis=1), np.sort(ref_picks[l], axis=1)), l
     assert rowwise_err(full[depth][rows], ref) <= EXACT_TOL
+
+
+def test_decode_stream_probe_moves_the_decode_weights_cleanly():
+    """The loads-only replica of the decode launch (a measurement aid) runs on the experts the
+    routing picks, lands every copy (no timeout flag) and refuses shapes the decode kernel does not
+    take."""
+    wl = synth.DECODE
+    host, dl = layer_for(wl)
+    inp = synth.make_inputs(wl, seed=3)
+    dm = moe.dims(1, wl.d, wl.E, wl.k, wl.F, wl.F_shared)
+    ws = moe.alloc_workspace(dm)
+    r = moe.alloc_routing(dm, 112)
+    moe.route(dm, dev(inp["logits"]), r, ws)
+    for _ in range(3):
+        moe.decode_stream_probe(dm, r["idx"][0], dl["routed"], dl["shared"], ws)
+    assert moe.read_error_flags(ws) == 0
+    with pytest.raises(moe.MoeError) as ei:
+        moe.decode_stream_probe(moe.dims(2, wl.d, wl.E, wl.k, wl.F, wl.F_shared), r["idx"][0], dl["routed"],
+                                dl["shared"], ws)
+    assert ei.value.status == 2
