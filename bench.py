@@ -258,12 +258,12 @@ def decode_bench(args, world, rank, local, device, pk):
     tokens = LAYERS * args.steps * world
     res = {
         "value": tokens / (ms_max / 1e3), "ms_per_step": ms_max / args.steps, "clocks": ck, "flags": flags,
-        "roofline": {"kernel": "decode_layer_kernel (one clustered launch per layer call)",
+        "roofline": {"kernel": "decode_layer_kernel + decode_reduce_kernel (the two launches of a layer call)",
                      "bound": "hbm", "achieved": per_step_bytes / step_s / 1e9, "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": per_step_bytes / step_s / 1e9 / pk["hbm_gbs"],
                      "traffic": DECODE_NCU_TRAFFIC,
                      "algorithmic_bytes_per_launch": per_call, "peak_source": pk["source"]},
-        "gpu_launches": LAYERS * args.steps,   # one decode_layer_kernel per layer call
+        "gpu_launches": 2 * LAYERS * args.steps,   # decode_layer_kernel and decode_reduce_kernel per layer call
     }
 
     # Hot-L2 single-layer figure (labelled as such, not the headline): one weight set, replayed,
@@ -513,9 +513,10 @@ def stack_bench(wl, steps, device, pk):
     log(f"{wl.name}: {ms / steps * 1e3:.1f} us per step")
     flags = moe.read_error_flags(ws)
     step_s = ms / 1e3 / steps
-    # every expert is touched at T = 2048; per layer also the router weights, the fp32 residual
-    # (read and written), h (bf16) and the logits
-    per_layer = layer_bytes(wl, wl.T, wl.E) + wl.E * wl.d * 2 + wl.T * wl.d * (4 + 4 + 2) + wl.T * wl.E * 4
+    # Every expert is touched at T = 2048.  Per layer: the layer's own algorithmic bytes (weights, its
+    # input h, the logits, y) and the router weights.  The fp32 residual update and the writes of h and
+    # the logits between layers are implementation overhead, not counted.
+    per_layer = layer_bytes(wl, wl.T, wl.E) + wl.E * wl.d * 2
     flops = LAYERS * (layer_flops(wl, wl.T) + 2 * wl.T * wl.d * wl.E)
     out = {"workload": wl.name, "value": wl.T / step_s, "unit": "tokens/s (through 40 layers)",
            "ms_per_step": ms / steps, "steps": steps, "weight_sets": LAYERS, "flags": flags,

@@ -243,6 +243,40 @@ __device__ __forceinline__ int cand_expert(uint64_t c) { return (int)(0xFFFFFFFF
 // (broadcast reads of the warp's keys from shared memory) and keeps its k best in `cand`
 // [kWarpsDec][k]; then the first 8 k threads rank those against each other and the k best land in
 // sel[0..k-1] in descending order.  `keys` holds kThreadsDec * NE entries.  Two block barriers.
+// The same for E <= 256 and k <= 8 with every loop unrolled: thread t holds expert t; it ranks its
+// key against its warp's 32 (16-byte broadcast reads), the warp's k best land in cand [8][8]
+// (rank order, zero padded); then threads 0..63 rank those 64 against each other and the k best
+// land in sel.  keys holds kThreadsDec entries.  Two block barriers.
+__device__ __forceinline__ void block_topk_small(const float* __restrict__ row, int E, int k, uint64_t* keys,
+                                                 uint64_t* cand, uint64_t* sel) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint64_t key = tid < E ? cand_key(__ldg(row + tid), tid) : 0ull;
+  keys[tid] = key;
+  if (lane < 8) cand[warp * 8 + lane] = 0ull;
+  __syncwarp();
+  const ulonglong2* wk = reinterpret_cast<const ulonglong2*>(keys + warp * 32);
+  int rank = 0;
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const ulonglong2 o = wk[c];
+    rank += (o.x > key ? 1 : 0) + (o.y > key ? 1 : 0);
+  }
+  if (key != 0ull && rank < k) cand[warp * 8 + rank] = key;
+  __syncthreads();
+  if (tid < kWarpsDec * 8) {
+    const uint64_t mine = cand[tid];
+    const ulonglong2* ck = reinterpret_cast<const ulonglong2*>(cand);
+    int r = 0;
+#pragma unroll
+    for (int c = 0; c < kWarpsDec * 4; ++c) {
+      const ulonglong2 o = ck[c];
+      r += (o.x > mine ? 1 : 0) + (o.y > mine ? 1 : 0);
+    }
+    if (mine != 0ull && r < k) sel[r] = mine;
+  }
+  __syncthreads();
+}
+
 template <int NE>
 __device__ __forceinline__ void block_topk(const float* __restrict__ row, int E, int k, uint64_t* keys,
                                            uint64_t* cand, uint64_t* sel) {
@@ -283,37 +317,56 @@ __device__ __forceinline__ void block_topk(const float* __restrict__ row, int E,
 // ---------------------------------------------------------------- weight copies of one CTA
 // Shared by the layer kernel and its loads-only replica, so both move exactly the same bytes.
 
-// Quarter q of the gate and up rows f0 .. f0+31 of expert e (scales and biases with quarter 0).
-// One thread per quarter; the four quarters are issued by four threads at once.
-__device__ __forceinline__ void issue_gate_up(const DecPlan& P, const QPtr& g, const QPtr& u, int e, int f0, int q,
-                                              uint32_t gcodes, uint32_t gsb, uint32_t bar) {
+// The weight copies of expert e for one CTA, issued by one warp, one copy per lane (an issuing
+// thread waits for the copy engine to take each request, so sixteen lanes get sixteen requests out
+// in the time of one), in the order the compute needs them: lane 0 first arms every barrier with
+// its byte count; then lanes 0, 1 copy the gate and up code rows of quarter 0, lanes 2..5 the
+// gate/up scales and biases (with quarter 0), lanes 6..11 the gate (even lane) and up (odd) code
+// rows of quarters 1..3, lanes 12..13 the down code boxes (the cluster's 64-byte column block of
+// box_rows rows each, by 2-D tensor copy) and lanes 14..15 the down scale and bias rows.
+// `which` selects groups of copies: 1 = quarter 0 with the gate/up scales and biases, 4 = quarters
+// 1..3, 2 = down (5 = all gate/up, 7 = everything).  bars: shared address of the five barriers
+// (gate/up quarters, then down), 8 bytes apart.
+__device__ __forceinline__ void issue_copies(const DecPlan& P, const QPtr& g, const QPtr& u, const QPtr& dn,
+                                             const CUtensorMap* map, int e, int f0, int r0, int kc0, uint32_t gcodes,
+                                             uint32_t gsb, uint32_t dcodes, uint32_t dsb, uint32_t bars, int which,
+                                             int lane) {
   const int d = P.d, G = P.G;
-  const uint32_t cb = kRQ * (d / 2), sb = RF * G * 2;
+  const uint32_t cb = kRQ * (d / 2), sb = RF * G * 2;    // code bytes per quarter and matrix; s/b bytes
+  const uint32_t rb = P.KC / 2, sbb = (uint32_t)P.DR * P.GF * 2;
   const size_t rowb = (size_t)e * P.F + f0;
-  const size_t row0 = rowb + q * kRQ;
-  mbar_arrive_expect_tx(bar, 2 * cb + (q == 0 ? 4 * sb : 0));
-  bulk_g2s(gcodes + (uint32_t)(q * kRQ) * (d / 2), g.codes + row0 * (d / 8), cb, bar);
-  bulk_g2s(gcodes + (uint32_t)(RF + q * kRQ) * (d / 2), u.codes + row0 * (d / 8), cb, bar);
-  if (q == 0) {
-    bulk_g2s(gsb + 0 * sb, g.scales + rowb * G, sb, bar);
-    bulk_g2s(gsb + 1 * sb, g.biases + rowb * G, sb, bar);
-    bulk_g2s(gsb + 2 * sb, u.scales + rowb * G, sb, bar);
-    bulk_g2s(gsb + 3 * sb, u.biases + rowb * G, sb, bar);
+  const size_t drow0 = (size_t)e * d + r0;
+  if (lane == 0) {
+    if (which & 1) mbar_arrive_expect_tx(bars, 2 * cb + 4 * sb);
+    if (which & 4)
+      for (int q = 1; q < kQuarters; ++q) mbar_arrive_expect_tx(bars + 8 * q, 2 * cb);
+    if (which & 2) mbar_arrive_expect_tx(bars + 8 * kQuarters, (uint32_t)P.DR * rb + 2u * sbb);
   }
-}
-
-// Down rows r0 .. r0+DR-1 of expert e over the cluster's columns kc0 .. kc0+KC-1 (the 64-byte
-// column block of each row, as 2-D tensor copies of box_rows rows) and their whole scale and bias
-// rows (contiguous).  One thread.
-__device__ __forceinline__ void issue_down(const DecPlan& P, const QPtr& qd, const CUtensorMap* map, int e, int r0,
-                                           int kc0, uint32_t dcodes, uint32_t dsb, uint32_t bar) {
-  const uint32_t rb = P.KC / 2;                 // code bytes per row and cluster
-  const uint32_t sbb = (uint32_t)P.DR * P.GF * 2;
-  const size_t row0 = (size_t)e * P.d + r0;
-  mbar_arrive_expect_tx(bar, (uint32_t)P.DR * rb + 2u * sbb);
-  for (int r = 0; r < P.DR; r += P.box_rows) tma_load_2d(dcodes + r * rb, map, bar, kc0 / 8, (int)(row0 + r));
-  bulk_g2s(dsb, qd.scales + row0 * P.GF, sbb, bar);
-  bulk_g2s(dsb + sbb, qd.biases + row0 * P.GF, sbb, bar);
+  __syncwarp();
+  // Each lane's role depends on the lane alone; `which` only switches roles off.
+  if (lane < 12) {
+    if (which & (lane < 6 ? 1 : 4)) {
+      if (lane >= 2 && lane < 6) {
+        const int i = lane - 2;
+        const uint16_t* src = i == 0 ? g.scales : i == 1 ? g.biases : i == 2 ? u.scales : u.biases;
+        bulk_g2s(gsb + i * sb, src + rowb * G, sb, bars);
+      } else {
+        const int c = lane < 2 ? lane : lane - 4;   // code copy 0..7: quarter c / 2, gate (even) or up (odd)
+        const int q = c >> 1, mat = c & 1;
+        const QPtr& m = mat ? u : g;
+        bulk_g2s(gcodes + (uint32_t)(mat * RF + q * kRQ) * (d / 2), m.codes + (rowb + q * kRQ) * (d / 8), cb,
+                 bars + 8 * q);
+      }
+    }
+  } else if (lane < 14) {
+    const int r = (lane - 12) * P.box_rows;   // 0 or box_rows
+    if ((which & 2) && r < P.DR) tma_load_2d(dcodes + r * rb, map, bars + 8 * kQuarters, kc0 / 8, (int)(drow0 + r));
+  } else if (lane < 16) {
+    if (which & 2) {
+      const uint16_t* src = lane == 14 ? dn.scales : dn.biases;
+      bulk_g2s(dsb + (lane - 14) * sbb, src + drow0 * P.GF, sbb, bars + 8 * kQuarters);
+    }
+  }
 }
 
 template <bool kMulti>
@@ -361,28 +414,25 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
   __syncthreads();
   cluster_arrive_relaxed();   // this CTA runs: its shared memory may now receive the cluster's h
 
-  auto issue_gu = [&](int e, int q) {
-    issue_gate_up(P, a.gate[wset], a.up[wset], e, f0, q, smem_u32(gcodes), smem_u32(gsb), smem_u32(&bars[q]));
-  };
-  auto issue_dn = [&](int e) {
-    issue_down(P, a.down[wset], &maps.down[wset], e, r0, kc0, smem_u32(dcodes), smem_u32(dsb),
-               smem_u32(&bars[kQuarters]));
+  // expert e's copies (which: 1 gate/up, 2 down, 3 both), by the calling warp
+  auto issue = [&](int e, int which) {
+    issue_copies(P, a.gate[wset], a.up[wset], a.down[wset], &maps.down[wset], e, f0, r0, kc0, smem_u32(gcodes),
+                 smem_u32(gsb), smem_u32(dcodes), smem_u32(dsb), smem_u32(&bars[0]), which, lane);
   };
 
   // Weights are never written upstream: the shared expert's copies start before the wait.
-  if (shared_cta && tid < kQuarters) issue_gu(0, tid);
-  if (shared_cta && tid == 32) issue_dn(0);
+  if (shared_cta && warp == 0) issue(0, 7);
   if (tid == 32) prefetch_tmap(&maps.down[wset]);
   pdl_wait();   // x and logits from upstream kernels are complete and visible past this point
 
   if (!kMulti) {
     if (!shared_cta) {
-      if (a.E <= kThreadsDec) block_topk<1>(a.logits, a.E, k, keys_s, cand, sel);
+      if (a.E <= kThreadsDec && k <= 8) block_topk_small(a.logits, a.E, k, keys_s, cand, sel);
+      else if (a.E <= kThreadsDec) block_topk<1>(a.logits, a.E, k, keys_s, cand, sel);
       else block_topk<kMaxE / kThreadsDec>(a.logits, a.E, k, keys_s, cand, sel);
       const int ej = cand_expert(sel[j]);
-      if (tid < kQuarters) issue_gu(ej, tid);
+      if (warp == 0) issue(ej, 1);   // quarter 0 first; the rest after this warp's x planes (below)
       if (tid == 0) e_s[0] = ej;
-      if (tid == 32) issue_dn(ej);
       if (warp == 2) {
         const float v = lane < k ? key_logit((uint32_t)(sel[lane] >> 32)) : 0.0f;
         const float w = softmax_tail(v, key_logit((uint32_t)(sel[0] >> 32)), k, lane);
@@ -401,7 +451,7 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
       e_s[warp] = ej;
       wgt_s[warp] = wj;
     }
-    if (warp == 0 && lane < kQuarters) issue_gu(ej, lane);
+    if (warp == 0) issue(ej, 7);
   }
   if (shared_cta) {
     // warp w: the shared-expert gates of tokens w, w + 8, ...
@@ -428,7 +478,6 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
   }
   pdl_launch_dependents();
   __syncthreads();   // e_s and wgt_s
-  if (kMulti && !shared_cta && tid == 32) issue_dn(e_s[0]);
   cluster_wait_acquire();   // every CTA of the cluster runs (pairs with the arrive above)
 
   // Tokens one after another.  The slot's weights stay in shared memory while the slot's expert
@@ -454,6 +503,9 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
     // a reduce-scatter leaves slot s fully summed in lane 4s.
     Planes xp;
     if (!planes_of_bf16(xr, xp) && active) raise_flag(a.err, kErrNonFinite);
+    // One token: the second wave of copies (quarters 1..3 and the down rows) leaves after every
+    // CTA's quarter-0 requests are queued, so each CTA's first quarter lands sooner.
+    if (!kMulti && !shared_cta && warp == 0) issue(e_t, 6);
     const float xsum = xp.sum;
     float v8[8];
 #pragma unroll
@@ -533,9 +585,9 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
     // gate/up rows are requested while this token's down share runs.  abort_s is only written
     // inside waits, so every thread of the CTA reads the same value here after the wait below.
     cluster_wait_acquire();     // every CTA's h has arrived
-    if (kMulti && tid < kQuarters && t + 1 < T && e_s[t + 1] != e_t && !abort_s) {
+    if (kMulti && warp == 0 && t + 1 < T && e_s[t + 1] != e_t && !abort_s) {
       fence_proxy_async_smem();   // this token's generic reads of the gate/up buffers come first
-      issue_gu(e_s[t + 1], tid);
+      issue(e_s[t + 1], 5);
     }
 
     // ---- down share: rows r0 .. r0+DR-1 over the cluster's columns kc0 .. kc0+KC-1.  GP lanes per
@@ -605,9 +657,9 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
       }
     }
     __syncthreads();   // this token's partials are stored; the down buffers are free
-    if (kMulti && tid == 32 && t + 1 < T && e_s[t + 1] != e_t && !abort_s) {
+    if (kMulti && warp == 0 && t + 1 < T && e_s[t + 1] != e_t && !abort_s) {
       fence_proxy_async_smem();   // this token's generic reads of the down buffers come first
-      issue_dn(e_s[t + 1]);
+      issue(e_s[t + 1], 2);
     }
 
   }
@@ -650,16 +702,13 @@ __global__ void __launch_bounds__(kThreadsDec, 2)
   }
   __syncthreads();
   auto issue = [&](int e) {
-    if (tid < kQuarters)
-      issue_gate_up(P, a.gate[wset], a.up[wset], e, f0, tid, smem_u32(sm + P.gu_codes), smem_u32(sm + P.gu_sb),
-                    smem_u32(&bars[tid]));
-    if (tid == 32)
-      issue_down(P, a.down[wset], &maps.down[wset], e, r0, kc0, smem_u32(sm + P.dn_codes), smem_u32(sm + P.dn_sb),
-                 smem_u32(&bars[kQuarters]));
+    issue_copies(P, a.gate[wset], a.up[wset], a.down[wset], &maps.down[wset], e, f0, r0, kc0,
+                 smem_u32(sm + P.gu_codes), smem_u32(sm + P.gu_sb), smem_u32(sm + P.dn_codes),
+                 smem_u32(sm + P.dn_sb), smem_u32(&bars[0]), 7, tid & 31);
   };
-  if (shared_cta) issue(0);
+  if (shared_cta && tid < 32) issue(0);
   pdl_wait();
-  if (!shared_cta) issue(__ldg(a.idx + j));
+  if (!shared_cta && tid < 32) issue(__ldg(a.idx + j));   // the same two waves as the layer kernel, back to back
   pdl_launch_dependents();
   for (int i = 0; i <= kQuarters; ++i) mbar_wait_warp(smem_u32(&bars[i]), 0, &abort_s, a.err);
   __syncthreads();
@@ -673,7 +722,7 @@ __global__ void __launch_bounds__(kThreadsDec, 2)
 }
 
 // y[t][r] = the sum of the NP partials of row r, one warp per four rows (float4), lane l summing
-// partials l, l + 32, ... in order, then a 32-lane butterfly: every lane ends with the same bits,
+// partials l, l + 32, ... in order (the first two loads in flight together), then a 32-lane butterfly: every lane ends with the same bits,
 // whatever the order in which the decode CTAs finished.  Grid (d / 32, T), 256 threads.
 __global__ void __launch_bounds__(256) decode_reduce_kernel(const ReduceArgs a) {
   // The next launch on the stream may start its prologue now: a decode launch reads nothing written
@@ -689,8 +738,11 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const ReduceArgs a) 
   const int sl = crank * P.NSC + i;
   const float4* base =
       reinterpret_cast<const float4*>(a.part + ((size_t)t * P.nslices + sl) * P.NP * kSliceRows + rr);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int p = lane; p < P.NP; p += 32) {
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 v0 = lane < P.NP ? __ldcg(base + (size_t)lane * (kSliceRows / 4)) : z;
+  const float4 v1 = lane + 32 < P.NP ? __ldcg(base + (size_t)(lane + 32) * (kSliceRows / 4)) : z;
+  float4 acc = make_float4(v0.x + v1.x, v0.y + v1.y, v0.z + v1.z, v0.w + v1.w);
+  for (int p = lane + 64; p < P.NP; p += 32) {
     const float4 v = __ldcg(base + (size_t)p * (kSliceRows / 4));
     acc.x += v.x;
     acc.y += v.y;
