@@ -1,14 +1,15 @@
 """CUDA path vs the CPU oracle, through the C ABI, on seeded inputs of every workload shape.
 
-Bars (written here, derived in the design doc):
+Bars:
   * routing tables (idx, counts, offsets, perm, inv, block map): bit-exact;
   * routing weights: relative error <= 1e-6 (fp32 expf vs float64);
-  * layer outputs: max over tokens of ||y_t - r_t|| / ||r_t|| <= 2e-3 against the exact oracle,
-    and <= 5e-4 against the oracle with fp16 GEMM operands (the rounding the tensor-core path
-    applies).  The second bar is one fp16 ulp of h (2^-11 relative): the kernel rounds h to fp16
-    from an fp32 value and the oracle from a float64 one, so elements of h that sit near a
-    rounding boundary may land one ulp apart; everything else left is accumulation order;
-  * the decode (T = 1) path computes in fp32 throughout: <= 2e-5 against the exact oracle.
+  * layer outputs: max over tokens of ||y_t - r_t|| / ||r_t|| <= 2e-3 against the exact oracle;
+  * the same against the oracle with fp16 GEMM operands and fp16 expert outputs (the roundings the
+    tensor-core path applies): <= 6e-4.  Measured on one GB300 over 5,248 rows of the tiny, prefill
+    and skewed workloads (11 seeded inputs): maximum 4.3e-4, 99th percentile 2.4e-4, median 1e-4
+    (fp32 accumulation moves a fraction of the fp16 roundings of h and of the expert outputs one
+    unit from the float64 oracle's); the bar is that maximum with 40 % headroom;
+  * the decode (T <= 8) path computes in fp32 and exact integers: <= 2e-5 against the exact oracle.
 """
 import numpy as np
 import pytest
@@ -21,7 +22,7 @@ from oracle import moe_oracle as O
 pytestmark = pytest.mark.gpu
 
 EXACT_TOL = 2e-3
-EMUL_TOL = 5e-4
+EMUL_TOL = 6e-4
 DECODE_TOL = 2e-5
 DECODE_MAX_T = 8   # layer calls of up to this many tokens take the fp32 decode kernel
 
@@ -472,59 +473,45 @@ def test_rmsnorm_router(T, d, E):
     assert rowwise_err(lgn, ref_lg.astype(np.float64)) <= 1e-5
 
 
-def test_stack_of_layers_tiny():
-    wl = synth.Workload("stack_tiny", T=64, d=256, E=16, k=2, F=128, F_shared=128)
-    L = 6
-    hosts = [synth.make_layer(wl, seed=l) for l in range(L)]
-    routers = [synth.make_router(wl, seed=l) for l in range(L)]
-    dls = [moe.to_device_layer(hh) for hh in hosts]
-    rng = np.random.default_rng(5)
-    x0 = rng.standard_normal((wl.T, wl.d)).astype(np.float32)
-    dm = moe.dims(wl.T, wl.d, wl.E, wl.k, wl.F, wl.F_shared)
-    ws = moe.alloc_workspace(dm)
-    x = dev(x0)
-    h = torch.empty((wl.T, wl.d), dtype=torch.int16, device="cuda")
-    lg = torch.empty((wl.T, wl.E), dtype=torch.float32, device="cuda")
-    y = torch.zeros((wl.T, wl.d), dtype=torch.float32, device="cuda")
-    picks = []
-    for l in range(L):
-        moe.rmsnorm_router(dm, x, y if l > 0 else None, dev(routers[l]["gamma"]), dev(routers[l]["w_router"]),
-                           1e-6, h, lg, ws)
-        r = moe.alloc_routing(dm, 112)
-        moe.layer_forward(dm, h, lg, dls[l]["routed"], dls[l]["shared"], dls[l]["w_sg"], y, ws, routing=r)
-        picks.append(r["idx"].cpu().numpy())
-    xf = x.cpu().numpy().astype(np.float64) + y.cpu().numpy()
-    assert moe.read_error_flags(ws) == 0
-    # Six layers compound the per-layer fp16-operand rounding (about 2e-4 of each layer's output),
-    # so the stack is compared with the oracle that applies the same operand rounding; what is
-    # left is accumulation order and one-ulp rounding flips of h (bf16 after the norm, fp16 after
-    # SwiGLU), which checks the composition: residual add, norm, router, layer.
-    ref, ref_picks = O.stack_tokens(x0, hosts, routers, wl.k, operands="fp16", out16=True)
-    same = np.ones(wl.T, bool)
-    for l in range(L):
-        same &= np.all(np.sort(picks[l], axis=1) == np.sort(ref_picks[l], axis=1), axis=1)
-    assert same.mean() >= 0.95, same.mean()      # expert-set flips need a near-tie at the k-th logit
-    assert rowwise_err(xf[same], ref[same]) <= EXACT_TOL
+class _DeviceStack:
+    """Expert-indexed view of a device tensor [n, ...] for the oracle: [e] copies that expert's slab
+    to the host (cached), so a 455 MB layer never has to be copied whole."""
+
+    def __init__(self, t, dtype):
+        self.t, self.dtype, self.cache = t, dtype, {}
+
+    def __getitem__(self, e):
+        e = int(e)
+        if e not in self.cache:
+            self.cache[e] = self.t[e].cpu().numpy().view(self.dtype)
+        return self.cache[e]
 
 
-def _host_layer(t):
-    """A device layer drawn by synth.torch_make_layer, as the numpy nesting the oracle reads."""
-    def q(m):
-        return {"codes": m["codes"].cpu().numpy().view(np.uint32), "scales": m["scales"].cpu().numpy().view(np.uint16),
-                "biases": m["biases"].cpu().numpy().view(np.uint16)}
-
+def _lazy_host_layer(t):
+    """A device layer drawn by synth.torch_make_layer, seen by the oracle one expert at a time."""
     def ex(e):
-        return {name: q(e[name]) for name in ("gate", "up", "down")}
+        return {name: {"codes": _DeviceStack(e[name]["codes"], np.uint32),
+                       "scales": _DeviceStack(e[name]["scales"], np.uint16),
+                       "biases": _DeviceStack(e[name]["biases"], np.uint16)} for name in ("gate", "up", "down")}
 
     return {"routed": ex(t["routed"]), "shared": ex(t["shared"]) if t["shared"] is not None else None,
             "w_sg": t["w_sg"].cpu().numpy().view(np.uint16)}
 
 
-def _run_stack(x0, dls, routers, wl, record):
-    """The stack as the benchmark launches it: per layer the pre-norm block (residual add,
-    RMSNorm, router GEMM) and the layer call on one workspace.  Returns the residual rows after
-    the layers in `record` (the last layer's y added) and each layer's expert picks."""
+def _stack_teacher_forced(x0, dls, routers, wl, rows, host_layer_of, emulate_every=1):
+    """Runs the stack as the benchmark launches it (per layer: pre-norm block through
+    moe_rmsnorm_router, then moe_layer_forward, one workspace) and checks every layer on the
+    sampled rows against the oracle fed the GPU's own layer inputs (teacher forcing):
+      * residual: x_l = x_{l-1} + y_{l-1} in fp32, bit for bit;
+      * norm: h_l within one bf16 ulp of RMSNorm(x_l) (fp32 vs float64 before the rounding);
+      * router: logits_l within 1e-5 (row-normwise) of h_l W_r^T on the GPU's h_l;
+      * routing: the layer's top-k equals the oracle's on the GPU's logits_l, bit for bit;
+      * layer: y_l within EXACT_TOL of the exact oracle -- every sampled token, every layer -- and
+        within EMUL_TOL of the fp16-operand oracle on every `emulate_every`-th layer and the last,
+        both on the GPU's h_l and logits_l.
+    Returns the largest exact and emulated errors seen."""
     T = x0.shape[0]
+    k = wl.k
     dm = moe.dims(T, wl.d, wl.E, wl.k, wl.F, wl.F_shared)
     ws = moe.alloc_workspace(dm)
     x = x0.clone()
@@ -532,46 +519,96 @@ def _run_stack(x0, dls, routers, wl, record):
     lg = torch.empty((T, wl.E), dtype=torch.float32, device="cuda")
     y = torch.empty((T, wl.d), dtype=torch.float32, device="cuda")
     r = moe.alloc_routing(dm, 112)
-    out, picks = {}, []
+    ri = torch.as_tensor(rows, device="cuda")
+    prev = None
+    worst = {"exact": 0.0, "emul": 0.0}
     for l in range(len(dls)):
         moe.rmsnorm_router(dm, x, y if l > 0 else None, dev(routers[l]["gamma"]), dev(routers[l]["w_router"]), 1e-6,
                            h, lg, ws)
         moe.layer_forward(dm, h, lg, dls[l]["routed"], dls[l]["shared"], dls[l]["w_sg"], y, ws, routing=r)
-        picks.append(r["idx"].cpu().numpy())
+        xs = x[ri].cpu().numpy()
+        hs = h[ri].cpu().numpy().view(np.uint16)
+        ls = lg[ri].cpu().numpy()
+        ys = y[ri].cpu().numpy()
+        idx = r["idx"][ri].cpu().numpy()
+        assert moe.read_error_flags(ws) == 0, l
+        if prev is not None:
+            assert np.array_equal(xs, prev[0] + prev[1]), l
+        prev = (xs, ys)
+        _, hbits = O.rmsnorm_bf16(xs.astype(np.float64), routers[l]["gamma"], 1e-6)
+        assert _bf16_ulps(hs, hbits).max() <= 1, l
+        ref_lg = O.router_logits(O.bf16_to_f64(hs), routers[l]["w_router"])
+        assert rowwise_err(ls, ref_lg.astype(np.float64)) <= 1e-5, l
+        assert np.array_equal(idx, O.route_topk(ls, k)[0]), l
+        host = host_layer_of(l)
+        for i in range(len(rows)):
+            ref, _, _ = O.moe_token(hs[i], ls[i], host, k)
+            e = rowwise_err(ys[i:i + 1], ref[None, :])
+            assert e <= EXACT_TOL, (l, rows[i], e)
+            worst["exact"] = max(worst["exact"], e)
+            if l % emulate_every == 0 or l == len(dls) - 1:
+                emu, _, _ = O.moe_token(hs[i], ls[i], host, k, operands="fp16", out16=True)
+                e = rowwise_err(ys[i:i + 1], emu[None, :])
+                assert e <= EMUL_TOL, (l, rows[i], e)
+                worst["emul"] = max(worst["emul"], e)
+    return worst
+
+
+def test_stack_of_layers_tiny():
+    """Six layers of the small shape, every token checked at every layer (teacher forcing)."""
+    wl = synth.Workload("stack_tiny", T=64, d=256, E=16, k=2, F=128, F_shared=128)
+    L = 6
+    hosts = [synth.make_layer(wl, seed=l) for l in range(L)]
+    routers = [synth.make_router(wl, seed=l) for l in range(L)]
+    dls = [moe.to_device_layer(hh) for hh in hosts]
+    x0 = dev(np.random.default_rng(5).standard_normal((wl.T, wl.d)).astype(np.float32))
+    _stack_teacher_forced(x0, dls, routers, wl, list(range(wl.T)), lambda l: hosts[l])
+
+
+def _run_stack(x0, dls, routers, wl, record):
+    """The stack as the benchmark launches it; returns the residual rows after the layers in
+    `record` (the last layer's y added)."""
+    T = x0.shape[0]
+    dm = moe.dims(T, wl.d, wl.E, wl.k, wl.F, wl.F_shared)
+    ws = moe.alloc_workspace(dm)
+    x = x0.clone()
+    h = torch.empty((T, wl.d), dtype=torch.int16, device="cuda")
+    lg = torch.empty((T, wl.E), dtype=torch.float32, device="cuda")
+    y = torch.empty((T, wl.d), dtype=torch.float32, device="cuda")
+    out = {}
+    for l in range(len(dls)):
+        moe.rmsnorm_router(dm, x, y if l > 0 else None, dev(routers[l]["gamma"]), dev(routers[l]["w_router"]), 1e-6,
+                           h, lg, ws)
+        moe.layer_forward(dm, h, lg, dls[l]["routed"], dls[l]["shared"], dls[l]["w_sg"], y, ws)
         if l + 1 in record:
             out[l + 1] = (x + y).cpu().numpy()
     assert moe.read_error_flags(ws) == 0
-    return out, picks
+    return out
 
 
-def test_stack_full_size_sampled_tokens():
-    """The 40-layer stack at its full size (T = 2048, d 2048, E 256, k 8, F 512, shared expert,
-    40 independent weight sets), launched as the benchmark launches it, on two sampled tokens
-    (one in the last, ragged token tile).
-
-    Over 40 random-weight layers the stack amplifies rounding differences: the residual update of
-    each layer is larger than the residual, so the kernels' ~1e-4 per-layer difference from the
-    fp16-emulating oracle grows to ~1e-2 by layer 16 and then flips near-tie expert choices; no
-    independent evaluation follows it to full depth.  So: (1) the first four layers against the
-    oracle (same expert choices, normwise tolerance of a layer output), and (2) all 40 layers
-    bit for bit against the same tokens run in a batch of 16 -- each token's result must not
-    depend on the batch it is computed in (tile composition, block map, slot order)."""
+def test_stack_full_size_teacher_forced():
+    """The 40-layer stack at its full size (T = 2048, d 2048, E 256, k 8, F 512, shared expert, 40
+    independent weight sets), launched as the benchmark launches it, checked at every layer on
+    three sampled tokens (the first, one inside, and the last, which sits in the ragged last
+    112-row tile) against the exact and the fp16-operand oracle fed the GPU's own layer inputs.
+    The residual update of each random-weight layer is larger than the residual, so independent
+    runs part ways by rounding after a dozen layers; feeding each layer the GPU's own inputs (the
+    teacher forcing of the pages' quality check) checks all 40 layers without dropping tokens.
+    Also: each token's result is bit for bit the same whether it runs in the 2048-token batch or
+    in a batch of 16 (tile composition, block map and slot order must not leak into a token)."""
     wl = synth.STACK
-    L, depth = 40, 4
-    rows = np.array([1234, wl.T - 1])
+    L = 40
+    rows = [0, 1234, wl.T - 1]
     dls = [synth.torch_make_layer(wl, seed=l, device="cuda") for l in range(L)]
     routers = [synth.make_router(wl, seed=l) for l in range(L)]
     x0 = torch.randn((wl.T, wl.d), generator=torch.Generator(device="cuda").manual_seed(7), device="cuda")
-    full, picks = _run_stack(x0, dls, routers, wl, {depth, L})
-    small_rows = torch.cat([torch.from_numpy(rows).cuda(), torch.arange(14, device="cuda")])
-    small, _ = _run_stack(x0[small_rows].contiguous(), dls, routers, wl, {L})
-    assert np.array_equal(full[L][rows], small[L][:2])
+    worst = _stack_teacher_forced(x0, dls, routers, wl, rows, lambda l: _lazy_host_layer(dls[l]), emulate_every=4)
+    print(f"stack teacher-forced worst row errors: exact {worst['exact']:.3e}, emulated {worst['emul']:.3e}")
+    full = _run_stack(x0, dls, routers, wl, {L})
+    sub = torch.cat([torch.as_tensor(rows, device="cuda"), torch.arange(3, 16, device="cuda")])
+    small = _run_stack(x0[sub].contiguous(), dls, routers, wl, {L})
+    assert np.array_equal(full[L][rows], small[L][:len(rows)])
     assert np.all(np.isfinite(full[L]))
-    ref, ref_picks = O.stack_tokens(x0.cpu().numpy()[rows], (_host_layer(dls[l]) for l in range(depth)),
-                                    routers[:depth], wl.k, operands="fp16", out16=True)
-    for l in range(depth):
-        assert np.array_equal(np.sort(picks[l][rows], axis=1), np.sort(ref_picks[l], axis=1)), l
-    assert rowwise_err(full[depth][rows], ref) <= EXACT_TOL
 
 
 def test_decode_stream_probe_moves_the_decode_weights_cleanly():
