@@ -338,6 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     uint32_t ph = 0, phw = 0;
     bool ok = true;
     bool bad = false;
+    float wmax = 0.0f;   // upper bound 15 |s| + |b| of this thread's |w| over the unit's row
     const int G = K / 64;
     // Scale and bias rows of this thread's weight row in a unit; the first 8-group block of the
     // next unit is loaded during the last block of the current one.
@@ -385,8 +386,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                                              : j == 4 ? pick_bf16<4>(cb) : pick_bf16<6>(cb));
           const float bf1 = bf16_bits_to_f32(j == 0 ? pick_bf16<1>(cb) : j == 2 ? pick_bf16<3>(cb)
                                              : j == 4 ? pick_bf16<5>(cb) : pick_bf16<7>(cb));
-          bad = bad || !(fmaf(15.0f, fabsf(sf0), fabsf(bf0)) <= 65504.0f) ||
-                !(fmaf(15.0f, fabsf(sf1), fabsf(bf1)) <= 65504.0f);
+          const float wm0 = fmaf(15.0f, fabsf(sf0), fabsf(bf0)), wm1 = fmaf(15.0f, fabsf(sf1), fabsf(bf1));
+          bad = bad || !(wm0 <= 65504.0f) || !(wm1 <= 65504.0f);
+          wmax = fmaxf(wmax, fmaxf(wm0, wm1));
           const __half2 s2[2] = {__float2half2_rn(sf0), __float2half2_rn(sf1)};
           const __half2 b2[2] = {__float2half2_rn(bf0), __float2half2_rn(bf1)};
           // codes of both chunks: the two-chunk stage s.  It holds 64-byte rows in the 64-byte
@@ -426,6 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           if (++sw == C::S_W) { sw = 0; phw ^= 1u; }
         }
       }
+      // A weight row whose every |w| is below 2^-12 (but not all zero) lives in fp16's subnormal
+      // range and loses precision there: range flag.
+      bad = bad || (wmax > 0.0f && wmax < 2.44140625e-4f);
+      wmax = 0.0f;
       if (has_next) {
         srow = srow_n;
         brow = brow_n;
@@ -438,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const uint32_t stg = sbase + C::OFF_STG + (uint32_t)q * 2048u;
     int li = 0;
     float amax = 0.0f;   // largest |value| rounded to fp16 (above 65504 it does not fit)
+    bool tiny = false;   // a token's h all in fp16's subnormal range (gate/up mode)
     Walk wk;
     walk_init(wk);
     for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++li) {
@@ -462,6 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const float gv = __uint_as_float(g[i]);
             const float hv = gv * __frcp_rn(1.0f + __expf(-gv)) * __uint_as_float(uu[i]);
             if (n0 + i < tl.z) amax = fmaxf(amax, fabsf(hv));
+            // a token whose h over this warp's 32 rows is nonzero but all below 2^-12 sits in fp16's
+            // subnormal range (tiny activations): range flag
+            const unsigned big = __ballot_sync(0xFFFFFFFFu, fabsf(hv) >= 2.44140625e-4f);
+            const unsigned nz = __ballot_sync(0xFFFFFFFFu, hv != 0.0f);
+            tiny = tiny || (n0 + i < tl.z && big == 0u && nz != 0u);
             st_shared_u16(stg + (uint32_t)(i * 32 + pos) * 2, __half_as_ushort(__float2half_rn(hv)));
           }
           __syncwarp();
@@ -522,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       __syncwarp();
       if (lane == 0) mbar_arrive(AE(b));
     }
-    if (__any_sync(0xFFFFFFFFu, !(amax <= 65504.0f)) && lane == 0) raise_flag(a.err, kErrFp16Range);
+    if (__any_sync(0xFFFFFFFFu, !(amax <= 65504.0f) || tiny) && lane == 0) raise_flag(a.err, kErrFp16Range);
   }
 
   // Wind down.  After a timeout, give copies that may still be in flight time to land before

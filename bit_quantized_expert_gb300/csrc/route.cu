@@ -15,6 +15,8 @@
 
 namespace moe {
 
+constexpr uint32_t kBf16TwoPowMinus12 = 0x3980u;   // 2^-12 as bf16 bits
+
 template <int NI>
 __global__ void __launch_bounds__(256) topk_kernel(RouteArgs a) {
   const int lane = threadIdx.x & 31;
@@ -28,23 +30,32 @@ __global__ void __launch_bounds__(256) topk_kernel(RouteArgs a) {
     a.w[(size_t)t * a.k + lane] = my_w;
   }
 
-  // Shared-expert gate logit x . w_sg (one pass over the token row).
-  if (a.x != nullptr && a.gs != nullptr && a.w_sg != nullptr) {
+  // One pass over the token row (layer path): the shared-expert gate logit x . w_sg, and the
+  // token's largest |x|.  The grouped GEMM takes x as fp16 operands: a token whose largest |x| is
+  // nonzero but below 2^-12 sits mostly in fp16's subnormal range and loses precision there, so it
+  // sets the range flag (values above the fp16 range set it when x is converted).
+  if (a.x != nullptr) {
+    const bool gate = a.gs != nullptr && a.w_sg != nullptr;
     const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)t * a.d);
     const uint4* wr = reinterpret_cast<const uint4*>(a.w_sg);
     float dot = 0.0f;
+    uint32_t xmax = 0;   // largest |x| as bf16 magnitude bits
     for (int ch = lane; ch < a.d / 8; ch += 32) {
-      const uint4 xv = __ldg(xr + ch), wv = __ldg(wr + ch);
+      const uint4 xv = __ldg(xr + ch);
+      const uint4 wv = gate ? __ldg(wr + ch) : make_uint4(0u, 0u, 0u, 0u);
       const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
+        xmax = max(xmax, max(xw[i] & 0x7FFFu, (xw[i] >> 16) & 0x7FFFu));
         dot = fmaf(bf16_bits_to_f32(xw[i] & 0xFFFFu), bf16_bits_to_f32(ww[i] & 0xFFFFu), dot);
         dot = fmaf(bf16_bits_to_f32(xw[i] >> 16), bf16_bits_to_f32(ww[i] >> 16), dot);
       }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, off);
-    if (lane == 0) a.gs[t] = 1.0f / (1.0f + expf(-dot));
+    xmax = __reduce_max_sync(0xFFFFFFFFu, xmax);
+    if (lane == 0 && gate) a.gs[t] = 1.0f / (1.0f + expf(-dot));
+    if (lane == 0 && xmax != 0u && xmax < kBf16TwoPowMinus12) raise_flag(a.err, kErrFp16Range);
   }
 }
 
