@@ -41,10 +41,10 @@ import synth  # noqa: E402
 METRIC = "MoE-layer tokens/s (decode T=1, prefill T=512/4096); % of HBM/tensor roofline"
 LAYERS = 40
 NI = 64   # distinct input rows per layer for decode
-# dram__bytes_read.sum + dram__bytes_write.sum of one decode_layer_kernel launch at the decode
-# shape, from one ncu capture of `bench.py --profile decode`; None whenever that kernel has
-# changed since the capture.
-DECODE_NCU_TRAFFIC = None
+# dram__bytes_read.sum + dram__bytes_write.sum of one decode layer call (its decode_layer_kernel and
+# decode_reduce_kernel launches) at the decode shape, from one ncu capture of
+# `bench.py --profile decode`; None whenever those kernels have changed since the capture.
+DECODE_NCU_TRAFFIC = 16300544
 
 
 def parse():

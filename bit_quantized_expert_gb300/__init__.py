@@ -23,7 +23,7 @@ EXPORTED = ("moe_status_string", "moe_max_tiles", "moe_workspace_bytes", "moe_ro
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_MISALIGNED",
           4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA"}
-ERR_WAIT_TIMEOUT, ERR_FP16_RANGE, ERR_BAD_ROUTING = 1, 2, 4
+ERR_WAIT_TIMEOUT, ERR_FP16_RANGE, ERR_BAD_ROUTING, ERR_NON_FINITE = 1, 2, 4, 8
 
 
 class MoeError(RuntimeError):

@@ -27,13 +27,22 @@
  *   - Inputs are never written.  Calls are reentrant; two calls may run concurrently only with
  *     distinct workspaces and outputs.
  *   - Errors are returned, never thrown.  Argument checks happen on the host before any launch.
- *     Conditions only the GPU can see (a bounded wait that timed out, a value outside the fp16
- *     operand range) set bits in the workspace's error word; read them with
- *     moe_read_error_flags.  Outputs are then invalid.
+ *     Conditions only the GPU can see set bits in the workspace's error word (sticky until read):
+ *       1  a bounded wait timed out (outputs invalid);
+ *       2  a value of the grouped-GEMM path left the fp16 operand range: above 65504, or a block
+ *          that sits in fp16's subnormal range and loses precision there (a token whose largest
+ *          |x| is below 2^-12, a weight row whose largest |w| is below 2^-12, or a token whose h
+ *          is below 2^-12 over a 32-row block of F);
+ *       4  routing tables inconsistent with the dims;
+ *       8  an activation of the decode path (x or h) is not finite.
+ *     Calls whose inputs may leave the fp16 operand range (more than eight tokens per call) must
+ *     check the word with moe_read_error_flags before trusting y; the decode path (up to eight
+ *     tokens) computes in exact integers and fp32 and has no range limit below fp32's.
  *   - T == 0 is a no-op that returns MOE_OK.
  *
  * Dimension limits: 1 <= k <= 32, k <= E <= 1024, d and F multiples of 128, F_shared == 0 (no
- * shared expert) or F_shared == F, T * (k + 1) < 2^31.
+ * shared expert) or F_shared == F, T * (k + 1) < 2^31.  (The tensor-core tiles take 128 rows of d
+ * and of F; the grouped-GEMM path also needs d % 256 == 0.)
  */
 #ifndef MOE_GB300_H_
 #define MOE_GB300_H_
@@ -114,19 +123,22 @@ size_t moe_max_tiles(const moe_dims* dims, int32_t tile_n);
 
 /* Workspace bytes needed by moe_route, moe_expert_forward and moe_layer_forward for these dims
  * (one size serves all three).  Returns 0 for invalid dims.  The first 4 bytes of the workspace are
- * its error word: kernels only ever set bits in it, so it is sticky across calls.  Bytes 8..15
- * hold the decode path's grid-barrier word (it returns to zero at the end of every decode launch).
- * Clear both once after allocating the workspace (moe_clear_error_flags); the rest needs no
- * initialisation. */
+ * its error word: kernels only ever set bits in it, so it is sticky across calls.  Clear it once
+ * after allocating the workspace (moe_clear_error_flags); the rest needs no initialisation. */
 size_t moe_workspace_bytes(const moe_dims* dims);
 
 /* Routing: top-k, weights, histogram, exclusive scan, permutation and block map of fp32
- * router logits [T, E].  Writes every field of *out (out->tile_n is an input). */
+ * router logits [T, E], all on the GPU with no host synchronisation ("Perplexity libera Lily...",
+ * section "Prefill: pesos comprimidos y enrutamiento en la GPU": histogram, prefix scan, scatter
+ * and block map in one command buffer).  Writes every field of *out (out->tile_n is an input).
+ * The workspace holds scratch for the tables. */
 moe_status moe_route(const moe_dims* dims, const float* logits, const moe_routing* out, void* workspace,
                      size_t workspace_bytes, void* stream);
 
-/* Expert outputs per slot (needs d % 256 == 0 and routing->tile_n <= 112; MOE_ERR_UNSUPPORTED
- * otherwise):
+/* Expert outputs per slot: the fused-dequant grouped GEMM ("Perplexity libera Lily...", section
+ * "Prefill: pesos comprimidos y enrutamiento en la GPU": 4-bit weights rebuilt tile by tile on
+ * chip, FP32 accumulation).  Needs d % 256 == 0 and routing->tile_n <= 112 (the activation stages
+ * hold 112 rows); MOE_ERR_UNSUPPORTED otherwise.
  * y_perm[p] = FFN_{e(p)}(x[token(p)]) for the T*k routed slots of
  * `routing`, followed (when `shared` is non-NULL) by the shared expert's outputs for the T
  * tokens in slots T*k .. T*k+T-1.  x bf16 [T, d]; y_perm fp32 [T*k + T, d] (or [T*k, d] without
@@ -136,16 +148,20 @@ moe_status moe_expert_forward(const moe_dims* dims, const uint16_t* x, const moe
                               const moe_experts* routed, const moe_experts* shared, float* y_perm,
                               void* workspace, size_t workspace_bytes, void* stream);
 
-/* The whole layer: y[t] = sum_j w[t,j] FFN_{idx[t,j]}(x_t) + sigmoid(x_t . w_sg) FFN_shared(x_t).
+/* The whole layer: y[t] = sum_j w[t,j] FFN_{idx[t,j]}(x_t) + sigmoid(x_t . w_sg) FFN_shared(x_t)
+ * (a router keeping 8 of 256 experts plus a shared expert every token uses: "Perplexity libera
+ * Lily...", section "Tres formas de carga en un mismo modelo"; at batch 1 the layer is bound by
+ * weight bandwidth: section "Decode: mover menos bytes por token").
  * x bf16 [T, d]; logits fp32 [T, E]; w_shared_gate bf16 [d] (ignored when shared is NULL);
  * y fp32 [T, d].  routing_out may be NULL; when given, its tables are filled as by moe_route.
- * T <= 8 runs the fused decode path (fp32 arithmetic on CUDA cores; one launch for all tokens,
- * each expert slot taking the tokens in turn) when d <= 2048, d % 64 == 0, F % 128 == 0, k < 32,
- * E <= 1024 and (k + 1) * F / 32 CTAs fit one per SM; otherwise, and for T > 8, the grouped-GEMM
- * path (fp16 tensor-core operands, fp32 accumulation; needs d % 256 == 0, and
- * routing_out->tile_n <= 112 when routing_out is given; MOE_ERR_UNSUPPORTED otherwise).  Its own
- * block map uses tiles of 112 rows.  The decode path's workspace holds (k + 1) * F / 32 * d
- * floats of partial outputs per token. */
+ * T <= 8 runs the decode path when d <= 2048 and k + 1 <= 32: two launches per call (the fused
+ * kernel -- routing in the kernel, exact integer dot products of the 4-bit codes with fixed-point
+ * activations, fp32 everywhere else; each expert slot takes the tokens in turn -- and a small
+ * kernel that sums its partial outputs in a fixed order).  Otherwise, and for T > 8, the
+ * grouped-GEMM path (fp16 tensor-core operands, fp32 accumulation; needs d % 256 == 0, and
+ * routing_out->tile_n <= 112 when routing_out is given; MOE_ERR_UNSUPPORTED otherwise); its own
+ * block map uses tiles of 112 rows.  The decode path's workspace holds
+ * 512 * ceil(d / 512) * (k + 1) * F / 128 floats of partial outputs per token. */
 moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const float* logits,
                              const moe_experts* routed, const moe_experts* shared, const uint16_t* w_shared_gate,
                              float* y, const moe_routing* routing_out, void* workspace, size_t workspace_bytes,
@@ -170,7 +186,9 @@ moe_status moe_layer_forward_host(const moe_dims* dims, const uint16_t* x_host, 
                                   const uint16_t* w_shared_gate, float* y_host, void* workspace,
                                   size_t workspace_bytes, void* stream);
 
-/* Pre-norm block of a stack of MoE layers (the step between two layers, not part of the layer):
+/* Pre-norm block of a stack of MoE layers (the step between two layers, not part of the layer; an
+ * addition for the 40-layer stack workload -- the pages' router scores 256 experts from the
+ * normalised hidden state, a linear router being the reading):
  * when y_prev is non-NULL, x_resid += y_prev (written back); then h = RMSNorm(x_resid) * gamma
  * = x / sqrt(mean(x^2) + eps) * gamma rounded to bf16, and router logits = h W_r^T with bf16
  * operands and fp32 accumulation on the tensor cores.  x_resid fp32 [T, d] (in/out); y_prev fp32
@@ -186,11 +204,13 @@ moe_status moe_rmsnorm_router(const moe_dims* dims, float* x_resid, const float*
  * forbids later cudaMalloc calls, a latency-critical decode loop that must never enter
  * cudaMalloc/cudaFree (they may synchronise the device), or a host program that holds only
  * pointers to weights, inputs and outputs.  Arguments and results are those of
- * moe_layer_forward with T == 1 (same kernels).
- *   - Scratch: a library-owned device array of 1.25 MB (+256 B) that every GPU which loads the
- *     library keeps until the process exits; it bounds (k + 1) * (F / 32) * d <= 327680.  Larger
- *     dims, T > 1, or dims the decode path does not take return MOE_ERR_UNSUPPORTED; T == 0
- *     returns MOE_OK.
+ * moe_layer_forward with T == 1 (same kernels), and dims outside moe_layer_forward's rules return
+ * its status codes.
+ *   - Scratch: a library-owned device array of 512 KB (+256 B) that every GPU which loads the
+ *     library keeps until the process exits; it bounds the decode path's partial outputs,
+ *     512 * ceil(d / 512) * (k + 1) * F / 128 <= 131072 floats (the decode workload, d 2048,
+ *     k 8, F 512, needs 73728).  Larger dims, T > 1, or dims the decode path does not take return
+ *     MOE_ERR_UNSUPPORTED; T == 0 returns MOE_OK.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
  *     that device current; make that first call before any stream capture.
  *   - All calls share the array: calls whose work overlaps on the GPU (different streams, or
@@ -201,15 +221,13 @@ moe_status moe_layer_forward_decode_noalloc(const moe_dims* dims, const uint16_t
                                             const moe_experts* routed, const moe_experts* shared,
                                             const uint16_t* w_shared_gate, float* y, void* stream);
 
-/* Enqueues the clearing of the workspace's error word (and, for workspaces of at least 16 bytes,
- * the decode grid-barrier word) on `stream` (no host synchronisation). */
+/* Enqueues the clearing of the workspace's error word on `stream` (no host synchronisation). */
 moe_status moe_clear_error_flags(void* workspace, size_t workspace_bytes, void* stream);
 
-/* Synchronises `stream`, copies the workspace's error word to *flags, then clears it (and the
- * decode grid-barrier word when bit 1 was set).  Bits:
- * 1 = a bounded device wait timed out, 2 = a value left the fp16 operand range,
- * 4 = routing tables inconsistent with the dims.  0 means every call since the last clear
- * completed cleanly. */
+/* Synchronises `stream`, copies the workspace's error word to *flags, then clears it.  Bits (see
+ * the conventions above): 1 = a bounded device wait timed out, 2 = a value left the fp16 operand
+ * range of the grouped-GEMM path, 4 = routing tables inconsistent with the dims, 8 = a decode-path
+ * activation is not finite.  0 means every call since the last clear completed cleanly. */
 moe_status moe_read_error_flags(void* workspace, size_t workspace_bytes, uint32_t* flags, void* stream);
 
 #ifdef __cplusplus
