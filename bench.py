@@ -56,7 +56,7 @@ def parse():
     p.add_argument("--no-extras", action="store_true", help="skip the prefill T=512 / T=4096 sub-measurements")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=50)
-    p.add_argument("--profile", choices=["decode", "prefill", "skewed", "stack"], default=None,
+    p.add_argument("--profile", choices=["decode", "prefill", "skewed", "stack", "attention"], default=None,
                    help="small eager run of one workload for ncu captures (prints a short summary only)")
     p.add_argument("--profile-sets", type=int, default=4, help="weight sets cycled in --profile mode")
     return p.parse_args()
@@ -534,6 +534,85 @@ def stack_bench(wl, steps, device, pk):
 
 # ------------------------------------------------------------------------------ CPU oracle
 
+def attention_bytes(wl):
+    """Algorithmic bytes of one decode-attention call: the keys and values of N positions for every
+    key/value head (bf16), the bf16 query heads and the fp32 output."""
+    return 2 * wl.Hkv * wl.N * wl.D * 2 + wl.Hq * wl.D * 2 + wl.Hq * wl.D * 4
+
+
+def attention_bench(wl, steps, device, pk):
+    """One step = one decode token through the model's ten full-attention layers at context N: each
+    layer has its own bf16 key/value cache (10 x N x 1 KB in HBM, larger than L2, so no layer's
+    cache is in L2 when it runs) and its own query; one library call per layer; CUDA-graph replay."""
+    import torch
+
+    import bit_quantized_expert_gb300 as moe
+    log(f"{wl.name}: generating {wl.layers} caches")
+    layers = [synth.torch_make_attention(wl.Hq, wl.Hkv, wl.D, wl.N, seed=l, device=device) for l in range(wl.layers)]
+    gd = moe.gqa_dims(wl.Hq, wl.Hkv, wl.D, wl.N)
+    ws = moe.alloc_gqa_workspace(gd, device)
+    o = torch.empty((wl.layers, wl.Hq, wl.D), dtype=torch.float32, device=device)
+    stream = torch.cuda.Stream(device=device)
+
+    def step():
+        for l, c in enumerate(layers):
+            moe.gqa_decode_attention(gd, c["q"], c["k"], c["v"], o[l], ws)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    stream.synchronize()
+    g = capture(step, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+    stream.synchronize()
+    ms = timed_graph_steps(g, 1, g, steps, stream)
+    # The same calls with a one-element torch kernel between them: it does not allow an early start,
+    # so each call's copies begin only after the previous call has finished (no overlap across
+    # calls); the separators' own time, measured alone, is subtracted.
+    sep = torch.zeros(1, device=device)
+
+    def step_sep():
+        for l, c in enumerate(layers):
+            sep.add_(1.0)
+            moe.gqa_decode_attention(gd, c["q"], c["k"], c["v"], o[l], ws)
+
+    def seps():
+        for _ in range(wl.layers):
+            sep.add_(1.0)
+
+    with torch.cuda.stream(stream):
+        step_sep()
+    stream.synchronize()
+    g_sep, g_seps = capture(step_sep, stream), capture(seps, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g_sep.replay()
+            g_seps.replay()
+    stream.synchronize()
+    ms_sep = timed_graph_steps(g_sep, 1, g_sep, steps, stream)
+    ms_seps = timed_graph_steps(g_seps, 1, g_seps, steps, stream)
+    flags = moe.read_error_flags(ws)
+    step_s = ms / 1e3 / steps
+    call_s = step_s / wl.layers
+    iso_s = (ms_sep - ms_seps) / 1e3 / steps / wl.layers
+    nbytes = attention_bytes(wl)
+    log(f"{wl.name}: {call_s * 1e6:.2f} us per layer call ({iso_s * 1e6:.2f} us without overlap across calls)")
+    out = {"workload": wl.name, "ms_per_step": ms / steps, "us_per_layer_call": call_s * 1e6, "steps": steps,
+           "layers": wl.layers, "flags": flags,
+           "value": 1.0 / step_s, "unit": "decode tokens/s through the attention layers",
+           "hbm": {"achieved": nbytes / call_s / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                   "frac": nbytes / call_s / 1e9 / pk["hbm_gbs"], "algorithmic_bytes_per_call": nbytes,
+                   "note": "per call: attn_block_kernel + attn_merge_kernel; peak is the measured copy rate"},
+           "us_per_layer_call_no_overlap": iso_s * 1e6,
+           "hbm_frac_no_overlap": nbytes / iso_s / 1e9 / pk["hbm_gbs"],
+           "gpu_launches_per_step": 2 * wl.layers}
+    del layers
+    torch.cuda.empty_cache()
+    return out
+
+
 def oracle_rate(budget_s: float, max_tokens: int | None = None):
     """The float64 oracle on decode tokens of one layer (its cost does not depend on the weights)."""
     from oracle import moe_oracle as O
@@ -594,6 +673,9 @@ def run_profile(args):
     torch.cuda.set_device(0)
     device = torch.device("cuda", 0)
     moe.load_library()
+    if args.profile == "attention":
+        run_profile_attention(args)
+        return
     wl = {"decode": synth.DECODE, "prefill": synth.PREFILL, "skewed": synth.SKEWED, "stack": synth.STACK}[args.profile]
     n = args.profile_sets
     layers = make_layers(wl, device, n)
@@ -618,6 +700,30 @@ def run_profile(args):
                       "wall_s": time.perf_counter() - t0}), flush=True)
 
 
+def run_profile_attention(args):
+    """Eager decode-attention calls at context 32768 over `profile_sets` (at least 6) distinct caches,
+    192 MB or more in all (larger than L2)."""
+    import torch
+
+    import bit_quantized_expert_gb300 as moe
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    moe.load_library()
+    wl = synth.GQA_32K
+    n = max(6, args.profile_sets)
+    layers = [synth.torch_make_attention(wl.Hq, wl.Hkv, wl.D, wl.N, seed=l, device=device) for l in range(n)]
+    gd = moe.gqa_dims(wl.Hq, wl.Hkv, wl.D, wl.N)
+    ws = moe.alloc_gqa_workspace(gd, device)
+    o = torch.empty((wl.Hq, wl.D), dtype=torch.float32, device=device)
+    torch.cuda.synchronize()
+    total = args.warmup + args.steps
+    for s in range(total):
+        c = layers[s % n]
+        moe.gqa_decode_attention(gd, c["q"], c["k"], c["v"], o, ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": wl.name, "calls": total, "caches": n, "flags": moe.read_error_flags(ws)}), flush=True)
+
+
 def main():
     args = parse()
     if args.profile is not None:
@@ -640,11 +746,12 @@ def main():
     pk = peaks()
 
     res = decode_bench(args, world, rank, local, device, pk)
-    extras = []
+    extras, attn = [], None
     if not args.no_extras and rank == 0:
         extras.append(prefill_bench(synth.PREFILL, 48, device, pk))
         extras.append(prefill_bench(synth.SKEWED, 24, device, pk))
         extras.append(stack_bench(synth.STACK, 5, device, pk))
+        attn = [attention_bench(w, 20, device, pk) for w in (synth.GQA_32K, synth.GQA_64K, synth.GQA_128K)]
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n, el = oracle_rate(20.0)
@@ -658,7 +765,7 @@ def main():
                 "gpu_launches": res["gpu_launches"], "clocks": res["clocks"], "error_flags": res["flags"],
                 "decode_hot_l2": res.get("hot_l2"), "decode_e2e_staged": res.get("e2e_staged"),
                 "decode_small_T": res.get("small_T"), "decode_loads_only": res.get("loads_only"),
-                "prefill": extras}
+                "prefill": extras, "gqa_decode_attention": attn}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

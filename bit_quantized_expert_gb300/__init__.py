@@ -15,11 +15,12 @@ import os
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG_DIR, "libmoe_gb300.so")
 
-# Symbols declared in include/moe.h and include/moe_probe.h.
+# Symbols declared in include/moe.h, include/gqa_attention.h and include/moe_probe.h.
 EXPORTED = ("moe_status_string", "moe_max_tiles", "moe_workspace_bytes", "moe_route",
             "moe_expert_forward", "moe_layer_forward", "moe_rmsnorm_router", "moe_clear_error_flags",
             "moe_read_error_flags", "moe_layer_forward_decode_noalloc", "moe_workspace_bytes_host",
-            "moe_layer_forward_host", "moe_decode_stream_probe")
+            "moe_layer_forward_host", "moe_decode_stream_probe", "gqa_decode_workspace_bytes",
+            "gqa_decode_attention")
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_MISALIGNED",
           4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA"}
@@ -43,6 +44,11 @@ class QMat(ctypes.Structure):
 
 class ExpertsC(ctypes.Structure):
     _fields_ = [("gate", QMat), ("up", QMat), ("down", QMat)]
+
+
+class GqaDims(ctypes.Structure):
+    _fields_ = [("n_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("n_ctx", ctypes.c_int32), ("capacity", ctypes.c_int32)]
 
 
 class RoutingC(ctypes.Structure):
@@ -89,6 +95,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_layer_forward_decode_noalloc.argtypes = [P(Dims), VP, VP, P(ExpertsC), P(ExpertsC), VP, VP, VP]
     lib.moe_decode_stream_probe.restype = ctypes.c_int
     lib.moe_decode_stream_probe.argtypes = [P(Dims), VP, P(ExpertsC), P(ExpertsC), VP, S, VP]
+    lib.gqa_decode_workspace_bytes.restype = S
+    lib.gqa_decode_workspace_bytes.argtypes = [P(GqaDims)]
+    lib.gqa_decode_attention.restype = ctypes.c_int
+    lib.gqa_decode_attention.argtypes = [P(GqaDims), VP, VP, VP, VP, VP, S, VP]
     lib.moe_clear_error_flags.restype = ctypes.c_int
     lib.moe_clear_error_flags.argtypes = [VP, S, VP]
     lib.moe_read_error_flags.restype = ctypes.c_int
@@ -248,6 +258,34 @@ def decode_stream_probe(dm: Dims, idx, routed: dict, shared: dict | None, worksp
     _check(load_library().moe_decode_stream_probe(ctypes.byref(dm), _ptr(idx), ctypes.byref(re),
                                                   ctypes.byref(se) if se is not None else None, _ptr(workspace),
                                                   workspace.numel(), _stream(stream)), "moe_decode_stream_probe")
+
+
+def gqa_dims(n_heads, n_kv_heads, head_dim, n_ctx, capacity=None) -> GqaDims:
+    return GqaDims(int(n_heads), int(n_kv_heads), int(head_dim), int(n_ctx),
+                   int(n_ctx if capacity is None else capacity))
+
+
+def gqa_workspace_bytes(gd: GqaDims) -> int:
+    n = load_library().gqa_decode_workspace_bytes(ctypes.byref(gd))
+    if n == 0:
+        raise MoeError(1, "gqa_decode_workspace_bytes")
+    return n
+
+
+def alloc_gqa_workspace(gd: GqaDims, device="cuda"):
+    """Workspace of the decode attention for these dims, its error word cleared."""
+    import torch
+    ws = torch.empty(gqa_workspace_bytes(gd), dtype=torch.uint8, device=device)
+    ws[:256].zero_()
+    return ws
+
+
+def gqa_decode_attention(gd: GqaDims, q, k_cache, v_cache, o, workspace, stream=None):
+    """o[h] = softmax(q[h] . K[g] / sqrt(128)) V[g] over the first n_ctx cached positions, g = h // (Hq/Hkv).
+    q bf16 [Hq, 128]; caches bf16 [Hkv, capacity, 128]; o fp32 [Hq, 128]."""
+    _check(load_library().gqa_decode_attention(ctypes.byref(gd), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o),
+                                               _ptr(workspace), workspace.numel(), _stream(stream)),
+           "gqa_decode_attention")
 
 
 def read_error_flags(workspace, stream=None) -> int:

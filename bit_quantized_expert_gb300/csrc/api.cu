@@ -110,11 +110,9 @@ moe_status check_routing(const moe_routing* r) {
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-// ---------------------------------------------------------------- TMA descriptors
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+}  // namespace
 
+// ---------------------------------------------------------------- TMA descriptors
 EncodeTiledFn encode_fn() {
   static EncodeTiledFn fn = nullptr;
   static std::once_flag once;
@@ -128,6 +126,8 @@ EncodeTiledFn encode_fn() {
   });
   return fn;
 }
+
+namespace {
 
 // Packed codes of n stacked [R, C] matrices as a 3-D uint32 tensor {C/8, R, n}; box 16 x 128 x 1
 // (128 codes of 128 rows = two quantisation groups of a tile, 64 bytes per row) in the 64-byte

@@ -138,6 +138,11 @@ struct StreamArgs {
 };
 cudaError_t launch_decode_stream(const DecodeMaps& maps, const StreamArgs& a, cudaStream_t st);
 // Encodes DecodeMaps::down[i] for n stacked [d, F] down matrices (api.cu); false on failure.
+// cuTensorMapEncodeTiled, fetched once from the driver (null if the driver lacks it).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn();
 bool encode_decode_down(CUtensorMap* m, const uint32_t* codes, int n, int d, int F);
 
 // Workspace head shared by the C ABI and the allocation-free entry point: the error word at 0.

@@ -1,4 +1,5 @@
-"""Seeded synthetic inputs for the 4-bit MoE layer (shared by the tests, the oracle checks and bench.py).
+"""Seeded synthetic inputs for the 4-bit MoE layer and the grouped-query decode attention (shared by
+the tests, the oracle checks and bench.py).
 
 This module only draws random numbers with the shapes and distributions of the
 workloads; it holds none of the layer's arithmetic (no dequantisation, routing,
@@ -15,6 +16,11 @@ is eight independent uniform nibbles), scale ~ U(0.005, 0.02) rounded to bf16,
 bias = -8 * scale * (1 + U(-0.05, 0.05)) rounded to bf16, x ~ N(0,1) rounded to bf16,
 router logits fp32 N(0,1) with a per-workload offset, shared-gate vector
 w_sg ~ N(0,1)/sqrt(d) rounded to bf16.
+
+Decode attention (16 query heads, 2 key/value heads, head size 128; contexts of 32K, 64K and
+128K positions as in the pages' measurements): the query q ~ N(0, q_scale^2) and the cached keys
+and values ~ N(0,1), all rounded to bf16, so the scaled scores q.k/sqrt(128) have standard
+deviation q_scale; a cache allocated beyond the context holds a given fill pattern there.
 """
 from __future__ import annotations
 
@@ -51,6 +57,23 @@ STACK = Workload("stack40_T2048_d2048_E256_k8_F512", T=2048, d=2048, E=256, k=8,
                  layers=40)
 
 WORKLOADS = {w.name: w for w in (TINY, DECODE, PREFILL, SKEWED, STACK)}
+
+
+@dataclasses.dataclass(frozen=True)
+class AttnWorkload:
+    name: str
+    Hq: int
+    Hkv: int
+    D: int
+    N: int
+    layers: int = 1
+
+
+# Decode attention of the model's ten full-attention layers at the pages' context lengths.
+GQA_SMALL = AttnWorkload("gqa_Hq16_Hkv2_D128_N4097", 16, 2, 128, 4097)
+GQA_32K = AttnWorkload("gqa_decode10_Hq16_Hkv2_D128_N32768", 16, 2, 128, 32768, layers=10)
+GQA_64K = AttnWorkload("gqa_decode10_Hq16_Hkv2_D128_N65536", 16, 2, 128, 65536, layers=10)
+GQA_128K = AttnWorkload("gqa_decode10_Hq16_Hkv2_D128_N131072", 16, 2, 128, 131072, layers=10)
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -129,6 +152,21 @@ def make_router(w: Workload, seed: int) -> dict:
     return {"gamma": gamma, "w_router": w_router}
 
 
+def make_attention(Hq: int, Hkv: int, D: int, N: int, capacity: int | None = None, seed: int = 0,
+                   q_scale: float = 1.0, tail_bits: int | None = None) -> dict:
+    """q bf16 [Hq, D]; k, v bf16 [Hkv, capacity, D] (bit patterns); positions >= N hold tail_bits
+    when given."""
+    rng = np.random.default_rng(seed + 3_000_017)
+    cap = N if capacity is None else capacity
+    q = f32_to_bf16_bits((rng.standard_normal((Hq, D)) * q_scale).astype(np.float32))
+    k = f32_to_bf16_bits(rng.standard_normal((Hkv, cap, D), dtype=np.float32))
+    v = f32_to_bf16_bits(rng.standard_normal((Hkv, cap, D), dtype=np.float32))
+    if tail_bits is not None and cap > N:
+        k[:, N:] = tail_bits
+        v[:, N:] = tail_bits
+    return {"q": q, "k": k, "v": v}
+
+
 # ----------------------------------------------------------------------------------------------
 # Device-side generation for the large benchmark workloads (same distributions, torch RNG stream).
 # ----------------------------------------------------------------------------------------------
@@ -174,3 +212,15 @@ def torch_make_inputs(w: Workload, seed: int, device, T: int | None = None) -> d
     elif w.logits == "zipf":
         logits = logits + torch.from_numpy(zipf_logit_bias(w.E)).to(device=device, dtype=torch.float32)[None, :]
     return {"x": x.view(torch.int16), "logits": logits.contiguous()}
+
+
+def torch_make_attention(Hq: int, Hkv: int, D: int, N: int, seed: int, device, q_scale: float = 1.0) -> dict:
+    """Same recipe as make_attention (capacity N), drawn with torch's generator on `device`."""
+    import torch
+
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed + 3_000_017)
+    q = (torch.randn((Hq, D), generator=gen, device=device) * q_scale).to(torch.bfloat16)
+    k = torch.randn((Hkv, N, D), generator=gen, device=device).to(torch.bfloat16)
+    v = torch.randn((Hkv, N, D), generator=gen, device=device).to(torch.bfloat16)
+    return {"q": q.view(torch.int16), "k": k.view(torch.int16), "v": v.view(torch.int16)}

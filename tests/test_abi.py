@@ -18,7 +18,7 @@ def _declared():
         if h.endswith(".h"):
             with open(os.path.join(ROOT, "include", h)) as f:
                 src = f.read()
-            names |= set(re.findall(r"^\s*(?:const\s+)?[\w\*\s]+?\b(moe_\w+)\s*\(", src, re.M))
+            names |= set(re.findall(r"^\s*(?:const\s+)?[\w\*\s]+?\b((?:moe|gqa)_\w+)\s*\(", src, re.M))
     return sorted(names)
 
 
@@ -134,3 +134,39 @@ def test_layer_host_entry_checks(lib):
     assert call(wsn=ws_h - 1) == 4
     assert call(wsn=ws_n) == 4
     assert call(dm=moe.dims(0, 256, 16, 2, 128, 128)) == 0   # T == 0: nothing to do
+
+
+def test_gqa_workspace_bytes(lib):
+    """256-byte head, then Hkv * min(ceil(N / 64), 256) blocks of 4160 bytes (1024 + 16 floats)."""
+    for Hq, Hkv, N in ((16, 2, 1), (16, 2, 64), (16, 2, 65), (16, 2, 32768), (16, 2, 131072), (8, 8, 1000)):
+        gd = moe.gqa_dims(Hq, Hkv, 128, N)
+        assert lib.gqa_decode_workspace_bytes(ctypes.byref(gd)) == 256 + Hkv * min(-(-N // 64), 256) * 4160
+
+
+@pytest.mark.parametrize("bad", [
+    dict(head_dim=64), dict(n_heads=18), dict(n_heads=32), dict(n_ctx=0), dict(n_ctx=10, capacity=9),
+    dict(n_kv_heads=0), dict(n_ctx=-1)])
+def test_gqa_invalid_dims_rejected(lib, bad):
+    args = dict(n_heads=16, n_kv_heads=2, head_dim=128, n_ctx=100, capacity=100)
+    args.update(bad)
+    gd = moe.GqaDims(**{k: int(v) for k, v in args.items()})
+    assert lib.gqa_decode_workspace_bytes(ctypes.byref(gd)) == 0
+
+
+def test_gqa_host_checks(lib):
+    """Statuses of include/gqa_attention.h, all returned before any CUDA work: 1 for a null pointer,
+    Hq % Hkv != 0, N < 1 or N > capacity; 2 for head_dim != 128 or more than 8 query heads per
+    key/value head; 3 for a misaligned pointer; 4 for a short workspace."""
+    gd = moe.gqa_dims(16, 2, 128, 100)
+    n = lib.gqa_decode_workspace_bytes(ctypes.byref(gd))
+    call = lambda dims=gd, q=16, k=16, v=16, o=16, ws=16, nb=n: lib.gqa_decode_attention(
+        ctypes.byref(dims), q, k, v, o, ws, nb, None)
+    assert call(q=None) == 1 and call(k=None) == 1 and call(v=None) == 1 and call(o=None) == 1
+    assert call(ws=None) == 1
+    assert call(q=18) == 3 and call(k=24) == 3 and call(o=20) == 3 and call(ws=8) == 3
+    assert call(nb=n - 1) == 4
+    assert call(dims=moe.gqa_dims(16, 3, 128, 100)) == 1
+    assert call(dims=moe.gqa_dims(16, 2, 128, 0)) == 1
+    assert call(dims=moe.gqa_dims(16, 2, 128, 101, 100)) == 1
+    assert call(dims=moe.gqa_dims(16, 2, 64, 100)) == 2
+    assert call(dims=moe.gqa_dims(32, 2, 128, 100)) == 2
