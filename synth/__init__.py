@@ -21,6 +21,11 @@ Decode attention (16 query heads, 2 key/value heads, head size 128; contexts of 
 128K positions as in the pages' measurements): the query q ~ N(0, q_scale^2) and the cached keys
 and values ~ N(0,1), all rounded to bf16, so the scaled scores q.k/sqrt(128) have standard
 deviation q_scale; a cache allocated beyond the context holds a given fill pattern there.
+
+Gated DeltaNet scan (16 heads, key and value size 128): q, k, v ~ N(0,1) rounded to bf16; the decay
+a = exp(g) ~ U(0.90, 0.999) per token and head (g = log a in fp32); the write strength
+b = sigmoid(z), z ~ N(0,1), in fp32; the initial state ~ N(0, 0.1^2) in fp32 (zero for a fresh
+prompt).
 """
 from __future__ import annotations
 
@@ -74,6 +79,22 @@ GQA_SMALL = AttnWorkload("gqa_Hq16_Hkv2_D128_N4097", 16, 2, 128, 4097)
 GQA_32K = AttnWorkload("gqa_decode10_Hq16_Hkv2_D128_N32768", 16, 2, 128, 32768, layers=10)
 GQA_64K = AttnWorkload("gqa_decode10_Hq16_Hkv2_D128_N65536", 16, 2, 128, 65536, layers=10)
 GQA_128K = AttnWorkload("gqa_decode10_Hq16_Hkv2_D128_N131072", 16, 2, 128, 131072, layers=10)
+
+
+@dataclasses.dataclass(frozen=True)
+class ScanWorkload:
+    name: str
+    T: int
+    H: int
+    D: int
+    layers: int = 1
+    fresh: bool = False   # zero initial state (a new prompt)
+
+
+# The model's thirty Gated DeltaNet layers: a decode token, and prompts of 512 and 2048 tokens.
+SCAN_DECODE = ScanWorkload("deltanet30_decode_T1_H16_D128", 1, 16, 128, layers=30)
+SCAN_512 = ScanWorkload("deltanet_prefill_T512_H16_D128", 512, 16, 128, fresh=True)
+SCAN_2048 = ScanWorkload("deltanet_prefill_T2048_H16_D128", 2048, 16, 128, fresh=True)
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -167,6 +188,18 @@ def make_attention(Hq: int, Hkv: int, D: int, N: int, capacity: int | None = Non
     return {"q": q, "k": k, "v": v}
 
 
+def make_scan(T: int, H: int, D: int, seed: int = 0, fresh: bool = False) -> dict:
+    """q, k, v bf16 [T, H, D] (bit patterns); g, beta fp32 [T, H]; S0 fp32 [H, D, D]."""
+    rng = np.random.default_rng(seed + 4_000_037)
+    q = f32_to_bf16_bits(rng.standard_normal((T, H, D), dtype=np.float32))
+    k = f32_to_bf16_bits(rng.standard_normal((T, H, D), dtype=np.float32))
+    v = f32_to_bf16_bits(rng.standard_normal((T, H, D), dtype=np.float32))
+    g = np.log(rng.uniform(0.90, 0.999, (T, H))).astype(np.float32)
+    beta = (1.0 / (1.0 + np.exp(-rng.standard_normal((T, H))))).astype(np.float32)
+    S0 = np.zeros((H, D, D), np.float32) if fresh else (rng.standard_normal((H, D, D)) * 0.1).astype(np.float32)
+    return {"q": q, "k": k, "v": v, "g": g, "beta": beta, "S0": S0}
+
+
 # ----------------------------------------------------------------------------------------------
 # Device-side generation for the large benchmark workloads (same distributions, torch RNG stream).
 # ----------------------------------------------------------------------------------------------
@@ -224,3 +257,17 @@ def torch_make_attention(Hq: int, Hkv: int, D: int, N: int, seed: int, device, q
     k = torch.randn((Hkv, N, D), generator=gen, device=device).to(torch.bfloat16)
     v = torch.randn((Hkv, N, D), generator=gen, device=device).to(torch.bfloat16)
     return {"q": q.view(torch.int16), "k": k.view(torch.int16), "v": v.view(torch.int16)}
+
+
+def torch_make_scan(T: int, H: int, D: int, seed: int, device, fresh: bool = False) -> dict:
+    """Same recipe as make_scan, drawn with torch's generator on `device`."""
+    import torch
+
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed + 4_000_037)
+    bf = lambda shape: torch.randn(shape, generator=gen, device=device).to(torch.bfloat16).view(torch.int16)
+    q, k, v = bf((T, H, D)), bf((T, H, D)), bf((T, H, D))
+    g = torch.empty((T, H), device=device).uniform_(0.90, 0.999, generator=gen).log()
+    beta = torch.sigmoid(torch.randn((T, H), generator=gen, device=device))
+    S0 = torch.zeros((H, D, D), device=device) if fresh else torch.randn((H, D, D), generator=gen, device=device) * 0.1
+    return {"q": q, "k": k, "v": v, "g": g, "beta": beta, "S0": S0}
