@@ -56,7 +56,7 @@ def parse():
     p.add_argument("--no-extras", action="store_true", help="skip the prefill T=512 / T=4096 sub-measurements")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=50)
-    p.add_argument("--profile", choices=["decode", "prefill", "skewed", "stack", "attention"], default=None,
+    p.add_argument("--profile", choices=["decode", "prefill", "skewed", "stack", "attention", "scan"], default=None,
                    help="small eager run of one workload for ncu captures (prints a short summary only)")
     p.add_argument("--profile-sets", type=int, default=4, help="weight sets cycled in --profile mode")
     return p.parse_args()
@@ -613,6 +613,78 @@ def attention_bench(wl, steps, device, pk):
     return out
 
 
+# fp32 FMA peak for the scan's roofline: 152 SMs x 128 fp32 lanes x 2 flops per FMA x the maximum SM
+# clock (MEASURED_PEAKS.json "sm_max_mhz", 2070 MHz on this pool): 80.5 TFLOP/s.
+def fp32_peak_tflops(pk):
+    return 152 * 128 * 2 * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+
+
+def scan_bytes(wl):
+    """Algorithmic bytes of one scan call: the state in and out (fp32), q, k, v (bf16), g and beta
+    (fp32) and o (fp32)."""
+    return 2 * wl.H * wl.D * wl.D * 4 + wl.T * wl.H * (3 * wl.D * 2 + 2 * 4 + wl.D * 4)
+
+
+def scan_flops(wl):
+    """Two 128-term dots and one 128-wide update per state row, token and head: 6 flops per state
+    element per token."""
+    return 6 * wl.T * wl.H * wl.D * wl.D
+
+
+def scan_bench(wl, steps, device, pk):
+    """One step = wl.layers scan calls (each layer with its own state, updated in place, and its own
+    inputs), replayed as a CUDA graph; L2 is flushed (a 256 MB write) before every timed step, outside
+    the timed region, so each step starts with the states and inputs in HBM."""
+    import torch
+
+    import bit_quantized_expert_gb300 as moe
+    layers = [synth.torch_make_scan(wl.T, wl.H, wl.D, seed=l, device=device, fresh=wl.fresh) for l in range(wl.layers)]
+    gd = moe.gdn_dims(wl.T, wl.H, wl.D, wl.D)
+    ws = moe.alloc_gdn_workspace(gd, device)
+    o = torch.empty((wl.layers, wl.T, wl.H, wl.D), dtype=torch.float32, device=device)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=device)
+    stream = torch.cuda.Stream(device=device)
+
+    def step():
+        for l, c in enumerate(layers):
+            moe.gdn_scan(gd, c["q"], c["k"], c["v"], c["g"], c["beta"], c["S0"], c["S0"], o[l], ws)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    stream.synchronize()
+    gr = capture(step, stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            gr.replay()
+        for e0, e1 in ev:
+            flush.fill_(1.0)
+            e0.record(stream)
+            gr.replay()
+            e1.record(stream)
+    stream.synchronize()
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in ev)
+    flags = moe.read_error_flags(ws)
+    step_s = ms / 1e3 / steps
+    call_s = step_s / wl.layers
+    nbytes, flops = scan_bytes(wl), scan_flops(wl)
+    peak_f = fp32_peak_tflops(pk)
+    log(f"{wl.name}: {call_s * 1e6:.2f} us per layer call")
+    out = {"workload": wl.name, "ms_per_step": ms / steps, "us_per_layer_call": call_s * 1e6, "steps": steps,
+           "layers": wl.layers, "flags": flags, "value": wl.T / call_s, "unit": "tokens/s per layer",
+           "hbm": {"achieved": nbytes / call_s / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                   "frac": nbytes / call_s / 1e9 / pk["hbm_gbs"], "algorithmic_bytes_per_call": nbytes},
+           "alu": {"achieved": flops / call_s / 1e12, "peak": peak_f, "unit": "TFLOP/s",
+                   "frac": flops / call_s / 1e12 / peak_f, "algorithmic_flops_per_call": flops,
+                   "note": "fp32 peak derived from 152 SMs x 128 lanes x 2 x max SM clock"},
+           "l2": "flushed before every timed step",
+           "gpu_launches_per_step": wl.layers}
+    del layers
+    torch.cuda.empty_cache()
+    return out
+
+
 def oracle_rate(budget_s: float, max_tokens: int | None = None):
     """The float64 oracle on decode tokens of one layer (its cost does not depend on the weights)."""
     from oracle import moe_oracle as O
@@ -676,6 +748,9 @@ def run_profile(args):
     if args.profile == "attention":
         run_profile_attention(args)
         return
+    if args.profile == "scan":
+        run_profile_scan(args)
+        return
     wl = {"decode": synth.DECODE, "prefill": synth.PREFILL, "skewed": synth.SKEWED, "stack": synth.STACK}[args.profile]
     n = args.profile_sets
     layers = make_layers(wl, device, n)
@@ -724,6 +799,29 @@ def run_profile_attention(args):
     print(json.dumps({"profile": wl.name, "calls": total, "caches": n, "flags": moe.read_error_flags(ws)}), flush=True)
 
 
+def run_profile_scan(args):
+    """Eager scan calls over a 512-token prompt (16 heads), cycling `profile_sets` input sets."""
+    import torch
+
+    import bit_quantized_expert_gb300 as moe
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    moe.load_library()
+    wl = synth.SCAN_512
+    n = max(2, args.profile_sets)
+    sets = [synth.torch_make_scan(wl.T, wl.H, wl.D, seed=l, device=device, fresh=wl.fresh) for l in range(n)]
+    gd = moe.gdn_dims(wl.T, wl.H)
+    ws = moe.alloc_gdn_workspace(gd, device)
+    o = torch.empty((wl.T, wl.H, wl.D), dtype=torch.float32, device=device)
+    torch.cuda.synchronize()
+    total = args.warmup + args.steps
+    for s in range(total):
+        c = sets[s % n]
+        moe.gdn_scan(gd, c["q"], c["k"], c["v"], c["g"], c["beta"], c["S0"], c["S0"], o, ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": wl.name, "calls": total, "sets": n, "flags": moe.read_error_flags(ws)}), flush=True)
+
+
 def main():
     args = parse()
     if args.profile is not None:
@@ -746,12 +844,13 @@ def main():
     pk = peaks()
 
     res = decode_bench(args, world, rank, local, device, pk)
-    extras, attn = [], None
+    extras, attn, scan = [], None, None
     if not args.no_extras and rank == 0:
         extras.append(prefill_bench(synth.PREFILL, 48, device, pk))
         extras.append(prefill_bench(synth.SKEWED, 24, device, pk))
         extras.append(stack_bench(synth.STACK, 5, device, pk))
         attn = [attention_bench(w, 20, device, pk) for w in (synth.GQA_32K, synth.GQA_64K, synth.GQA_128K)]
+        scan = [scan_bench(w, 10, device, pk) for w in (synth.SCAN_DECODE, synth.SCAN_512, synth.SCAN_2048)]
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n, el = oracle_rate(20.0)
@@ -765,7 +864,7 @@ def main():
                 "gpu_launches": res["gpu_launches"], "clocks": res["clocks"], "error_flags": res["flags"],
                 "decode_hot_l2": res.get("hot_l2"), "decode_e2e_staged": res.get("e2e_staged"),
                 "decode_small_T": res.get("small_T"), "decode_loads_only": res.get("loads_only"),
-                "prefill": extras, "gqa_decode_attention": attn}
+                "prefill": extras, "gqa_decode_attention": attn, "deltanet_scan": scan}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -15,12 +15,13 @@ import os
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG_DIR, "libmoe_gb300.so")
 
-# Symbols declared in include/moe.h, include/gqa_attention.h and include/moe_probe.h.
+# Symbols declared in include/moe.h, include/gqa_attention.h, include/deltanet_scan.h and
+# include/moe_probe.h.
 EXPORTED = ("moe_status_string", "moe_max_tiles", "moe_workspace_bytes", "moe_route",
             "moe_expert_forward", "moe_layer_forward", "moe_rmsnorm_router", "moe_clear_error_flags",
             "moe_read_error_flags", "moe_layer_forward_decode_noalloc", "moe_workspace_bytes_host",
             "moe_layer_forward_host", "moe_decode_stream_probe", "gqa_decode_workspace_bytes",
-            "gqa_decode_attention")
+            "gqa_decode_attention", "gdn_scan_workspace_bytes", "gdn_scan")
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_MISALIGNED",
           4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA"}
@@ -49,6 +50,10 @@ class ExpertsC(ctypes.Structure):
 class GqaDims(ctypes.Structure):
     _fields_ = [("n_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("n_ctx", ctypes.c_int32), ("capacity", ctypes.c_int32)]
+
+
+class GdnDims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32)]
 
 
 class RoutingC(ctypes.Structure):
@@ -99,6 +104,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gqa_decode_workspace_bytes.argtypes = [P(GqaDims)]
     lib.gqa_decode_attention.restype = ctypes.c_int
     lib.gqa_decode_attention.argtypes = [P(GqaDims), VP, VP, VP, VP, VP, S, VP]
+    lib.gdn_scan_workspace_bytes.restype = S
+    lib.gdn_scan_workspace_bytes.argtypes = [P(GdnDims)]
+    lib.gdn_scan.restype = ctypes.c_int
+    lib.gdn_scan.argtypes = [P(GdnDims), VP, VP, VP, VP, VP, VP, VP, VP, VP, S, VP]
     lib.moe_clear_error_flags.restype = ctypes.c_int
     lib.moe_clear_error_flags.argtypes = [VP, S, VP]
     lib.moe_read_error_flags.restype = ctypes.c_int
@@ -286,6 +295,27 @@ def gqa_decode_attention(gd: GqaDims, q, k_cache, v_cache, o, workspace, stream=
     _check(load_library().gqa_decode_attention(ctypes.byref(gd), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o),
                                                _ptr(workspace), workspace.numel(), _stream(stream)),
            "gqa_decode_attention")
+
+
+def gdn_dims(T, H, d_k=128, d_v=128) -> GdnDims:
+    return GdnDims(int(T), int(H), int(d_k), int(d_v))
+
+
+def alloc_gdn_workspace(gd: GdnDims, device="cuda"):
+    """Workspace of the Gated DeltaNet scan (its error word), cleared."""
+    import torch
+    n = load_library().gdn_scan_workspace_bytes(ctypes.byref(gd))
+    if n == 0:
+        raise MoeError(1, "gdn_scan_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def gdn_scan(gd: GdnDims, q, k, v, g, beta, state_in, state_out, o, workspace, stream=None):
+    """Gated delta rule over gd.T tokens: q, k, v bf16 [T, H, 128]; g, beta fp32 [T, H];
+    state_in / state_out fp32 [H, 128, 128] (may be the same tensor); o fp32 [T, H, 128]."""
+    _check(load_library().gdn_scan(ctypes.byref(gd), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in),
+                                   _ptr(state_out), _ptr(o), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "gdn_scan")
 
 
 def read_error_flags(workspace, stream=None) -> int:

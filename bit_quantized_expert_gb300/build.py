@@ -1,4 +1,4 @@
-"""Build the sm_103a MoE and decode-attention library in-tree: one nvcc process per translation unit (in parallel),
+"""Build the sm_103a library (MoE layer, decode attention, DeltaNet scan) in-tree: one nvcc process per translation unit (in parallel),
 then one link step.  Output: bit_quantized_expert_gb300/libmoe_gb300.so.
 
     python -m bit_quantized_expert_gb300.build [--force]
@@ -15,7 +15,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
-SOURCES = ["api.cu", "route.cu", "gemm.cu", "decode.cu", "router.cu", "noalloc.cu", "attention.cu"]
+SOURCES = ["api.cu", "route.cu", "gemm.cu", "decode.cu", "router.cu", "noalloc.cu", "attention.cu", "deltanet.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-v"]

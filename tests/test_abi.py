@@ -18,7 +18,7 @@ def _declared():
         if h.endswith(".h"):
             with open(os.path.join(ROOT, "include", h)) as f:
                 src = f.read()
-            names |= set(re.findall(r"^\s*(?:const\s+)?[\w\*\s]+?\b((?:moe|gqa)_\w+)\s*\(", src, re.M))
+            names |= set(re.findall(r"^\s*(?:const\s+)?[\w\*\s]+?\b((?:moe|gqa|gdn)_\w+)\s*\(", src, re.M))
     return sorted(names)
 
 
@@ -170,3 +170,19 @@ def test_gqa_host_checks(lib):
     assert call(dims=moe.gqa_dims(16, 2, 128, 101, 100)) == 1
     assert call(dims=moe.gqa_dims(16, 2, 64, 100)) == 2
     assert call(dims=moe.gqa_dims(32, 2, 128, 100)) == 2
+
+
+def test_gdn_workspace_and_host_checks(lib):
+    """include/deltanet_scan.h: the workspace is the 256-byte error-word head; 1 for a null pointer,
+    T < 0 or H < 1; 2 for sizes other than 128; 3 for a misaligned pointer; 4 for a short workspace."""
+    gd = moe.gdn_dims(64, 16)
+    assert lib.gdn_scan_workspace_bytes(ctypes.byref(gd)) == 256
+    for bad in (moe.gdn_dims(-1, 16), moe.gdn_dims(4, 0), moe.gdn_dims(4, 16, 64), moe.gdn_dims(4, 16, 128, 256)):
+        assert lib.gdn_scan_workspace_bytes(ctypes.byref(bad)) == 0
+    call = lambda dims=gd, q=16, k=16, v=16, g=16, b=16, si=16, so=16, o=16, ws=16, nb=256: lib.gdn_scan(
+        ctypes.byref(dims), q, k, v, g, b, si, so, o, ws, nb, None)
+    assert call(q=None) == 1 and call(si=None) == 1 and call(so=None) == 1 and call(ws=None) == 1
+    assert call(dims=moe.gdn_dims(-3, 16)) == 1 and call(dims=moe.gdn_dims(3, 0)) == 1
+    assert call(dims=moe.gdn_dims(3, 16, 64, 64)) == 2
+    assert call(k=24) == 3 and call(g=20) == 3 and call(so=8) == 3
+    assert call(nb=255) == 4
