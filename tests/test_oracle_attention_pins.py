@@ -98,3 +98,19 @@ def test_position_order_does_not_matter():
     a = A.gqa_decode_attention(q, k, v)
     b = A.gqa_decode_attention(q, k[:, perm], v[:, perm])
     assert np.allclose(a, b, rtol=1e-13, atol=1e-15)
+
+
+def test_large_scores_do_not_overflow():
+    """Scores of several thousand (far beyond exp's range): the result is the value of the single
+    highest-scoring position, finite, as the softmax's definition gives."""
+    D, N = 64, 6
+    q = np.zeros((1, D))
+    q[0, 0] = 256.0
+    k = np.zeros((1, N, D))
+    k[0, :, 0] = 128.0
+    k[0, 3, 0] = 256.0                      # score 8192 against 4096 for the others
+    rng = np.random.default_rng(6)
+    v = rng.standard_normal((1, N, D))
+    o = A.gqa_decode_attention(_bits(q), _bits(k), _bits(v))
+    assert np.isfinite(o).all()
+    assert np.array_equal(o[0], A.bf16_to_f64(_bits(v))[0, 3])
