@@ -629,3 +629,80 @@ def test_decode_stream_probe_moves_the_decode_weights_cleanly():
         moe.decode_stream_probe(moe.dims(2, wl.d, wl.E, wl.k, wl.F, wl.F_shared), r["idx"][0], dl["routed"],
                                 dl["shared"], ws)
     assert ei.value.status == 2
+
+
+def test_graph_replay_of_layer_calls():
+    """Three layers of a small stack (residual add, RMSNorm and router, then the layer on the
+    grouped-GEMM path), captured in one CUDA graph and replayed twice: bit for bit the eager result,
+    and each replayed layer's output within the exact bar of the oracle fed that layer's inputs.
+    The same for four decode layer calls in a graph (the decode launch and its reduce launch per
+    call, under programmatic dependent launch)."""
+    wl = synth.Workload("graph_mid", T=200, d=512, E=32, k=4, F=256, F_shared=256)
+    L = 3
+    hosts = [synth.make_layer(wl, seed=l) for l in range(L)]
+    routers = [synth.make_router(wl, seed=l) for l in range(L)]
+    dls = [moe.to_device_layer(hh) for hh in hosts]
+    dm = moe.dims(wl.T, wl.d, wl.E, wl.k, wl.F, wl.F_shared)
+    ws = moe.alloc_workspace(dm)
+    x0 = dev(np.random.default_rng(9).standard_normal((wl.T, wl.d)).astype(np.float32))
+    x = x0.clone()
+    hs = [torch.empty((wl.T, wl.d), dtype=torch.int16, device="cuda") for _ in range(L)]
+    lgs = [torch.empty((wl.T, wl.E), dtype=torch.float32, device="cuda") for _ in range(L)]
+    ys = [torch.empty((wl.T, wl.d), dtype=torch.float32, device="cuda") for _ in range(L)]
+    gam = [dev(r["gamma"]) for r in routers]
+    wr = [dev(r["w_router"]) for r in routers]
+
+    def chain():
+        for l in range(L):
+            moe.rmsnorm_router(dm, x, ys[l - 1] if l > 0 else None, gam[l], wr[l], 1e-6, hs[l], lgs[l], ws)
+            moe.layer_forward(dm, hs[l], lgs[l], dls[l]["routed"], dls[l]["shared"], dls[l]["w_sg"], ys[l], ws)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        chain()
+    s.synchronize()
+    eager = [y.cpu().numpy() for y in ys]
+    eager_x = x.cpu().numpy()
+    x.copy_(x0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        chain()
+    for _ in range(2):
+        x.copy_(x0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(x.cpu().numpy(), eager_x)
+        for l in range(L):
+            assert np.array_equal(ys[l].cpu().numpy(), eager[l]), l
+    assert moe.read_error_flags(ws) == 0
+    for l in range(L):
+        ref = O.moe_layer(hs[l].cpu().numpy().view(np.uint16), lgs[l].cpu().numpy(), hosts[l], wl.k)["y"]
+        assert rowwise_err(ys[l].cpu().numpy(), ref) <= EXACT_TOL, l
+
+    # decode: four layer calls of one token each in one graph
+    wd = synth.DECODE
+    host, dl = layer_for(wd)
+    dmd = moe.dims(1, wd.d, wd.E, wd.k, wd.F, wd.F_shared)
+    wsd = moe.alloc_workspace(dmd)
+    inp = synth.make_inputs(wd, seed=13, T=4)
+    xs, lgd = dev(inp["x"]), dev(inp["logits"])
+    yd = torch.empty((4, wd.d), dtype=torch.float32, device="cuda")
+
+    def dchain():
+        for t in range(4):
+            moe.layer_forward(dmd, xs[t:t + 1], lgd[t:t + 1], dl["routed"], dl["shared"], dl["w_sg"], yd[t:t + 1], wsd)
+
+    with torch.cuda.stream(s):
+        dchain()
+    s.synchronize()
+    eager_d = yd.cpu().numpy()
+    gd = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gd, stream=s):
+        dchain()
+    yd.zero_()
+    gd.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(yd.cpu().numpy(), eager_d)
+    assert moe.read_error_flags(wsd) == 0
+    ref = O.moe_layer(inp["x"], inp["logits"], host, wd.k)["y"]
+    assert rowwise_err(eager_d, ref) <= DECODE_TOL
