@@ -58,6 +58,7 @@ constexpr int kMaxE = 1024;
 constexpr int kThreadsDec = 256;
 constexpr int kWarpsDec = kThreadsDec / 32;
 constexpr int kSliceRows = 128;        // rows of y per combine slice
+constexpr int kMaxDecodeD = 2048;      // one quantisation group of the gate/up rows per lane
 
 // ---------------------------------------------------------------- exact integer dot products
 // Activations v_c become 23-bit two's-complement fixed point V_c = round(v_c 2^(22-e)), with e the
@@ -106,18 +107,19 @@ __device__ __forceinline__ void pack4(int v0, int v1, int v2, int v3, uint32_t& 
 // The 64 bf16 activations of one quantisation group (eight uint4 = columns 0..63) -> planes with
 // one exponent.  Returns false when a value is not finite.
 __device__ __forceinline__ bool planes_of_bf16(const uint4 (&xr)[8], Planes& P) {
-  uint32_t mb = 0;
-  float sum = 0.0f;
+  uint32_t mb4[4] = {0u, 0u, 0u, 0u};
+  float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // four partial sums: a short dependency chain
 #pragma unroll
   for (int c8 = 0; c8 < 8; ++c8) {
     const uint32_t wv[4] = {xr[c8].x, xr[c8].y, xr[c8].z, xr[c8].w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      mb = max(mb, (wv[i] << 16) & 0x7FFF0000u);
-      mb = max(mb, wv[i] & 0x7FFF0000u);
-      sum += bf16_bits_to_f32(wv[i] & 0xFFFFu) + bf16_bits_to_f32(wv[i] >> 16);
+      mb4[i] = max(mb4[i], max((wv[i] << 16) & 0x7FFF0000u, wv[i] & 0x7FFF0000u));
+      sum4[i] += bf16_bits_to_f32(wv[i] & 0xFFFFu) + bf16_bits_to_f32(wv[i] >> 16);
     }
   }
+  const uint32_t mb = max(max(mb4[0], mb4[1]), max(mb4[2], mb4[3]));
+  const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
   const int e = block_exponent(mb);
   const float sc = pow2i(22 - e);
   P.scale[0] = P.scale[1] = pow2i(e - 22);
@@ -404,6 +406,9 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
   __shared__ float hloc[RF];   // this CTA's h (rows f0 .. f0+31)
   __shared__ int vloc[RF];     // ... as 23-bit fixed point
   __shared__ int abort_s;
+  // One token: x is copied into shared memory as soon as the dependency wait ends, so its latency
+  // overlaps the top-k instead of queueing behind the weight copies issued after it.
+  __shared__ __align__(16) uint4 xs[kMulti ? 1 : kMaxDecodeD / 8];
   const int T = kMulti ? (a.T > 0 ? a.T : 1) : 1;
 
   if (tid == 0) {
@@ -424,6 +429,10 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
   if (shared_cta && warp == 0) issue(0, 7);
   if (tid == 32) prefetch_tmap(&maps.down[wset]);
   pdl_wait();   // x and logits from upstream kernels are complete and visible past this point
+  if (!kMulti) {   // 16-byte piece i at i ^ ((i / 8) % 8): lane l's eight pieces fall in distinct banks
+    for (int i = tid; i < d / 8; i += kThreadsDec) cp_async_16(smem_u32(&xs[i ^ ((i >> 3) & 7)]), a.x + (size_t)i * 8);
+    cp_async_commit();
+  }
 
   if (!kMulti) {
     if (!shared_cta) {
@@ -477,7 +486,8 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
     }
   }
   pdl_launch_dependents();
-  __syncthreads();   // e_s and wgt_s
+  if (!kMulti) cp_async_wait<0>();
+  __syncthreads();   // e_s and wgt_s (and, for one token, x in shared memory)
   cluster_wait_acquire();   // every CTA of the cluster runs (pairs with the arrive above)
 
   // Tokens one after another.  The slot's weights stay in shared memory while the slot's expert
@@ -496,8 +506,9 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
     uint4 xr[8];
 #pragma unroll
     for (int c8 = 0; c8 < 8; ++c8)
-      xr[c8] = active ? __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * d) + lane * 8 + c8)
-                      : make_uint4(0u, 0u, 0u, 0u);
+      xr[c8] = !active ? make_uint4(0u, 0u, 0u, 0u)
+               : kMulti ? __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * d) + lane * 8 + c8)
+                        : xs[(lane * 8 + c8) ^ (lane & 7)];
 
     // ---- gate/up: warp w computes gate and up of rows q*8 + w (q = 0..3) as slots s = 2q + mat;
     // a reduce-scatter leaves slot s fully summed in lane 4s.
