@@ -44,7 +44,7 @@ NI = 64   # distinct input rows per layer for decode
 # dram__bytes_read.sum + dram__bytes_write.sum of one decode layer call (its decode_layer_kernel and
 # decode_reduce_kernel launches) at the decode shape, from one ncu capture of
 # `bench.py --profile decode`; None whenever those kernels have changed since the capture.
-DECODE_NCU_TRAFFIC = 16300544
+DECODE_NCU_TRAFFIC = 16300672
 
 
 def parse():

@@ -440,7 +440,7 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
       else if (a.E <= kThreadsDec) block_topk<1>(a.logits, a.E, k, keys_s, cand, sel);
       else block_topk<kMaxE / kThreadsDec>(a.logits, a.E, k, keys_s, cand, sel);
       const int ej = cand_expert(sel[j]);
-      if (warp == 0) issue(ej, 1);   // quarter 0 first; the rest after this warp's x planes (below)
+      if (warp == 0) issue(ej, 7);   // all of the slot's weight copies at once
       if (tid == 0) e_s[0] = ej;
       if (warp == 2) {
         const float v = lane < k ? key_logit((uint32_t)(sel[lane] >> 32)) : 0.0f;
@@ -514,9 +514,6 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
     // a reduce-scatter leaves slot s fully summed in lane 4s.
     Planes xp;
     if (!planes_of_bf16(xr, xp) && active) raise_flag(a.err, kErrNonFinite);
-    // One token: the second wave of copies (quarters 1..3 and the down rows) leaves after every
-    // CTA's quarter-0 requests are queued, so each CTA's first quarter lands sooner.
-    if (!kMulti && !shared_cta && warp == 0) issue(e_t, 6);
     const float xsum = xp.sum;
     float v8[8];
 #pragma unroll
@@ -719,7 +716,7 @@ __global__ void __launch_bounds__(kThreadsDec, 2)
   };
   if (shared_cta && tid < 32) issue(0);
   pdl_wait();
-  if (!shared_cta && tid < 32) issue(__ldg(a.idx + j));   // the same two waves as the layer kernel, back to back
+  if (!shared_cta && tid < 32) issue(__ldg(a.idx + j));   // the same copies as the layer kernel, all at once
   pdl_launch_dependents();
   for (int i = 0; i <= kQuarters; ++i) mbar_wait_warp(smem_u32(&bars[i]), 0, &abort_s, a.err);
   __syncthreads();
