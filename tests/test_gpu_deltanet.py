@@ -113,6 +113,29 @@ def test_split_calls_are_bit_identical():
     assert torch.equal(s_all, s2) and torch.equal(s_all, s_rep) and np.array_equal(o_all, o_rep)
 
 
+@pytest.mark.parametrize("T", [63, 64, 65, 95, 96, 97])
+def test_lengths_around_staging_chunks(T):
+    """Lengths on both sides of two and three 32-token staging chunks, from a non-zero state."""
+    inp = synth.make_scan(T, 3, 128, seed=T)
+    o, s_out, flags = _run(inp, T, 3)
+    assert flags == 0
+    _check(o, s_out, inp, T, "chunks")
+
+
+def test_strong_decay_and_repeated_keys():
+    """Decay down to 0.05 per token and a run of twenty identical keys written with strength 0.99:
+    still within the bar."""
+    T, H = 192, 2
+    inp = synth.make_scan(T, H, 128, seed=23)
+    rng = np.random.default_rng(24)
+    inp["g"] = np.log(rng.uniform(0.05, 1.0, (T, H))).astype(np.float32)
+    inp["k"][10:30] = inp["k"][10]
+    inp["beta"][10:30] = 0.99
+    o, s_out, flags = _run(inp, T, H)
+    assert flags == 0
+    _check(o, s_out, inp, T, "strong decay")
+
+
 def test_zero_keys_only_decay():
     """Tokens whose key is all zeros write nothing (k^ = 0): the state only decays."""
     T, H = 40, 2
