@@ -7,7 +7,8 @@ MoE layers, each with its own seeded weight set (40 x 455 MB = 18.2 GB resident 
 no layer's experts are in L2 when it runs) and its own precomputed input row.  `value` counts
 MoE-layer tokens per second (40 per step per GPU).  The line also carries, under `prefill`,
 one layer call at T = 512 and at T = 4096 (Zipf-skewed routing) and the 40-layer stack at
-T = 2048 (pre-norm block + layer per layer), and a hot-L2 single-layer decode figure.
+T = 2048 (pre-norm block + layer per layer), the two layer calls again with bf16 tensor-core
+operands (`operands`: "bf16"), and a hot-L2 single-layer decode figure.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-extras]
 
@@ -416,13 +417,15 @@ def decode_bench(args, world, rank, local, device, pk):
     return res
 
 
-def prefill_bench(wl, steps, device, pk):
-    """One step = one layer call over T tokens; 40 weight sets cycled; CUDA-graph replay."""
+def prefill_bench(wl, steps, device, pk, operands="fp16"):
+    """One step = one layer call over T tokens; 40 weight sets cycled; CUDA-graph replay.
+    operands: the grouped GEMM's tensor-core operand type ("fp16", or "bf16" through
+    moe_layer_forward_opts)."""
     import torch
 
     import bit_quantized_expert_gb300 as moe
     n_sets = 8 if wl.T >= 4096 else 16
-    log(f"{wl.name}: generating {n_sets} weight sets")
+    log(f"{wl.name} ({operands} operands): generating {n_sets} weight sets")
     layers = make_layers(wl, device, n_sets)
     ins = [synth.torch_make_inputs(wl, seed=1000 + l, device=device) for l in range(n_sets)]
     y = torch.empty((wl.T, wl.d), dtype=torch.float32, device=device)
@@ -433,7 +436,7 @@ def prefill_bench(wl, steps, device, pk):
 
     def step(s):
         l = s % n_sets
-        layers[l].forward(ins[l]["x"], ins[l]["logits"], y, ws)
+        layers[l].forward(ins[l]["x"], ins[l]["logits"], y, ws, operands=operands)
 
     with torch.cuda.stream(stream):
         for s in range(3):
@@ -446,25 +449,27 @@ def prefill_bench(wl, steps, device, pk):
     stream.synchronize()
     steps = max(n_sets, steps // n_sets * n_sets)
     ms = timed_graph_steps(g_many, n_sets, g_one, steps, stream)
-    log(f"{wl.name}: {ms / steps * 1e3:.1f} us per step")
+    log(f"{wl.name} ({operands} operands): {ms / steps * 1e3:.1f} us per step")
     flags = moe.read_error_flags(ws)
     # touched experts per weight set (from the routing of that set's inputs)
     touched = []
     for l in range(n_sets):
         with torch.cuda.stream(stream):
-            layers[l].forward(ins[l]["x"], ins[l]["logits"], y, ws, routing=routing)
+            layers[l].forward(ins[l]["x"], ins[l]["logits"], y, ws, routing=routing, operands=operands)
         stream.synchronize()
         touched.append(int((routing["counts"] > 0).sum().item()))
     step_s = ms / 1e3 / steps
     bytes_avg = sum(layer_bytes(wl, wl.T, t) for t in touched) / n_sets
     flops = layer_flops(wl, wl.T)
-    out = {"workload": wl.name, "value": wl.T / step_s, "unit": "tokens/s", "ms_per_step": ms / steps,
+    out = {"workload": wl.name, "operands": operands, "value": wl.T / step_s, "unit": "tokens/s",
+           "ms_per_step": ms / steps,
            "steps": steps, "weight_sets": n_sets, "flags": flags,
            "hbm": {"achieved": bytes_avg / step_s / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
                    "frac": bytes_avg / step_s / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": bytes_avg},
            "tensor": {"achieved": flops / step_s / 1e12, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                       "frac": flops / step_s / 1e12 / pk["bf16_tflops"], "algorithmic_flops": flops,
-                      "note": "fp16 operands; peak is the measured bf16 dense rate (same nominal rate)"},
+                      "note": f"{operands} operands; peak is the measured bf16 dense rate (fp16 and bf16 share "
+                              "the nominal rate)"},
            # top-k, chunk histogram, chunk scan (with the GEMM walk order), chunk scatter, x permute,
            # gate/up GEMM, down GEMM, combine
            "gpu_launches_per_step": 8}
@@ -848,6 +853,8 @@ def main():
     if not args.no_extras and rank == 0:
         extras.append(prefill_bench(synth.PREFILL, 48, device, pk))
         extras.append(prefill_bench(synth.SKEWED, 24, device, pk))
+        extras.append(prefill_bench(synth.PREFILL, 48, device, pk, operands="bf16"))
+        extras.append(prefill_bench(synth.SKEWED, 24, device, pk, operands="bf16"))
         extras.append(stack_bench(synth.STACK, 5, device, pk))
         attn = [attention_bench(w, 20, device, pk) for w in (synth.GQA_32K, synth.GQA_64K, synth.GQA_128K)]
         scan = [scan_bench(w, 10, device, pk) for w in (synth.SCAN_DECODE, synth.SCAN_512, synth.SCAN_2048)]

@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(PKG_DIR, "libmoe_gb300.so")
 # Symbols declared in include/moe.h, include/gqa_attention.h, include/deltanet_scan.h and
 # include/moe_probe.h.
 EXPORTED = ("moe_status_string", "moe_max_tiles", "moe_workspace_bytes", "moe_route",
-            "moe_expert_forward", "moe_layer_forward", "moe_rmsnorm_router", "moe_clear_error_flags",
+            "moe_expert_forward", "moe_layer_forward", "moe_layer_forward_opts", "moe_rmsnorm_router",
+            "moe_clear_error_flags",
             "moe_read_error_flags", "moe_layer_forward_decode_noalloc", "moe_workspace_bytes_host",
             "moe_layer_forward_host", "moe_decode_stream_probe", "gqa_decode_workspace_bytes",
             "gqa_decode_attention", "gdn_scan_workspace_bytes", "gdn_scan")
@@ -26,6 +27,8 @@ EXPORTED = ("moe_status_string", "moe_max_tiles", "moe_workspace_bytes", "moe_ro
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_MISALIGNED",
           4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA"}
 ERR_WAIT_TIMEOUT, ERR_FP16_RANGE, ERR_BAD_ROUTING, ERR_NON_FINITE = 1, 2, 4, 8
+OPT_BF16_OPERANDS = 1
+_OPERAND_OPTS = {"fp16": 0, "bf16": OPT_BF16_OPERANDS}
 
 
 class MoeError(RuntimeError):
@@ -90,6 +93,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_expert_forward.argtypes = [P(Dims), VP, P(RoutingC), P(ExpertsC), P(ExpertsC), VP, VP, S, VP]
     lib.moe_layer_forward.restype = ctypes.c_int
     lib.moe_layer_forward.argtypes = [P(Dims), VP, VP, P(ExpertsC), P(ExpertsC), VP, VP, P(RoutingC), VP, S, VP]
+    lib.moe_layer_forward_opts.restype = ctypes.c_int
+    lib.moe_layer_forward_opts.argtypes = [P(Dims), VP, VP, P(ExpertsC), P(ExpertsC), VP, VP, P(RoutingC), VP, S, VP,
+                                           ctypes.c_uint32]
     lib.moe_rmsnorm_router.restype = ctypes.c_int
     lib.moe_rmsnorm_router.argtypes = [P(Dims), VP, VP, VP, VP, ctypes.c_float, VP, VP, VP, S, VP]
     lib.moe_workspace_bytes_host.restype = S
@@ -235,13 +241,16 @@ def expert_forward(dm: Dims, x, routing: dict, routed: dict, shared: dict | None
 
 
 def layer_forward(dm: Dims, x, logits, routed: dict, shared: dict | None, w_sg, y, workspace,
-                  routing: dict | None = None, stream=None):
+                  routing: dict | None = None, stream=None, operands: str = "fp16"):
+    """operands: the grouped-GEMM path's tensor-core operand type, "fp16" (moe_layer_forward) or
+    "bf16" (moe_layer_forward_opts with MOE_OPT_BF16_OPERANDS)."""
     re, se = experts_struct(routed), experts_struct(shared)
     r = routing_struct(routing) if routing is not None else None
-    _check(load_library().moe_layer_forward(ctypes.byref(dm), _ptr(x), _ptr(logits), ctypes.byref(re),
-                                            ctypes.byref(se) if se is not None else None, _ptr(w_sg), _ptr(y),
-                                            ctypes.byref(r) if r is not None else None, _ptr(workspace),
-                                            workspace.numel(), _stream(stream)), "moe_layer_forward")
+    _check(load_library().moe_layer_forward_opts(ctypes.byref(dm), _ptr(x), _ptr(logits), ctypes.byref(re),
+                                                 ctypes.byref(se) if se is not None else None, _ptr(w_sg), _ptr(y),
+                                                 ctypes.byref(r) if r is not None else None, _ptr(workspace),
+                                                 workspace.numel(), _stream(stream), _OPERAND_OPTS[operands]),
+           "moe_layer_forward_opts")
 
 
 def rmsnorm_router(dm: Dims, x_resid, y_prev, gamma, w_router, eps: float, h_out, logits_out, workspace,
@@ -354,14 +363,19 @@ class Layer:
             _ptr(self.w_sg), _host_ptr(y_host), _ptr(workspace), workspace.numel(), _stream(stream)),
             "moe_layer_forward_host")
 
-    def forward(self, x, logits, y, workspace, routing: dict | None = None, stream=None):
+    def forward(self, x, logits, y, workspace, routing: dict | None = None, stream=None, operands: str = "fp16"):
+        """operands: "fp16" (moe_layer_forward) or "bf16" (moe_layer_forward_opts with bf16
+        tensor-core operands on the grouped-GEMM path)."""
         dm = self.dims(x.shape[0])
         r = routing_struct(routing) if routing is not None else None
-        _check(load_library().moe_layer_forward(ctypes.byref(dm), _ptr(x), _ptr(logits), ctypes.byref(self._re),
-                                                ctypes.byref(self._se) if self._se is not None else None,
-                                                _ptr(self.w_sg), _ptr(y), ctypes.byref(r) if r is not None else None,
-                                                _ptr(workspace), workspace.numel(), _stream(stream)),
-               "moe_layer_forward")
+        lib = load_library()
+        args = (ctypes.byref(dm), _ptr(x), _ptr(logits), ctypes.byref(self._re),
+                ctypes.byref(self._se) if self._se is not None else None, _ptr(self.w_sg), _ptr(y),
+                ctypes.byref(r) if r is not None else None, _ptr(workspace), workspace.numel(), _stream(stream))
+        if operands == "fp16":
+            _check(lib.moe_layer_forward(*args), "moe_layer_forward")
+        else:
+            _check(lib.moe_layer_forward_opts(*args, _OPERAND_OPTS[operands]), "moe_layer_forward_opts")
 
 
 def to_device_layer(layer: dict, device="cuda") -> dict:

@@ -225,8 +225,8 @@ RoutingPtrs caller_routing(const moe_routing* r) {
 
 cudaError_t run_routing(const moe_dims& d, const float* logits, const RoutingPtrs& R, const uint16_t* x,
                         const uint16_t* w_sg, float* gs, int32_t* chunk, uint32_t* err, cudaStream_t st,
-                        int32_t* sched = nullptr) {
-  RouteArgs ra{logits, d.T, d.E, d.k, d.d, R.idx, R.w, x, w_sg, gs, err};
+                        int32_t* sched = nullptr, bool bf = false) {
+  RouteArgs ra{logits, d.T, d.E, d.k, d.d, R.idx, R.w, x, w_sg, gs, err, bf ? 1 : 0};
   cudaError_t e = launch_topk(ra, st);
   if (e != cudaSuccess) return e;
   TablesArgs ta{R.idx, d.T, d.E, d.k, R.tile_n, d.F_shared > 0 ? 1 : 0, R.counts, R.offsets, R.perm, R.inv,
@@ -236,11 +236,11 @@ cudaError_t run_routing(const moe_dims& d, const float* logits, const RoutingPtr
 
 QPtr qptr(const moe_qmat& q) { return QPtr{q.codes, q.scales, q.biases}; }
 
-// x rows in slot order (fp16), gate/up GEMM (h), then down GEMM (expert outputs: fp32 y_perm, or
-// fp16 y16 when y16 is non-null) over the block map in R.
+// x rows in slot order (fp16, or bf16 when bf is set), gate/up GEMM (h), then down GEMM (expert
+// outputs: fp32 y_perm, or 16-bit y16 when y16 is non-null) over the block map in R.
 moe_status run_experts(const moe_dims& d, const RoutingPtrs& R, const moe_experts* routed, const moe_experts* shared,
                        const uint16_t* x, uint16_t* xperm, uint16_t* h, float* y_perm, uint16_t* y16,
-                       int32_t* sched, uint32_t* err, cudaStream_t st, bool sched_ready = false) {
+                       int32_t* sched, uint32_t* err, cudaStream_t st, bool sched_ready = false, bool bf = false) {
   // the down GEMM pairs 128-row blocks of the output dimension; activation stages hold 112 rows
   if (d.d % 256 != 0 || R.tile_n > kGemmMaxTileN) return MOE_ERR_UNSUPPORTED;
   const bool sh = shared != nullptr && d.F_shared > 0;
@@ -259,7 +259,7 @@ moe_status run_experts(const moe_dims& d, const RoutingPtrs& R, const moe_expert
             encode_f16_rows(&m0.x, xperm, slots, d.d, kGemmMaxTileN) &&
             encode_f16_rows(&m1.h16, h, slots, d.F, 16) && encode_f16_rows(&m0.x16, xperm, slots, d.d, 16);
   if (!ok) return MOE_ERR_CUDA;
-  PermuteArgs pa{x, R.perm, d.T, d.k, d.d, (int)slots, xperm, err};
+  PermuteArgs pa{x, R.perm, d.T, d.k, d.d, (int)slots, xperm, err, bf ? 1 : 0};
   if (launch_permute_x(pa, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (!sched_ready) {   // the layer path's routing already wrote it
     ScheduleArgs sa{R.tiles, R.num_tiles, R.tile_n, sched, err};
@@ -285,6 +285,7 @@ moe_status run_experts(const moe_dims& d, const RoutingPtrs& R, const moe_expert
   a.y_perm = y_perm;
   a.y16 = y16;
   a.err = err;
+  a.bf16 = bf ? 1 : 0;
   a.mat[0][0] = qptr(routed->gate);
   a.mat[0][1] = qptr(s_or_r->gate);
   a.mat[1][0] = qptr(routed->up);
@@ -373,6 +374,16 @@ moe_status moe_expert_forward(const moe_dims* dims, const uint16_t* x, const moe
 moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const float* logits, const moe_experts* routed,
                              const moe_experts* shared, const uint16_t* w_shared_gate, float* y,
                              const moe_routing* routing_out, void* workspace, size_t workspace_bytes, void* stream) {
+  return moe_layer_forward_opts(dims, x, logits, routed, shared, w_shared_gate, y, routing_out, workspace,
+                                workspace_bytes, stream, 0u);
+}
+
+moe_status moe_layer_forward_opts(const moe_dims* dims, const uint16_t* x, const float* logits,
+                                  const moe_experts* routed, const moe_experts* shared,
+                                  const uint16_t* w_shared_gate, float* y, const moe_routing* routing_out,
+                                  void* workspace, size_t workspace_bytes, void* stream, uint32_t options) {
+  if (options & ~(uint32_t)MOE_OPT_BF16_OPERANDS) return MOE_ERR_INVALID_ARG;
+  const bool bf = (options & MOE_OPT_BF16_OPERANDS) != 0;
   moe_status s = check_dims(dims);
   if (s != MOE_OK) return s;
   if ((s = check_experts(routed)) != MOE_OK) return s;
@@ -434,13 +445,13 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
   uint16_t* xperm = at<uint16_t>(workspace, L.xperm);
   float* gs = sh ? at<float>(workspace, L.gs) : nullptr;
   cudaError_t e = run_routing(d, logits, R, x, sh ? w_shared_gate : nullptr, gs, at<int32_t>(workspace, L.chunk), err, st,
-                              at<int32_t>(workspace, L.sched));
+                              at<int32_t>(workspace, L.sched), bf);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   uint16_t* y16 = at<uint16_t>(workspace, L.yperm);
   s = run_experts(d, R, routed, sh ? shared : nullptr, x, xperm, at<uint16_t>(workspace, L.h), nullptr, y16,
-                  at<int32_t>(workspace, L.sched), err, st, true);
+                  at<int32_t>(workspace, L.sched), err, st, true, bf);
   if (s != MOE_OK) return s;
-  CombineArgs cb{nullptr, y16, R.inv, R.w, gs, d.T, d.k, d.d, y};
+  CombineArgs cb{nullptr, y16, R.inv, R.w, gs, d.T, d.k, d.d, y, bf ? 1 : 0};
   return cuda_status(launch_combine(cb, st));
 }
 

@@ -25,7 +25,9 @@
 //     epilogue of one unit overlap the MMAs of the next.
 //   * Operands are fp16 (the dequantised weights, x and h), accumulation fp32.  Within every
 //     8-element K chunk both operands are stored in the order (0,4,1,5,2,6,3,7), which lets the
-//     dequant turn one 32-bit code word into four fp16 pairs with one LOP3 each.
+//     dequant turn one 32-bit code word into four fp16 pairs with one LOP3 each.  An instantiation
+//     with bf16 operands (BF) serves callers that ask for them: the same roles and layout, bf16
+//     weights w = q*s + b (one rounding), x as given, bf16 h, and bf16 expert outputs.
 //   * Every wait is bounded (mbar_wait); on timeout the CTA sets the error word and winds down.
 #include "common.cuh"
 #include "kernels.h"
@@ -127,7 +129,25 @@ __device__ __forceinline__ void dequant_word(uint32_t q, __half2 s2, __half2 b2,
   }
 }
 
-template <int MODE>
+// The same for bf16 operands.  bf16 keeps 7 mantissa bits, so each code is shifted into bits 0-3 of
+// 128.0's mantissa (128 + q exactly) on its own and brought back by subtracting 128; then one bf16
+// fma gives w = q * s + b with a single rounding.
+__device__ __forceinline__ void dequant_word_bf16(uint32_t q, __nv_bfloat162 s2, __nv_bfloat162 b2, uint32_t (&o)[4]) {
+  const __nv_bfloat162 k128 = __halves2bfloat162(__ushort_as_bfloat16(0x4300), __ushort_as_bfloat16(0x4300));
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const uint32_t t = ((q >> (4 * p)) & 0x000F000Fu) | 0x43004300u;   // codes p and p + 4
+    __nv_bfloat162 v = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t), k128);   // exact codes
+    v = __hfma2(v, s2, b2);
+    o[p] = *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+__device__ __forceinline__ uint16_t f32_to_16(float v, bool bf) {
+  return bf ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
+}
+
+template <int MODE, bool BF>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
   using C = Cfg<MODE>;
   constexpr int NMAT = C::NMAT;
@@ -297,7 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const int b = li & 1;
         if (!mbar_wait(AE(b), ((li >> 1) & 1) ^ 1u, abort_s, a.err)) break;
         tc_fence_after();
-        const uint32_t idesc = idesc_f16_f32(kBM, n_inst);
+        // A and B formats: fp16 (0) or bf16 (1) in bits 7-9 and 10-12
+        const uint32_t idesc = idesc_f16_f32(kBM, n_inst) | (BF ? ((1u << 7) | (1u << 10)) : 0u);
         const uint32_t d0 = tmem + (uint32_t)(b * C::ACC_COLS);
         bool ok = true;
         for (int kc = 0; kc < KC; kc += 2) {
@@ -387,10 +408,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           const float bf1 = bf16_bits_to_f32(j == 0 ? pick_bf16<1>(cb) : j == 2 ? pick_bf16<3>(cb)
                                              : j == 4 ? pick_bf16<5>(cb) : pick_bf16<7>(cb));
           const float wm0 = fmaf(15.0f, fabsf(sf0), fabsf(bf0)), wm1 = fmaf(15.0f, fabsf(sf1), fabsf(bf1));
-          bad = bad || !(wm0 <= 65504.0f) || !(wm1 <= 65504.0f);
-          wmax = fmaxf(wmax, fmaxf(wm0, wm1));
+          if (!BF) {
+            bad = bad || !(wm0 <= 65504.0f) || !(wm1 <= 65504.0f);
+            wmax = fmaxf(wmax, fmaxf(wm0, wm1));
+          }
           const __half2 s2[2] = {__float2half2_rn(sf0), __float2half2_rn(sf1)};
           const __half2 b2[2] = {__float2half2_rn(bf0), __float2half2_rn(bf1)};
+          const __nv_bfloat162 sb2[2] = {__float2bfloat162_rn(sf0), __float2bfloat162_rn(sf1)};   // exact: bf16 given
+          const __nv_bfloat162 bb2[2] = {__float2bfloat162_rn(bf0), __float2bfloat162_rn(bf1)};
           // codes of both chunks: the two-chunk stage s.  It holds 64-byte rows in the 64-byte
           // swizzle: 16-byte piece c of row i sits at piece c ^ ((i >> 1) & 3), which keeps the
           // lanes' loads free of bank conflicts; chunk hc is pieces 2 hc and 2 hc + 1.
@@ -412,7 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
             for (int wd = 0; wd < NW; ++wd) {
               uint32_t o[4];
-              dequant_word(words[NW * hc + wd], s2[hc], b2[hc], o);
+              if (BF) dequant_word_bf16(words[NW * hc + wd], sb2[hc], bb2[hc], o);
+              else dequant_word(words[NW * hc + wd], s2[hc], b2[hc], o);
               st_shared_v4(dst + ((((uint32_t)(w0 + wd)) ^ swz) << 4), o[0], o[1], o[2], o[3]);
             }
           }
@@ -464,17 +490,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           uint32_t uu[16];
           tmem_ld16x2_wait(tb + n0, tb + 128 + n0, g, uu);
           const int pos = (lane & ~7) | chunk_pos(lane & 7);   // stored operand order of h
+          uint32_t big_m = 0u, nz_m = 0u;   // bit i: this lane's h of token n0 + i is >= 2^-12 / nonzero
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float gv = __uint_as_float(g[i]);
             const float hv = gv * __frcp_rn(1.0f + __expf(-gv)) * __uint_as_float(uu[i]);
             if (n0 + i < tl.z) amax = fmaxf(amax, fabsf(hv));
+            big_m |= (fabsf(hv) >= 2.44140625e-4f ? 1u : 0u) << i;
+            nz_m |= (hv != 0.0f ? 1u : 0u) << i;
+            st_shared_u16(stg + (uint32_t)(i * 32 + pos) * 2, f32_to_16(hv, BF));
+          }
+          if (!BF) {
             // a token whose h over this warp's 32 rows is nonzero but all below 2^-12 sits in fp16's
             // subnormal range (tiny activations): range flag
-            const unsigned big = __ballot_sync(0xFFFFFFFFu, fabsf(hv) >= 2.44140625e-4f);
-            const unsigned nz = __ballot_sync(0xFFFFFFFFu, hv != 0.0f);
-            tiny = tiny || (n0 + i < tl.z && big == 0u && nz != 0u);
-            st_shared_u16(stg + (uint32_t)(i * 32 + pos) * 2, __half_as_ushort(__float2half_rn(hv)));
+            const uint32_t big = __reduce_or_sync(0xFFFFFFFFu, big_m), nz = __reduce_or_sync(0xFFFFFFFFu, nz_m);
+            const uint32_t live = tl.z - n0 >= 16 ? 0xFFFFu : ((1u << (tl.z - n0)) - 1u);
+            tiny = tiny || ((nz & ~big & live) != 0u);
           }
           __syncwarp();
 #pragma unroll
@@ -500,8 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 const float v0 = __uint_as_float(g[i]), v1 = __uint_as_float(g1[i]);
                 if (n0 + i < tl.z) amax = fmaxf(amax, fabsf(v0));
                 if (n0 + 16 + i < tl.z) amax = fmaxf(amax, fabsf(v1));
-                st_shared_u16(stg + (uint32_t)(i * 32 + lane) * 2, __half_as_ushort(__float2half_rn(v0)));
-                st_shared_u16(stg + (uint32_t)((i + 16) * 32 + lane) * 2, __half_as_ushort(__float2half_rn(v1)));
+                st_shared_u16(stg + (uint32_t)(i * 32 + lane) * 2, f32_to_16(v0, BF));
+                st_shared_u16(stg + (uint32_t)((i + 16) * 32 + lane) * 2, f32_to_16(v1, BF));
               }
               __syncwarp();
 #pragma unroll
@@ -534,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       __syncwarp();
       if (lane == 0) mbar_arrive(AE(b));
     }
-    if (__any_sync(0xFFFFFFFFu, !(amax <= 65504.0f) || tiny) && lane == 0) raise_flag(a.err, kErrFp16Range);
+    if (!BF && __any_sync(0xFFFFFFFFu, !(amax <= 65504.0f) || tiny) && lane == 0) raise_flag(a.err, kErrFp16Range);
   }
 
   // Wind down.  After a timeout, give copies that may still be in flight time to land before
@@ -553,8 +584,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 }
 
 // y[t] = sum_j w[t,j] Y[inv[t,j]] + gs[t] Y[T*k + t], fp32 accumulation in j order.  Y is read as
-// fp16 (the layer path) or fp32 (expert outputs handed in by a caller), 8 or 4 values per load.
-template <bool HALF>
+// fp16 or bf16 (the layer path) or fp32 (expert outputs handed in by a caller), 8 or 4 values per load.
+template <bool HALF, bool BF>
 __global__ void combine_kernel(CombineArgs a) {
   constexpr int V = HALF ? 8 : 4;
   const int t = blockIdx.x;
@@ -570,9 +601,14 @@ __global__ void combine_kernel(CombineArgs a) {
         const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&qw[i]));
-          v[2 * i] = f.x;
-          v[2 * i + 1] = f.y;
+          if (BF) {
+            v[2 * i] = bf16_bits_to_f32(qw[i] & 0xFFFFu);
+            v[2 * i + 1] = bf16_bits_to_f32(qw[i] >> 16);
+          } else {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&qw[i]));
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+          }
         }
       } else {
         const float4 q = __ldg(reinterpret_cast<const float4*>(a.y_perm + row * a.d) + c);
@@ -594,11 +630,12 @@ __global__ void combine_kernel(CombineArgs a) {
 }
 
 // Row s of the gate/up activation operand: x of the token routed to slot s (slots below T*k
-// through the permutation, the shared expert's slots T*k + t are token t), converted to fp16 in
-// the operand chunk order.  Writing the rows in slot order lets the GEMM fetch every activation
+// through the permutation, the shared expert's slots T*k + t are token t), converted to fp16 (or
+// kept in bf16) in the operand chunk order.  Writing the rows in slot order lets the GEMM fetch every activation
 // tile with one TMA box load.
 constexpr int kPermRows = 8;   // rows per CTA step: eight independent loads in flight per thread
 
+template <bool BF>
 __global__ void __launch_bounds__(256) permute_x_kernel(PermuteArgs a) {
   const int nch = a.d / 8;
   const int Tk = a.T * a.k;
@@ -620,20 +657,29 @@ __global__ void __launch_bounds__(256) permute_x_kernel(PermuteArgs a) {
       for (int i = 0; i < kPermRows; ++i) {
         if (tok[i] < 0) continue;
         const uint32_t xw[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
-        float xf[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          xf[2 * e] = bf16_bits_to_f32(xw[e] & 0xFFFFu);
-          xf[2 * e + 1] = bf16_bits_to_f32(xw[e] >> 16);
-        }
         // stored order (0,4,1,5,2,6,3,7): word p holds logical elements (p, p+4)
         uint32_t o[4];
+        if (BF) {   // bf16 bits as given
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const __half lo = __float2half_rn(xf[p]);
-          const __half hi = __float2half_rn(xf[p + 4]);
-          bad = bad || (__hisinf(lo) != 0) || (__hisinf(hi) != 0);
-          o[p] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+          for (int p = 0; p < 4; ++p) {
+            const uint32_t lo = (xw[p >> 1] >> (16 * (p & 1))) & 0xFFFFu;
+            const uint32_t hi = (xw[(p + 4) >> 1] >> (16 * (p & 1))) & 0xFFFFu;
+            o[p] = lo | (hi << 16);
+          }
+        } else {
+          float xf[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            xf[2 * e] = bf16_bits_to_f32(xw[e] & 0xFFFFu);
+            xf[2 * e + 1] = bf16_bits_to_f32(xw[e] >> 16);
+          }
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const __half lo = __float2half_rn(xf[p]);
+            const __half hi = __float2half_rn(xf[p + 4]);
+            bad = bad || (__hisinf(lo) != 0) || (__hisinf(hi) != 0);
+            o[p] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+          }
         }
         reinterpret_cast<uint4*>(a.xperm + (size_t)(s0 + i) * a.d)[ch] = make_uint4(o[0], o[1], o[2], o[3]);
       }
@@ -651,21 +697,29 @@ cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmArgs& a, int g
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Cfg<0>::BYTES);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<1>::BYTES);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    const int b0 = (int)Cfg<0>::BYTES, b1 = (int)Cfg<1>::BYTES;
+    if ((e = cudaFuncSetAttribute(gemm_kernel<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, b0)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(gemm_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, b1)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(gemm_kernel<0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, b0)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(gemm_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, b1)) != cudaSuccess)
+      return e;
     configured_dev = dev;
   }
-  if (mode == 0) gemm_kernel<0><<<grid, kThreads, Cfg<0>::BYTES, st>>>(maps, a);
-  else gemm_kernel<1><<<grid, kThreads, Cfg<1>::BYTES, st>>>(maps, a);
+  if (a.bf16) {
+    if (mode == 0) gemm_kernel<0, true><<<grid, kThreads, Cfg<0>::BYTES, st>>>(maps, a);
+    else gemm_kernel<1, true><<<grid, kThreads, Cfg<1>::BYTES, st>>>(maps, a);
+  } else {
+    if (mode == 0) gemm_kernel<0, false><<<grid, kThreads, Cfg<0>::BYTES, st>>>(maps, a);
+    else gemm_kernel<1, false><<<grid, kThreads, Cfg<1>::BYTES, st>>>(maps, a);
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
-  if (a.y16 != nullptr) combine_kernel<true><<<a.T, 256, 0, st>>>(a);
-  else combine_kernel<false><<<a.T, 256, 0, st>>>(a);
+  if (a.y16 == nullptr) combine_kernel<false, false><<<a.T, 256, 0, st>>>(a);
+  else if (a.bf16) combine_kernel<true, true><<<a.T, 256, 0, st>>>(a);
+  else combine_kernel<true, false><<<a.T, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -673,7 +727,8 @@ cudaError_t launch_permute_x(const PermuteArgs& a, cudaStream_t st) {
   if (a.slots <= 0) return cudaSuccess;
   const int steps = (a.slots + kPermRows - 1) / kPermRows;
   const int grid = steps < 152 * 8 ? steps : 152 * 8;
-  permute_x_kernel<<<grid, 256, 0, st>>>(a);
+  if (a.bf16) permute_x_kernel<true><<<grid, 256, 0, st>>>(a);
+  else permute_x_kernel<false><<<grid, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 

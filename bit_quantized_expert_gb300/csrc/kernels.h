@@ -18,6 +18,7 @@ struct RouteArgs {
   const uint16_t* w_sg;  // bf16 [d] or null
   float* gs;             // [T] shared gate, or null
   uint32_t* err;
+  int bf16;              // the GEMM takes x as bf16: no fp16 range check of x
 };
 cudaError_t launch_topk(const RouteArgs& a, cudaStream_t st);
 
@@ -71,10 +72,11 @@ struct GemmArgs {
   const int32_t* perm;       // slot -> assignment (gate/up gathers x rows)
   QPtr mat[2][2];            // [matrix][routed/shared]: scales and biases read by the dequant warps
   int T, k, E, d, F;
-  uint16_t* h;               // gate/up output: fp16 [slots, F], operand chunk order
+  uint16_t* h;               // gate/up output: 16-bit [slots, F], operand chunk order
   float* y_perm;             // down output: fp32 [slots, d] (when y16 is null)
-  uint16_t* y16;             // down output: fp16 [slots, d], or null
+  uint16_t* y16;             // down output: 16-bit [slots, d], or null
   uint32_t* err;
+  int bf16;                  // operands (weights, x, h) and y16 in bf16 rather than fp16
 };
 size_t gemm_smem_bytes(int mode);
 cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmArgs& a, int grid, cudaStream_t st);
@@ -87,6 +89,7 @@ struct CombineArgs {
   const float* gs;        // [T] or null (no shared expert)
   int T, k, d;
   float* y;               // [T, d]
+  int bf16;               // y16 holds bf16 rather than fp16
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
 
@@ -94,8 +97,9 @@ struct PermuteArgs {
   const uint16_t* x;      // bf16 [T, d]
   const int32_t* perm;    // [T*k] slot -> assignment t*k + j
   int T, k, d, slots;     // slots = T*k (+ T with a shared expert)
-  uint16_t* xperm;        // fp16 [slots, d] operand chunk order: row s = x[token(s)]
+  uint16_t* xperm;        // fp16 (bf16 when bf16 is set) [slots, d] operand chunk order: row s = x[token(s)]
   uint32_t* err;
+  int bf16;
 };
 cudaError_t launch_permute_x(const PermuteArgs& a, cudaStream_t st);
 

@@ -33,7 +33,8 @@ __global__ void __launch_bounds__(256) topk_kernel(RouteArgs a) {
   // One pass over the token row (layer path): the shared-expert gate logit x . w_sg, and the
   // token's largest |x|.  The grouped GEMM takes x as fp16 operands: a token whose largest |x| is
   // nonzero but below 2^-12 sits mostly in fp16's subnormal range and loses precision there, so it
-  // sets the range flag (values above the fp16 range set it when x is converted).
+  // sets the range flag (values above the fp16 range set it when x is converted).  With bf16
+  // operands x is used as given and there is no such edge.
   if (a.x != nullptr) {
     const bool gate = a.gs != nullptr && a.w_sg != nullptr;
     const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)t * a.d);
@@ -55,7 +56,7 @@ __global__ void __launch_bounds__(256) topk_kernel(RouteArgs a) {
     for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, off);
     xmax = __reduce_max_sync(0xFFFFFFFFu, xmax);
     if (lane == 0 && gate) a.gs[t] = 1.0f / (1.0f + expf(-dot));
-    if (lane == 0 && xmax != 0u && xmax < kBf16TwoPowMinus12) raise_flag(a.err, kErrFp16Range);
+    if (lane == 0 && !a.bf16 && xmax != 0u && xmax < kBf16TwoPowMinus12) raise_flag(a.err, kErrFp16Range);
   }
 }
 

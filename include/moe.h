@@ -167,6 +167,22 @@ moe_status moe_layer_forward(const moe_dims* dims, const uint16_t* x, const floa
                              float* y, const moe_routing* routing_out, void* workspace, size_t workspace_bytes,
                              void* stream);
 
+/* Option bits of moe_layer_forward_opts. */
+#define MOE_OPT_BF16_OPERANDS 1u
+
+/* moe_layer_forward with options; options == 0 is moe_layer_forward.
+ * MOE_OPT_BF16_OPERANDS: the grouped-GEMM path takes bf16 tensor-core operands instead of fp16
+ * (the MMA rate is the same): w = q * s + b rounded once to bf16, x as given, h and the expert
+ * outputs rounded to bf16; accumulation and the weighted combine stay fp32.  bf16 has fp32's
+ * exponent range, so this path raises none of fp16's range flags (error bit 2), at about twice
+ * the rounding error of fp16 operands (8 significant bits against 11).  Calls that run the decode
+ * path (T <= 8) are unaffected: it has no tensor-core operands.
+ * Returns MOE_ERR_INVALID_ARG for an unknown option bit; otherwise as moe_layer_forward. */
+moe_status moe_layer_forward_opts(const moe_dims* dims, const uint16_t* x, const float* logits,
+                                  const moe_experts* routed, const moe_experts* shared,
+                                  const uint16_t* w_shared_gate, float* y, const moe_routing* routing_out,
+                                  void* workspace, size_t workspace_bytes, void* stream, uint32_t options);
+
 /* moe_layer_forward with the input and output in host memory: copies x_host (bf16 [T, d]) and
  * logits_host (fp32 [T, E]) to a staging area at the end of the workspace, runs the layer, and
  * copies y (fp32 [T, d]) back to y_host -- the copies and the kernels queued on `stream` in that

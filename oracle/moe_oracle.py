@@ -209,9 +209,10 @@ def expert_ffn(xe, Wg, Wu, Wd, operands=None, out16=False):
 
     operands: None for the exact path, or "fp16"/"bf16" to round the GEMM operands
     (weights, activations and h) to that type first, as the tensor-core path does.
-    out16: also round the expert's output rows to fp16, as the layer path of the tensor-core
-    kernels stores them before the weighted combine (an emulation choice only: the pages fix
-    no intermediate precision; the exact oracle never rounds).
+    out16: also round the expert's output rows to a 16-bit type before the weighted combine, as
+    the layer path of the tensor-core kernels stores them: True or "fp16" for fp16, "bf16" for
+    bf16 (an emulation choice only: the pages fix no intermediate precision; the exact oracle
+    never rounds).
     """
     rnd = _ROUNDERS[operands]
     if rnd is not None:
@@ -222,7 +223,9 @@ def expert_ffn(xe, Wg, Wu, Wd, operands=None, out16=False):
     if rnd is not None:
         h = rnd(h)
     out = h @ Wd.T
-    return round_fp16(out) if out16 else out
+    if not out16:
+        return out
+    return round_bf16(out) if out16 == "bf16" else round_fp16(out)
 
 
 def shared_gate(x, w_sg_bits):

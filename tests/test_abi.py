@@ -116,6 +116,24 @@ def test_layer_host_checks(lib):
     assert call(dm=dm_ns) == 1                 # a shared expert given but dims say none
 
 
+def test_layer_options_host_checks(lib):
+    """moe_layer_forward_opts: an unknown option bit is refused before anything else; with a known
+    one the argument checks of moe_layer_forward apply (these calls fail on the host, no launch)."""
+    dm = moe.dims(4, 256, 16, 2, 128, 128)
+    ws_n = moe.workspace_bytes(dm)
+    q = moe.QMat(16, 16, 16)
+    ex = moe.ExpertsC(q, q, q)
+    call = lambda opts, **kw: lib.moe_layer_forward_opts(
+        ctypes.byref(dm), kw.get("x", 16), 16, ctypes.byref(ex), ctypes.byref(ex), 16, kw.get("y", 16), None, 16,
+        ws_n, None, opts)
+    assert moe.OPT_BF16_OPERANDS == 1
+    for bad in (2, 4, 0x80000000, 0xFFFFFFFF):
+        assert call(bad) == 1, bad
+    assert call(moe.OPT_BF16_OPERANDS, x=None) == 1
+    assert call(moe.OPT_BF16_OPERANDS, y=8) == 3
+    assert call(0, y=8) == 3
+
+
 def test_layer_host_entry_checks(lib):
     """The host-buffer entry point refuses what it must before touching the GPU."""
     dm = moe.dims(4, 256, 16, 2, 128, 128)

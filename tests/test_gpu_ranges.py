@@ -8,7 +8,11 @@ into the subnormal range (small activations with small weights); the caller chec
 moe_read_error_flags.  A few tiny
 weight rows among normal ones barely move a layer's output, and the layer stays within the exact
 bar.  The decode path (up to eight tokens) computes in exact integers and fp32 and has no such
-edges: it matches the exact oracle at any of these magnitudes and raises no flag.
+edges: it matches the exact oracle at any of these magnitudes and raises no flag.  With bf16
+tensor-core operands (moe_layer_forward_opts) the grouped-GEMM path has fp32's exponent range:
+the same inputs raise no flag; scaled x stays within the bf16 bar of the exact oracle, and the
+weights far above fp16's range match the oracle that rounds the same operands to bf16 (there
+bf16's 8 significant bits alone put the oracle itself 8.8e-2 from the exact layer).
 """
 import numpy as np
 import pytest
@@ -21,6 +25,8 @@ from oracle import moe_oracle as O
 pytestmark = pytest.mark.gpu
 
 EXACT_TOL = 2e-3
+BF16_EXACT_TOL = 6e-3   # bf16 operands: derived in test_gpu_parity.py
+BF16_EMUL_TOL = 4.2e-3
 DECODE_TOL = 2e-5
 RANGE_FLAG = 2
 
@@ -46,12 +52,13 @@ def _rowwise_err(y, ref):
     return float((np.linalg.norm(y - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-300)).max())
 
 
-def _run(wl, host, x_bits, logits, T):
+def _run(wl, host, x_bits, logits, T, operands="fp16"):
     dl = moe.to_device_layer(host)
     dm = moe.dims(T, wl.d, wl.E, wl.k, wl.F, wl.F_shared)
     ws = moe.alloc_workspace(dm)
     y = torch.empty((T, wl.d), dtype=torch.float32, device="cuda")
-    moe.layer_forward(dm, _dev(x_bits[:T]), _dev(logits[:T]), dl["routed"], dl["shared"], dl["w_sg"], y, ws)
+    moe.layer_forward(dm, _dev(x_bits[:T]), _dev(logits[:T]), dl["routed"], dl["shared"], dl["w_sg"], y, ws,
+                      operands=operands)
     return y.cpu().numpy(), moe.read_error_flags(ws)
 
 
@@ -71,6 +78,9 @@ def test_out_of_range_x_flags_the_gemm_path_and_decode_stays_exact(scale):
     lg = synth.make_logits(rng, wl)
     _, flags = _run(wl, host, x, lg, wl.T)
     assert flags & RANGE_FLAG
+    y, flags = _run(wl, host, x, lg, wl.T, operands="bf16")
+    assert flags == 0
+    assert _rowwise_err(y, O.moe_layer(x, lg, host, wl.k)["y"]) <= BF16_EXACT_TOL
     for T in (1, 3):
         y, flags = _run(wl, host, x, lg, T)
         assert flags == 0
@@ -133,6 +143,10 @@ def test_weights_above_fp16_range_flag_the_gemm_path():
     inp = synth.make_inputs(wl, seed=7)
     _, flags = _run(wl, host, inp["x"], inp["logits"], wl.T)
     assert flags & RANGE_FLAG
+    y, flags = _run(wl, host, inp["x"], inp["logits"], wl.T, operands="bf16")
+    assert flags == 0
+    emu = O.moe_layer(inp["x"], inp["logits"], host, wl.k, operands="bf16", out16="bf16")["y"]
+    assert _rowwise_err(y, emu) <= BF16_EMUL_TOL
     y, flags = _run(wl, host, inp["x"], inp["logits"], 1)
     assert flags == 0
     ref = O.moe_layer(inp["x"][:1], inp["logits"][:1], host, wl.k)["y"]

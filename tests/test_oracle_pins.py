@@ -376,6 +376,25 @@ def test_operand_rounding_error_sizes():
         assert err.max() < bound, (mode, err.max())
 
 
+def test_expert_output_rounding_types():
+    """out16 rounds an expert's output rows to the named 16-bit type: with "bf16" every value is a
+    bf16 (low 16 bits of its float32 zero) within half a bf16 unit (2^-8 relative: 8 significant
+    bits) of the unrounded
+    value; with True or "fp16" every value is an fp16, and some keep more bits than bf16 holds."""
+    wl = synth.TINY
+    layer = synth.make_layer(wl)
+    x = O.bf16_to_f64(synth.make_inputs(wl)["x"])
+    W = O.expert_weights(layer["routed"], 3)
+    raw = O.expert_ffn(x, *W)
+    bf = O.expert_ffn(x, *W, out16="bf16")
+    assert np.all((bf.astype(np.float32).view(np.uint32) & 0xFFFF) == 0)
+    assert np.all(np.abs(bf - raw) <= 2.0 ** -8 * np.abs(raw) * (1 + 1e-12))
+    for flag in (True, "fp16"):
+        h = O.expert_ffn(x, *W, out16=flag)
+        assert np.array_equal(h, np.float16(raw).astype(np.float64))
+        assert np.any((h.astype(np.float32).view(np.uint32) & 0xFFFF) != 0)
+
+
 def test_rmsnorm_constant_row_closed_form():
     d = 128
     gamma = synth.f32_to_bf16_bits(np.ones(d, np.float32))
