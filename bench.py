@@ -60,6 +60,8 @@ def parse():
     p.add_argument("--profile", choices=["decode", "prefill", "skewed", "stack", "attention", "scan"], default=None,
                    help="small eager run of one workload for ncu captures (prints a short summary only)")
     p.add_argument("--profile-sets", type=int, default=4, help="weight sets cycled in --profile mode")
+    p.add_argument("--profile-operands", choices=["fp16", "bf16"], default="fp16",
+                   help="tensor-core operand type of the grouped-GEMM path in --profile mode")
     return p.parse_args()
 
 
@@ -773,7 +775,7 @@ def run_profile(args):
             i = s % NI
             layers[l].forward(ins[l]["x"][i:i + 1], ins[l]["logits"][i:i + 1], y, ws)
         else:
-            layers[l].forward(ins[l]["x"], ins[l]["logits"], y, ws)
+            layers[l].forward(ins[l]["x"], ins[l]["logits"], y, ws, operands=args.profile_operands)
     torch.cuda.synchronize()
     flags = moe.read_error_flags(ws)
     print(json.dumps({"profile": wl.name, "calls": total, "weight_sets": n, "flags": flags,

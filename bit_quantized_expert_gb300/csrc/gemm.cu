@@ -146,6 +146,15 @@ __device__ __forceinline__ void dequant_word_bf16(uint32_t q, __nv_bfloat162 s2,
 __device__ __forceinline__ uint16_t f32_to_16(float v, bool bf) {
   return bf ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
 }
+// Two values rounded to fp16 or bf16 by one packed conversion: a in the low half, b in the high.
+__device__ __forceinline__ uint32_t f32x2_to_16x2(float a, float b, bool bf) {
+  if (bf) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  }
+  const __half2 v = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
 
 template <int MODE, bool BF>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
@@ -531,8 +540,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 const float v0 = __uint_as_float(g[i]), v1 = __uint_as_float(g1[i]);
                 if (n0 + i < tl.z) amax = fmaxf(amax, fabsf(v0));
                 if (n0 + 16 + i < tl.z) amax = fmaxf(amax, fabsf(v1));
-                st_shared_u16(stg + (uint32_t)(i * 32 + lane) * 2, f32_to_16(v0, BF));
-                st_shared_u16(stg + (uint32_t)((i + 16) * 32 + lane) * 2, f32_to_16(v1, BF));
+                const uint32_t pk = f32x2_to_16x2(v0, v1, BF);
+                st_shared_u16(stg + (uint32_t)(i * 32 + lane) * 2, (uint16_t)(pk & 0xFFFFu));
+                st_shared_u16(stg + (uint32_t)((i + 16) * 32 + lane) * 2, (uint16_t)(pk >> 16));
               }
               __syncwarp();
 #pragma unroll
@@ -585,9 +595,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
 // y[t] = sum_j w[t,j] Y[inv[t,j]] + gs[t] Y[T*k + t], fp32 accumulation in j order.  Y is read as
 // fp16 or bf16 (the layer path) or fp32 (expert outputs handed in by a caller), 8 or 4 values per load.
+// An fp16 value h, with its magnitude bits moved up by 13 into a float's exponent and mantissa,
+// reads as h * 2^-112 exactly (normal and subnormal h alike); the sign moves up by 16.  Scaling the
+// weight by 2^112 instead makes fmaf(w * 2^112, that float, acc) the same operation as
+// fmaf(w, h, acc): the weights are at most 1, so w * 2^112 is exact.
+__device__ __forceinline__ float fp16_bits_scaled(uint32_t h) {
+  return __uint_as_float(((h & 0x7FFFu) << 13) | ((h & 0x8000u) << 16));
+}
+
 template <bool HALF, bool BF>
 __global__ void combine_kernel(CombineArgs a) {
   constexpr int V = HALF ? 8 : 4;
+  // fp16 rows: weights scaled by 2^112 (see fp16_bits_scaled)
+  const float wscale = (HALF && !BF) ? 5192296858534827628530496329220096.0f : 1.0f;
   const int t = blockIdx.x;
   const int nv = a.d / V;
   for (int c = threadIdx.x; c < nv; c += blockDim.x) {
@@ -605,9 +625,8 @@ __global__ void combine_kernel(CombineArgs a) {
             v[2 * i] = bf16_bits_to_f32(qw[i] & 0xFFFFu);
             v[2 * i + 1] = bf16_bits_to_f32(qw[i] >> 16);
           } else {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&qw[i]));
-            v[2 * i] = f.x;
-            v[2 * i + 1] = f.y;
+            v[2 * i] = fp16_bits_scaled(qw[i] & 0xFFFFu);
+            v[2 * i + 1] = fp16_bits_scaled(qw[i] >> 16);
           }
         }
       } else {
@@ -621,8 +640,8 @@ __global__ void combine_kernel(CombineArgs a) {
       for (int i = 0; i < V; ++i) acc[i] = fmaf(wv, v[i], acc[i]);
     };
     for (int j = 0; j < a.k; ++j)
-      add_row((size_t)__ldg(a.inv + (size_t)t * a.k + j), __ldg(a.w + (size_t)t * a.k + j));
-    if (a.gs != nullptr) add_row((size_t)a.T * a.k + t, __ldg(a.gs + t));
+      add_row((size_t)__ldg(a.inv + (size_t)t * a.k + j), __ldg(a.w + (size_t)t * a.k + j) * wscale);
+    if (a.gs != nullptr) add_row((size_t)a.T * a.k + t, __ldg(a.gs + t) * wscale);
     float4* yo = reinterpret_cast<float4*>(a.y + (size_t)t * a.d + (size_t)c * V);
     yo[0] = make_float4(acc[0], acc[1], acc[2 % V], acc[3 % V]);
     if (HALF) yo[1] = make_float4(acc[4 % V], acc[5 % V], acc[6 % V], acc[7 % V]);
@@ -675,10 +694,9 @@ __global__ void __launch_bounds__(256) permute_x_kernel(PermuteArgs a) {
           }
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
-            const __half lo = __float2half_rn(xf[p]);
-            const __half hi = __float2half_rn(xf[p + 4]);
-            bad = bad || (__hisinf(lo) != 0) || (__hisinf(hi) != 0);
-            o[p] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+            o[p] = f32x2_to_16x2(xf[p], xf[p + 4], false);
+            // an infinity in either half: x above fp16's range
+            bad = bad || ((o[p] & 0x7FFFu) == 0x7C00u) || ((o[p] & 0x7FFF0000u) == 0x7C000000u);
           }
         }
         reinterpret_cast<uint4*>(a.xperm + (size_t)(s0 + i) * a.d)[ch] = make_uint4(o[0], o[1], o[2], o[3]);
