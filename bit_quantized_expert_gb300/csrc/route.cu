@@ -17,11 +17,33 @@ namespace moe {
 
 constexpr uint32_t kBf16TwoPowMinus12 = 0x3980u;   // 2^-12 as bf16 bits
 
+constexpr int kGateBatch = 8;   // 16-byte loads of x (and of w_sg) in flight per lane
+
 template <int NI>
 __global__ void __launch_bounds__(256) topk_kernel(RouteArgs a) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= a.T) return;
+  // Layer path: one pass over the token row gives the shared-expert gate logit x . w_sg and the
+  // token's largest |x|.  The row's first kGateBatch loads per lane go out before the top-k, so
+  // their latency overlaps the ranking, and every batch is loaded whole before its arithmetic
+  // (the sum runs over the row in the same order either way).
+  const bool has_x = a.x != nullptr;
+  const bool gate = has_x && a.gs != nullptr && a.w_sg != nullptr;
+  const int nch = has_x ? a.d / 8 : 0;
+  const uint4* xr = has_x ? reinterpret_cast<const uint4*>(a.x + (size_t)t * a.d) : nullptr;
+  const uint4* wr = reinterpret_cast<const uint4*>(a.w_sg);
+  uint4 xv[kGateBatch], wv[kGateBatch];
+  auto load_batch = [&](int ch0) {
+#pragma unroll
+    for (int i = 0; i < kGateBatch; ++i) {
+      const int ch = ch0 + lane + 32 * i;
+      xv[i] = ch < nch ? __ldg(xr + ch) : make_uint4(0u, 0u, 0u, 0u);
+      wv[i] = gate && ch < nch ? __ldg(wr + ch) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  if (has_x) load_batch(0);
+
   int my_e;
   float my_w;
   warp_topk_softmax<NI>(a.logits + (size_t)t * a.E, a.E, a.k, &my_e, &my_w);
@@ -30,26 +52,26 @@ __global__ void __launch_bounds__(256) topk_kernel(RouteArgs a) {
     a.w[(size_t)t * a.k + lane] = my_w;
   }
 
-  // One pass over the token row (layer path): the shared-expert gate logit x . w_sg, and the
-  // token's largest |x|.  The grouped GEMM takes x as fp16 operands: a token whose largest |x| is
-  // nonzero but below 2^-12 sits mostly in fp16's subnormal range and loses precision there, so it
-  // sets the range flag (values above the fp16 range set it when x is converted).  With bf16
-  // operands x is used as given and there is no such edge.
-  if (a.x != nullptr) {
-    const bool gate = a.gs != nullptr && a.w_sg != nullptr;
-    const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)t * a.d);
-    const uint4* wr = reinterpret_cast<const uint4*>(a.w_sg);
+  // The grouped GEMM takes x as fp16 operands: a token whose largest |x| is nonzero but below
+  // 2^-12 sits mostly in fp16's subnormal range and loses precision there, so it sets the range
+  // flag (values above the fp16 range set it when x is converted).  With bf16 operands x is used
+  // as given and there is no such edge.
+  if (has_x) {
     float dot = 0.0f;
     uint32_t xmax = 0;   // largest |x| as bf16 magnitude bits
-    for (int ch = lane; ch < a.d / 8; ch += 32) {
-      const uint4 xv = __ldg(xr + ch);
-      const uint4 wv = gate ? __ldg(wr + ch) : make_uint4(0u, 0u, 0u, 0u);
-      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
+    for (int ch0 = 0; ch0 < nch; ch0 += 32 * kGateBatch) {
+      if (ch0 > 0) load_batch(ch0);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        xmax = max(xmax, max(xw[i] & 0x7FFFu, (xw[i] >> 16) & 0x7FFFu));
-        dot = fmaf(bf16_bits_to_f32(xw[i] & 0xFFFFu), bf16_bits_to_f32(ww[i] & 0xFFFFu), dot);
-        dot = fmaf(bf16_bits_to_f32(xw[i] >> 16), bf16_bits_to_f32(ww[i] >> 16), dot);
+      for (int b = 0; b < kGateBatch; ++b) {
+        const uint32_t xw[4] = {xv[b].x, xv[b].y, xv[b].z, xv[b].w}, ww[4] = {wv[b].x, wv[b].y, wv[b].z, wv[b].w};
+        if (ch0 + lane + 32 * b < nch) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            xmax = max(xmax, max(xw[i] & 0x7FFFu, (xw[i] >> 16) & 0x7FFFu));
+            dot = fmaf(bf16_bits_to_f32(xw[i] & 0xFFFFu), bf16_bits_to_f32(ww[i] & 0xFFFFu), dot);
+            dot = fmaf(bf16_bits_to_f32(xw[i] >> 16), bf16_bits_to_f32(ww[i] >> 16), dot);
+          }
+        }
       }
     }
 #pragma unroll
@@ -151,8 +173,16 @@ __global__ void __launch_bounds__(1024, 1) chunk_scan_kernel(TablesArgs a) {
   const bool owner = tid < E * tpe;
   const int per = (nc + tpe - 1) / tpe;
   const int c_lo = owner ? min(nc, p * per) : 0, c_hi = owner ? min(nc, (p + 1) * per) : 0;
+  // The first kScanKeep counts of a thread's range stay in registers between the two passes
+  // (every range up to T = 4096 tokens with E <= 256); the rest are read again.
+  constexpr int kScanKeep = 32;
+  int keep[kScanKeep];
   int sum = 0;
-  for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+#pragma unroll
+  for (int i = 0; i < kScanKeep; ++i) keep[i] = c_lo + i < c_hi ? __ldcg(a.chunk + (size_t)(c_lo + i) * E + e) : 0;
+#pragma unroll
+  for (int i = 0; i < kScanKeep; ++i) sum += keep[i];
+  for (int c0 = c_lo + kScanKeep; c0 < c_hi; c0 += 16) {
     int v[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = c0 + i < c_hi ? __ldcg(a.chunk + (size_t)(c0 + i) * E + e) : 0;
@@ -164,7 +194,13 @@ __global__ void __launch_bounds__(1024, 1) chunk_scan_kernel(TablesArgs a) {
   int run = 0, cnt = 0;
   if (owner) {
     for (int q = 0; q < p; ++q) run += part_s[q * E + e];
-    for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+#pragma unroll
+    for (int i = 0; i < kScanKeep; ++i)
+      if (c_lo + i < c_hi) {
+        a.chunk[(size_t)(c_lo + i) * E + e] = run;
+        run += keep[i];
+      }
+    for (int c0 = c_lo + kScanKeep; c0 < c_hi; c0 += 16) {
       int v[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) v[i] = c0 + i < c_hi ? __ldcg(a.chunk + (size_t)(c0 + i) * E + e) : 0;
