@@ -165,11 +165,19 @@ constexpr int kHBlockWords = 32;
 constexpr int kC = 4;
 
 // Geometry and shared-memory plan of one launch (byte offsets, 16-byte aligned regions).
+// Dynamic shared memory of one decode CTA, at most: one token (the kernel also holds ~15 KB of
+// static shared memory), several tokens (0.5 KB static).
+constexpr uint32_t kDecPlanMax = 200 * 1024;
+constexpr uint32_t kDecPlanMaxMulti = 224 * 1024;
+
 struct DecPlan {
-  int d, F, k1, G, GF, S, C, NQ, DR, KC, GP, NSC, nslices, NP, grid, box_rows;
-  uint32_t gu_codes, gu_sb, dn_codes, dn_sb, hclu, bytes;
-  // multi: several tokens per launch (two h exchange slots, alternating by token)
-  __host__ __device__ DecPlan(int d_, int F_, int k1_, bool multi) : d(d_), F(F_), k1(k1_) {
+  int d, F, k1, G, GF, S, C, NQ, DR, KC, GP, NSC, nslices, NP, grid, box_rows, x_smem;
+  uint32_t gu_codes, gu_sb, dn_codes, dn_sb, hclu, xs, bytes;
+  // multi: several tokens per launch, nt of them (two h exchange slots, alternating by token; x
+  // staging sized for nt)
+  __host__ __device__ DecPlan(int d_, int F_, int k1_, bool multi, int nt = kDecodeMaxTokens)
+      : d(d_), F(F_), k1(k1_) {
+    const uint32_t cap = multi ? kDecPlanMaxMulti : kDecPlanMax;
     G = d / 64;
     GF = F / 64;
     S = F / RF;
@@ -191,6 +199,13 @@ struct DecPlan {
     dn_sb = o;     o += 4u * DR * GF;             // [s|b][DR][GF] bf16: whole scale and bias rows
     o = (o + 15u) & ~15u;
     hclu = o;      o += (multi ? 2u : 1u) * 4u * KC;   // h of the cluster's columns, fp32, per exchange slot
+    o = (o + 127u) & ~127u;
+    // Several tokens: every token's x row copied in at the start (bf16 [nt][d]) when it fits, so
+    // that no token's x load queues behind the weight copies in flight.
+    const uint32_t x_bytes = (uint32_t)nt * (uint32_t)d * 2u;
+    x_smem = (multi && o + x_bytes <= cap) ? 1 : 0;
+    xs = o;
+    if (x_smem) o += x_bytes;
     bytes = (o + 15u) & ~15u;
   }
 };
@@ -378,7 +393,7 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
   extern __shared__ __align__(128) uint8_t sm[];
   const int d = a.d, F = a.F, k = a.k;
   const int k1 = k + (a.has_shared ? 1 : 0);
-  const DecPlan P(d, F, k1, kMulti);
+  const DecPlan P(d, F, k1, kMulti, kMulti ? (a.T > 0 ? a.T : 1) : 1);
   const int G = P.G, GF = P.GF;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x;
@@ -392,8 +407,6 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
   const bool shared_cta = (j == k);
   const int wset = shared_cta ? 1 : 0;
 
-  uint32_t* gcodes = reinterpret_cast<uint32_t*>(sm + P.gu_codes);   // gate [RF][d/8], then up
-  uint16_t* gsb = reinterpret_cast<uint16_t*>(sm + P.gu_sb);         // [g.s | g.b | u.s | u.b][RF][G]
   uint32_t* dcodes = reinterpret_cast<uint32_t*>(sm + P.dn_codes);   // [DR][KC/8]
   uint16_t* dsb = reinterpret_cast<uint16_t*>(sm + P.dn_sb);         // [s | b][DR][GF]
   float* hclu = reinterpret_cast<float*>(sm + P.hclu);               // [2][KC]
@@ -419,10 +432,16 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
   __syncthreads();
   cluster_arrive_relaxed();   // this CTA runs: its shared memory may now receive the cluster's h
 
-  // expert e's copies (which: 1 gate/up, 2 down, 3 both), by the calling warp
+  // Fetches of the slot's weights, counted by lane 0 of warp 0 (the issuing warp) for the
+  // wind-down: gate/up rows and down rows.
+  int gu_issued = 0, dn_issued = 0;
+  // expert e's copies (which: 5 gate/up, 2 down, 7 both) by the calling warp
   auto issue = [&](int e, int which) {
-    issue_copies(P, a.gate[wset], a.up[wset], a.down[wset], &maps.down[wset], e, f0, r0, kc0, smem_u32(gcodes),
-                 smem_u32(gsb), smem_u32(dcodes), smem_u32(dsb), smem_u32(&bars[0]), which, lane);
+    issue_copies(P, a.gate[wset], a.up[wset], a.down[wset], &maps.down[wset], e, f0, r0, kc0,
+                 smem_u32(sm + P.gu_codes), smem_u32(sm + P.gu_sb), smem_u32(dcodes), smem_u32(dsb),
+                 smem_u32(&bars[0]), which, lane);
+    if (which & 5) ++gu_issued;
+    if (which & 2) ++dn_issued;
   };
 
   // Weights are never written upstream: the shared expert's copies start before the wait.
@@ -431,6 +450,14 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
   pdl_wait();   // x and logits from upstream kernels are complete and visible past this point
   if (!kMulti) {   // 16-byte piece i at i ^ ((i / 8) % 8): lane l's eight pieces fall in distinct banks
     for (int i = tid; i < d / 8; i += kThreadsDec) cp_async_16(smem_u32(&xs[i ^ ((i >> 3) & 7)]), a.x + (size_t)i * 8);
+    cp_async_commit();
+  } else if (P.x_smem) {   // several tokens: every token's row, the same layout per token
+    uint4* xm = reinterpret_cast<uint4*>(sm + P.xs);
+    const int pr = d / 8;
+    for (int i = tid; i < T * pr; i += kThreadsDec) {
+      const int tk = i / pr, pc = i % pr;
+      cp_async_16(smem_u32(&xm[tk * pr + (pc ^ ((pc >> 3) & 7))]), a.x + (size_t)tk * d + (size_t)pc * 8);
+    }
     cp_async_commit();
   }
 
@@ -486,29 +513,32 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
     }
   }
   pdl_launch_dependents();
-  if (!kMulti) cp_async_wait<0>();
-  __syncthreads();   // e_s and wgt_s (and, for one token, x in shared memory)
+  if (!kMulti || P.x_smem) cp_async_wait<0>();
+  __syncthreads();   // e_s and wgt_s (and x in shared memory)
   cluster_wait_acquire();   // every CTA of the cluster runs (pairs with the arrive above)
 
-  // Tokens one after another.  The slot's weights stay in shared memory while the slot's expert
-  // stays the same (always for the shared expert), and are fetched again when it changes; every
-  // fetch is one phase of the copy barriers, so waits use the parity of the fetch count.
+  // Tokens one after another.  Consecutive tokens of the slot with the same expert form a run
+  // (always one run for the shared expert); the slot's weights stay in shared memory for a run
+  // and are fetched again for the next; every fetch is one phase of the copy barriers, so waits
+  // use the parity of the run index.
   const bool active = lane < G;
-  int loads = 1;   // weight fetches so far (token 0's are in flight)
+  const uint32_t* gcodes = reinterpret_cast<const uint32_t*>(sm + P.gu_codes);   // gate [RF][d/8], then up
+  const uint16_t* gsb = reinterpret_cast<const uint16_t*>(sm + P.gu_sb);         // [g.s|g.b|u.s|u.b][RF][G]
+  int run = 0;
 #pragma unroll 1
   for (int t = 0; t < T; ++t) {
     const int e_t = e_s[t];
-    const bool refetch = t > 0 && e_t != e_s[t - 1];
-    if (refetch) ++loads;   // requested during the previous token
-    const uint32_t ph = (uint32_t)(loads - 1) & 1u;
+    if (t > 0 && e_t != e_s[t - 1]) ++run;   // requested during the previous token
+    const uint32_t ph = (uint32_t)run & 1u;
     float* hx = hclu + (t & 1) * P.KC;   // this token's exchange slot
     // x: lane l owns quantisation group l (64 inputs)
     uint4 xr[8];
 #pragma unroll
     for (int c8 = 0; c8 < 8; ++c8)
       xr[c8] = !active ? make_uint4(0u, 0u, 0u, 0u)
-               : kMulti ? __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * d) + lane * 8 + c8)
-                        : xs[(lane * 8 + c8) ^ (lane & 7)];
+               : !kMulti ? xs[(lane * 8 + c8) ^ (lane & 7)]
+               : P.x_smem ? reinterpret_cast<const uint4*>(sm + P.xs)[t * (d / 8) + ((lane * 8 + c8) ^ (lane & 7))]
+                          : __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * d) + lane * 8 + c8);
 
     // ---- gate/up: warp w computes gate and up of rows q*8 + w (q = 0..3) as slots s = 2q + mat;
     // a reduce-scatter leaves slot s fully summed in lane 4s.
@@ -594,6 +624,7 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
     // inside waits, so every thread of the CTA reads the same value here after the wait below.
     cluster_wait_acquire();     // every CTA's h has arrived
     if (kMulti && warp == 0 && t + 1 < T && e_s[t + 1] != e_t && !abort_s) {
+      // this token ends its run: the gate/up buffers are free
       fence_proxy_async_smem();   // this token's generic reads of the gate/up buffers come first
       issue(e_s[t + 1], 5);
     }
@@ -674,8 +705,11 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
 
   // ---- wind down: after a timeout, copies still in flight must land before the CTA exits.
   if (tid == 0 && abort_s) {
-    const uint32_t last = (uint32_t)(loads - 1) & 1u;   // parity of the last fetch issued
+    // every barrier waits for the parity of its last fetch (thread 0 armed them all)
     for (int i = 0; i <= kQuarters; ++i) {
+      const int n = i < kQuarters ? gu_issued : dn_issued;
+      if (n == 0) continue;
+      const uint32_t last = (uint32_t)(n - 1) & 1u;
       const long long t0 = clock64();
       while (!mbar_try_wait(smem_u32(&bars[i]), last) && clock64() - t0 < 4000000ll) {
       }
@@ -770,7 +804,7 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const ReduceArgs a) 
 constexpr int kMaxDev = 64;
 bool g_ready[kMaxDev];
 std::mutex g_dev_mu;
-constexpr size_t kDecSmemMax = 200 * 1024;
+constexpr size_t kDecSmemMax = kDecPlanMax;
 
 cudaError_t ensure_attrs() {
   int dev = 0;
@@ -779,9 +813,12 @@ cudaError_t ensure_attrs() {
   if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_dev_mu);
   if (!g_ready[dev]) {
+    if ((e = cudaFuncSetAttribute(decode_layer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kDecPlanMax)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(decode_layer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kDecPlanMaxMulti)) != cudaSuccess)
+      return e;
     for (auto f : {decode_layer_kernel<false>, decode_layer_kernel<true>}) {
-      if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecSmemMax)) != cudaSuccess)
-        return e;
       if ((e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100)) != cudaSuccess) return e;
     }
     if ((e = cudaFuncSetAttribute(decode_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -804,8 +841,7 @@ bool decode_supported(int d, int E, int k, int F) {
   // One quantisation group per lane in the gate/up rows: d <= 2048 (and d a multiple of 64).
   // F a multiple of 128: 32 gate/up rows per CTA and whole quantisation groups per cluster.
   if (k1 > 32 || E > kMaxE || d > 2048 || d % 64 != 0 || F % 128 != 0) return false;
-  const DecPlan P(d, F, k1, true);
-  if (P.bytes > kDecSmemMax) return false;
+  if (DecPlan(d, F, k1, false).bytes > kDecPlanMax || DecPlan(d, F, k1, true).bytes > kDecPlanMaxMulti) return false;
   return true;
 }
 
@@ -871,7 +907,7 @@ cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& a, cudaStrea
   if (!decode_supported(a.d, a.E, a.k, a.F)) return cudaErrorInvalidConfiguration;
   cudaError_t e = ensure_attrs();
   if (e != cudaSuccess) return e;
-  const DecPlan P(a.d, a.F, k1, a.T > 1);
+  const DecPlan P(a.d, a.F, k1, a.T > 1, a.T > 0 ? a.T : 1);
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kC;
