@@ -166,9 +166,9 @@ constexpr int kC = 4;
 
 // Geometry and shared-memory plan of one launch (byte offsets, 16-byte aligned regions).
 // Dynamic shared memory of one decode CTA, at most: one token (the kernel also holds ~15 KB of
-// static shared memory), several tokens (0.5 KB static).
+// static shared memory), several tokens (~21 KB static: the several-token ranking tables).
 constexpr uint32_t kDecPlanMax = 200 * 1024;
-constexpr uint32_t kDecPlanMaxMulti = 224 * 1024;
+constexpr uint32_t kDecPlanMaxMulti = 200 * 1024;
 
 struct DecPlan {
   int d, F, k1, G, GF, S, C, NQ, DR, KC, GP, NSC, nslices, NP, grid, box_rows, x_smem;
@@ -294,6 +294,60 @@ __device__ __forceinline__ void block_topk_small(const float* __restrict__ row, 
   __syncthreads();
 }
 
+// block_topk_small for T tokens at once (E <= 256, k <= 8, T <= kDecodeMaxTokens): logits [T][E];
+// thread t holds expert t of every token, ranks each key against its warp's 32 of the same token,
+// and the warp's k best per token land in cand [T][8][8]; then each of the T x 64 candidates is
+// ranked against its token's 64 and the k best land in sel [T][8].  keys holds T x kThreadsDec
+// entries.  Every token's selection is the one block_topk_small makes.  Two block barriers.
+// `between` runs after the logit loads are issued and before their values are used.
+template <typename Between>
+__device__ __forceinline__ void block_topk_small_tokens(const float* __restrict__ logits, int E, int k, int T,
+                                                        uint64_t* keys, uint64_t* cand, uint64_t* sel,
+                                                        Between between) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float lv[kDecodeMaxTokens];
+#pragma unroll
+  for (int t = 0; t < kDecodeMaxTokens; ++t) lv[t] = (t < T && tid < E) ? __ldg(logits + (size_t)t * E + tid) : 0.0f;
+  between();
+  uint64_t key[kDecodeMaxTokens];
+#pragma unroll
+  for (int t = 0; t < kDecodeMaxTokens; ++t) {
+    key[t] = (t < T && tid < E) ? cand_key(lv[t], tid) : 0ull;
+    if (t < T) {
+      keys[t * kThreadsDec + tid] = key[t];
+      if (lane < 8) cand[(t * kWarpsDec + warp) * 8 + lane] = 0ull;
+    }
+  }
+  __syncwarp();
+#pragma unroll
+  for (int t = 0; t < kDecodeMaxTokens; ++t) {
+    if (t < T) {
+      const ulonglong2* wk = reinterpret_cast<const ulonglong2*>(keys + t * kThreadsDec + warp * 32);
+      int rank = 0;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const ulonglong2 o = wk[c];
+        rank += (o.x > key[t] ? 1 : 0) + (o.y > key[t] ? 1 : 0);
+      }
+      if (key[t] != 0ull && rank < k) cand[(t * kWarpsDec + warp) * 8 + rank] = key[t];
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < T * kWarpsDec * 8; i += kThreadsDec) {
+    const int t = i / (kWarpsDec * 8);
+    const uint64_t mine = cand[i];
+    const ulonglong2* ck = reinterpret_cast<const ulonglong2*>(cand + t * kWarpsDec * 8);
+    int r = 0;
+#pragma unroll
+    for (int c = 0; c < kWarpsDec * 4; ++c) {
+      const ulonglong2 o = ck[c];
+      r += (o.x > mine ? 1 : 0) + (o.y > mine ? 1 : 0);
+    }
+    if (mine != 0ull && r < k) sel[t * 8 + r] = mine;
+  }
+  __syncthreads();
+}
+
 template <int NE>
 __device__ __forceinline__ void block_topk(const float* __restrict__ row, int E, int k, uint64_t* keys,
                                            uint64_t* cand, uint64_t* sel) {
@@ -412,7 +466,9 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
   float* hclu = reinterpret_cast<float*>(sm + P.hclu);               // [2][KC]
   __shared__ __align__(8) uint64_t bars[kQuarters + 1];   // gate/up quarters, then the down rows
   __shared__ __align__(16) uint64_t cand[kWarpsDec * 32];
-  __shared__ __align__(16) uint64_t keys_s[kMulti ? 1 : kMaxE];
+  __shared__ __align__(16) uint64_t keys_s[kMulti ? kDecodeMaxTokens * kThreadsDec : kMaxE];
+  __shared__ __align__(16) uint64_t cand_t[kMulti ? kDecodeMaxTokens * kWarpsDec * 8 : 1];
+  __shared__ uint64_t sel_t[kMulti ? kDecodeMaxTokens * 8 : 1];
   __shared__ uint64_t sel[32];
   __shared__ int e_s[kDecodeMaxTokens];
   __shared__ float wgt_s[kDecodeMaxTokens];    // w_j (routed) or the shared-expert gate, per token
@@ -451,7 +507,10 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
   if (!kMulti) {   // 16-byte piece i at i ^ ((i / 8) % 8): lane l's eight pieces fall in distinct banks
     for (int i = tid; i < d / 8; i += kThreadsDec) cp_async_16(smem_u32(&xs[i ^ ((i >> 3) & 7)]), a.x + (size_t)i * 8);
     cp_async_commit();
-  } else if (P.x_smem) {   // several tokens: every token's row, the same layout per token
+  }
+  // Several tokens: every token's row of x, the same layout per token.  On the block-ranking path
+  // the copies go out right after the logit loads, so that those do not queue behind them.
+  auto stage_x = [&]() {
     uint4* xm = reinterpret_cast<uint4*>(sm + P.xs);
     const int pr = d / 8;
     for (int i = tid; i < T * pr; i += kThreadsDec) {
@@ -459,7 +518,9 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
       cp_async_16(smem_u32(&xm[tk * pr + (pc ^ ((pc >> 3) & 7))]), a.x + (size_t)tk * d + (size_t)pc * 8);
     }
     cp_async_commit();
-  }
+  };
+  const bool block_rank = kMulti && !shared_cta && a.E <= kThreadsDec && k <= 8;
+  if (kMulti && P.x_smem && !block_rank) stage_x();
 
   if (!kMulti) {
     if (!shared_cta) {
@@ -475,6 +536,22 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
         if (lane == j) wgt_s[0] = w;
       }
     }
+  } else if (block_rank) {
+    // every token ranked by the whole CTA at once (the one-token ranking, per token); warp t then
+    // takes token t's softmax, and token 0's copies go out
+    block_topk_small_tokens(a.logits, a.E, k, T, keys_s, cand_t, sel_t, [&]() {
+      if (P.x_smem) stage_x();
+    });
+    if (warp < T) {
+      const uint64_t* st = sel_t + warp * 8;
+      const float v = lane < k ? key_logit((uint32_t)(st[lane] >> 32)) : 0.0f;
+      const float w = softmax_tail(v, key_logit((uint32_t)(st[0] >> 32)), k, lane);
+      if (lane == j) {
+        e_s[warp] = cand_expert(st[j]);
+        wgt_s[warp] = w;
+      }
+    }
+    if (warp == 0) issue(cand_expert(sel_t[j]), 7);
   } else if (warp < T && !shared_cta) {
     // warp t routes token t; token 0's gate/up rows are requested as soon as its expert is known
     int e;
