@@ -199,7 +199,7 @@ struct DecPlan {
     dn_sb = o;     o += 4u * DR * GF;             // [s|b][DR][GF] bf16: whole scale and bias rows
     o = (o + 15u) & ~15u;
     hclu = o;      o += (multi ? 2u : 1u) * 4u * KC;   // h of the cluster's columns, fp32, per exchange slot
-    o = (o + 127u) & ~127u;
+    if (multi) o = (o + 127u) & ~127u;
     // Several tokens: every token's x row copied in at the start (bf16 [nt][d]) when it fits, so
     // that no token's x load queues behind the weight copies in flight.
     const uint32_t x_bytes = (uint32_t)nt * (uint32_t)d * 2u;
@@ -496,8 +496,8 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
     issue_copies(P, a.gate[wset], a.up[wset], a.down[wset], &maps.down[wset], e, f0, r0, kc0,
                  smem_u32(sm + P.gu_codes), smem_u32(sm + P.gu_sb), smem_u32(dcodes), smem_u32(dsb),
                  smem_u32(&bars[0]), which, lane);
-    if (which & 5) ++gu_issued;
-    if (which & 2) ++dn_issued;
+    if (kMulti && (which & 5)) ++gu_issued;   // one token: one fetch of each, counted below
+    if (kMulti && (which & 2)) ++dn_issued;
   };
 
   // Weights are never written upstream: the shared expert's copies start before the wait.
@@ -784,7 +784,7 @@ __global__ void __launch_bounds__(kThreadsDec, 1)
   if (tid == 0 && abort_s) {
     // every barrier waits for the parity of its last fetch (thread 0 armed them all)
     for (int i = 0; i <= kQuarters; ++i) {
-      const int n = i < kQuarters ? gu_issued : dn_issued;
+      const int n = !kMulti ? 1 : i < kQuarters ? gu_issued : dn_issued;
       if (n == 0) continue;
       const uint32_t last = (uint32_t)(n - 1) & 1u;
       const long long t0 = clock64();
