@@ -652,9 +652,13 @@ def scan_bench(wl, steps, device, pk):
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=device)
     stream = torch.cuda.Stream(device=device)
 
+    # A decode step (several layers, one token each): each layer's state was last written by its own
+    # scan of the previous step, so it may be read before the preceding launch ends.
+    early = wl.layers > 1
+
     def step():
         for l, c in enumerate(layers):
-            moe.gdn_scan(gd, c["q"], c["k"], c["v"], c["g"], c["beta"], c["S0"], c["S0"], o[l], ws)
+            moe.gdn_scan(gd, c["q"], c["k"], c["v"], c["g"], c["beta"], c["S0"], c["S0"], o[l], ws, early_state=early)
 
     with torch.cuda.stream(stream):
         for _ in range(3):

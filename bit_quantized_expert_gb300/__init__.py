@@ -22,7 +22,7 @@ EXPORTED = ("moe_status_string", "moe_max_tiles", "moe_workspace_bytes", "moe_ro
             "moe_clear_error_flags",
             "moe_read_error_flags", "moe_layer_forward_decode_noalloc", "moe_workspace_bytes_host",
             "moe_layer_forward_host", "moe_decode_stream_probe", "gqa_decode_workspace_bytes",
-            "gqa_decode_attention", "gdn_scan_workspace_bytes", "gdn_scan")
+            "gqa_decode_attention", "gdn_scan_workspace_bytes", "gdn_scan", "gdn_scan_opts")
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_MISALIGNED",
           4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA"}
@@ -114,6 +114,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gdn_scan_workspace_bytes.argtypes = [P(GdnDims)]
     lib.gdn_scan.restype = ctypes.c_int
     lib.gdn_scan.argtypes = [P(GdnDims), VP, VP, VP, VP, VP, VP, VP, VP, VP, S, VP]
+    lib.gdn_scan_opts.restype = ctypes.c_int
+    lib.gdn_scan_opts.argtypes = [P(GdnDims), VP, VP, VP, VP, VP, VP, VP, VP, VP, S, VP, ctypes.c_uint32]
     lib.moe_clear_error_flags.restype = ctypes.c_int
     lib.moe_clear_error_flags.argtypes = [VP, S, VP]
     lib.moe_read_error_flags.restype = ctypes.c_int
@@ -319,12 +321,21 @@ def alloc_gdn_workspace(gd: GdnDims, device="cuda"):
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
-def gdn_scan(gd: GdnDims, q, k, v, g, beta, state_in, state_out, o, workspace, stream=None):
+GDN_OPT_STATE_EARLY = 1
+
+
+def gdn_scan(gd: GdnDims, q, k, v, g, beta, state_in, state_out, o, workspace, stream=None, early_state=False):
     """Gated delta rule over gd.T tokens: q, k, v bf16 [T, H, 128]; g, beta fp32 [T, H];
-    state_in / state_out fp32 [H, 128, 128] (may be the same tensor); o fp32 [T, H, 128]."""
-    _check(load_library().gdn_scan(ctypes.byref(gd), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in),
-                                   _ptr(state_out), _ptr(o), _ptr(workspace), workspace.numel(), _stream(stream)),
-           "gdn_scan")
+    state_in / state_out fp32 [H, 128, 128] (may be the same tensor); o fp32 [T, H, 128].
+    early_state: GDN_OPT_STATE_EARLY (gdn_scan_opts): the state is read before the preceding work on
+    the stream finishes, which must then not write it."""
+    lib = load_library()
+    args = (ctypes.byref(gd), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in), _ptr(state_out), _ptr(o),
+            _ptr(workspace), workspace.numel(), _stream(stream))
+    if early_state:
+        _check(lib.gdn_scan_opts(*args, GDN_OPT_STATE_EARLY), "gdn_scan_opts")
+    else:
+        _check(lib.gdn_scan(*args), "gdn_scan")
 
 
 def read_error_flags(workspace, stream=None) -> int:

@@ -94,6 +94,7 @@ struct ScanArgs {
   float* o;
   uint32_t* err;
   int T, H;
+  int early_state;   // state_in may be read before the dependency wait (GDN_OPT_STATE_EARLY)
 };
 
 __global__ void __launch_bounds__(kThreadsScan, 1)
@@ -115,8 +116,12 @@ __global__ void __launch_bounds__(kThreadsScan, 1)
     mbar_fence_init();
   }
   __syncthreads();
-  pdl_wait();   // every input may come from the kernel before this one
-  pdl_launch_dependents();
+  // Every input may come from the kernel before this one -- except, with early_state, the state,
+  // which the scan warps then read before their own wait.
+  if (!a.early_state || warp >= kScanWarps) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
 
   int issued = 0;   // chunks whose copies the issuing lane (staging warp 0, lane 0) has issued
   if (warp >= kScanWarps) {
@@ -220,6 +225,10 @@ __global__ void __launch_bounds__(kThreadsScan, 1)
         s[4 * j + 2] = v4.z;
         s[4 * j + 3] = v4.w;
       }
+    }
+    if (a.early_state) {   // the state is in registers; the token inputs come after the wait
+      pdl_wait();
+      pdl_launch_dependents();
     }
     const size_t o_step = (size_t)a.H * kSD;
     float* __restrict__ o_out = a.o + (size_t)h * kSD + r0 + warp * 4;
@@ -336,6 +345,14 @@ extern "C" size_t gdn_scan_workspace_bytes(const gdn_dims* dims) {
 extern "C" moe_status gdn_scan(const gdn_dims* dims, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                const float* g, const float* beta, const float* state_in, float* state_out, float* o,
                                void* workspace, size_t workspace_bytes, void* stream) {
+  return gdn_scan_opts(dims, q, k, v, g, beta, state_in, state_out, o, workspace, workspace_bytes, stream, 0u);
+}
+
+extern "C" moe_status gdn_scan_opts(const gdn_dims* dims, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                    const float* g, const float* beta, const float* state_in, float* state_out,
+                                    float* o, void* workspace, size_t workspace_bytes, void* stream,
+                                    uint32_t options) {
+  if (options & ~(uint32_t)GDN_OPT_STATE_EARLY) return MOE_ERR_INVALID_ARG;
   const int st = check_scan_dims(dims);
   if (st != MOE_OK) return (moe_status)st;
   if (state_in == nullptr || state_out == nullptr || workspace == nullptr) return MOE_ERR_INVALID_ARG;
@@ -373,6 +390,7 @@ extern "C" moe_status gdn_scan(const gdn_dims* dims, const uint16_t* q, const ui
   a.err = static_cast<uint32_t*>(workspace);
   a.T = dims->T;
   a.H = dims->H;
+  a.early_state = (options & GDN_OPT_STATE_EARLY) ? 1 : 0;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;

@@ -67,6 +67,21 @@ moe_status gdn_scan(const gdn_dims* dims, const uint16_t* q, const uint16_t* k, 
                     const float* beta, const float* state_in, float* state_out, float* o, void* workspace,
                     size_t workspace_bytes, void* stream);
 
+/* Option bits of gdn_scan_opts. */
+#define GDN_OPT_STATE_EARLY 1u
+
+/* gdn_scan with options; options == 0 is gdn_scan.
+ * GDN_OPT_STATE_EARLY: state_in is read before the preceding work on the stream has finished (the
+ * scan warps load their rows of S before the programmatic-launch wait, so the load overlaps the
+ * end of that work; q, k, v, g and beta are still read after it).  The caller promises that the
+ * work immediately preceding this call on the stream does not write state_in: in a decode loop
+ * each layer's state was last written by that layer's own scan of the previous token, many
+ * launches earlier.  Results are identical to gdn_scan's.
+ * Returns MOE_ERR_INVALID_ARG for an unknown option bit; otherwise as gdn_scan. */
+moe_status gdn_scan_opts(const gdn_dims* dims, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                         const float* g, const float* beta, const float* state_in, float* state_out, float* o,
+                         void* workspace, size_t workspace_bytes, void* stream, uint32_t options);
+
 #ifdef __cplusplus
 }
 #endif

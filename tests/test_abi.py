@@ -204,3 +204,9 @@ def test_gdn_workspace_and_host_checks(lib):
     assert call(dims=moe.gdn_dims(3, 16, 64, 64)) == 2
     assert call(k=24) == 3 and call(g=20) == 3 and call(so=8) == 3
     assert call(nb=255) == 4
+    # gdn_scan_opts: an unknown option bit is refused; with the known one the same checks apply
+    opts = lambda o, **kw: lib.gdn_scan_opts(ctypes.byref(kw.get("dims", gd)), kw.get("q", 16), 16, 16, 16, 16, 16, 16,
+                                             16, 16, kw.get("nb", 256), None, o)
+    assert moe.GDN_OPT_STATE_EARLY == 1
+    assert opts(2) == 1 and opts(0x80000000) == 1
+    assert opts(1, q=None) == 1 and opts(1, q=24) == 3 and opts(1, nb=255) == 4

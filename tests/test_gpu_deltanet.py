@@ -95,6 +95,31 @@ def test_decode_step_in_place():
     _check(np.stack(outs), S, inp, 3, "decode")
 
 
+def test_early_state_read_is_bit_identical():
+    """GDN_OPT_STATE_EARLY only moves the state load ahead of the dependency wait: a decode loop over
+    several layers, each with its own state updated in place, gives the same bits with and without
+    it."""
+    H, layers, steps = 16, 3, 4
+    inps = [synth.make_scan(steps, H, 128, seed=60 + l) for l in range(layers)]
+    gd = moe.gdn_dims(1, H)
+    ws = moe.alloc_gdn_workspace(gd)
+    outs = {}
+    for early in (False, True):
+        S = [_dev(inp["S0"]) for inp in inps]
+        o = torch.empty((1, H, 128), dtype=torch.float32, device="cuda")
+        got = []
+        for t in range(steps):
+            for l, inp in enumerate(inps):
+                one = {key: _dev(np.ascontiguousarray(val[t:t + 1])) for key, val in inp.items() if key != "S0"}
+                moe.gdn_scan(gd, one["q"], one["k"], one["v"], one["g"], one["beta"], S[l], S[l], o, ws,
+                             early_state=early)
+                got.append(o.cpu().numpy().copy())
+        outs[early] = (got, [s_.cpu().numpy() for s_ in S])
+    assert moe.read_error_flags(ws) == 0
+    assert all(np.array_equal(a, b) for a, b in zip(outs[False][0], outs[True][0]))
+    assert all(np.array_equal(a, b) for a, b in zip(outs[False][1], outs[True][1]))
+
+
 def test_split_calls_are_bit_identical():
     """150 tokens in one call, and as 100 then 50 tokens with the state passed on: identical bits
     (every token's arithmetic is the same and the state passes through fp32 memory unchanged); a
