@@ -38,10 +38,7 @@ namespace {
 constexpr int kD = 128;                        // head size
 constexpr int kTileN = 64;                     // positions per tile
 constexpr int kStages = 6;                     // tiles held per CTA (landed or in flight)
-#ifndef ATTN_IN_FLIGHT
-#define ATTN_IN_FLIGHT 4
-#endif
-constexpr int kInFlight = ATTN_IN_FLIGHT;      // copies in flight per CTA
+constexpr int kInFlight = 4;                   // tiles in flight per CTA (swept: 1, 2, 3, 4, 6)
 static_assert(kInFlight >= 1 && kInFlight <= kStages, "in-flight window");
 constexpr int kConsumerWarps = 8;              // two groups of four, alternate tiles
 constexpr int kThreadsAttn = (kConsumerWarps + 1) * 32;
