@@ -184,6 +184,15 @@ def make_layers(wl, device, n):
     return layers
 
 
+def on_stream(stream):
+    """Context that makes `stream` current after it waits for the work already queued on the
+    default stream.  Inputs, weights and workspace clears are made there, and a side stream does
+    not wait for the default stream by itself."""
+    import torch
+    stream.wait_stream(torch.cuda.default_stream(stream.device))
+    return torch.cuda.stream(stream)
+
+
 def capture(fn, stream):
     import torch
     g = torch.cuda.CUDAGraph()
@@ -197,7 +206,7 @@ def timed_graph_steps(graph_of_g, g_steps, graph_of_1, steps, stream):
     import torch
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     reps, rest = divmod(steps, g_steps)
-    with torch.cuda.stream(stream):
+    with on_stream(stream):
         start.record(stream)
         for _ in range(reps):
             graph_of_g.replay()
@@ -226,7 +235,7 @@ def decode_bench(args, world, rank, local, device, pk):
         for l in range(LAYERS):
             layers[l].forward(ins[l]["x"][i:i + 1], ins[l]["logits"][i:i + 1], y[l, i:i + 1], ws)
 
-    with torch.cuda.stream(stream):
+    with on_stream(stream):
         for s in range(args.warmup):
             step(s)
     stream.synchronize()
@@ -234,7 +243,7 @@ def decode_bench(args, world, rank, local, device, pk):
     log("decode: warm-up done; capturing graphs")
     g_many = capture(lambda: [step(s) for s in range(G)], stream)
     g_one = capture(lambda: step(0), stream)
-    with torch.cuda.stream(stream):
+    with on_stream(stream):
         g_many.replay()
     stream.synchronize()
     if moe.read_error_flags(ws) != 0:
@@ -275,11 +284,11 @@ def decode_bench(args, world, rank, local, device, pk):
         i = s % NI
         layers[0].forward(ins[0]["x"][i:i + 1], ins[0]["logits"][i:i + 1], y[0, i:i + 1], ws)
 
-    with torch.cuda.stream(stream):
+    with on_stream(stream):
         for s in range(3):
             hot_step(s)
     g_hot = capture(lambda: [hot_step(s) for s in range(LAYERS)], stream)
-    with torch.cuda.stream(stream):
+    with on_stream(stream):
         g_hot.replay()
     stream.synchronize()
     hot_calls = LAYERS * max(1, args.steps // 4)
@@ -305,11 +314,11 @@ def decode_bench(args, world, rank, local, device, pk):
         for l in range(LAYERS):
             moe.decode_stream_probe(dm, idx[l][i], layers[l].routed, layers[l].shared, ws)
 
-    with torch.cuda.stream(stream):
+    with on_stream(stream):
         for s in range(3):
             probe_step(s)
     g_probe = capture(lambda: [probe_step(s) for s in range(G)], stream)
-    with torch.cuda.stream(stream):
+    with on_stream(stream):
         g_probe.replay()
     stream.synchronize()
     p_steps = max(G, args.steps // 2 // G * G)
@@ -336,10 +345,10 @@ def decode_bench(args, world, rank, local, device, pk):
             for l in range(LAYERS):
                 layers[l].forward(ins[l]["x"][i:i + T], ins[l]["logits"][i:i + T], ys[:T], ws_s)
 
-        with torch.cuda.stream(stream):
+        with on_stream(stream):
             small_step(0)
         g_s = capture(lambda: [small_step(s) for s in range(4)], stream)
-        with torch.cuda.stream(stream):
+        with on_stream(stream):
             g_s.replay()
         stream.synchronize()
         reps = max(1, args.steps // 40)
@@ -387,7 +396,7 @@ def decode_bench(args, world, rank, local, device, pk):
     n_e2e = max(1, min(args.steps, args.e2e_steps))
 
     def timed_host_steps(fn):
-        with torch.cuda.stream(stream):
+        with on_stream(stream):
             for s in range(2):
                 fn(s)
             stream.synchronize()
@@ -440,13 +449,13 @@ def prefill_bench(wl, steps, device, pk, operands="fp16"):
         l = s % n_sets
         layers[l].forward(ins[l]["x"], ins[l]["logits"], y, ws, operands=operands)
 
-    with torch.cuda.stream(stream):
+    with on_stream(stream):
         for s in range(3):
             step(s)
     stream.synchronize()
     g_many = capture(lambda: [step(s) for s in range(n_sets)], stream)
     g_one = capture(lambda: step(0), stream)
-    with torch.cuda.stream(stream):
+    with on_stream(stream):
         g_many.replay()
     stream.synchronize()
     steps = max(n_sets, steps // n_sets * n_sets)
@@ -456,7 +465,7 @@ def prefill_bench(wl, steps, device, pk, operands="fp16"):
     # touched experts per weight set (from the routing of that set's inputs)
     touched = []
     for l in range(n_sets):
-        with torch.cuda.stream(stream):
+        with on_stream(stream):
             layers[l].forward(ins[l]["x"], ins[l]["logits"], y, ws, routing=routing, operands=operands)
         stream.synchronize()
         touched.append(int((routing["counts"] > 0).sum().item()))
@@ -509,11 +518,11 @@ def stack_bench(wl, steps, device, pk):
                                h, lg, ws)
             layers[l].forward(h, lg, y, ws)
 
-    with torch.cuda.stream(stream):
+    with on_stream(stream):
         step()
     stream.synchronize()
     g = capture(step, stream)
-    with torch.cuda.stream(stream):
+    with on_stream(stream):
         g.replay()
     stream.synchronize()
     ms = timed_graph_steps(g, 1, g, steps, stream)
@@ -565,12 +574,12 @@ def attention_bench(wl, steps, device, pk):
         for l, c in enumerate(layers):
             moe.gqa_decode_attention(gd, c["q"], c["k"], c["v"], o[l], ws)
 
-    with torch.cuda.stream(stream):
+    with on_stream(stream):
         for _ in range(3):
             step()
     stream.synchronize()
     g = capture(step, stream)
-    with torch.cuda.stream(stream):
+    with on_stream(stream):
         for _ in range(3):
             g.replay()
     stream.synchronize()
@@ -589,11 +598,11 @@ def attention_bench(wl, steps, device, pk):
         for _ in range(wl.layers):
             sep.add_(1.0)
 
-    with torch.cuda.stream(stream):
+    with on_stream(stream):
         step_sep()
     stream.synchronize()
     g_sep, g_seps = capture(step_sep, stream), capture(seps, stream)
-    with torch.cuda.stream(stream):
+    with on_stream(stream):
         for _ in range(3):
             g_sep.replay()
             g_seps.replay()
@@ -660,13 +669,13 @@ def scan_bench(wl, steps, device, pk):
         for l, c in enumerate(layers):
             moe.gdn_scan(gd, c["q"], c["k"], c["v"], c["g"], c["beta"], c["S0"], c["S0"], o[l], ws, early_state=early)
 
-    with torch.cuda.stream(stream):
+    with on_stream(stream):
         for _ in range(3):
             step()
     stream.synchronize()
     gr = capture(step, stream)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    with torch.cuda.stream(stream):
+    with on_stream(stream):
         for _ in range(3):
             gr.replay()
         for e0, e1 in ev:

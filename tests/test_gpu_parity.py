@@ -699,6 +699,7 @@ def test_graph_replay_of_layer_calls():
             moe.layer_forward(dm, hs[l], lgs[l], dls[l]["routed"], dls[l]["shared"], dls[l]["w_sg"], ys[l], ws)
 
     s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())   # the setup above ran on the default stream
     with torch.cuda.stream(s):
         chain()
     s.synchronize()
@@ -733,6 +734,7 @@ def test_graph_replay_of_layer_calls():
         for t in range(4):
             moe.layer_forward(dmd, xs[t:t + 1], lgd[t:t + 1], dl["routed"], dl["shared"], dl["w_sg"], yd[t:t + 1], wsd)
 
+    s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
         dchain()
     s.synchronize()
