@@ -22,7 +22,8 @@ EXPORTED = ("moe_status_string", "moe_max_tiles", "moe_workspace_bytes", "moe_ro
             "moe_clear_error_flags",
             "moe_read_error_flags", "moe_layer_forward_decode_noalloc", "moe_workspace_bytes_host",
             "moe_layer_forward_host", "moe_decode_stream_probe", "gqa_decode_workspace_bytes",
-            "gqa_decode_attention", "gdn_scan_workspace_bytes", "gdn_scan", "gdn_scan_opts")
+            "gqa_decode_attention", "gdn_scan_workspace_bytes", "gdn_scan", "gdn_scan_opts",
+            "moe_wait_timeout_probe")
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_MISALIGNED",
           4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA"}
@@ -106,6 +107,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_layer_forward_decode_noalloc.argtypes = [P(Dims), VP, VP, P(ExpertsC), P(ExpertsC), VP, VP, VP]
     lib.moe_decode_stream_probe.restype = ctypes.c_int
     lib.moe_decode_stream_probe.argtypes = [P(Dims), VP, P(ExpertsC), P(ExpertsC), VP, S, VP]
+    lib.moe_wait_timeout_probe.restype = ctypes.c_int
+    lib.moe_wait_timeout_probe.argtypes = [VP, S, ctypes.c_longlong, VP]
     lib.gqa_decode_workspace_bytes.restype = S
     lib.gqa_decode_workspace_bytes.argtypes = [P(GqaDims)]
     lib.gqa_decode_attention.restype = ctypes.c_int
@@ -278,6 +281,13 @@ def decode_stream_probe(dm: Dims, idx, routed: dict, shared: dict | None, worksp
     _check(load_library().moe_decode_stream_probe(ctypes.byref(dm), _ptr(idx), ctypes.byref(re),
                                                   ctypes.byref(se) if se is not None else None, _ptr(workspace),
                                                   workspace.numel(), _stream(stream)), "moe_decode_stream_probe")
+
+
+def wait_timeout_probe(workspace, limit_cycles: int, stream=None):
+    """Make the library's bounded device wait run out after limit_cycles SM cycles: the error word
+    of the workspace gets the timeout bit (ERR_WAIT_TIMEOUT) and nothing else changes."""
+    _check(load_library().moe_wait_timeout_probe(_ptr(workspace), workspace.numel(), int(limit_cycles),
+                                                 _stream(stream)), "moe_wait_timeout_probe")
 
 
 def gqa_dims(n_heads, n_kv_heads, head_dim, n_ctx, capacity=None) -> GqaDims:

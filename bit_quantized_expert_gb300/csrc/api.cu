@@ -570,6 +570,15 @@ moe_status moe_rmsnorm_router(const moe_dims* dims, float* x_resid, const float*
   return cuda_status(launch_router(maps, ra, st));
 }
 
+moe_status moe_wait_timeout_probe(void* workspace, size_t workspace_bytes, long long limit_cycles, void* stream) {
+  if (limit_cycles < 1 || limit_cycles > 4000000000ll) return MOE_ERR_INVALID_ARG;
+  moe_status s = check_ptr(workspace);
+  if (s != MOE_OK) return s == MOE_ERR_INVALID_ARG ? MOE_ERR_WORKSPACE : s;
+  if (workspace_bytes < kWsHeadBytes) return MOE_ERR_WORKSPACE;
+  return cuda_status(launch_wait_probe(static_cast<uint32_t*>(workspace), limit_cycles,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_decode_stream_probe(const moe_dims* dims, const int32_t* idx, const moe_experts* routed,
                                    const moe_experts* shared, void* workspace, size_t workspace_bytes, void* stream) {
   moe_status s = check_dims(dims);

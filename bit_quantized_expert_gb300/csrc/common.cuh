@@ -64,16 +64,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase of `parity` to complete.  Gives up (returns false) when the CTA-wide
-// abort word is set by another role, or after kWaitTimeoutCycles, in which case it sets the
-// abort word and the timeout flag.  No wait in these kernels is unbounded.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_s,
-                                          uint32_t* err) {
+// abort word is set by another role, or after `limit` cycles, in which case it sets the abort
+// word and the timeout flag.  No wait in these kernels is unbounded: they all use
+// kWaitTimeoutCycles (mbar_wait); only the wait probe passes a shorter limit.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, volatile int* abort_s, uint32_t* err,
+                                              long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_s) return false;
-    if (clock64() - t0 > kWaitTimeoutCycles) {
+    if (clock64() - t0 > limit) {
       *abort_s = 1;
       raise_flag(err, kErrWaitTimeout);
       return false;
@@ -81,14 +82,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_s,
+                                          uint32_t* err) {
+  return mbar_wait_for(bar, parity, abort_s, err, kWaitTimeoutCycles);
+}
+
 // The same wait for a whole warp that next executes warp-collective (.sync.aligned)
 // instructions such as tcgen05.ld: mbar_wait is a per-lane polling loop, so lanes may leave it at
 // different iterations; the warp is reconverged and agrees on the outcome before returning.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_s,
-                                               uint32_t* err) {
-  const bool ok = mbar_wait(bar, parity, abort_s, err);
+__device__ __forceinline__ bool mbar_wait_warp_for(uint32_t bar, uint32_t parity, volatile int* abort_s,
+                                                   uint32_t* err, long long limit) {
+  const bool ok = mbar_wait_for(bar, parity, abort_s, err, limit);
   __syncwarp();
   return __all_sync(0xFFFFFFFFu, ok);
+}
+
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_s,
+                                               uint32_t* err) {
+  return mbar_wait_warp_for(bar, parity, abort_s, err, kWaitTimeoutCycles);
 }
 
 // ------------------------------------------------------------------------------------------

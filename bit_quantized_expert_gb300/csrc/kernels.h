@@ -43,6 +43,8 @@ struct ScheduleArgs {
   uint32_t* err;
 };
 cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t st);
+// One CTA whose waits on an mbarrier that nothing completes give up after `limit` cycles (route.cu).
+cudaError_t launch_wait_probe(uint32_t* err, long long limit, cudaStream_t st);
 cudaError_t launch_tables(const TablesArgs& a, cudaStream_t st);
 
 // ---------------------------------------------------------------- grouped GEMM (gemm.cu)

@@ -324,6 +324,29 @@ cudaError_t launch_topk(const RouteArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// The library's bounded waits, made to run out: thread 0 waits on an mbarrier that nothing
+// completes until `limit` cycles pass, gives up, sets the CTA's abort word and the timeout bit of
+// the error word; warp 1 then waits on the same barrier collectively and leaves through the abort
+// word at once, all lanes with the same outcome.  Nothing else is touched.
+__global__ void __launch_bounds__(64) wait_probe_kernel(uint32_t* err, long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_s;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_s = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)mbar_wait_for(smem_u32(&bar), 0, &abort_s, err, limit);
+  __syncthreads();
+  if (threadIdx.x >= 32) (void)mbar_wait_warp_for(smem_u32(&bar), 0, &abort_s, err, limit);
+}
+
+cudaError_t launch_wait_probe(uint32_t* err, long long limit, cudaStream_t st) {
+  wait_probe_kernel<<<1, 64, 0, st>>>(err, limit);
+  return cudaGetLastError();
+}
+
 __global__ void __launch_bounds__(1024, 1) schedule_kernel(ScheduleArgs a) {
   __shared__ int pw[kMaxPartialTiles];
   __shared__ int pidx[kMaxPartialTiles];

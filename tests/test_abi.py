@@ -37,6 +37,16 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_wait_probe_host_checks(lib):
+    """moe_wait_timeout_probe refuses a limit outside 1 .. 4e9 cycles and a missing, short or
+    misaligned workspace before launching anything."""
+    f = lib.moe_wait_timeout_probe
+    assert f(256, 256, 0, None) == 1 and f(256, 256, 4000000001, None) == 1 and f(256, 256, -5, None) == 1
+    assert f(None, 256, 1000, None) == 4
+    assert f(256, 255, 1000, None) == 4
+    assert f(264, 256, 1000, None) == 3
+
+
 def test_status_strings(lib):
     for code, name in moe.STATUS.items():
         assert lib.moe_status_string(code).decode().startswith(name)

@@ -168,6 +168,27 @@ def run_layer(wl, host, dl, inp, tile_n=None, T=None, operands="fp16"):
     return out
 
 
+def test_bounded_wait_times_out_and_the_context_survives():
+    """The library's bounded device wait, made to run out after about a millisecond
+    (moe_wait_timeout_probe: a thread, then a whole warp, waiting on an mbarrier that nothing
+    completes).  The timeout bit is reported and nothing else.  A layer call on the same workspace
+    right after it, prefill then decode, is clean and matches the oracle."""
+    for wl, tol in ((synth.TINY, EXACT_TOL), (synth.DECODE, 2e-5)):
+        host, dl = layer_for(wl)
+        inp = synth.make_inputs(wl, seed=77, T=wl.T)
+        dm = moe.dims(wl.T, wl.d, wl.E, wl.k, wl.F, wl.F_shared)
+        ws = moe.alloc_workspace(dm)
+        moe.clear_error_flags(ws)
+        moe.wait_timeout_probe(ws, 2_000_000)
+        assert moe.read_error_flags(ws) == moe.ERR_WAIT_TIMEOUT
+        assert moe.read_error_flags(ws) == 0   # reading clears the word
+        y = torch.empty((wl.T, wl.d), dtype=torch.float32, device="cuda")
+        moe.layer_forward(dm, dev(inp["x"]), dev(inp["logits"]), dl["routed"], dl["shared"], dl["w_sg"], y, ws)
+        assert moe.read_error_flags(ws) == 0
+        ref = O.moe_layer(inp["x"], inp["logits"], host, wl.k)["y"]
+        assert rowwise_err(y.cpu().numpy(), ref) <= tol, wl.name
+
+
 def test_layer_tiny_exact_and_emulated():
     wl = synth.TINY
     host, dl = layer_for(wl)
