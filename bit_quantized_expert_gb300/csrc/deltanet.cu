@@ -251,6 +251,10 @@ __global__ void __launch_bounds__(kThreadsScan, 1)
       if (!mbar_wait_warp(smem_u32(&ready[b]), (c / kBufs) & 1, &abort_s, a.err)) break;
       base = pin(sm_base);
       const int nt = min(kChunk, a.T - c * kChunk);
+      // Each token's output is stored during the next token, after that token's operand loads:
+      // a store placed before them would keep them (possible alias) behind this token's chain.
+      float o_prev = 0.f;
+      uint32_t o_prev_addr = 0u;
 #pragma unroll 2
       for (int tt = 0; tt < nt; ++tt) {
         const int t = c * kChunk + tt;
@@ -259,6 +263,7 @@ __global__ void __launch_bounds__(kThreadsScan, 1)
         slice(kq_addr(kOffNQ, t), qv);
         const float4 sc = lds4(base + kOffSc + b * (kChunk * 16) + tt * 16);
         const float vi = lds1(base + kOffV + b * (kChunk * kRowsPerCta * 4) + (tt * kRowsPerCta + row) * 4);
+        if (tt > 0 && lr == 0) sts1(o_prev_addr, o_prev);
         float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f, y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -280,9 +285,10 @@ __global__ void __launch_bounds__(kThreadsScan, 1)
         const float at = sc.x, ci = sc.y * (vi - at * x);
 #pragma unroll
         for (int e = 0; e < 16; ++e) s[e] = fmaf(ci, kv[e], at * s[e]);
-        if (lr == 0)
-          sts1(sm_base + kOffO + b * (kChunk * kRowsPerCta * 4) + (tt * kRowsPerCta + row) * 4, fmaf(at, y, ci * sc.z));
+        o_prev = fmaf(at, y, ci * sc.z);
+        o_prev_addr = sm_base + kOffO + b * (kChunk * kRowsPerCta * 4) + (tt * kRowsPerCta + row) * 4;
       }
+      if (nt > 0 && lr == 0) sts1(o_prev_addr, o_prev);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&done[b]));
       if (lane < nt) {
