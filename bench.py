@@ -374,10 +374,11 @@ def decode_bench(args, world, rank, local, device, pk):
     ls = [[lh[l][i:i + 1] for i in range(NI)] for l in range(LAYERS)]
     ys = [[yh[l, i:i + 1] for i in range(NI)] for l in range(LAYERS)]
 
+    # The step's inputs are in host memory before the step is queued: MOE_OPT_HOST_INPUTS_READY.
     def e2e_step(s):
         i = s % NI
         for l in range(LAYERS):
-            layers[l].forward_host(xs[l][i], ls[l][i], ys[l][i], ws_h, sh)
+            layers[l].forward_host(xs[l][i], ls[l][i], ys[l][i], ws_h, sh, inputs_ready=True)
 
     # The same through staged copies: x and logits copied to device buffers, the device-pointer
     # layer call, y copied back (three copy-engine transfers per layer call on the stream).
@@ -415,8 +416,10 @@ def decode_bench(args, world, rank, local, device, pk):
     res["e2e"] = {"value": LAYERS * n_e2e * world / (e2e_ms / 1e3), "unit": "tokens/s",
                   "h2d_bytes_per_step": LAYERS * (wl.d * 2 + wl.E * 4), "d2h_bytes_per_step": LAYERS * wl.d * 4,
                   "steps": n_e2e,
-                  "launch": "one moe_layer_forward_host call per layer on pinned host buffers: the decode "
-                            "kernel reads x and logits from host memory and writes y there"}
+                  "launch": "one moe_layer_forward_host_opts call per layer on pinned host buffers "
+                            "(MOE_OPT_HOST_INPUTS_READY: inputs written by the host before the step): a "
+                            "staging kernel reads x and logits from host memory, the decode kernel writes "
+                            "y there"}
     res["e2e_staged"] = {"value": LAYERS * n_e2e * world / (staged_ms / 1e3), "unit": "tokens/s",
                          "launch": "per layer call: 2 H2D copies, moe_layer_forward on device buffers, "
                                    "1 D2H copy, all on one stream"}

@@ -23,12 +23,13 @@ EXPORTED = ("moe_status_string", "moe_max_tiles", "moe_workspace_bytes", "moe_ro
             "moe_read_error_flags", "moe_layer_forward_decode_noalloc", "moe_workspace_bytes_host",
             "moe_layer_forward_host", "moe_decode_stream_probe", "gqa_decode_workspace_bytes",
             "gqa_decode_attention", "gdn_scan_workspace_bytes", "gdn_scan", "gdn_scan_opts",
-            "moe_wait_timeout_probe")
+            "moe_wait_timeout_probe", "moe_layer_forward_host_opts")
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_MISALIGNED",
           4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA"}
 ERR_WAIT_TIMEOUT, ERR_FP16_RANGE, ERR_BAD_ROUTING, ERR_NON_FINITE = 1, 2, 4, 8
 OPT_BF16_OPERANDS = 1
+OPT_HOST_INPUTS_READY = 1
 _OPERAND_OPTS = {"fp16": 0, "bf16": OPT_BF16_OPERANDS}
 
 
@@ -103,6 +104,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_workspace_bytes_host.argtypes = [P(Dims)]
     lib.moe_layer_forward_host.restype = ctypes.c_int
     lib.moe_layer_forward_host.argtypes = [P(Dims), VP, VP, P(ExpertsC), P(ExpertsC), VP, VP, VP, S, VP]
+    lib.moe_layer_forward_host_opts.restype = ctypes.c_int
+    lib.moe_layer_forward_host_opts.argtypes = [P(Dims), VP, VP, P(ExpertsC), P(ExpertsC), VP, VP, VP, S, VP,
+                                                ctypes.c_uint32]
     lib.moe_layer_forward_decode_noalloc.restype = ctypes.c_int
     lib.moe_layer_forward_decode_noalloc.argtypes = [P(Dims), VP, VP, P(ExpertsC), P(ExpertsC), VP, VP, VP]
     lib.moe_decode_stream_probe.restype = ctypes.c_int
@@ -370,19 +374,24 @@ class Layer:
     def dims(self, T: int) -> Dims:
         return dims(T, self.d, self.E, self.k, self.F, self.F if self.shared is not None else 0)
 
-    def forward_host(self, x_host, logits_host, y_host, workspace, stream=None):
+    def forward_host(self, x_host, logits_host, y_host, workspace, stream=None, inputs_ready=False):
         """The layer on host tensors, queued on the stream (a torch stream, a raw handle, or None
         for the current one).  Pinned, 16-byte-aligned tensors at T = 1 are read and written by
         the decode kernel in place; otherwise the library stages them with copies (asynchronous
-        for pinned memory)."""
+        for pinned memory).  inputs_ready: MOE_OPT_HOST_INPUTS_READY (moe_layer_forward_host_opts):
+        x_host and logits_host are final when the call is made, so they may be read before the
+        preceding work on the stream finishes."""
         T = x_host.shape[0]
         dm = self._dims.get(T)
         if dm is None:
             dm = self._dims[T] = self.dims(T)
-        _check(load_library().moe_layer_forward_host(
-            ctypes.byref(dm), _host_ptr(x_host), _host_ptr(logits_host), ctypes.byref(self._re), self._se_ref,
-            _ptr(self.w_sg), _host_ptr(y_host), _ptr(workspace), workspace.numel(), _stream(stream)),
-            "moe_layer_forward_host")
+        lib = load_library()
+        args = (ctypes.byref(dm), _host_ptr(x_host), _host_ptr(logits_host), ctypes.byref(self._re), self._se_ref,
+                _ptr(self.w_sg), _host_ptr(y_host), _ptr(workspace), workspace.numel(), _stream(stream))
+        if inputs_ready:
+            _check(lib.moe_layer_forward_host_opts(*args, OPT_HOST_INPUTS_READY), "moe_layer_forward_host_opts")
+        else:
+            _check(lib.moe_layer_forward_host(*args), "moe_layer_forward_host")
 
     def forward(self, x, logits, y, workspace, routing: dict | None = None, stream=None, operands: str = "fp16"):
         """operands: "fp16" (moe_layer_forward) or "bf16" (moe_layer_forward_opts with bf16

@@ -501,6 +501,15 @@ moe_status moe_layer_forward_host(const moe_dims* dims, const uint16_t* x_host, 
                                   const moe_experts* routed, const moe_experts* shared,
                                   const uint16_t* w_shared_gate, float* y_host, void* workspace,
                                   size_t workspace_bytes, void* stream) {
+  return moe_layer_forward_host_opts(dims, x_host, logits_host, routed, shared, w_shared_gate, y_host, workspace,
+                                     workspace_bytes, stream, 0u);
+}
+
+moe_status moe_layer_forward_host_opts(const moe_dims* dims, const uint16_t* x_host, const float* logits_host,
+                                       const moe_experts* routed, const moe_experts* shared,
+                                       const uint16_t* w_shared_gate, float* y_host, void* workspace,
+                                       size_t workspace_bytes, void* stream, uint32_t options) {
+  if (options & ~(uint32_t)MOE_OPT_HOST_INPUTS_READY) return MOE_ERR_INVALID_ARG;
   moe_status s = check_dims(dims);
   if (s != MOE_OK) return s;
   if (dims->T == 0) return MOE_OK;
@@ -532,6 +541,7 @@ moe_status moe_layer_forward_host(const moe_dims* dims, const uint16_t* x_host, 
       sa.lg_dst = logits;
       sa.x_units = (int)T * dims->d * 2 / 16;
       sa.lg_n = (int)T * dims->E;
+      sa.early = (options & MOE_OPT_HOST_INPUTS_READY) ? 1 : 0;
       if (launch_stage_in(sa, st) != cudaSuccess) return MOE_ERR_CUDA;
       return moe_layer_forward(dims, x, logits, routed, shared, w_shared_gate, static_cast<float*>(ym), nullptr,
                                workspace, layout_of(*dims).total, stream);

@@ -926,34 +926,39 @@ constexpr int kStageThreads = 256;
 constexpr int kStageIn = 4;   // loads in flight per thread per round
 
 __global__ void __launch_bounds__(kStageThreads) stage_in_kernel(const StageArgs a) {
+  // Rounds of kStageIn 16-byte loads of x and kStageIn loads of logits per thread.  The stores go
+  // to workspace buffers that the previous kernel may still read, so they follow the dependency
+  // wait; with a.early the host inputs are final when the call is made and the first round of
+  // reads goes out before the wait (its latency across the CPU-GPU link overlaps that kernel).
+  const int tid = threadIdx.x;
+  constexpr int kStep = kStageThreads * kStageIn;
+  uint4 xv[kStageIn];
+  float lv[kStageIn];
+  auto load = [&](int base) {
+#pragma unroll
+    for (int c = 0; c < kStageIn; ++c) {
+      const int i = base + c * kStageThreads + tid;
+      if (i < a.x_units) xv[c] = a.x_src[i];
+      if (i < a.lg_n) lv[c] = a.lg_src[i];
+    }
+  };
+  auto store = [&](int base) {
+#pragma unroll
+    for (int c = 0; c < kStageIn; ++c) {
+      const int i = base + c * kStageThreads + tid;
+      if (i < a.x_units) a.x_dst[i] = xv[c];
+      if (i < a.lg_n) a.lg_dst[i] = lv[c];
+    }
+  };
+  if (a.early) load(0);
   pdl_wait();   // the previous kernel, the last reader of the destination buffers, is complete
   pdl_launch_dependents();
-  const int tid = threadIdx.x;
-  for (int base = 0; base < a.x_units; base += kStageThreads * kStageIn) {
-    uint4 v[kStageIn];
-#pragma unroll
-    for (int c = 0; c < kStageIn; ++c) {
-      const int i = base + c * kStageThreads + tid;
-      if (i < a.x_units) v[c] = a.x_src[i];
-    }
-#pragma unroll
-    for (int c = 0; c < kStageIn; ++c) {
-      const int i = base + c * kStageThreads + tid;
-      if (i < a.x_units) a.x_dst[i] = v[c];
-    }
-  }
-  for (int base = 0; base < a.lg_n; base += kStageThreads * kStageIn) {
-    float v[kStageIn];
-#pragma unroll
-    for (int c = 0; c < kStageIn; ++c) {
-      const int i = base + c * kStageThreads + tid;
-      if (i < a.lg_n) v[c] = a.lg_src[i];
-    }
-#pragma unroll
-    for (int c = 0; c < kStageIn; ++c) {
-      const int i = base + c * kStageThreads + tid;
-      if (i < a.lg_n) a.lg_dst[i] = v[c];
-    }
+  if (!a.early) load(0);
+  store(0);
+  const int n = a.x_units > a.lg_n ? a.x_units : a.lg_n;
+  for (int base = kStep; base < n; base += kStep) {
+    load(base);
+    store(base);
   }
 }
 

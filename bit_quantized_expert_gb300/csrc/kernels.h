@@ -168,6 +168,7 @@ struct StageArgs {
   float* lg_dst;
   int x_units;   // 16-byte units of x
   int lg_n;      // floats of logits
+  int early;     // the first round of host reads goes out before the dependency wait
 };
 cudaError_t launch_stage_in(const StageArgs& a, cudaStream_t st);
 

@@ -202,6 +202,22 @@ moe_status moe_layer_forward_host(const moe_dims* dims, const uint16_t* x_host, 
                                   const uint16_t* w_shared_gate, float* y_host, void* workspace,
                                   size_t workspace_bytes, void* stream);
 
+/* Option bits of moe_layer_forward_host_opts. */
+#define MOE_OPT_HOST_INPUTS_READY 1u
+
+/* moe_layer_forward_host with options; options == 0 is moe_layer_forward_host.
+ * MOE_OPT_HOST_INPUTS_READY: x_host and logits_host hold their final values when the call is made
+ * (no work queued on the stream before the call writes them).  On the staging-kernel path (T <= 8,
+ * page-locked mapped buffers) the kernel then reads them before the preceding work on the stream
+ * has finished, so their latency across the CPU-GPU link overlaps that work; the workspace is
+ * still written only after it.  Results are identical to moe_layer_forward_host's; the copy path
+ * is unaffected.  Returns MOE_ERR_INVALID_ARG for an unknown option bit; otherwise as
+ * moe_layer_forward_host. */
+moe_status moe_layer_forward_host_opts(const moe_dims* dims, const uint16_t* x_host, const float* logits_host,
+                                       const moe_experts* routed, const moe_experts* shared,
+                                       const uint16_t* w_shared_gate, float* y_host, void* workspace,
+                                       size_t workspace_bytes, void* stream, uint32_t options);
+
 /* Pre-norm block of a stack of MoE layers (the step between two layers, not part of the layer; an
  * addition for the 40-layer stack workload -- the pages' router scores 256 experts from the
  * normalised hidden state, a linear router being the reading):

@@ -162,6 +162,15 @@ def test_layer_host_entry_checks(lib):
     assert call(wsn=ws_h - 1) == 4
     assert call(wsn=ws_n) == 4
     assert call(dm=moe.dims(0, 256, 16, 2, 128, 128)) == 0   # T == 0: nothing to do
+    # moe_layer_forward_host_opts: unknown option bits refused first; the known one checks alike
+    opts = lambda o, **kw: lib.moe_layer_forward_host_opts(
+        ctypes.byref(kw.get("dm", dm)), kw.get("x", 16), 16, ctypes.byref(ex), ctypes.byref(ex), 16, 16,
+        kw.get("ws", 16), ws_h, None, o)
+    assert moe.OPT_HOST_INPUTS_READY == 1
+    for bad in (2, 0x80000000, 0xFFFFFFFF):
+        assert opts(bad) == 1, bad
+    assert opts(1, x=None) == 1 and opts(1, ws=None) == 4
+    assert opts(1, dm=moe.dims(0, 256, 16, 2, 128, 128)) == 0
 
 
 def test_gqa_workspace_bytes(lib):

@@ -355,7 +355,7 @@ def test_layer_host_entry_matches_device_entry(memory):
     and the grouped-GEMM path (T = 37): with page-locked, mapped, aligned buffers at T <= 3 the
     staging kernel reads host memory and the decode kernel writes y there (y only when it comes
     from cudaHostAlloc; registered memory takes the copy for y); pageable or unaligned buffers,
-    and T > 3, take the copies."""
+    and T > 3, take the copies.  With MOE_OPT_HOST_INPUTS_READY the bits are the same."""
     wl = synth.TINY
     host, dl = layer_for(wl)
     layer = moe.Layer(dl["routed"], dl["shared"], dl["w_sg"], wl.d, wl.E, wl.k, wl.F)
@@ -388,6 +388,12 @@ def test_layer_host_entry_matches_device_entry(memory):
         assert moe.read_error_flags(ws) == 0
         ref = run_layer(wl, host, dl, inp, T=T)["y"]
         assert np.array_equal(yh.numpy(), ref), (memory, T)
+        # MOE_OPT_HOST_INPUTS_READY (host reads before the dependency wait): the same bits
+        yh.fill_(float("nan"))
+        layer.forward_host(xh, lh, yh, ws, inputs_ready=True)
+        torch.cuda.synchronize()
+        assert moe.read_error_flags(ws) == 0
+        assert np.array_equal(yh.numpy(), ref), (memory, T, "inputs ready")
     for b in registered:
         rt = torch.cuda.cudart()
         assert rt.cudaHostUnregister(b.data_ptr()) == rt.cudaError.success
